@@ -1,0 +1,489 @@
+"""Benchmark of one decode step of the paged KV-cache hot path on GB300.
+
+A step is one pass of the whole hot path over one batch: the cache write of
+every sequence's new token (slots from the library's block manager), then paged
+decode attention (partition launch + log-sum-exp reduce launch) over all cached
+tokens, new token included.
+
+Default workload: the 13B-shaped MHA decode batch (64 sequences, 40 query = 40
+KV heads, head_dim 128, fp16, block size 16, lognormal lengths with median 300
+and sigma 1.0 clipped to [1, 2048], pool = blocks + 10% shuffled).
+
+value     = algorithmic KV-read bytes of decode attention / device step time
+            (CUDA events on the launching stream; L2 flushed between steps).
+e2e       = the same bytes / end-to-end step time through the public API with
+            pinned host buffers: H2D of q, new K/V, slots, tables and lengths,
+            the library calls, D2H of the output.
+roofline  = the partition kernel alone: its algorithmic bytes / its event time,
+            against the measured HBM copy bandwidth.
+cpu_baseline / --impl reference = the fp64 oracle on the host cores.
+
+Under torchrun with N ranks each rank runs an independent replica of the
+workload on its own GPU (the path shards by sequence with no exchange step);
+value = bytes of all ranks / max rank time.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+METRIC = "paged decode attn KV-read GB/s (% of GB300 HBM peak); seq-tokens/s per layer"
+NOMINAL_HBM_GBS = 8000.0
+FALLBACK_HBM_GBS = 6800.0
+FLUSH_BYTES = 512 << 20  # > 129 MB L2
+
+
+def attention_bytes(lens, Hq, Hkv, D, elt, B=16) -> int:
+    """Algorithmic bytes decode attention must move: K and V rows of the cached
+    tokens (no padded block tails), the int32 table entries, the context length,
+    one query and one output row per query head."""
+    lens = np.asarray(lens, dtype=np.int64)
+    nb = (lens + B - 1) // B
+    return int((2 * lens * Hkv * D * elt + 4 * nb + 4 + 2 * Hq * D * elt).sum())
+
+
+def kv_write_bytes(num_tokens, Hkv, D, elt) -> int:
+    return int(num_tokens * (2 * 2 * Hkv * D * elt + 4))
+
+
+def measured_peak():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return float(d["hbm_gbs"]), "measured"
+    except Exception:
+        return FALLBACK_HBM_GBS, "fallback"
+
+
+def profile_traffic(kernel_tag: str):
+    """Per-launch DRAM bytes from the committed ncu summary of this kernel, if the
+    kernel source is unchanged since it was captured."""
+    path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
+    src = os.path.join(ROOT, "paged_kv_cache_166_gb300", "csrc", "decode_attention.cu")
+    try:
+        text = open(path).read()
+        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        fields = dict(l.strip("- ").split(": ", 1) for l in text.splitlines()
+                      if l.startswith("- ") and ": " in l)
+        if fields.get("source_sha") != sha:
+            return None
+        return int(fields["traffic_bytes_per_launch"])
+    except Exception:
+        return None
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples taken while the timed region runs."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.t = threading.Thread(target=self._read, daemon=True)
+            self.t.start()
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.2)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.lines:
+            return None
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for l in self.lines:
+            parts = [p.strip() for p in l.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": float(np.median(sm)), "sm_max_mhz": float(max(mx)),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# --------------------------------------------------------------------------------------
+# workload construction through the library (block manager -> tables, slots)
+# --------------------------------------------------------------------------------------
+def build_batch(name: str, device, rank: int = 0):
+    import torch
+    from paged_kv_cache_166_gb300 import BlockAllocator
+    from paged_kv_cache_166_gb300 import workloads as W
+
+    w = W.WORKLOADS[name]
+    seed = w.seed + 1000 * rank
+    lens = W.context_lengths(w)
+    if rank:
+        import dataclasses
+        lens = W.context_lengths(dataclasses.replace(w, seed=seed)) if w.length_kind != "fixed" else lens
+    B = w.block_size
+    blocks = int(((lens + B - 1) // B).sum())
+    NB = w.fixed_pool_blocks or int(math.ceil(blocks * (1 + w.pool_spare))) + 1
+    alloc = BlockAllocator(NB, B, W.pool_order(NB, seed))
+    sids = [alloc.create() for _ in range(len(lens))]
+    for s, t in zip(sids, lens):
+        alloc.append(s, int(t) - 1)
+    new_slots = np.array([alloc.append(s, 1)[0][0] for s in sids], dtype=np.int32)
+    maxb = int(((lens + B - 1) // B).max())
+    tables, ctx = alloc.export_tables(sids, maxb)
+    dt = W.torch_dtype(w.dtype)
+    S, Hq, Hkv, D = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim
+    kc = torch.empty((NB, Hkv, B, D), dtype=dt, device=device)
+    vc = torch.empty_like(kc)
+    W.fill_normal_(kc, seed, W.STREAM_K_POOL)
+    W.fill_normal_(vc, seed, W.STREAM_V_POOL)
+    host = {
+        "q": W.normal_tensor((S, Hq, D), w.dtype, seed, W.STREAM_Q, "cpu"),
+        "k_new": W.normal_tensor((S, Hkv, D), w.dtype, seed, W.STREAM_K_NEW, "cpu"),
+        "v_new": W.normal_tensor((S, Hkv, D), w.dtype, seed, W.STREAM_V_NEW, "cpu"),
+        "slots": torch.from_numpy(new_slots),
+        "tables": torch.from_numpy(tables),
+        "ctx": torch.from_numpy(ctx),
+    }
+    host = {k: v.pin_memory() for k, v in host.items()}
+    dev = {k: v.to(device) for k, v in host.items()}
+    return w, lens, NB, kc, vc, host, dev
+
+
+# --------------------------------------------------------------------------------------
+# oracle timing on the host (cpu_baseline and --impl reference)
+# --------------------------------------------------------------------------------------
+def _oracle_task(args):
+    from oracle import paged_attention
+    q, kc, vc, table, t, scale = args
+    t0 = time.perf_counter()
+    paged_attention.paged_attention(q[None], kc, vc, table[None], np.array([t]), scale)
+    return time.perf_counter() - t0
+
+
+def oracle_inputs(name: str, seqs=None):
+    """Per-sequence oracle inputs of the workload, built on the host with the
+    oracle's own block manager and the shared generators (fp32 arrays hold the
+    fp16/bf16 draws exactly)."""
+    import torch
+    from oracle.block_manager import BlockManager
+    from paged_kv_cache_166_gb300 import workloads as W
+    w = W.WORKLOADS[name]
+    lens = W.context_lengths(w)
+    B = w.block_size
+    seqs = list(range(len(lens))) if seqs is None else seqs
+    tasks = []
+    for s in seqs:
+        t = int(lens[s])
+        nb = -(-t // B)
+        # values drawn per sequence from the workload seed (the timing depends only on shapes)
+        kc = W.normal_tensor((nb, w.num_kv_heads, B, w.head_dim), w.dtype, w.seed * 7919 + s,
+                             W.STREAM_K_POOL).float().numpy()
+        vc = W.normal_tensor((nb, w.num_kv_heads, B, w.head_dim), w.dtype, w.seed * 7919 + s,
+                             W.STREAM_V_POOL).float().numpy()
+        q = W.normal_tensor((w.num_q_heads, w.head_dim), w.dtype, w.seed * 7919 + s,
+                            W.STREAM_Q).float().numpy()
+        mgr = BlockManager(nb, B)
+        sid = mgr.create()
+        mgr.append(sid, t)
+        table = np.asarray(mgr.tables[sid], dtype=np.int32)
+        tasks.append((q, kc, vc, table, t, w.scale))
+    return w, lens, seqs, tasks
+
+
+def time_oracle(name: str, budget_s: float = 15.0, steps: int = 1):
+    """Wall time of the oracle over a bounded sample of the workload on all host
+    cores (one single-threaded process per core, spawned)."""
+    import multiprocessing as mp
+    cores = os.cpu_count() or 1
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    w, lens, _, _ = oracle_inputs(name, [])
+    order = list(np.argsort(-lens))  # longest first: a sample that covers the tail
+    ctx = mp.get_context("spawn")
+    with ctx.Pool(cores) as pool:
+        # calibrate on a few sequences, then size the sample to the budget
+        probe = order[:min(len(order), cores)]
+        _, _, _, tasks = oracle_inputs(name, probe)
+        t0 = time.perf_counter()
+        pool.map(_oracle_task, tasks)
+        per_tok = (time.perf_counter() - t0) / max(1, sum(int(lens[s]) for s in probe))
+        want_tokens = budget_s / max(per_tok, 1e-9)
+        sample, tok = [], 0
+        for s in order:
+            if tok >= want_tokens and sample:
+                break
+            sample.append(int(s))
+            tok += int(lens[s])
+        _, _, _, tasks = oracle_inputs(name, sample)
+        times = []
+        for _ in range(steps):
+            t0 = time.perf_counter()
+            pool.map(_oracle_task, tasks)
+            times.append(time.perf_counter() - t0)
+    elt = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
+    nbytes = attention_bytes(lens[sample], w.num_q_heads, w.num_kv_heads, w.head_dim, elt)
+    return {"seconds": times, "bytes": nbytes, "tokens": int(lens[sample].sum()),
+            "num_seqs": len(sample), "total_seqs": int(len(lens)), "cores": cores}
+
+
+# --------------------------------------------------------------------------------------
+def native(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    # the oracle pool is spawned before the first GPU call of this process
+    cpu = time_oracle(args.workload, budget_s=args.cpu_budget) if (rank == 0 and world == 1 and
+                                                                     not args.no_cpu_baseline) else None
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_166_gb300 as pkv
+
+    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, rank)
+    S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    elt = kc.element_size()
+    MAXB = dev["tables"].shape[1]
+    out = torch.empty_like(dev["q"])
+    ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, kc.dtype, args.num_warps), dtype=torch.uint8,
+                     device=device)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    stream = torch.cuda.current_stream(device)
+    attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B)
+    write_bytes = kv_write_bytes(S, Hkv, D, elt)
+
+    def step():
+        pkv.paged_kv_write(dev["k_new"], dev["v_new"], dev["slots"], kc, vc)
+        e1.record(stream)
+        pkv.paged_decode_attention_partition(dev["q"], kc, vc, dev["tables"], dev["ctx"],
+                                             w.scale, out, ws, args.num_warps)
+        e2.record(stream)
+        pkv.paged_decode_attention_reduce(dev["ctx"], MAXB, Hkv, B, out, ws, args.num_warps)
+
+    e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+    if pkv.decode_status(ws) != 0:
+        raise RuntimeError("device status reported an error during warm-up")
+
+    step_ms, part_ms = [], []
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clocks:
+        t_wall = time.perf_counter()
+        for _ in range(args.steps):
+            flush.zero_()              # L2 flush, outside the timed events
+            e0.record(stream)
+            step()
+            e3.record(stream)
+            e3.synchronize()
+            step_ms.append(e0.elapsed_time(e3))
+            part_ms.append(e1.elapsed_time(e2))
+        torch.cuda.synchronize()
+        wall = time.perf_counter() - t_wall
+    if world > 1:
+        dist.barrier()
+    ms = float(np.mean(step_ms))
+    pms = float(np.mean(part_ms))
+
+    # end to end through the public API with pinned host buffers
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    d2h = out.numel() * out.element_size()
+
+    def e2e_step():
+        for k in host:
+            dev[k].copy_(host[k], non_blocking=True)
+        pkv.paged_kv_write(dev["k_new"], dev["v_new"], dev["slots"], kc, vc)
+        pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws,
+                                   args.num_warps)
+        out_h.copy_(out, non_blocking=True)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = []
+    for _ in range(args.steps):
+        flush.zero_()
+        e0.record(stream)
+        e2e_step()
+        e3.record(stream)
+        e3.synchronize()
+        e2e_ms.append(e0.elapsed_time(e3))
+    e2e = float(np.mean(e2e_ms))
+    status = pkv.decode_status(ws)
+    if status:
+        raise RuntimeError(f"device status {status} after the timed steps")
+
+    if world > 1:
+        t = torch.tensor([ms, e2e], dtype=torch.float64, device=device)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms, e2e = float(t[0]), float(t[1])
+    if rank != 0:
+        if world > 1:
+            dist.destroy_process_group()
+        return
+
+    peak, peak_kind = measured_peak()
+    total_bytes = attn_bytes * world
+    gbs = total_bytes / (ms * 1e-3) / 1e9
+    part_gbs = attn_bytes / (pms * 1e-3) / 1e9
+    traffic = profile_traffic(f"decode_partition_{args.workload}")
+    line = {
+        "metric": METRIC,
+        "value": round(gbs, 1),
+        "unit": "GB/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms, 4),
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": w.dtype,
+        "data": "synthetic",
+        "config": {
+            "workload": f"{w.name}: {S} seqs, {Hq} q / {Hkv} kv heads, head_dim {D}, {w.dtype}, "
+                        f"block 16, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks",
+            "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
+            "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
+            "step": "paged_kv_write (1 new token/seq) + decode attention (partition + reduce)",
+            "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
+            "num_warps": args.num_warps or pkv.default_num_warps(D, kc.dtype),
+            "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+        },
+        "pct_of_peak": {"measured_copy": round(100 * gbs / peak, 1),
+                        "nominal_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
+                        "peak_kind": peak_kind},
+        "seq_tokens_per_s": round(int(lens.sum()) * world / (ms * 1e-3), 1),
+        "attention_only": {"kv_gbs_partition_kernel": round(part_gbs, 1),
+                           "partition_ms": round(pms, 4)},
+        "roofline": {
+            "bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(part_gbs / peak, 4), "traffic": traffic,
+            "kernel": "decode_partition_kernel", "bytes_per_launch": attn_bytes,
+            "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+        },
+        "e2e": {"value": round(total_bytes / (e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+                "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": int(h2d),
+                "d2h_bytes_per_step": int(d2h)},
+        "gpu_launches": 3 * args.steps,
+        "clocks": clocks.summary(),
+        "wall_s_timed_loop": round(wall, 3),
+    }
+    if cpu is not None:
+        cs = float(np.median(cpu["seconds"]))
+        line["cpu_baseline"] = {
+            "value": round(cpu["bytes"] / cs / 1e9, 4), "unit": "GB/s", "cores": cpu["cores"],
+            "kind": "oracle",
+            "sample": f"{cpu['num_seqs']} of {cpu['total_seqs']} sequences (longest first, "
+                      f"{cpu['tokens']} tokens), fp64 numpy oracle, one spawned process per core",
+            "seconds": round(cs, 3)}
+    print(json.dumps(line), flush=True)
+    if world > 1:
+        dist.destroy_process_group()
+
+
+def reference(args):
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    if rank != 0:
+        return
+    res = None
+    times = []
+    for i in range(args.warmup + args.steps):
+        r = time_oracle(args.workload, budget_s=args.ref_budget, steps=1)
+        if i >= args.warmup:
+            times.append(r["seconds"][0])
+            res = r
+    from paged_kv_cache_166_gb300 import workloads as W
+    w = W.WORKLOADS[args.workload]
+    sec = float(np.mean(times))
+    gbs = res["bytes"] / sec / 1e9
+    sample = (f"{res['num_seqs']} of {res['total_seqs']} sequences (longest first, "
+              f"{res['tokens']} tokens) per step, fp64 numpy oracle, one spawned process per core")
+    print(json.dumps({
+        "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
+        "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": f"{w.name} (host oracle on a bounded sample)"},
+        "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": res["cores"],
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["native", "reference"], default="native")
+    ap.add_argument("--workload", default="mha13b",
+                    choices=["tiny", "mha13b", "gqa70b", "prefix", "longctx"])
+    ap.add_argument("--num-warps", type=int, default=0)
+    ap.add_argument("--cpu-budget", type=float, default=10.0)
+    ap.add_argument("--ref-budget", type=float, default=5.0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
+    if args.workload == "prefix":
+        ap.error("the shared-prefix workload is a parity case; bench the decode batches")
+    (reference if args.impl == "reference" else native)(args)
+
+
+if __name__ == "__main__":
+    main()

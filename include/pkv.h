@@ -1,0 +1,284 @@
+/*
+ * pkv.h — C ABI of the GB300 paged KV-cache decode library (libpkv.so).
+ *
+ * The library implements the data-parallel hot path of PagedAttention:
+ *   - the cache write that scatters each new token's K and V into its slot,
+ *   - single-token decode attention read through per-sequence block tables,
+ *     split over the context and merged with a log-sum-exp reduce,
+ *   - the whole-block copy that copy-on-write needs,
+ *   - a host-side block manager (O(1) free list, per-block refcounts, fork,
+ *     append with copy-on-write, free).
+ *
+ * Conventions (all entry points):
+ *   - Every function returns an int status: PKV_OK (0) or a negative PKV_ERR_*.
+ *     No C++ exception crosses the ABI.  pkv_last_error_string() returns a
+ *     thread-local message describing the last failure in the calling thread.
+ *   - Device pointers are plain CUDA device addresses owned by the caller; the
+ *     library never allocates or frees device memory.  Host pointers are
+ *     caller-owned host memory.  Block-manager handles are owned by the library
+ *     and released with pkv_allocator_destroy.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Device calls
+ *     only enqueue work on it and return; results are ready once the stream is
+ *     synchronised.  A status of PKV_ERR_CUDA means a launch or API call failed.
+ *   - Cache layout (per layer, K and V as two separate tensors):
+ *       [num_blocks, num_kv_heads, block_size, head_dim], row-major, contiguous,
+ *     the layout "PagedAttention: How vLLM Borrowed Virtual Memory to Unlock GPU
+ *     Serving at Scale" gives in section "The Custom CUDA Kernel".  One physical
+ *     block id indexes the same block in every layer's tensors.
+ *   - Slot of logical position p of a sequence with block table bt:
+ *       slot(p) = bt[p / block_size] * block_size + p % block_size
+ *     ("What is paged attention?", section "How it works").  Token slot s lives at
+ *     cache[s / block_size, :, s % block_size, :].
+ *   - dtype codes: PKV_F32, PKV_F16, PKV_BF16; q, out, k, v and the caches share
+ *     one dtype.  Index tensors are int32.
+ */
+#ifndef PKV_H_
+#define PKV_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum pkv_status {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = -1,  /* bad pointer, size, shape, alignment or id */
+  PKV_ERR_DTYPE = -2,        /* unknown dtype code */
+  PKV_ERR_OUT_OF_BLOCKS = -3,/* block manager cannot serve the request; state unchanged */
+  PKV_ERR_CUDA = -4,         /* a CUDA runtime/driver call failed (see message) */
+  PKV_ERR_UNSUPPORTED = -5,  /* valid request outside what the kernels implement */
+  PKV_ERR_DEVICE = -6        /* a kernel reported a device-side error (see pkv_decode_status) */
+};
+
+enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 };
+
+/* Device-side status bits recorded by the decode kernels in the workspace. */
+enum pkv_device_status {
+  PKV_DEV_BAD_CONTEXT_LEN = 1, /* a context length was < 0 or > max_blocks_per_seq * block_size; clamped */
+  PKV_DEV_BAD_BLOCK_ID = 2,    /* a block-table entry was outside [0, num_blocks); read as zeros */
+  PKV_DEV_WAIT_TIMEOUT = 4     /* a copy into shared memory did not complete within ~1 s; unit skipped */
+};
+
+/* Message of the last failure in this thread ("" if none).  Never NULL. */
+const char* pkv_last_error_string(void);
+
+/* Library version, encoded as major*10000 + minor*100 + patch. */
+int pkv_version(void);
+
+/* ------------------------------------------------------------------------- */
+/* Cache write                                                                */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * pkv_kv_write — scatter new tokens' K and V into their cache slots.
+ *
+ * Follows the decode step "write the new token's K,V into the last block"
+ * ("PagedAttention and vLLM: Virtual Memory for the KV Cache", section
+ * "L2 — Mechanism", allocation lifecycle) with the slot formula above:
+ *   for i < num_tokens, h < num_kv_heads with s = slot_mapping[i] >= 0:
+ *     k_cache[s / block_size, h, s % block_size, :] = k[i, h, :]   (bit copy)
+ *     v_cache[s / block_size, h, s % block_size, :] = v[i, h, :]
+ *
+ * k, v          device, [num_tokens, num_kv_heads, head_dim], contiguous.
+ * slot_mapping  device int32 [num_tokens].  A negative slot marks a padding
+ *               token and writes nothing.  Slots >= num_blocks*block_size are
+ *               skipped.  Two tokens with the same slot: the result is one of
+ *               the two rows (unspecified which).
+ * k_cache, v_cache  device caches in the layout above, updated in place.
+ * Requirements: head_dim * element size a multiple of 16 bytes; all pointers
+ * 16-byte aligned; num_blocks*block_size < 2^31.  num_tokens == 0 is a no-op.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_CUDA.
+ */
+int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int32_t num_tokens,
+                 void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                 int32_t block_size, int32_t head_dim, int32_t dtype, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Decode attention                                                           */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * pkv_decode_workspace_size — bytes of device workspace pkv_decode_attention needs.
+ *
+ * The workspace holds the per-piece softmax partials of contexts that are split
+ * across warps plus a status word.  Its size depends only on the head shape, the
+ * dtype and the number of worker warps the launch uses (num_warps; 0 = the
+ * default for the current device), never on the context lengths or the batch.
+ * Before its first use the workspace must be zero-filled (the status word is
+ * sticky: kernels only set bits in it; pkv_decode_status reads and clears it).
+ * One workspace must not be used by two launches that may run concurrently.
+ */
+int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                              int32_t dtype, int32_t num_warps, size_t* bytes);
+
+/*
+ * pkv_decode_attention — single-token decode attention over a block-paged cache.
+ *
+ * For every sequence s < num_seqs and query head h < num_q_heads, with
+ * G = num_q_heads / num_kv_heads, g = h / G and t = context_lens[s]:
+ *   out[s, h, :] = sum_{p<t} w_p * V[slot(p), g, :] / sum_{p<t} w_p,
+ *   w_p = exp(scale * q[s, h, :] . K[slot(p), g, :] - max_p(...)),
+ * i.e. softmax(q K^T * scale) V over the sequence's t cached positions read
+ * through its block table — the same attention a contiguous cache gives
+ * ("PagedAttention — how vLLM stopped wasting 80% of your GPU memory", section
+ * "The PagedAttention kernel: computing attention over scattered blocks").
+ * t counts the token being decoded, whose K/V must already be in the cache
+ * (write with pkv_kv_write first).  t == 0 yields a zero row.
+ *
+ * Work is split into equal runs of (sequence, KV head, block) steps over all
+ * worker warps; a context cut by a run boundary is finished as several partial
+ * softmax states merged in fixed order by a log-sum-exp reduce ("two-pass
+ * reduction ... numerically stable merge", "PagedAttention: How vLLM Borrowed
+ * Virtual Memory...", section "The Custom CUDA Kernel").  Results depend only on
+ * the values, context lengths and num_warps — never on which physical blocks
+ * hold the data — and are bit-identical between runs.
+ *
+ * q             device [num_seqs, num_q_heads, head_dim], contiguous.
+ * k_cache, v_cache  device caches [num_blocks, num_kv_heads, block_size, head_dim].
+ * block_tables  device int32 [num_seqs, max_blocks_per_seq]; entries past
+ *               ceil(t / block_size) are never read.
+ * context_lens  device int32 [num_seqs].
+ * scale         softmax scale (typically 1/sqrt(head_dim)).
+ * out           device [num_seqs, num_q_heads, head_dim], written in full.
+ * workspace     device, >= pkv_decode_workspace_size(...) bytes, 256-byte aligned,
+ *               zero-filled before first use.
+ * num_warps     worker warps (0 = device default); pass the same value given to
+ *               pkv_decode_workspace_size.
+ * Supported: block_size 16; dtype F16/BF16 with head_dim 64, 128 or 256, or F32
+ * with head_dim 32, 64 or 128; G in {1, 2, 4, 8}; num_seqs <= 2048;
+ * num_blocks*num_kv_heads*16 < 2^31; num_seqs*max_blocks_per_seq*num_kv_heads < 2^31.
+ * Invalid device data (a context length outside [0, max_blocks_per_seq*16], a
+ * block id outside [0, num_blocks)) never faults: it is clamped or read as zeros
+ * and recorded in the workspace status word (see pkv_decode_status).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, float scale, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream);
+
+/*
+ * The two launches pkv_decode_attention makes, exposed separately so that a caller
+ * can time them apart.  pkv_decode_attention_partition runs every worker warp
+ * over its run of blocks and writes finished rows of `out` plus the partial
+ * states of split contexts into the workspace; pkv_decode_attention_reduce then
+ * merges the partial states into `out` and writes the zero rows of empty
+ * contexts.  Calling both, in this order on one stream, with identical
+ * arguments, is exactly pkv_decode_attention.
+ */
+int pkv_decode_attention_partition(const void* q, const void* k_cache, const void* v_cache,
+                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                   const int32_t* context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                                   int32_t block_size, int32_t num_blocks, float scale, void* out,
+                                   void* workspace, size_t workspace_bytes, int32_t num_warps,
+                                   int32_t dtype, void* stream);
+int pkv_decode_attention_reduce(const int32_t* context_lens, int32_t max_blocks_per_seq,
+                                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                int32_t head_dim, int32_t block_size, void* out, void* workspace,
+                                size_t workspace_bytes, int32_t num_warps, int32_t dtype,
+                                void* stream);
+
+/*
+ * pkv_decode_status — read and clear the device status word of a workspace.
+ * Synchronises `stream`, copies the word to *status (PKV_DEV_* bits, 0 = clean)
+ * and zeroes it on the device.
+ */
+int pkv_decode_status(void* workspace, int32_t* status, void* stream);
+
+/* Number of worker warps the default launch uses on the current device. */
+int pkv_decode_default_warps(int32_t head_dim, int32_t dtype, int32_t* num_warps);
+
+/* ------------------------------------------------------------------------- */
+/* Copy-on-write block copy                                                   */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * pkv_copy_blocks — copy whole physical blocks, K and V, for copy-on-write.
+ *
+ * For each pair i < num_pairs: block src = pairs[2i] is copied onto block
+ * dst = pairs[2i+1] in both caches (all KV heads and slots: block_elems =
+ * num_kv_heads*block_size*head_dim elements each).  This is the data copy of
+ * "allocates a new physical block, copies the content" ("PagedAttention: How
+ * vLLM Borrowed Virtual Memory...", section "Copy-on-Write for Beam Search and
+ * Parallel Sampling").  Pairs with an id outside [0, num_blocks) are skipped.
+ * A dst that is also some pair's src, or two pairs with one dst: unspecified.
+ * src_dst_pairs is device int32 [num_pairs, 2].  block_elems * element size
+ * must be a multiple of 16 bytes and both caches 16-byte aligned.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_CUDA.
+ */
+int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int32_t num_pairs,
+                    int32_t num_blocks, int64_t block_elems, int32_t dtype, void* stream);
+
+/* ------------------------------------------------------------------------- */
+/* Host block manager                                                         */
+/* ------------------------------------------------------------------------- */
+/*
+ * The block manager of "PagedAttention: How vLLM Borrowed Virtual Memory...",
+ * sections "The OS-Inspired Insight" and "Walking Through the Lifecycle", and
+ * "What is paged attention?", section "How it works":
+ *   - a fixed pool of num_blocks blocks; allocation pops the free list, freeing
+ *     pushes it, both O(1).  The free list is a stack whose first pops return
+ *     pop_order[0], pop_order[1], ... (ascending ids when pop_order is NULL);
+ *   - a refcount per block counts the table entries that point at it; a block
+ *     returns to the free list when its count reaches 0;
+ *   - fork copies a table and increments every block in it;
+ *   - appending position p: if p % block_size == 0 a new block is pushed on the
+ *     table (never a copy); otherwise, if the last block is shared (refcount > 1),
+ *     the writer gets a fresh block, the (old, new) copy-on-write pair is
+ *     reported, the old block is decremented and the new one replaces it;
+ *     the slot is table[p / block_size] * block_size + p % block_size;
+ *   - freeing a sequence decrements its table in reverse order.
+ * Sequence ids are 0, 1, 2, ... in creation order and never reused.
+ * Every failing call leaves the state unchanged.  A handle is not thread-safe.
+ */
+typedef struct pkv_allocator pkv_allocator_t;
+
+int pkv_allocator_create(int32_t num_blocks, int32_t block_size, const int32_t* pop_order,
+                         pkv_allocator_t** out);
+int pkv_allocator_destroy(pkv_allocator_t* a);
+
+int pkv_block_alloc(pkv_allocator_t* a, int32_t* block_id);   /* PKV_ERR_OUT_OF_BLOCKS if empty */
+int pkv_block_incref(pkv_allocator_t* a, int32_t block_id);   /* block must be allocated */
+int pkv_block_decref(pkv_allocator_t* a, int32_t block_id);   /* block must be allocated */
+int pkv_block_refcount(pkv_allocator_t* a, int32_t block_id, int32_t* refcount);
+int pkv_num_free_blocks(pkv_allocator_t* a, int32_t* num_free);
+
+int pkv_seq_create(pkv_allocator_t* a, int32_t* seq);
+int pkv_seq_fork(pkv_allocator_t* a, int32_t parent, int32_t* child);
+int pkv_seq_free(pkv_allocator_t* a, int32_t seq);
+
+/* Blocks an append of n_tokens would take from the free list (CoW copy included). */
+int pkv_seq_blocks_needed(pkv_allocator_t* a, int32_t seq, int32_t n_tokens, int32_t* needed);
+
+/*
+ * Append n_tokens positions to seq, all or nothing.  slots_out (host int32
+ * [n_tokens], may be NULL when n_tokens == 0) receives each position's slot.
+ * cow_pair_out (host int32 [2]) receives the copy-on-write (src, dst) pair and
+ * *n_cow is set to 0 or 1 (only the first appended position can need a copy).
+ * PKV_ERR_OUT_OF_BLOCKS if the pool cannot serve every block the append needs.
+ */
+int pkv_seq_append(pkv_allocator_t* a, int32_t seq, int32_t n_tokens, int32_t* slots_out,
+                   int32_t* cow_pair_out, int32_t* n_cow);
+
+int pkv_seq_len(pkv_allocator_t* a, int32_t seq, int32_t* len);
+/* Copies up to `capacity` ids of seq's table to ids_out; *n = table length. */
+int pkv_seq_table(pkv_allocator_t* a, int32_t seq, int32_t* ids_out, int32_t capacity, int32_t* n);
+
+/*
+ * Export the tables of `num` sequences as a row-major host int32
+ * [num, max_blocks] array (entries past a table's end are 0) and their lengths
+ * into ctx_out [num].  PKV_ERR_INVALID_ARG if a table is longer than max_blocks.
+ */
+int pkv_export_tables(pkv_allocator_t* a, const int32_t* seqs, int32_t num, int32_t max_blocks,
+                      int32_t* tables_out, int32_t* ctx_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H_ */

@@ -1,0 +1,24 @@
+"""GB300-native paged KV-cache decode path (PagedAttention hot path).
+
+Public API (all device work runs in libpkv.so's sm_103a kernels):
+
+* ``paged_kv_write(k, v, slot_mapping, k_cache, v_cache)``
+* ``paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out)``
+* ``paged_copy_blocks(k_cache, v_cache, src_dst_pairs)``
+* ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free)
+
+The library is loaded on first use; importing this package needs no GPU.
+"""
+from .allocator import BlockAllocator  # noqa: F401
+from ._native import OutOfBlocks, PkvError  # noqa: F401
+
+
+def __getattr__(name):
+    # torch-facing ops are imported lazily so that host-only users (the block
+    # manager, the workload generators) do not need torch's CUDA runtime.
+    if name in ("paged_kv_write", "paged_decode_attention", "paged_copy_blocks",
+                "paged_decode_attention_partition", "paged_decode_attention_reduce",
+                "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
+        from . import ops
+        return getattr(ops, name)
+    raise AttributeError(name)

@@ -1,0 +1,113 @@
+"""Python handle on the library's host block manager (pkv_allocator_* in the C ABI)."""
+from __future__ import annotations
+
+import ctypes
+from typing import List, Optional, Sequence, Tuple
+
+import numpy as np
+
+from . import _native as N
+
+_I32P = ctypes.POINTER(ctypes.c_int32)
+
+
+def _ptr(a: np.ndarray):
+    return a.ctypes.data_as(_I32P)
+
+
+class BlockAllocator:
+    """Free list, refcounts, fork, append with copy-on-write and free over a fixed pool.
+
+    ``pop_order`` fixes which ids the free list hands out first (a permutation of
+    ``range(num_blocks)``; ascending when omitted).
+    """
+
+    def __init__(self, num_blocks: int, block_size: int,
+                 pop_order: Optional[Sequence[int]] = None):
+        self._lib = N.lib()
+        h = ctypes.c_void_p()
+        order = None
+        if pop_order is not None:
+            order = np.ascontiguousarray(np.asarray(pop_order, dtype=np.int32))
+            if order.shape != (num_blocks,):
+                raise ValueError("pop_order must have num_blocks entries")
+        N.check(self._lib.pkv_allocator_create(num_blocks, block_size,
+                                               _ptr(order) if order is not None else None,
+                                               ctypes.byref(h)))
+        self._h = h
+        self.num_blocks = num_blocks
+        self.block_size = block_size
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            self._lib.pkv_allocator_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def _out(self, fn, *args) -> int:
+        v = ctypes.c_int32(0)
+        N.check(fn(self._h, *args, ctypes.byref(v)))
+        return v.value
+
+    # blocks
+    def alloc(self) -> int:
+        return self._out(self._lib.pkv_block_alloc)
+
+    def incref(self, b: int) -> None:
+        N.check(self._lib.pkv_block_incref(self._h, b))
+
+    def decref(self, b: int) -> None:
+        N.check(self._lib.pkv_block_decref(self._h, b))
+
+    def refcount(self, b: int) -> int:
+        return self._out(self._lib.pkv_block_refcount, b)
+
+    def num_free(self) -> int:
+        return self._out(self._lib.pkv_num_free_blocks)
+
+    # sequences
+    def create(self) -> int:
+        return self._out(self._lib.pkv_seq_create)
+
+    def fork(self, parent: int) -> int:
+        return self._out(self._lib.pkv_seq_fork, parent)
+
+    def free(self, seq: int) -> None:
+        N.check(self._lib.pkv_seq_free(self._h, seq))
+
+    def blocks_needed(self, seq: int, n: int) -> int:
+        return self._out(self._lib.pkv_seq_blocks_needed, seq, n)
+
+    def append(self, seq: int, n: int) -> Tuple[np.ndarray, List[Tuple[int, int]]]:
+        """Append n tokens; returns (slots int32 [n], [(src, dst)] copy-on-write pairs)."""
+        slots = np.empty(max(n, 1), dtype=np.int32)
+        pair = np.zeros(2, dtype=np.int32)
+        ncow = ctypes.c_int32(0)
+        N.check(self._lib.pkv_seq_append(self._h, seq, n, _ptr(slots), _ptr(pair),
+                                         ctypes.byref(ncow)))
+        cows = [(int(pair[0]), int(pair[1]))] if ncow.value else []
+        return slots[:n], cows
+
+    def length(self, seq: int) -> int:
+        return self._out(self._lib.pkv_seq_len, seq)
+
+    def table(self, seq: int) -> List[int]:
+        n = ctypes.c_int32(0)
+        N.check(self._lib.pkv_seq_table(self._h, seq, None, 0, ctypes.byref(n)))
+        buf = np.empty(max(n.value, 1), dtype=np.int32)
+        N.check(self._lib.pkv_seq_table(self._h, seq, _ptr(buf), n.value, ctypes.byref(n)))
+        return buf[:n.value].tolist()
+
+    def export_tables(self, seqs: Sequence[int], max_blocks: int):
+        """Row-padded int32 [len(seqs), max_blocks] table (padding 0) and int32 lengths."""
+        s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        tab = np.zeros((len(s), max_blocks), dtype=np.int32)
+        ctx = np.zeros(len(s), dtype=np.int32)
+        N.check(self._lib.pkv_export_tables(self._h, _ptr(s), len(s), max_blocks, _ptr(tab),
+                                            _ptr(ctx)))
+        return tab, ctx

@@ -1,0 +1,100 @@
+// Library-wide host plumbing: error messages, version, device queries and the
+// TMA tensor-map encoder (reached through the runtime's driver entry point, so
+// the library links no driver stub and loads on machines without a GPU).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_runtime.h>
+
+#include <cstdarg>
+#include <cstdio>
+#include <mutex>
+
+#include "internal.h"
+
+namespace pkv {
+namespace {
+thread_local char g_message[512] = {0};
+}
+
+int fail(int code, const char* fmt, ...) {
+  va_list ap;
+  va_start(ap, fmt);
+  vsnprintf(g_message, sizeof(g_message), fmt, ap);
+  va_end(ap);
+  return code;
+}
+
+int ok() {
+  g_message[0] = 0;
+  return PKV_OK;
+}
+
+int cuda_fail(cudaError_t e, const char* what) {
+  return fail(PKV_ERR_CUDA, "%s failed: %s (%s)", what, cudaGetErrorName(e),
+              cudaGetErrorString(e));
+}
+
+int device_sm_count(int* sms, int* device) {
+  static std::once_flag flags[64];
+  static int counts[64];
+  int dev = 0;
+  PKV_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::call_once(flags[dev], [&] {
+    int n = 0;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) n = 0;
+    counts[dev] = n;
+  });
+  if (counts[dev] <= 0) return fail(PKV_ERR_CUDA, "could not query the SM count of device %d", dev);
+  *sms = counts[dev];
+  *device = dev;
+  return PKV_OK;
+}
+
+namespace {
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static std::once_flag flag;
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  std::call_once(flag, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+}  // namespace
+
+int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t rows,
+                     int32_t head_dim, int32_t box_cols) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  CUtensorMapDataType dt;
+  switch (dtype) {
+    case PKV_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
+    case PKV_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
+    case PKV_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
+    default: return fail(PKV_ERR_DTYPE, "unknown dtype %d", dtype);
+  }
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * element_bytes(dtype)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 16u};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKV_OK;
+}
+
+}  // namespace pkv
+
+extern "C" {
+
+const char* pkv_last_error_string(void) { return pkv::g_message; }
+
+int pkv_version(void) { return 100; }
+
+}  // extern "C"

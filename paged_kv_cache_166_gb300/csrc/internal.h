@@ -1,0 +1,44 @@
+// Host-side helpers shared by the library's CUDA translation units.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "pkv.h"
+#include "status.h"
+
+namespace pkv {
+
+inline int element_bytes(int32_t dtype) {
+  switch (dtype) {
+    case PKV_F32: return 4;
+    case PKV_F16: return 2;
+    case PKV_BF16: return 2;
+    default: return 0;
+  }
+}
+
+// Records a failed CUDA call and returns PKV_ERR_CUDA.
+int cuda_fail(cudaError_t e, const char* what);
+
+#define PKV_CUDA(call)                                      \
+  do {                                                      \
+    cudaError_t e_ = (call);                                \
+    if (e_ != cudaSuccess) return ::pkv::cuda_fail(e_, #call); \
+  } while (0)
+
+// Number of SMs of the current device (cached per device).
+int device_sm_count(int* sms, int* device);
+
+// Encodes a 2-D TMA map over a cache viewed as [rows, head_dim] with rows of
+// head_dim elements, boxes of [16 rows x box_cols elements], 128-byte swizzle.
+int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t rows,
+                     int32_t head_dim, int32_t box_cols);
+
+inline bool aligned(const void* p, uintptr_t a) {
+  return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
+}
+
+}  // namespace pkv

@@ -1,0 +1,122 @@
+// Cache write (scatter of new tokens into their slots) and whole-block copy for
+// copy-on-write.  Both are pure data movement in 16-byte vectors: each thread
+// moves one 16-byte piece of one row, so a warp covers contiguous bytes of a
+// [head_dim] row on both sides.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#include "internal.h"
+
+namespace pkv {
+namespace {
+
+// For token t, KV head h, vector c of the row:
+//   cache[slot / B, h, slot % B, c] = src[t, h, c]   (slot = slot_mapping[t] >= 0).
+// The cache-write step of "PagedAttention and vLLM: Virtual Memory for the KV
+// Cache", section "L2 — Mechanism" (allocation lifecycle), with the slot formula of
+// "What is paged attention?", section "How it works".
+__global__ void kv_write_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                const int32_t* __restrict__ slots, int64_t total_vecs,
+                                int32_t Hkv, int32_t B, int32_t row_vecs, int64_t num_slots,
+                                uint4* __restrict__ kc, uint4* __restrict__ vc) {
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs;
+       i += stride) {
+    const int64_t th = i / row_vecs;
+    const int32_t c = static_cast<int32_t>(i - th * row_vecs);
+    const int64_t t = th / Hkv;
+    const int32_t h = static_cast<int32_t>(th - t * Hkv);
+    const int32_t slot = __ldg(slots + t);
+    if (slot < 0 || slot >= num_slots) continue;
+    const int64_t dst = ((static_cast<int64_t>(slot / B) * Hkv + h) * B + slot % B) * row_vecs + c;
+    kc[dst] = __ldg(k + i);
+    vc[dst] = __ldg(v + i);
+  }
+}
+
+// For pair p: block dst = pairs[2p+1] becomes a copy of block src = pairs[2p]
+// ("allocates a new physical block, copies the content", "PagedAttention: How
+// vLLM Borrowed Virtual Memory...", section "Copy-on-Write for Beam Search and
+// Parallel Sampling").
+__global__ void copy_blocks_kernel(uint4* __restrict__ kc, uint4* __restrict__ vc,
+                                   const int32_t* __restrict__ pairs, int32_t n, int32_t NB,
+                                   int64_t block_vecs) {
+  const int64_t total = static_cast<int64_t>(n) * block_vecs;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t p = i / block_vecs;
+    const int64_t c = i - p * block_vecs;
+    const int32_t src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
+    if (src < 0 || src >= NB || dst < 0 || dst >= NB) continue;
+    kc[dst * block_vecs + c] = kc[src * block_vecs + c];
+    vc[dst * block_vecs + c] = vc[src * block_vecs + c];
+  }
+}
+
+int grid_for(int64_t work, int threads) {
+  int sms = 0, dev = 0;
+  if (device_sm_count(&sms, &dev) != PKV_OK) sms = 132;
+  const int64_t want = (work + threads - 1) / threads;
+  const int64_t cap = static_cast<int64_t>(sms) * 16;
+  return static_cast<int>(want < cap ? (want > 0 ? want : 1) : cap);
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" {
+
+int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int32_t num_tokens,
+                 void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                 int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
+  const int elt = element_bytes(dtype);
+  PKV_REQUIRE(elt != 0, PKV_ERR_DTYPE, "unknown dtype %d", dtype);
+  PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && num_kv_heads > 0 && block_size > 0 &&
+                  head_dim > 0,
+              PKV_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0)");
+  PKV_REQUIRE((static_cast<int64_t>(head_dim) * elt) % 16 == 0, PKV_ERR_INVALID_ARG,
+              "head_dim * element size must be a multiple of 16 bytes");
+  PKV_REQUIRE(static_cast<int64_t>(num_blocks) * block_size < (int64_t(1) << 31),
+              PKV_ERR_INVALID_ARG, "num_blocks * block_size must be < 2^31");
+  if (num_tokens == 0) return ok();
+  PKV_REQUIRE(k && v && slot_mapping && k_cache && v_cache, PKV_ERR_INVALID_ARG, "NULL pointer");
+  PKV_REQUIRE(aligned(k, 16) && aligned(v, 16) && aligned(k_cache, 16) && aligned(v_cache, 16),
+              PKV_ERR_INVALID_ARG, "k, v and caches must be 16-byte aligned");
+  const int32_t row_vecs = static_cast<int32_t>(static_cast<int64_t>(head_dim) * elt / 16);
+  const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * row_vecs;
+  const int threads = 256;
+  kv_write_kernel<<<grid_for(total, threads), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k), static_cast<const uint4*>(v), slot_mapping, total,
+      num_kv_heads, block_size, row_vecs, static_cast<int64_t>(num_blocks) * block_size,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
+  PKV_CUDA(cudaGetLastError());
+  return ok();
+}
+
+int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int32_t num_pairs,
+                    int32_t num_blocks, int64_t block_elems, int32_t dtype, void* stream) {
+  const int elt = element_bytes(dtype);
+  PKV_REQUIRE(elt != 0, PKV_ERR_DTYPE, "unknown dtype %d", dtype);
+  PKV_REQUIRE(num_pairs >= 0 && num_blocks > 0 && block_elems > 0, PKV_ERR_INVALID_ARG,
+              "bad sizes");
+  PKV_REQUIRE((block_elems * elt) % 16 == 0, PKV_ERR_INVALID_ARG,
+              "block_elems * element size must be a multiple of 16 bytes");
+  if (num_pairs == 0) return ok();
+  PKV_REQUIRE(k_cache && v_cache && src_dst_pairs, PKV_ERR_INVALID_ARG, "NULL pointer");
+  PKV_REQUIRE(aligned(k_cache, 16) && aligned(v_cache, 16), PKV_ERR_INVALID_ARG,
+              "caches must be 16-byte aligned");
+  const int64_t block_vecs = block_elems * elt / 16;
+  const int threads = 256;
+  copy_blocks_kernel<<<grid_for(num_pairs * block_vecs, threads), threads, 0,
+                       static_cast<cudaStream_t>(stream)>>>(
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src_dst_pairs, num_pairs,
+      num_blocks, block_vecs);
+  PKV_CUDA(cudaGetLastError());
+  return ok();
+}
+
+}  // extern "C"

@@ -1,0 +1,170 @@
+"""Torch-facing binding of the paged decode path: argument marshalling only.
+
+Every function checks shapes, dtypes and devices, then calls the C ABI of
+libpkv.so with raw device pointers and torch's current CUDA stream.  All the
+work happens in the library's kernels; nothing here computes attention.
+"""
+from __future__ import annotations
+
+import ctypes
+from typing import Optional
+
+import torch
+
+from . import _native as N
+
+_DTYPES = {torch.float32: N.PKV_F32, torch.float16: N.PKV_F16, torch.bfloat16: N.PKV_BF16}
+_WORKSPACES: dict = {}
+
+
+def dtype_code(t: torch.Tensor) -> int:
+    try:
+        return _DTYPES[t.dtype]
+    except KeyError:
+        raise TypeError(f"unsupported dtype {t.dtype}") from None
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def _check_cuda(*ts) -> torch.device:
+    dev = ts[0].device
+    for t in ts:
+        if not t.is_cuda:
+            raise ValueError("tensors must be CUDA tensors")
+        if t.device != dev:
+            raise ValueError("tensors must be on one device")
+        if not t.is_contiguous():
+            raise ValueError("tensors must be contiguous")
+    return dev
+
+
+def _check_index(t: torch.Tensor, name: str) -> None:
+    if t.dtype != torch.int32:
+        raise TypeError(f"{name} must be int32")
+
+
+def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                   k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """Scatter k, v [T, Hkv, D] into k_cache, v_cache [NB, Hkv, B, D] at slot_mapping [T]."""
+    dev = _check_cuda(k, v, slot_mapping, k_cache, v_cache)
+    _check_index(slot_mapping, "slot_mapping")
+    if k.shape != v.shape or k_cache.shape != v_cache.shape or k.dim() != 3 or k_cache.dim() != 4:
+        raise ValueError("expected k, v [T, Hkv, D] and caches [NB, Hkv, B, D]")
+    T, Hkv, D = k.shape
+    NB, Hkv2, B, D2 = k_cache.shape
+    if (Hkv, D) != (Hkv2, D2) or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch between tokens, slots and caches")
+    if not (k.dtype == v.dtype == k_cache.dtype == v_cache.dtype):
+        raise TypeError("k, v and caches must share a dtype")
+    N.check(N.lib().pkv_kv_write(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                                 k_cache.data_ptr(), v_cache.data_ptr(), NB, Hkv, B, D,
+                                 dtype_code(k), _stream(dev)))
+
+
+def default_num_warps(head_dim: int, dtype: torch.dtype) -> int:
+    n = ctypes.c_int32(0)
+    N.check(N.lib().pkv_decode_default_warps(head_dim, _DTYPES[dtype], ctypes.byref(n)))
+    return n.value
+
+
+def workspace_bytes(num_q_heads: int, num_kv_heads: int, head_dim: int, dtype: torch.dtype,
+                    num_warps: int = 0) -> int:
+    n = ctypes.c_size_t(0)
+    N.check(N.lib().pkv_decode_workspace_size(num_q_heads, num_kv_heads, head_dim,
+                                              _DTYPES[dtype], num_warps, ctypes.byref(n)))
+    return n.value
+
+
+def get_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
+    """A zero-filled device workspace of at least ``nbytes``, cached per device and
+    stream (one workspace must not serve two launches that may overlap)."""
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+    ws = _WORKSPACES.get(key)
+    if ws is None or ws.numel() < nbytes:
+        ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = ws
+    return ws
+
+
+def _decode_shapes(q, k_cache, v_cache, block_tables, context_lens, out):
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape:
+        raise ValueError("expected q [S, Hq, D] and caches [NB, Hkv, B, D]")
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    if D2 != D or out.shape != q.shape:
+        raise ValueError("head_dim mismatch or out shape != q shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks] and context_lens [S]")
+    if not (q.dtype == k_cache.dtype == v_cache.dtype == out.dtype):
+        raise TypeError("q, caches and out must share a dtype")
+    _check_index(block_tables, "block_tables")
+    _check_index(context_lens, "context_lens")
+    return S, Hq, D, NB, Hkv, B, block_tables.shape[1]
+
+
+def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                           block_tables: torch.Tensor, context_lens: torch.Tensor, scale: float,
+                           out: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                           num_warps: int = 0) -> torch.Tensor:
+    """Decode attention of q [S, Hq, D] over the paged caches; writes and returns out."""
+    dev = _check_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
+    S, Hq, D, NB, Hkv, B, MAXB = _decode_shapes(q, k_cache, v_cache, block_tables,
+                                                context_lens, out)
+    need = workspace_bytes(Hq, Hkv, D, q.dtype, num_warps)
+    ws = get_workspace(dev, need) if workspace is None else workspace
+    if ws.numel() * ws.element_size() < need:
+        raise ValueError(f"workspace smaller than the {need} bytes needed")
+    N.check(N.lib().pkv_decode_attention(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), MAXB,
+        context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), out.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), num_warps, dtype_code(q), _stream(dev)))
+    return out
+
+
+def paged_decode_attention_partition(q, k_cache, v_cache, block_tables, context_lens, scale, out,
+                                     workspace, num_warps: int = 0) -> None:
+    """First launch of paged_decode_attention (per-warp runs + partial states)."""
+    dev = _check_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
+    S, Hq, D, NB, Hkv, B, MAXB = _decode_shapes(q, k_cache, v_cache, block_tables,
+                                                context_lens, out)
+    N.check(N.lib().pkv_decode_attention_partition(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), MAXB,
+        context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), out.data_ptr(),
+        workspace.data_ptr(), workspace.numel() * workspace.element_size(), num_warps,
+        dtype_code(q), _stream(dev)))
+
+
+def paged_decode_attention_reduce(context_lens, max_blocks_per_seq: int, num_kv_heads: int,
+                                  block_size: int, out, workspace, num_warps: int = 0) -> None:
+    """Second launch of paged_decode_attention (log-sum-exp merge of split contexts)."""
+    dev = _check_cuda(context_lens, out, workspace)
+    S, Hq, D = out.shape
+    N.check(N.lib().pkv_decode_attention_reduce(
+        context_lens.data_ptr(), max_blocks_per_seq, S, Hq, num_kv_heads, D, block_size,
+        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
+        num_warps, dtype_code(out), _stream(dev)))
+
+
+def decode_status(workspace: torch.Tensor) -> int:
+    """Reads and clears the device status bits the decode kernels recorded."""
+    v = ctypes.c_int32(0)
+    N.check(N.lib().pkv_decode_status(workspace.data_ptr(), ctypes.byref(v),
+                                      _stream(workspace.device)))
+    return v.value
+
+
+def paged_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
+                      src_dst_pairs: torch.Tensor) -> None:
+    """Copy whole blocks src -> dst (pairs [n, 2] int32 on the caches' device)."""
+    dev = _check_cuda(k_cache, v_cache, src_dst_pairs)
+    _check_index(src_dst_pairs, "src_dst_pairs")
+    n = src_dst_pairs.numel() // 2
+    if src_dst_pairs.numel() != 2 * n:
+        raise ValueError("src_dst_pairs must hold pairs")
+    NB = k_cache.shape[0]
+    block_elems = k_cache[0].numel()
+    N.check(N.lib().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
+                                    src_dst_pairs.data_ptr(), n, NB, block_elems,
+                                    dtype_code(k_cache), _stream(dev)))

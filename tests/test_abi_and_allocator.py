@@ -1,0 +1,213 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+* libpkv.so loads without a GPU and exports every function include/pkv.h declares,
+  each with a ctypes signature in the binding.
+* The library's block manager matches the oracle model bit for bit — tables,
+  lengths, slots, copy-on-write pairs, refcounts and free counts after every
+  operation — on the pages' worked examples and on seeded random operation
+  sequences; failing calls leave both unchanged.
+"""
+import os
+import re
+
+import numpy as np
+import pytest
+
+from conftest import ROOT
+from oracle.block_manager import BlockManager, InvalidOperation, OutOfBlocks as OracleOOB
+
+pkv = pytest.importorskip("paged_kv_cache_166_gb300")
+from paged_kv_cache_166_gb300 import _native as N  # noqa: E402
+from paged_kv_cache_166_gb300 import BlockAllocator  # noqa: E402
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def header_functions():
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(pkv_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_library_exports_every_declared_function():
+    names = header_functions()
+    assert len(names) >= 20
+    lib = N.lib()
+    for name in names:
+        assert hasattr(lib, name), name
+        assert name in N.SIGNATURES, f"no binding signature for {name}"
+    assert set(N.SIGNATURES) == set(names)
+    assert lib.pkv_version() >= 100
+
+
+def test_error_codes_and_messages_without_gpu():
+    lib = N.lib()
+    import ctypes
+    n = ctypes.c_size_t()
+    assert lib.pkv_decode_workspace_size(6, 4, 128, N.PKV_BF16, 8, ctypes.byref(n)) == N.PKV_ERR_INVALID_ARG
+    assert b"head counts" in lib.pkv_last_error_string()
+    assert lib.pkv_decode_workspace_size(8, 1, 128, 9, 8, ctypes.byref(n)) == N.PKV_ERR_DTYPE
+    assert lib.pkv_decode_workspace_size(8, 1, 96, N.PKV_BF16, 8, ctypes.byref(n)) == N.PKV_ERR_UNSUPPORTED
+    assert lib.pkv_decode_workspace_size(8, 1, 128, N.PKV_BF16, 8, ctypes.byref(n)) == N.PKV_OK
+    assert n.value == 256 + 2 * 8 * 8 * 2 * 4 + 2 * 8 * 8 * 128 * 4
+    assert lib.pkv_kv_write(None, None, None, 0, None, None, 4, 2, 16, 100, N.PKV_F16, None) == N.PKV_ERR_INVALID_ARG
+
+
+class Pair:
+    """Drives the library's block manager and the oracle model with the same operations."""
+
+    def __init__(self, nb, bs, order=None):
+        self.c = BlockAllocator(nb, bs, order)
+        self.o = BlockManager(nb, bs, order)
+        self.nb = nb
+
+    def compare(self):
+        for b in range(self.nb):
+            assert self.c.refcount(b) == self.o.refcount[b]
+        assert self.c.num_free() == self.o.num_free()
+        for sid in self.o.tables:
+            assert self.c.table(sid) == self.o.tables[sid]
+            assert self.c.length(sid) == self.o.lengths[sid]
+
+    def create(self):
+        a, b = self.c.create(), self.o.create()
+        assert a == b
+        return a
+
+    def fork(self, p):
+        a, b = self.c.fork(p), self.o.fork(p)
+        assert a == b
+        return a
+
+    def free(self, s):
+        self.c.free(s)
+        self.o.free(s)
+
+    def append(self, s, n):
+        need = self.o.blocks_needed(s, n)
+        assert self.c.blocks_needed(s, n) == need
+        try:
+            so, co = self.o.append(s, n)
+        except OracleOOB:
+            with pytest.raises(N.OutOfBlocks):
+                self.c.append(s, n)
+            return None
+        sc, cc = self.c.append(s, n)
+        assert list(sc) == so
+        assert cc == co
+        return so, co
+
+
+def test_worked_example_matches_oracle(golden):
+    from test_oracle_block_manager import run_script
+    run_script(golden("worked_example_b4.txt"), BlockAllocatorView)
+
+
+class BlockAllocatorView:
+    """Adapter exposing the oracle's attribute view on top of the library handle."""
+
+    def __init__(self, nb, bs):
+        self.a = BlockAllocator(nb, bs)
+        self.nb = nb
+        self.live = set()
+
+    def create(self):
+        s = self.a.create(); self.live.add(s); return s
+
+    def fork(self, p):
+        s = self.a.fork(p); self.live.add(s); return s
+
+    def free(self, s):
+        self.a.free(s); self.live.discard(s)
+
+    def append(self, s, n):
+        slots, cows = self.a.append(s, n)
+        return list(slots), cows
+
+    def num_free(self):
+        return self.a.num_free()
+
+    @property
+    def tables(self):
+        return {s: self.a.table(s) for s in self.live}
+
+    @property
+    def refcount(self):
+        return [self.a.refcount(b) for b in range(self.nb)]
+
+
+def test_eight_requests_and_parallel_sampling_match_oracle():
+    p = Pair(3072, 16)
+    for length in (180, 220, 260, 310, 400, 520, 1400, 1900):
+        s = p.create()
+        p.append(s, length)
+    p.compare()
+    assert p.c.num_free() == 2744
+    q = Pair(1000, 16)
+    parent = q.create()
+    q.append(parent, 1000)
+    kids = [q.fork(parent) for _ in range(3)]
+    for s in [parent] + kids:
+        q.append(s, 200)
+    q.compare()
+    assert 1000 - q.c.num_free() == 114
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_operations_bit_exact(seed):
+    r = np.random.default_rng(seed)
+    B = int(r.choice([1, 2, 4, 16]))
+    NB = int(r.integers(8, 96))
+    p = Pair(NB, B, r.permutation(NB).astype(np.int32))
+    live = []
+    for _ in range(500):
+        op = r.integers(0, 10)
+        if op < 2 or not live:
+            live.append(p.create())
+        elif op < 7:
+            p.append(live[r.integers(len(live))], int(r.integers(0, 3 * B + 2)))
+        elif op < 8:
+            live.append(p.fork(live[r.integers(len(live))]))
+        else:
+            p.free(live.pop(r.integers(len(live))))
+        p.compare()
+
+
+def test_export_tables_matches_oracle():
+    p = Pair(64, 4, np.random.default_rng(3).permutation(64).astype(np.int32))
+    seqs = [p.create() for _ in range(5)]
+    for i, s in enumerate(seqs):
+        p.append(s, 3 * i + 1)
+    kid = p.fork(seqs[3])
+    p.append(kid, 2)
+    order = [kid, seqs[0], seqs[4]]
+    tc, cc = p.c.export_tables(order, 6)
+    to, co = p.o.export_tables(order, 6)
+    assert np.array_equal(tc, to) and np.array_equal(cc, co)
+    with pytest.raises(N.PkvError):
+        p.c.export_tables(order, 2)
+
+
+def test_library_rejects_bad_operations_without_state_change():
+    a = BlockAllocator(4, 4)
+    s = a.create()
+    a.append(s, 16)
+    with pytest.raises(N.OutOfBlocks):
+        a.append(s, 1)
+    assert a.length(s) == 16 and a.num_free() == 0
+    with pytest.raises(N.PkvError):
+        a.decref(99)
+    with pytest.raises(N.PkvError):
+        a.free(7)
+    with pytest.raises(N.PkvError):
+        BlockAllocator(4, 4, pop_order=[0, 1, 1, 2])
+    a.free(s)
+    assert a.num_free() == 4
+    with pytest.raises(N.PkvError):
+        a.free(s)
+    with pytest.raises(N.PkvError):
+        a.incref(0)

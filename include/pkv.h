@@ -193,6 +193,46 @@ int pkv_decode_status(void* workspace, int32_t* status, void* stream);
 /* Number of worker warps the default launch uses on the current device. */
 int pkv_decode_default_warps(int32_t head_dim, int32_t dtype, int32_t* num_warps);
 
+/*
+ * pkv_decode_attention_static_scratch — pkv_decode_attention for callers that
+ * cannot allocate device memory.  (The pages have no counterpart: this is a
+ * deployment variant of the same computation.)
+ *
+ * Some callers cannot hand the library a workspace: serving engines that give
+ * every byte of HBM to the KV block pool at start-up and forbid allocations
+ * afterwards, plugins running inside a host framework that owns all device
+ * memory, and latency-critical decode loops where cudaMalloc's implicit device
+ * synchronisation is not acceptable.  This entry point takes the same arguments
+ * as pkv_decode_attention minus the workspace, and keeps the split-context
+ * partial states in a fixed scratch array of PKV_STATIC_SCRATCH_BYTES that is
+ * part of the library's device image: every GPU that loads the library holds
+ * that memory until the process exits.  The call itself allocates nothing (no
+ * cudaMalloc, no cudaFree, no allocating library routine).
+ *
+ * The first call on a device resolves the array's device address for that
+ * device (cudaGetSymbolAddress) and sets the kernels' shared-memory limit; make
+ * that first call before any stream capture.  The scratch status word is
+ * cleared at the start of each call; device-side status bits are not reported
+ * by this entry point (use pkv_decode_attention with a workspace and
+ * pkv_decode_status to read them).
+ *
+ * All calls on a device share the one array, which keeps the last call's
+ * contents.  Calls that may overlap on the GPU (on different streams, or from
+ * different host threads without ordering) race on it and give wrong results:
+ * order them on one stream.  A request whose partial states need more than
+ * PKV_STATIC_SCRATCH_BYTES (pkv_decode_workspace_size with the same head shape,
+ * dtype and num_warps) is rejected with PKV_ERR_UNSUPPORTED before any work is
+ * enqueued; a smaller num_warps needs less scratch.
+ */
+#define PKV_STATIC_SCRATCH_BYTES (16u << 20)
+int pkv_decode_attention_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                        const int32_t* context_lens, int32_t num_seqs,
+                                        int32_t num_q_heads, int32_t num_kv_heads,
+                                        int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                                        float scale, void* out, int32_t num_warps, int32_t dtype,
+                                        void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Copy-on-write block copy                                                   */
 /* ------------------------------------------------------------------------- */

@@ -25,6 +25,8 @@ PKV_DEV_BAD_CONTEXT_LEN = 1
 PKV_DEV_BAD_BLOCK_ID = 2
 PKV_DEV_WAIT_TIMEOUT = 4
 
+PKV_STATIC_SCRATCH_BYTES = 16 << 20
+
 _i32 = ctypes.c_int32
 _i64 = ctypes.c_int64
 _p = ctypes.c_void_p
@@ -46,6 +48,9 @@ SIGNATURES = {
                                                    _sz, _i32, _i32, _p]),
     "pkv_decode_status": (ctypes.c_int, [_p, _pi32, _p]),
     "pkv_decode_default_warps": (ctypes.c_int, [_i32, _i32, _pi32]),
+    "pkv_decode_attention_static_scratch": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _i32, _i32,
+                                                           _i32, _i32, _i32, _i32, _f, _p, _i32,
+                                                           _i32, _p]),
     "pkv_copy_blocks": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i64, _i32, _p]),
     "pkv_allocator_create": (ctypes.c_int, [_i32, _i32, _pi32, ctypes.POINTER(_p)]),
     "pkv_allocator_destroy": (ctypes.c_int, [_p]),

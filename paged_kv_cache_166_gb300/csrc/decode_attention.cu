@@ -1022,3 +1022,70 @@ int pkv_decode_status(void* workspace, int32_t* status, void* stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------------
+// Entry point for callers that cannot allocate device memory: the partial states
+// live in a fixed array of the library's device image instead of a caller
+// workspace.  The host only ever passes the array's device address, resolved per
+// device with cudaGetSymbolAddress; the array's name in host code is a host-side
+// stand-in and is never handed to a kernel.
+// ---------------------------------------------------------------------------------
+namespace pkv {
+namespace {
+
+static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
+
+// Device address of g_static_scratch for the current device, resolved once per
+// device with that device current.
+int static_scratch_address(void** ptr) {
+  static std::once_flag flags[64];
+  static void* addrs[64];
+  static cudaError_t errs[64];
+  int dev = 0;
+  PKV_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::call_once(flags[dev], [&] {
+    void* p = nullptr;
+    errs[dev] = cudaGetSymbolAddress(&p, g_static_scratch);
+    addrs[dev] = p;
+  });
+  if (errs[dev] != cudaSuccess) return cuda_fail(errs[dev], "cudaGetSymbolAddress(static scratch)");
+  *ptr = addrs[dev];
+  return PKV_OK;
+}
+
+}  // namespace
+}  // namespace pkv
+
+extern "C" int pkv_decode_attention_static_scratch(
+    const void* q, const void* k_cache, const void* v_cache, const int32_t* block_tables,
+    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+    int32_t num_blocks, float scale, void* out, int32_t num_warps, int32_t dtype, void* stream) {
+  PKV_REQUIRE(element_bytes(dtype) != 0, PKV_ERR_DTYPE, "unknown dtype %d", dtype);
+  PKV_REQUIRE(num_q_heads > 0 && num_kv_heads > 0 && num_q_heads % num_kv_heads == 0,
+              PKV_ERR_INVALID_ARG, "bad head counts %d / %d", num_q_heads, num_kv_heads);
+  PKV_REQUIRE(supported_head_dim(dtype, head_dim), PKV_ERR_UNSUPPORTED,
+              "head_dim %d unsupported for dtype %d", head_dim, dtype);
+  PKV_REQUIRE(num_warps >= 0, PKV_ERR_INVALID_ARG, "negative num_warps");
+  int W = num_warps;
+  if (W == 0) {
+    W = default_warps(dtype, head_dim);
+    if (W < 0) return W;
+  }
+  const size_t need = workspace_bytes_for(num_q_heads / num_kv_heads, head_dim, W);
+  PKV_REQUIRE(need <= PKV_STATIC_SCRATCH_BYTES, PKV_ERR_UNSUPPORTED,
+              "this launch needs %zu bytes of scratch but the static scratch holds %u bytes; "
+              "pass a smaller num_warps or use pkv_decode_attention with a workspace",
+              need, PKV_STATIC_SCRATCH_BYTES);
+  void* scratch = nullptr;
+  int rc = static_scratch_address(&scratch);
+  if (rc != PKV_OK) return rc;
+  // The status word is the only part of the scratch that must start at zero.
+  if (num_seqs > 0)
+    PKV_CUDA(cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+  return pkv_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                              num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
+                              num_blocks, scale, out, scratch, PKV_STATIC_SCRATCH_BYTES, W, dtype,
+                              stream);
+}

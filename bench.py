@@ -2,8 +2,8 @@
 
 A step is one pass of the whole hot path over one batch: the cache write of
 every sequence's new token (slots from the library's block manager), then paged
-decode attention (partition launch + log-sum-exp reduce launch) over all cached
-tokens, new token included.
+decode attention over all cached tokens, new token included (one launch; split
+contexts are merged inside it).
 
 Default workload: the 13B-shaped MHA decode batch (64 sequences, 40 query = 40
 KV heads, head_dim 128, fp16, block size 16, lognormal lengths with median 300
@@ -14,8 +14,9 @@ value     = algorithmic KV-read bytes of decode attention / device step time
 e2e       = the same bytes / end-to-end step time through the public API with
             pinned host buffers: H2D of q, new K/V, slots, tables and lengths,
             the library calls, D2H of the output.
-roofline  = the partition kernel alone: its algorithmic bytes / its event time,
-            against the measured HBM copy bandwidth.
+roofline  = the decode-attention kernel alone (timed in its own loop, L2 flushed):
+            its algorithmic bytes / its event time, against the measured HBM
+            copy bandwidth.
 cpu_baseline / --impl reference = the fp64 oracle on the host cores.
 
 Under torchrun with N ranks each rank runs an independent replica of the
@@ -301,13 +302,10 @@ def native(args):
 
     def step():
         pkv.paged_kv_write(dev["k_new"], dev["v_new"], dev["slots"], kc, vc)
-        e1.record(stream)
-        pkv.paged_decode_attention_partition(dev["q"], kc, vc, dev["tables"], dev["ctx"],
-                                             w.scale, out, ws, args.num_warps)
-        e2.record(stream)
-        pkv.paged_decode_attention_reduce(dev["ctx"], MAXB, Hkv, B, out, ws, args.num_warps)
+        pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws,
+                                   args.num_warps)
 
-    e0, e1, e2, e3 = (torch.cuda.Event(enable_timing=True) for _ in range(4))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
         flush.zero_()
         step()
@@ -315,7 +313,7 @@ def native(args):
     if pkv.decode_status(ws) != 0:
         raise RuntimeError("device status reported an error during warm-up")
 
-    step_ms, part_ms = [], []
+    step_ms = []
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
@@ -325,15 +323,26 @@ def native(args):
             flush.zero_()              # L2 flush, outside the timed events
             e0.record(stream)
             step()
-            e3.record(stream)
-            e3.synchronize()
-            step_ms.append(e0.elapsed_time(e3))
-            part_ms.append(e1.elapsed_time(e2))
+            e1.record(stream)
+            e1.synchronize()
+            step_ms.append(e0.elapsed_time(e1))
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
     if world > 1:
         dist.barrier()
     ms = float(np.mean(step_ms))
+
+    # the dominant kernel alone (decode attention, one launch), for the roofline
+    part_ms = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0.record(stream)
+        pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws,
+                                   args.num_warps)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            part_ms.append(e0.elapsed_time(e1))
     pms = float(np.mean(part_ms))
 
     # end to end through the public API with pinned host buffers
@@ -358,9 +367,9 @@ def native(args):
         flush.zero_()
         e0.record(stream)
         e2e_step()
-        e3.record(stream)
-        e3.synchronize()
-        e2e_ms.append(e0.elapsed_time(e3))
+        e1.record(stream)
+        e1.synchronize()
+        e2e_ms.append(e0.elapsed_time(e1))
     e2e = float(np.mean(e2e_ms))
     status = pkv.decode_status(ws)
     if status:
@@ -379,7 +388,7 @@ def native(args):
     total_bytes = attn_bytes * world
     gbs = total_bytes / (ms * 1e-3) / 1e9
     part_gbs = attn_bytes / (pms * 1e-3) / 1e9
-    traffic = profile_traffic(f"decode_partition_{args.workload}")
+    traffic = profile_traffic(f"decode_attention_{args.workload}")
     line = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -398,7 +407,7 @@ def native(args):
                         f"block 16, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks",
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
             "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
-            "step": "paged_kv_write (1 new token/seq) + decode attention (partition + reduce)",
+            "step": "paged_kv_write (1 new token/seq) + paged decode attention (one launch)",
             "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
             "num_warps": args.num_warps or pkv.default_num_warps(D, kc.dtype),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -407,18 +416,17 @@ def native(args):
                         "nominal_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
                         "peak_kind": peak_kind},
         "seq_tokens_per_s": round(int(lens.sum()) * world / (ms * 1e-3), 1),
-        "attention_only": {"kv_gbs_partition_kernel": round(part_gbs, 1),
-                           "partition_ms": round(pms, 4)},
+        "attention_only": {"kv_gbs": round(part_gbs, 1), "ms": round(pms, 4)},
         "roofline": {
             "bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(part_gbs / peak, 4), "traffic": traffic,
-            "kernel": "decode_partition_kernel", "bytes_per_launch": attn_bytes,
+            "kernel": "decode_attention_kernel", "bytes_per_launch": attn_bytes,
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         },
         "e2e": {"value": round(total_bytes / (e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
                 "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 3 * args.steps,
+        "gpu_launches": 2 * args.steps,
         "clocks": clocks.summary(),
         "wall_s_timed_loop": round(wall, 3),
     }

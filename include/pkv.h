@@ -58,7 +58,8 @@ enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 };
 enum pkv_device_status {
   PKV_DEV_BAD_CONTEXT_LEN = 1, /* a context length was < 0 or > max_blocks_per_seq * block_size; clamped */
   PKV_DEV_BAD_BLOCK_ID = 2,    /* a block-table entry was outside [0, num_blocks); read as zeros */
-  PKV_DEV_WAIT_TIMEOUT = 4     /* a copy into shared memory did not complete within ~1 s; unit skipped */
+  PKV_DEV_WAIT_TIMEOUT = 4,    /* a copy into shared memory did not complete within ~1 s; unit skipped */
+  PKV_DEV_WORKSPACE_MISMATCH = 8 /* the workspace was last used with another (num_warps, group, head_dim) */
 };
 
 /* Message of the last failure in this thread ("" if none).  Never NULL. */
@@ -102,12 +103,18 @@ int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int3
 /*
  * pkv_decode_workspace_size — bytes of device workspace pkv_decode_attention needs.
  *
- * The workspace holds the per-piece softmax partials of contexts that are split
- * across warps plus a status word.  Its size depends only on the head shape, the
- * dtype and the number of worker warps the launch uses (num_warps; 0 = the
- * default for the current device), never on the context lengths or the batch.
- * Before its first use the workspace must be zero-filled (the status word is
- * sticky: kernels only set bits in it; pkv_decode_status reads and clears it).
+ * The workspace holds a status word, one merge ticket per worker warp and the
+ * per-piece softmax partial states of contexts that are split across warps.  Its
+ * size depends only on the head shape, the dtype and the number of worker warps
+ * the launch uses (num_warps; 0 = the default for the current device), never on
+ * the context lengths or the batch.  A workspace belongs to one layout, i.e. one
+ * (num_q_heads / num_kv_heads, head_dim, num_warps): zero-fill it before its first
+ * use and before using it under another layout (a launch that finds another
+ * layout's leftovers sets PKV_DEV_WORKSPACE_MISMATCH and its output is not to be
+ * trusted).  Every launch leaves the merge tickets at zero again; the status
+ * word is sticky (kernels only set bits in it; pkv_decode_status reads and
+ * clears it).  After a launch that reported PKV_DEV_WAIT_TIMEOUT, zero-fill the
+ * workspace again before reuse.
  * One workspace must not be used by two launches that may run concurrently.
  */
 int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
@@ -127,13 +134,16 @@ int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t
  * t counts the token being decoded, whose K/V must already be in the cache
  * (write with pkv_kv_write first).  t == 0 yields a zero row.
  *
- * Work is split into equal runs of (sequence, KV head, block) steps over all
- * worker warps; a context cut by a run boundary is finished as several partial
- * softmax states merged in fixed order by a log-sum-exp reduce ("two-pass
- * reduction ... numerically stable merge", "PagedAttention: How vLLM Borrowed
- * Virtual Memory...", section "The Custom CUDA Kernel").  Results depend only on
- * the values, context lengths and num_warps — never on which physical blocks
- * hold the data — and are bit-identical between runs.
+ * One kernel launch.  Work is split into equal runs of (sequence, KV head,
+ * block) steps over all worker warps; a context cut by a run boundary is
+ * finished as several partial softmax states, which the last warp to finish a
+ * piece merges in fixed order with a log-sum-exp ("two-pass reduction ...
+ * numerically stable merge", "PagedAttention: How vLLM Borrowed Virtual
+ * Memory...", section "The Custom CUDA Kernel").  Results depend only on the
+ * values, context lengths and num_warps — never on which physical blocks hold
+ * the data — and are bit-identical between runs.  The launch uses programmatic
+ * stream serialisation, so its prologue overlaps a pkv_kv_write queued just
+ * before it on the same stream; every cache read still follows that write.
  *
  * q             device [num_seqs, num_q_heads, head_dim], contiguous.
  * k_cache, v_cache  device caches [num_blocks, num_kv_heads, block_size, head_dim].
@@ -160,28 +170,6 @@ int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                          int32_t num_blocks, float scale, void* out, void* workspace,
                          size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream);
-
-/*
- * The two launches pkv_decode_attention makes, exposed separately so that a caller
- * can time them apart.  pkv_decode_attention_partition runs every worker warp
- * over its run of blocks and writes finished rows of `out` plus the partial
- * states of split contexts into the workspace; pkv_decode_attention_reduce then
- * merges the partial states into `out` and writes the zero rows of empty
- * contexts.  Calling both, in this order on one stream, with identical
- * arguments, is exactly pkv_decode_attention.
- */
-int pkv_decode_attention_partition(const void* q, const void* k_cache, const void* v_cache,
-                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                   const int32_t* context_lens, int32_t num_seqs,
-                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                   int32_t block_size, int32_t num_blocks, float scale, void* out,
-                                   void* workspace, size_t workspace_bytes, int32_t num_warps,
-                                   int32_t dtype, void* stream);
-int pkv_decode_attention_reduce(const int32_t* context_lens, int32_t max_blocks_per_seq,
-                                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                int32_t head_dim, int32_t block_size, void* out, void* workspace,
-                                size_t workspace_bytes, int32_t num_warps, int32_t dtype,
-                                void* stream);
 
 /*
  * pkv_decode_status — read and clear the device status word of a workspace.

@@ -17,7 +17,6 @@ def __getattr__(name):
     # torch-facing ops are imported lazily so that host-only users (the block
     # manager, the workload generators) do not need torch's CUDA runtime.
     if name in ("paged_kv_write", "paged_decode_attention", "paged_copy_blocks",
-                "paged_decode_attention_partition", "paged_decode_attention_reduce",
                 "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
         from . import ops
         return getattr(ops, name)

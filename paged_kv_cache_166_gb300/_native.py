@@ -24,6 +24,7 @@ PKV_F32, PKV_F16, PKV_BF16 = 0, 1, 2
 PKV_DEV_BAD_CONTEXT_LEN = 1
 PKV_DEV_BAD_BLOCK_ID = 2
 PKV_DEV_WAIT_TIMEOUT = 4
+PKV_DEV_WORKSPACE_MISMATCH = 8
 
 PKV_STATIC_SCRATCH_BYTES = 16 << 20
 
@@ -41,11 +42,6 @@ SIGNATURES = {
     "pkv_decode_workspace_size": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "pkv_decode_attention": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
                                             _i32, _f, _p, _p, _sz, _i32, _i32, _p]),
-    "pkv_decode_attention_partition": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32,
-                                                      _i32, _i32, _i32, _f, _p, _p, _sz, _i32,
-                                                      _i32, _p]),
-    "pkv_decode_attention_reduce": (ctypes.c_int, [_p, _i32, _i32, _i32, _i32, _i32, _i32, _p, _p,
-                                                   _sz, _i32, _i32, _p]),
     "pkv_decode_status": (ctypes.c_int, [_p, _pi32, _p]),
     "pkv_decode_default_warps": (ctypes.c_int, [_i32, _i32, _pi32]),
     "pkv_decode_attention_static_scratch": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _i32, _i32,

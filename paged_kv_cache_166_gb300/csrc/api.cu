@@ -68,7 +68,7 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }  // namespace
 
 int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t rows,
-                     int32_t head_dim, int32_t box_cols) {
+                     int32_t cols, int32_t box_cols, int32_t box_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   CUtensorMapDataType dt;
@@ -78,9 +78,9 @@ int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t 
     case PKV_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
     default: return fail(PKV_ERR_DTYPE, "unknown dtype %d", dtype);
   }
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(head_dim), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(head_dim) * element_bytes(dtype)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), 16u};
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * element_bytes(dtype)};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1u, 1u};
   CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

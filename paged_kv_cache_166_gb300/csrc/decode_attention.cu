@@ -20,19 +20,28 @@
 //     bulk-copied alongside the first tile of each (s, g);
 //   * the block-table entries of the run are prefetched 32 at a time into shared
 //     memory with cp.async, a window ahead of the loads that need them;
+//   * the stage of a step is refilled as soon as its arithmetic is done (moving
+//     the tile to registers first and refilling at once measured slower: it only
+//     adds requests to an already saturated memory system);
 //   * the warp keeps an fp32 online-softmax state (running max and sum, rescaled
 //     accumulator) per query head of the group.
-// A (s, g) whose steps lie in one run is finished by that warp; one cut by run
-// boundaries leaves one partial state per piece, and the reduce kernel merges the
-// pieces in logical order with a log-sum-exp ("two-pass reduction ... numerically
-// stable merge", "PagedAttention: How vLLM Borrowed Virtual Memory...", section
-// "The Custom CUDA Kernel").  Cut points depend only on the context lengths and
-// the warp count, so results never depend on physical block ids.
+// A (s, g) whose steps lie in one run is finished by that warp.  One cut by run
+// boundaries leaves one partial state per piece; each piece's warp takes a ticket
+// when its run ends, and the warp holding the last ticket merges the pieces in
+// logical order with a log-sum-exp ("two-pass reduction ... numerically stable
+// merge", "PagedAttention: How vLLM Borrowed Virtual Memory...", section "The
+// Custom CUDA Kernel") — no warp ever waits for another.  Cut points depend only
+// on the context lengths and the warp count, and the merge order is fixed, so
+// results never depend on physical block ids or on which warp merges.
 //
 // fp16/bf16: every query head of the group reuses each gathered tile; scores are
 // S^T[16 tokens x 8 heads] = K[16 x D] Q^T on the tensor cores (m16n8k16, fp32
 // accumulate), P^T is re-laid out in registers with movmatrix, and
 // O^T[D x 8] += V^T P^T on the tensor cores.  fp32: CUDA-core FMA.
+//
+// The kernel is launched with programmatic stream serialisation: its prologue
+// (schedule, block-table prefetch) overlaps the tail of the preceding cache
+// write, and griddepcontrol.wait orders every K/V read after that write.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -47,10 +56,34 @@
 
 namespace pkv {
 
+// Build-time tuning knobs (defaults are the measured best on GB300).
+#ifndef PKV_WARPS_PER_CTA
+#define PKV_WARPS_PER_CTA 4
+#endif
+#ifndef PKV_MAX_STAGES
+#define PKV_MAX_STAGES 8
+#endif
+#ifndef PKV_EARLY_RELEASE
+#define PKV_EARLY_RELEASE 0
+#endif
+// One TMA box per K or V tile (128-byte half-row view) when head_dim * elt <= 256 B.
+#ifndef PKV_SINGLE_BOX
+#define PKV_SINGLE_BOX 0
+#endif
+// Start-up cost of a (sequence, KV head) unit in quarter steps, for group sizes
+// below 4 and from 4 up (query copy, finalise, output write).
+#ifndef PKV_UNIT_COST_SMALL_G
+#define PKV_UNIT_COST_SMALL_G 2
+#endif
+#ifndef PKV_UNIT_COST_LARGE_G
+#define PKV_UNIT_COST_LARGE_G 4
+#endif
+
 constexpr int kTok = 16;                 // tokens per cache block (kernel requirement)
 constexpr int kSwizzleRow = 128;         // bytes per swizzled shared-memory row
 constexpr int kSubTile = kTok * kSwizzleRow;  // one swizzled [16 x 128 B] sub-tile
-constexpr int kWarps = 4;                // worker warps per CTA
+constexpr int kWarps = PKV_WARPS_PER_CTA;     // worker warps per CTA
+constexpr int kMaxStages = PKV_MAX_STAGES;    // per-warp pipeline depth limit
 constexpr int kMaxSeqs = 2048;
 constexpr int kMaxGroup = 8;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait before giving up
@@ -61,13 +94,16 @@ struct DecodeArgs {
   void* out;
   const int32_t* block_tables;
   const int32_t* context_lens;
-  float* part_ml;  // [2 * total_warps, G, 2]  (max in log2 units, sum)
-  float* part_o;   // [2 * total_warps, G, D]  (unnormalised accumulator)
+  float* part_ml;    // [2 * total_warps, G, 2]  (max in log2 units, sum)
+  float* part_o;     // [2 * total_warps, G, D]  (unnormalised accumulator)
+  int32_t* tickets;  // [total_warps], zero between launches
   int32_t* status;
   int32_t S, Hq, Hkv, G, MAXB, NB;
   int32_t total_warps;
+  int32_t stages;    // per-warp pipeline depth
   int32_t q_bytes;   // G * D * elt
   int32_t q_stride;  // per-stage q slot
+  int32_t unit_cost; // start-up cost of a unit, in quarter steps
   float scale_log2;  // scale * log2(e)
 };
 
@@ -77,22 +113,24 @@ struct Shape {
   static constexpr int kTileBytes = kTok * D * kElt;
   static constexpr int kSub = D * kElt / kSwizzleRow;     // sub-tiles per tile
   static constexpr int kBoxCols = kSwizzleRow / kElt;      // elements per sub-tile row
-  static constexpr int kStages = 16384 / kTileBytes;       // 32 KB of K+V stages per warp
-  static constexpr int kStageBytes = 2 * kTileBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;       // K and V tile
+  // fp16/bf16 tiles up to head_dim 128 fit in registers: release the stage early
+  static constexpr bool kEarlyRelease = PKV_EARLY_RELEASE && (kElt == 2) && (D <= 128);
+  // one box per tile: rows of the tile are viewed as kSub half-rows of 128 B
+  static constexpr bool kSingleBox = PKV_SINGLE_BOX && (kSub <= 2);
   static_assert(kSub * kSwizzleRow == D * kElt, "head_dim * elt must be a multiple of 128 B");
-  static_assert(kStages >= 2, "pipeline needs two stages");
 };
 
 struct SmemLayout {
-  uint32_t tiles, q, bars, ids, ctx, pre, scratch, total;
+  uint32_t tiles, q, bars, ids, ctx, pre, prew, scratch, total;
 };
 
-__host__ __device__ inline SmemLayout smem_layout(int tile_bytes, int stages, int q_stride,
+__host__ __device__ inline SmemLayout smem_layout(int stage_bytes, int stages, int q_stride,
                                                   int S) {
   SmemLayout L;
   uint32_t off = 0;
   L.tiles = off;
-  off += kWarps * stages * 2 * tile_bytes;
+  off += kWarps * stages * stage_bytes;
   L.q = off;
   off += kWarps * stages * q_stride;
   off = (off + 15u) & ~15u;
@@ -104,39 +142,31 @@ __host__ __device__ inline SmemLayout smem_layout(int tile_bytes, int stages, in
   off += S * 4;
   L.pre = off;
   off += (S + 1) * 4;
+  L.prew = off;
+  off += (S + 1) * 4;
   off = (off + 15u) & ~15u;
   L.scratch = off;
-  off += 32 * 4;
+  off += 2 * 32 * 4;
   L.total = off + 1024;  // slack for aligning the tiles to 1024 B
   return L;
 }
 
-__host__ __device__ inline SmemLayout reduce_smem_layout(int S) {
-  SmemLayout L{};
-  uint32_t off = 0;
-  L.ctx = off;
-  off += S * 4;
-  L.pre = off;
-  off += (S + 1) * 4;
-  off = (off + 15u) & ~15u;
-  L.scratch = off;
-  off += 32 * 4;
-  L.total = off;
-  return L;
-}
-
 // ---------------------------------------------------------------------------------
-// Schedule: per-sequence step counts and their prefix sums, built by every CTA.
-// pre[s] = sum_{s' < s} ceil(ctx[s'] / 16) * Hkv;  pre[S] = total steps.
+// Schedule, built by every CTA from the context lengths:
+//   pre[s]  = sum_{s' < s} nb(s') * Hkv            flat step index of (s, 0, 0)
+//   prew[s] = sum_{s' < s} Hkv * (4 nb(s') + c)    its cost in quarter steps
+// with nb = ceil(ctx / 16) and c the unit start-up cost (0 for empty sequences).
+// Warp w owns the steps whose cost position lies in [w R, (w+1) R): equal cost,
+// not equal step count, so warps holding many short contexts get fewer steps.
 // ---------------------------------------------------------------------------------
 __device__ void build_schedule(const int32_t* __restrict__ context_lens, int S, int MAXB, int Hkv,
-                               int32_t* ctx_s, int32_t* pre, int32_t* scratch,
-                               int32_t* status) {
+                               int unit_cost, int32_t* ctx_s, int32_t* pre, int32_t* prew,
+                               int32_t* scratch, int32_t* status) {
   const int limit = MAXB * kTok;
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     int c = context_lens[s];
     if (c < 0 || c > limit) {
-      if (status != nullptr && blockIdx.x == 0) atomicOr(status, PKV_DEV_BAD_CONTEXT_LEN);
+      if (blockIdx.x == 0) atomicOr(status, PKV_DEV_BAD_CONTEXT_LEN);
       c = c < 0 ? 0 : limit;
     }
     ctx_s[s] = c;
@@ -145,32 +175,61 @@ __device__ void build_schedule(const int32_t* __restrict__ context_lens, int S, 
   const int T = blockDim.x, tid = threadIdx.x, lane = tid & 31, wid = tid >> 5, nw = T >> 5;
   const int chunk = (S + T - 1) / T;
   const int b0 = min(S, tid * chunk), b1 = min(S, b0 + chunk);
-  int local = 0;
-  for (int s = b0; s < b1; ++s) local += ((ctx_s[s] + kTok - 1) / kTok) * Hkv;
-  int x = local;
+  auto steps_of = [&](int s) { return ((ctx_s[s] + kTok - 1) / kTok) * Hkv; };
+  auto cost_of = [&](int s) {
+    const int nb = (ctx_s[s] + kTok - 1) / kTok;
+    return nb > 0 ? Hkv * (4 * nb + unit_cost) : 0;
+  };
+  int local = 0, localw = 0;
+  for (int s = b0; s < b1; ++s) {
+    local += steps_of(s);
+    localw += cost_of(s);
+  }
+  int x = local, xw = localw;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    int y = __shfl_up_sync(0xffffffffu, x, o);
-    if (lane >= o) x += y;
+    const int y = __shfl_up_sync(0xffffffffu, x, o);
+    const int yw = __shfl_up_sync(0xffffffffu, xw, o);
+    if (lane >= o) {
+      x += y;
+      xw += yw;
+    }
   }
-  if (lane == 31) scratch[wid] = x;
+  if (lane == 31) {
+    scratch[wid] = x;
+    scratch[32 + wid] = xw;
+  }
   __syncthreads();
   if (wid == 0) {
     int v = lane < nw ? scratch[lane] : 0;
+    int vw = lane < nw ? scratch[32 + lane] : 0;
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
-      int y = __shfl_up_sync(0xffffffffu, v, o);
-      if (lane >= o) v += y;
+      const int y = __shfl_up_sync(0xffffffffu, v, o);
+      const int yw = __shfl_up_sync(0xffffffffu, vw, o);
+      if (lane >= o) {
+        v += y;
+        vw += yw;
+      }
     }
-    if (lane < nw) scratch[lane] = v;
+    if (lane < nw) {
+      scratch[lane] = v;
+      scratch[32 + lane] = vw;
+    }
   }
   __syncthreads();
   int run = x - local + (wid > 0 ? scratch[wid - 1] : 0);
+  int runw = xw - localw + (wid > 0 ? scratch[32 + wid - 1] : 0);
   for (int s = b0; s < b1; ++s) {
     pre[s] = run;
-    run += ((ctx_s[s] + kTok - 1) / kTok) * Hkv;
+    prew[s] = runw;
+    run += steps_of(s);
+    runw += cost_of(s);
   }
-  if (tid == T - 1) pre[S] = run;
+  if (tid == T - 1) {
+    pre[S] = run;
+    prew[S] = runw;
+  }
   __syncthreads();
 }
 
@@ -198,6 +257,37 @@ __device__ __forceinline__ Cursor cursor_at(const int32_t* pre, int S, int Hkv, 
   return c;
 }
 
+// Flat index of the first step whose cost position is >= P (total steps if none).
+// Step j of unit g of sequence s sits at prew[s] + g (4 nb + c) + c + 4 j.
+__device__ __forceinline__ int flat_at_cost(const int32_t* pre, const int32_t* prew, int S, int Hkv,
+                                            int unit_cost, int64_t P) {
+  if (P >= prew[S]) return pre[S];
+  int lo = 0, hi = S;  // prew[lo] <= P < prew[hi]
+  while (hi - lo > 1) {
+    const int mid = (lo + hi) >> 1;
+    if (prew[mid] <= P) lo = mid; else hi = mid;
+  }
+  const int nb = (pre[lo + 1] - pre[lo]) / Hkv;
+  const int us = 4 * nb + unit_cost;
+  const int r = static_cast<int>(P - prew[lo]);
+  int g = r / us;
+  const int r2 = r - g * us;
+  int j = r2 <= unit_cost ? 0 : (r2 - unit_cost + 3) / 4;
+  if (j >= nb) {  // past this unit's last step: the next unit's first
+    j = 0;
+    ++g;
+  }
+  return pre[lo] + g * nb + j;
+}
+
+// Warp owning step j of unit (s, g) for runs of R quarter steps.
+__device__ __forceinline__ int owner_of(const int32_t* pre, const int32_t* prew, int Hkv,
+                                        int unit_cost, int s, int g, int j, int64_t R) {
+  const int nb = (pre[s + 1] - pre[s]) / Hkv;
+  const int64_t pos = prew[s] + static_cast<int64_t>(g) * (4 * nb + unit_cost) + unit_cost + 4 * j;
+  return static_cast<int>(pos / R);
+}
+
 __device__ __forceinline__ void advance(Cursor& c, const int32_t* pre, int S, int Hkv) {
   if (++c.j < c.nb) return;
   c.j = 0;
@@ -214,14 +304,26 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* pre, int S, in
 // Tile layout in shared memory: kSub sub-tiles of [16 rows x 128 B]; the 16-byte
 // chunk c of row r sits at chunk position c ^ (r & 7) (the TMA 128-byte swizzle).
 // ---------------------------------------------------------------------------------
-__device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk16) {
-  return tile + (chunk16 >> 3) * kSubTile + row * kSwizzleRow +
-         (((chunk16 & 7) ^ (row & 7)) << 4);
+// Single-box tiles are instead [16 * kSub half-rows x 128 B], half-row r*kSub + c
+// holding chunks 8c..8c+7 of token row r.
+template <int kSub, bool kSingleBox>
+__device__ __forceinline__ uint32_t tile_offset(int row, int chunk16) {
+  if constexpr (kSingleBox) {
+    const int hr = row * kSub + (chunk16 >> 3);
+    return hr * kSwizzleRow + (((chunk16 & 7) ^ (hr & 7)) << 4);
+  } else {
+    return (chunk16 >> 3) * kSubTile + row * kSwizzleRow + (((chunk16 & 7) ^ (row & 7)) << 4);
+  }
 }
 
 template <typename T, int D>
 struct MmaState {
   static constexpr int KS = D / 16;
+  static constexpr int kSub = D * static_cast<int>(sizeof(T)) / kSwizzleRow;
+  static constexpr bool kSingle = PKV_SINGLE_BOX && (kSub <= 2);
+  static __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk16) {
+    return tile + tile_offset<kSub, kSingle>(row, chunk16);
+  }
   float o[KS][4];   // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
   uint32_t qb[KS][2];
   float m0, m1, l0, l1;  // heads 2*tig and 2*tig+1 (log2 units for m)
@@ -247,29 +349,42 @@ struct MmaState {
     }
   }
 
-  __device__ __forceinline__ void step(uint32_t ktile, uint32_t vtile, int valid,
-                                       float scale_log2, int lane) {
-    const int gid = lane >> 2, tig = lane & 3;
+  // K as the A operand of S^T = K Q^T: ldmatrix matrices
+  // {tok 0-7, d lo}, {tok 8-15, d lo}, {tok 0-7, d hi}, {tok 8-15, d hi} per k-step.
+  static __device__ __forceinline__ void load_k(uint32_t ktile, int ks, int lane,
+                                                uint32_t (&a)[4]) {
     const int mi = lane >> 3, r = lane & 7;
-    // S^T = K Q^T : A = K rows (tokens) x d, ldmatrix matrices
-    // {tok 0-7, d lo}, {tok 8-15, d lo}, {tok 0-7, d hi}, {tok 8-15, d hi}.
+    ptx::ldsm_x4(swz(ktile, r + (mi & 1) * 8, ks * 2 + (mi >> 1)), a);
+  }
+  // V^T as the A operand of O^T += V^T P^T: transposing ldmatrix of matrices
+  // {tok 0-7, d lo}, {tok 0-7, d hi}, {tok 8-15, d lo}, {tok 8-15, d hi} per m-tile.
+  static __device__ __forceinline__ void load_v(uint32_t vtile, int mt, int lane,
+                                                uint32_t (&a)[4]) {
+    const int mi = lane >> 3, r = lane & 7;
+    ptx::ldsm_x4_trans(swz(vtile, r + (mi >> 1) * 8, mt * 2 + (mi & 1)), a);
+  }
+
+  __device__ __forceinline__ void scores(const uint32_t (&kf)[KS][4], int valid,
+                                         float scale_log2, int lane, float (&x)[4]) {
+    const int gid = lane >> 2;
     float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
-    const int tok_a = r + (mi & 1) * 8;
 #pragma unroll
     for (int ks = 0; ks < KS; ++ks) {
-      uint32_t a[4];
-      ptx::ldsm_x4(swz(ktile, tok_a, ks * 2 + (mi >> 1)), a);
-      if (ks & 1) ptx::mma_16816<T>(c1, a, qb[ks][0], qb[ks][1]);
-      else ptx::mma_16816<T>(c0, a, qb[ks][0], qb[ks][1]);
+      if (ks & 1) ptx::mma_16816<T>(c1, kf[ks], qb[ks][0], qb[ks][1]);
+      else ptx::mma_16816<T>(c0, kf[ks], qb[ks][0], qb[ks][1]);
     }
-    // c[0]: (tok gid, head 2tig)  c[1]: (gid, 2tig+1)  c[2]: (gid+8, 2tig)  c[3]: (gid+8, 2tig+1)
-    float x0 = (c0[0] + c1[0]) * scale_log2, x1 = (c0[1] + c1[1]) * scale_log2;
-    float x2 = (c0[2] + c1[2]) * scale_log2, x3 = (c0[3] + c1[3]) * scale_log2;
+    // x[0]: (tok gid, head 2tig)  x[1]: (gid, 2tig+1)  x[2]: (gid+8, 2tig)  x[3]: (gid+8, 2tig+1)
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = (c0[i] + c1[i]) * scale_log2;
     if (valid < kTok) {
-      if (gid >= valid) x0 = x1 = -INFINITY;
-      if (gid + 8 >= valid) x2 = x3 = -INFINITY;
+      if (gid >= valid) x[0] = x[1] = -INFINITY;
+      if (gid + 8 >= valid) x[2] = x[3] = -INFINITY;
     }
-    float mx0 = fmaxf(x0, x2), mx1 = fmaxf(x1, x3);
+  }
+
+  // Online-softmax update; returns P^T as the B operand [16 tokens x 8 heads].
+  __device__ __forceinline__ void softmax(const float (&x)[4], uint32_t& pb0, uint32_t& pb1) {
+    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
 #pragma unroll
     for (int off = 4; off < 32; off <<= 1) {
       mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
@@ -277,8 +392,8 @@ struct MmaState {
     }
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
     const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    const float p0 = exp2f(x0 - mn0), p1 = exp2f(x1 - mn1);
-    const float p2 = exp2f(x2 - mn0), p3 = exp2f(x3 - mn1);
+    const float p0 = exp2f(x[0] - mn0), p1 = exp2f(x[1] - mn1);
+    const float p2 = exp2f(x[2] - mn0), p3 = exp2f(x[3] - mn1);
     l0 = l0 * al0 + (p0 + p2);
     l1 = l1 * al1 + (p1 + p3);
     m0 = mn0;
@@ -290,26 +405,64 @@ struct MmaState {
       o[mt][2] *= al0;
       o[mt][3] *= al1;
     }
-    // P^T as the B operand [16 tokens x 8 heads]: transpose the (tokens x heads)
-    // accumulator halves in registers.
-    const uint32_t pb0 = ptx::movmatrix_trans(ptx::pack2<T>(p0, p1));
-    const uint32_t pb1 = ptx::movmatrix_trans(ptx::pack2<T>(p2, p3));
-    // O^T += V^T P^T : A = V^T (d x tokens) via transposing ldmatrix of matrices
-    // {tok 0-7, d lo}, {tok 0-7, d hi}, {tok 8-15, d lo}, {tok 8-15, d hi}.
-    uint32_t mlo = 0xffffffffu, mhi = 0xffffffffu;
-    if (valid < kTok) {  // rows past the context may hold anything, NaN included
-      mlo = (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
-      mhi = (2 * tig + 8 < valid ? 0x0000ffffu : 0u) | (2 * tig + 9 < valid ? 0xffff0000u : 0u);
+    // transpose the (tokens x heads) halves in registers
+    pb0 = ptx::movmatrix_trans(ptx::pack2<T>(p0, p1));
+    pb1 = ptx::movmatrix_trans(ptx::pack2<T>(p2, p3));
+  }
+
+  // Rows past the context may hold anything, NaN included: zero their V lanes.
+  static __device__ __forceinline__ void mask_v(uint32_t (&a)[4], int valid, int lane) {
+    const int tig = lane & 3;
+    const uint32_t mlo =
+        (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
+    const uint32_t mhi =
+        (2 * tig + 8 < valid ? 0x0000ffffu : 0u) | (2 * tig + 9 < valid ? 0xffff0000u : 0u);
+    a[0] &= mlo;
+    a[1] &= mlo;
+    a[2] &= mhi;
+    a[3] &= mhi;
+  }
+
+  // Whole step from registers (tile already loaded).
+  __device__ __forceinline__ void step_regs(const uint32_t (&kf)[KS][4], uint32_t (&vf)[KS][4],
+                                            int valid, float scale_log2, int lane) {
+    float x[4];
+    scores(kf, valid, scale_log2, lane, x);
+    uint32_t pb0, pb1;
+    softmax(x, pb0, pb1);
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      if (valid < kTok) mask_v(vf[mt], valid, lane);
+      ptx::mma_16816<T>(o[mt], vf[mt], pb0, pb1);
     }
-    const int tok_v = r + (mi >> 1) * 8;
+  }
+
+  // Whole step reading the tile from shared memory as it goes.
+  __device__ __forceinline__ void step_smem(uint32_t ktile, uint32_t vtile, int valid,
+                                            float scale_log2, int lane) {
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a[4];
+      load_k(ktile, ks, lane, a);
+      if (ks & 1) ptx::mma_16816<T>(c1, a, qb[ks][0], qb[ks][1]);
+      else ptx::mma_16816<T>(c0, a, qb[ks][0], qb[ks][1]);
+    }
+    const int gid = lane >> 2;
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = (c0[i] + c1[i]) * scale_log2;
+    if (valid < kTok) {
+      if (gid >= valid) x[0] = x[1] = -INFINITY;
+      if (gid + 8 >= valid) x[2] = x[3] = -INFINITY;
+    }
+    uint32_t pb0, pb1;
+    softmax(x, pb0, pb1);
 #pragma unroll
     for (int mt = 0; mt < KS; ++mt) {
       uint32_t a[4];
-      ptx::ldsm_x4_trans(swz(vtile, tok_v, mt * 2 + (mi & 1)), a);
-      a[0] &= mlo;
-      a[1] &= mlo;
-      a[2] &= mhi;
-      a[3] &= mhi;
+      load_v(vtile, mt, lane, a);
+      if (valid < kTok) mask_v(a, valid, lane);
       ptx::mma_16816<T>(o[mt], a, pb0, pb1);
     }
   }
@@ -362,6 +515,8 @@ struct MmaState {
 template <int D>
 struct FmaState {
   static constexpr int E = D / 32;  // elements of a row per lane: d = lane + 32 * e
+  static constexpr int kSub = D * 4 / kSwizzleRow;
+  static constexpr bool kSingle = PKV_SINGLE_BOX && (kSub <= 2);
   float qv[kMaxGroup][E];
   float acc[kMaxGroup][E];
   float m[kMaxGroup], l[kMaxGroup];
@@ -385,10 +540,9 @@ struct FmaState {
   }
 
   static __device__ __forceinline__ float at(const uint8_t* tile, int t, int d) {
-    const int chunk = d >> 2;  // 16-byte chunk of the 128-byte sub-tile row
-    const uint8_t* p = tile + (chunk >> 3) * kSubTile + t * kSwizzleRow +
-                       (((chunk & 7) ^ (t & 7)) << 4) + (d & 3) * 4;
-    return *reinterpret_cast<const float*>(p);
+    const int chunk = d >> 2;  // 16-byte chunk of the 128-byte row
+    return *reinterpret_cast<const float*>(tile + tile_offset<kSub, kSingle>(t, chunk) +
+                                           (d & 3) * 4);
   }
 
   __device__ __forceinline__ void step(const uint8_t* kt, const uint8_t* vt, int valid,
@@ -460,32 +614,132 @@ struct FmaState {
   }
 };
 
+// Partial-state slot of warp w's piece of a cut (s, g): 2w+1 if the (s, g) starts
+// inside w's run (w is its first warp), else 2w.
+__device__ __forceinline__ int64_t piece_slot(int w, int first_warp) {
+  return w == first_warp ? 2 * static_cast<int64_t>(w) + 1 : 2 * static_cast<int64_t>(w);
+}
+
+// Log-sum-exp merge of the pieces of (s, g) held by warps w0..w1, in that order:
+// M = max_i m_i;  out = sum_i 2^(m_i - M) o_i / sum_i 2^(m_i - M) l_i.
+// The warp's lanes split the G heads and, within a head, the head_dim; the lanes
+// of one head share the max over pieces, and piece loads are issued two at a
+// time so the merge costs a few L2 round trips, not one per value.
+template <typename T, int D, int G>
+__device__ void merge_pieces_g(const DecodeArgs& a, int s, int g, int w0, int w1, int lane) {
+  constexpr int LPH = 32 / G;          // lanes per head
+  constexpr int E = D / LPH;           // contiguous elements of the row per lane
+  const int h = lane / LPH, sub = lane % LPH;
+  float M = -INFINITY;
+  for (int w = w0 + sub; w <= w1; w += LPH)
+    M = fmaxf(M, __ldcg(a.part_ml + (piece_slot(w, w0) * G + h) * 2));
+#pragma unroll
+  for (int off = 1; off < LPH; off <<= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+  float lsum = 0.f;
+  float acc[E];
+#pragma unroll
+  for (int e = 0; e < E; ++e) acc[e] = 0.f;
+#pragma unroll 2
+  for (int w = w0; w <= w1; ++w) {
+    const int64_t slot = piece_slot(w, w0);
+    const float* ml = a.part_ml + (slot * G + h) * 2;
+    const float* po = a.part_o + (slot * G + h) * D + sub * E;
+    const float wt = exp2f(__ldcg(ml) - M);
+    lsum = fmaf(wt, __ldcg(ml + 1), lsum);
+    if constexpr (E % 4 == 0) {
+#pragma unroll
+      for (int e = 0; e < E; e += 4) {
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(po + e));
+        acc[e] = fmaf(wt, v.x, acc[e]);
+        acc[e + 1] = fmaf(wt, v.y, acc[e + 1]);
+        acc[e + 2] = fmaf(wt, v.z, acc[e + 2]);
+        acc[e + 3] = fmaf(wt, v.w, acc[e + 3]);
+      }
+    } else {
+#pragma unroll
+      for (int e = 0; e < E; ++e) acc[e] = fmaf(wt, __ldcg(po + e), acc[e]);
+    }
+  }
+  const float inv = 1.f / lsum;
+  T* const row = reinterpret_cast<T*>(a.out) + (static_cast<int64_t>(s) * a.Hq + g * G + h) * D +
+                 sub * E;
+#pragma unroll
+  for (int e = 0; e < E; ++e) row[e] = ptx::from_float<T>(acc[e] * inv);
+}
+
+template <typename T, int D>
+__device__ void merge_pieces(const DecodeArgs& a, int s, int g, int w0, int w1, int lane) {
+  switch (a.G) {
+    case 1: merge_pieces_g<T, D, 1>(a, s, g, w0, w1, lane); break;
+    case 2: merge_pieces_g<T, D, 2>(a, s, g, w0, w1, lane); break;
+    case 4: merge_pieces_g<T, D, 4>(a, s, g, w0, w1, lane); break;
+    default: merge_pieces_g<T, D, 8>(a, s, g, w0, w1, lane); break;
+  }
+}
+
+// A cut (s, g) whose piece this warp finished: merged by the last piece to finish.
+struct CutUnit {
+  int s, g, w0, w1;
+};
+
 // ---------------------------------------------------------------------------------
-// Partition kernel: every warp streams its run of steps.
+// The decode kernel: one persistent pass of every worker warp over its run.
 // ---------------------------------------------------------------------------------
 template <typename T, int D>
 __global__ void __launch_bounds__(kWarps * 32, 1)
-    decode_partition_kernel(const __grid_constant__ CUtensorMap kmap,
+    decode_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using Sh = Shape<T, D>;
-  constexpr int NS = Sh::kStages;
+  const int NS = a.stages;
   extern __shared__ uint8_t smem_raw[];
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+    if (blockIdx.x == 0) {
+      // Words 1..3 of the status area record the layout (warps, group, head_dim)
+      // of the last launch; a workspace reused under another layout holds stale
+      // tickets, which is reported rather than silently mis-merged.
+      int32_t* sig = a.status + 1;
+      const int32_t w = __ldcg(sig), g = __ldcg(sig + 1), d = __ldcg(sig + 2);
+      if (w != 0 && (w != a.total_warps || g != a.G || d != D))
+        atomicOr(a.status, PKV_DEV_WORKSPACE_MISMATCH);
+      sig[0] = a.total_warps;
+      sig[1] = a.G;
+      sig[2] = D;
+    }
+  }
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base_s = (raw + 1023u) & ~1023u;
   uint8_t* const base = smem_raw + (base_s - raw);
-  const SmemLayout L = smem_layout(Sh::kTileBytes, NS, a.q_stride, a.S);
+  const SmemLayout L = smem_layout(Sh::kStageBytes, NS, a.q_stride, a.S);
   int32_t* const ctx_s = reinterpret_cast<int32_t*>(base + L.ctx);
   int32_t* const pre = reinterpret_cast<int32_t*>(base + L.pre);
-  build_schedule(a.context_lens, a.S, a.MAXB, a.Hkv, ctx_s, pre,
+  int32_t* const prew = reinterpret_cast<int32_t*>(base + L.prew);
+  build_schedule(a.context_lens, a.S, a.MAXB, a.Hkv, a.unit_cost, ctx_s, pre, prew,
                  reinterpret_cast<int32_t*>(base + L.scratch), a.status);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * kWarps + warp;
-  const int total = pre[a.S];
+  const int S = a.S, Hkv = a.Hkv, MAXB = a.MAXB;
+  const int total = pre[S];
   const int W = a.total_warps;
-  const int run_len = (total + W - 1) / W;
-  const int f0 = gw < W ? min(total, gw * run_len) : total;
-  const int f1 = min(total, f0 + run_len);
+  const int UC = a.unit_cost;
+  // Runs of R quarter steps; R is at least the widest gap between consecutive
+  // step positions (4 + UC), so every warp between the first and the last owner
+  // of a unit holds a piece of it.
+  const int64_t R = max(static_cast<int64_t>((prew[S] + W - 1) / W), static_cast<int64_t>(4 + UC));
+  T* const out = reinterpret_cast<T*>(a.out);
+
+  // Rows of empty contexts are zero.
+  if (gw < W) {
+    for (int s = gw; s < S; s += W) {
+      if (pre[s + 1] != pre[s]) continue;
+      T* const rows = out + static_cast<int64_t>(s) * a.Hq * D;
+      for (int i = lane; i < a.Hq * D; i += 32) rows[i] = ptx::from_float<T>(0.f);
+    }
+  }
+  const int f0 = gw < W ? flat_at_cost(pre, prew, S, Hkv, UC, gw * R) : total;
+  const int f1 = gw < W ? flat_at_cost(pre, prew, S, Hkv, UC, (gw + 1) * R) : total;
   const int nsteps = f1 - f0;
   if (nsteps <= 0) return;
 
@@ -495,10 +749,8 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const uint32_t bars = base_s + L.bars + warp * NS * 8;
   const int32_t* const ids = reinterpret_cast<const int32_t*>(base + L.ids) + warp * 64;
   const uint32_t ids_s = base_s + L.ids + warp * 64 * 4;
-  const int S = a.S, Hkv = a.Hkv, MAXB = a.MAXB;
 
   if (lane == 0) {
-#pragma unroll
     for (int st = 0; st < NS; ++st) ptx::mbar_init(bars + 8 * st, 1);
     ptx::fence_barrier_init();
   }
@@ -519,11 +771,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   ptx::cp_async_wait<1>();
   __syncwarp();
 
+  // Every K/V read below comes after the preceding grid (the cache write of the
+  // new tokens) has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
   const uint64_t policy = ptx::policy_evict_first();
   const int32_t rows_total = a.NB * Hkv * kTok;
   const char* const qbase = reinterpret_cast<const char*>(a.q);
 
   Cursor pc = cursor_at(pre, S, Hkv, f0);
+  int p_stage = 0;
   auto issue = [&](int m) {  // warp-uniform; lane 0 issues the copies of local step m
     if ((m & 31) == 0 && m > 0) {
       load_window((m >> 5) + 1);
@@ -531,10 +788,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       __syncwarp();
     }
     if (lane == 0) {
-      const int st = m % NS;
       const int id = ids[((m >> 5) & 1) * 32 + (m & 31)];
       const bool need_q = (m == 0) || (pc.j == 0);
-      const uint32_t bar = bars + 8 * st;
+      const uint32_t bar = bars + 8 * p_stage;
       ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
       int32_t y;
       if (static_cast<uint32_t>(id) < static_cast<uint32_t>(a.NB)) {
@@ -543,20 +799,26 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         atomicOr(a.status, PKV_DEV_BAD_BLOCK_ID);
         y = rows_total;  // a box wholly past the end: the TMA unit fills it with zeros
       }
-      const uint32_t kt = tiles + st * Sh::kStageBytes;
+      const uint32_t kt = tiles + p_stage * Sh::kStageBytes;
       const uint32_t vt = kt + Sh::kTileBytes;
+      if constexpr (Sh::kSingleBox) {
+        ptx::tma_load_2d(kt, &kmap, 0, y * Sh::kSub, bar, policy);
+        ptx::tma_load_2d(vt, &vmap, 0, y * Sh::kSub, bar, policy);
+      } else {
 #pragma unroll
-      for (int c = 0; c < Sh::kSub; ++c)
-        ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
+        for (int c = 0; c < Sh::kSub; ++c)
+          ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
 #pragma unroll
-      for (int c = 0; c < Sh::kSub; ++c)
-        ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
+        for (int c = 0; c < Sh::kSub; ++c)
+          ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
+      }
       if (need_q) {
         const char* src =
             qbase + (static_cast<int64_t>(pc.s) * a.Hq + pc.g * a.G) * D * Sh::kElt;
-        ptx::bulk_load(qslot_s + st * a.q_stride, src, a.q_bytes, bar);
+        ptx::bulk_load(qslot_s + p_stage * a.q_stride, src, a.q_bytes, bar);
       }
     }
+    if (++p_stage == NS) p_stage = 0;
     advance(pc, pre, S, Hkv);
   };
 
@@ -567,33 +829,55 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   State st_;
   Cursor cc = cursor_at(pre, S, Hkv, f0);
   int first_j = cc.j;
-  T* const out = reinterpret_cast<T*>(a.out);
+  CutUnit cut[2];
+  int ncut = 0;
+  int c_stage = 0;
+  uint32_t parity = 0;
 
   for (int n = 0; n < nsteps; ++n) {
-    const int st = n % NS;
-    const uint32_t parity = (n / NS) & 1;
-    const bool ok = ptx::mbar_wait(bars + 8 * st, parity, kWaitLimitNs);
+    const uint32_t bar = bars + 8 * c_stage;
+    const bool ok = ptx::mbar_wait(bar, parity, kWaitLimitNs);
     if (!__all_sync(0xffffffffu, ok)) {
       if (lane == 0) atomicOr(a.status, PKV_DEV_WAIT_TIMEOUT);
-      const int last = min(nsteps, n + NS);
-      for (int k = n; k < last; ++k)
-        ptx::mbar_wait(bars + 8 * (k % NS), (k / NS) & 1, kWaitLimitNs / 8);
+      // give the copies already issued a bounded chance to land, then leave
+      int st = c_stage;
+      uint32_t ph = parity;
+      for (int k = n; k < min(nsteps, n + NS); ++k) {
+        ptx::mbar_wait(bars + 8 * st, ph, kWaitLimitNs / 8);
+        if (++st == NS) { st = 0; ph ^= 1u; }
+      }
       ptx::cp_async_wait<0>();
       return;
     }
     if (n == 0 || cc.j == 0) {
-      st_.load_q(qslot + st * a.q_stride, a.G, lane);
+      st_.load_q(qslot + c_stage * a.q_stride, a.G, lane);
       st_.reset();
       first_j = cc.j;
     }
     const int valid = (cc.j == cc.nb - 1) ? ctx_s[cc.s] - cc.j * kTok : kTok;
-    const uint32_t kt = tiles + st * Sh::kStageBytes;
-    if constexpr (sizeof(T) == 2) {
-      st_.step(kt, kt + Sh::kTileBytes, valid, a.scale_log2, lane);
+    const uint32_t kt = tiles + c_stage * Sh::kStageBytes;
+    if constexpr (Sh::kEarlyRelease) {
+      constexpr int KS = D / 16;
+      uint32_t kf[KS][4], vf[KS][4];
+#pragma unroll
+      for (int i = 0; i < KS; ++i) {
+        MmaState<T, D>::load_k(kt, i, lane, kf[i]);
+        MmaState<T, D>::load_v(kt + Sh::kTileBytes, i, lane, vf[i]);
+      }
+      __syncwarp();
+      if (n + NS < nsteps) issue(n + NS);
+      st_.step_regs(kf, vf, valid, a.scale_log2, lane);
     } else {
-      const uint8_t* ktp = base + (kt - base_s);
-      st_.step(ktp, ktp + Sh::kTileBytes, valid, a.scale_log2, a.G, lane);
+      if constexpr (sizeof(T) == 2) {
+        st_.step_smem(kt, kt + Sh::kTileBytes, valid, a.scale_log2, lane);
+      } else {
+        const uint8_t* ktp = base + (kt - base_s);
+        st_.step(ktp, ktp + Sh::kTileBytes, valid, a.scale_log2, a.G, lane);
+      }
+      __syncwarp();
+      if (n + NS < nsteps) issue(n + NS);
     }
+    if (++c_stage == NS) { c_stage = 0; parity ^= 1u; }
     const bool unit_end = (cc.j == cc.nb - 1);
     if (unit_end || n == nsteps - 1) {
       st_.reduce_sums();
@@ -603,76 +887,33 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
         const int slot = 2 * gw + (first_j == 0 ? 1 : 0);
         st_.write_partial(a.part_o + static_cast<int64_t>(slot) * a.G * D,
                           a.part_ml + static_cast<int64_t>(slot) * a.G * 2, a.G, lane);
+        cut[ncut++] = CutUnit{cc.s, cc.g, owner_of(pre, prew, Hkv, UC, cc.s, cc.g, 0, R),
+                              owner_of(pre, prew, Hkv, UC, cc.s, cc.g, cc.nb - 1, R)};
       }
     }
     advance(cc, pre, S, Hkv);
-    __syncwarp();
-    if (n + NS < nsteps) issue(n + NS);
   }
   ptx::cp_async_wait<0>();
-}
 
-// ---------------------------------------------------------------------------------
-// Reduce kernel: merges the pieces of every cut (s, g) in logical order and
-// writes zero rows for empty contexts.  Warp w merges the (s, g) that starts in
-// its run and continues past it; the pieces come from warps w, w+1, ..., w_last,
-// stored at slot 2w+1 for w and slot 2w' for the later warps.
-// ---------------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32)
-    decode_reduce_kernel(const DecodeArgs a) {
-  extern __shared__ uint8_t smem_raw[];
-  const SmemLayout L = reduce_smem_layout(a.S);
-  int32_t* const ctx_s = reinterpret_cast<int32_t*>(smem_raw + L.ctx);
-  int32_t* const pre = reinterpret_cast<int32_t*>(smem_raw + L.pre);
-  build_schedule(a.context_lens, a.S, a.MAXB, a.Hkv, ctx_s, pre,
-                 reinterpret_cast<int32_t*>(smem_raw + L.scratch), nullptr);
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kWarps + warp;
-  const int W = a.total_warps;
-  if (gw >= W) return;
-  const int total = pre[a.S];
-  const int run_len = (total + W - 1) / W;
-  T* const out = reinterpret_cast<T*>(a.out);
-  const int f0 = min(total, gw * run_len);
-  const int f1 = min(total, f0 + run_len);
-  if (f1 > f0) {
-    const Cursor c = cursor_at(pre, a.S, a.Hkv, f1 - 1);
-    const int u0 = pre[c.s] + c.g * c.nb;
-    const int u1 = u0 + c.nb;
-    if (u0 >= f0 && u1 > f1) {
-      const int w_last = (u1 - 1) / run_len;
-      T* const rows = out + (static_cast<int64_t>(c.s) * a.Hq + c.g * a.G) * D;
-      for (int h = 0; h < a.G; ++h) {
-        float M = -INFINITY;
-        for (int w = gw; w <= w_last; ++w) {
-          const int slot = w == gw ? 2 * w + 1 : 2 * w;
-          M = fmaxf(M, a.part_ml[(static_cast<int64_t>(slot) * a.G + h) * 2]);
-        }
-        float lsum = 0.f;
-        float acc[D / 32];
-#pragma unroll
-        for (int e = 0; e < D / 32; ++e) acc[e] = 0.f;
-        for (int w = gw; w <= w_last; ++w) {
-          const int64_t slot = w == gw ? 2 * w + 1 : 2 * w;
-          const float* ml = a.part_ml + (slot * a.G + h) * 2;
-          const float wt = exp2f(ml[0] - M);
-          lsum += wt * ml[1];
-          const float* po = a.part_o + (slot * a.G + h) * D;
-#pragma unroll
-          for (int e = 0; e < D / 32; ++e) acc[e] = fmaf(wt, po[lane + 32 * e], acc[e]);
-        }
-        const float inv = 1.f / lsum;
-#pragma unroll
-        for (int e = 0; e < D / 32; ++e)
-          rows[h * D + lane + 32 * e] = ptx::from_float<T>(acc[e] * inv);
+  // Tickets of the cut (s, g) this warp took part in; the last piece merges.
+  if (ncut > 0) {
+    __threadfence();
+    __syncwarp();
+    int t0 = 0, t1 = 0;
+    if (lane == 0) {
+      t0 = atomicAdd(a.tickets + cut[0].w0, 1);
+      if (ncut > 1) t1 = atomicAdd(a.tickets + cut[1].w0, 1);
+    }
+    t0 = __shfl_sync(0xffffffffu, t0, 0);
+    t1 = __shfl_sync(0xffffffffu, t1, 0);
+    for (int i = 0; i < ncut; ++i) {
+      const CutUnit& u = cut[i];
+      if ((i == 0 ? t0 : t1) == u.w1 - u.w0) {
+        __threadfence();
+        merge_pieces<T, D>(a, u.s, u.g, u.w0, u.w1, lane);
+        if (lane == 0) a.tickets[u.w0] = 0;  // ready for the next launch
       }
     }
-  }
-  for (int s = gw; s < a.S; s += W) {
-    if (pre[s + 1] != pre[s]) continue;
-    T* const rows = out + static_cast<int64_t>(s) * a.Hq * D;
-    for (int i = lane; i < a.Hq * D; i += 32) rows[i] = ptx::from_float<T>(0.f);
   }
 }
 
@@ -703,11 +944,22 @@ bool supported_head_dim(int32_t dtype, int32_t D) {
   return D == 64 || D == 128 || D == 256;
 }
 
-template <typename T, int D>
-int max_partition_smem() {
-  using Sh = Shape<T, D>;
-  return static_cast<int>(
-      smem_layout(Sh::kTileBytes, Sh::kStages, kMaxGroup * D * Sh::kElt, kMaxSeqs).total);
+// Opt-in shared memory per block of the current device (cached per device).
+int device_smem_optin(int* bytes) {
+  static std::once_flag flags[64];
+  static int values[64];
+  int dev = 0;
+  PKV_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::call_once(flags[dev], [&] {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      v = 0;
+    values[dev] = v;
+  });
+  if (values[dev] <= 0) return fail(PKV_ERR_CUDA, "could not query shared memory of device %d", dev);
+  *bytes = values[dev];
+  return PKV_OK;
 }
 
 template <typename T, int D>
@@ -718,64 +970,49 @@ int ensure_smem_attr() {
   int dev = 0;
   PKV_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  int optin = 0;
+  int rc = device_smem_optin(&optin);
+  if (rc != PKV_OK) return rc;
   std::call_once(flags[dev], [&] {
-    results[dev] = cudaFuncSetAttribute(decode_partition_kernel<T, D>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        max_partition_smem<T, D>());
+    results[dev] = cudaFuncSetAttribute(decode_attention_kernel<T, D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   });
   if (results[dev] != cudaSuccess)
     return cuda_fail(static_cast<cudaError_t>(results[dev]), "cudaFuncSetAttribute");
   return PKV_OK;
 }
 
-template <typename T, int D>
-int default_warps_for() {
-  // One full wave of the partition kernel: SMs x resident CTAs x warps per CTA,
-  // computed once per device at the largest shared-memory footprint the kernel
-  // can request, so the count never depends on the batch.
-  static std::once_flag flags[64];
-  static int results[64];
+// One CTA of kWarps warps per SM (the kernel sizes its pipeline to fill the SM's
+// shared memory), so the default warp count is SMs x kWarps.
+int default_warps(int32_t dtype, int32_t D) {
+  if (!supported_head_dim(dtype, D))
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for dtype %d", D, dtype);
   int sms = 0, dev = 0;
   int rc = device_sm_count(&sms, &dev);
   if (rc != PKV_OK) return rc;
-  rc = ensure_smem_attr<T, D>();
-  if (rc != PKV_OK) return rc;
-  std::call_once(flags[dev], [&] {
-    int per_sm = 0;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, decode_partition_kernel<T, D>,
-                                                      kWarps * 32,
-                                                      max_partition_smem<T, D>()) != cudaSuccess)
-      per_sm = 0;
-    results[dev] = per_sm;
-  });
-  if (results[dev] < 1) return fail(PKV_ERR_UNSUPPORTED, "partition kernel does not fit on an SM");
-  return sms * results[dev] * kWarps;
+  return sms * kWarps;
 }
 
-int default_warps(int32_t dtype, int32_t D) {
-#define PKV_CASE(DT, TT, DD) \
-  if (dtype == DT && D == DD) return default_warps_for<TT, DD>();
-  PKV_CASE(PKV_BF16, __nv_bfloat16, 64)
-  PKV_CASE(PKV_BF16, __nv_bfloat16, 128)
-  PKV_CASE(PKV_BF16, __nv_bfloat16, 256)
-  PKV_CASE(PKV_F16, __half, 64)
-  PKV_CASE(PKV_F16, __half, 128)
-  PKV_CASE(PKV_F16, __half, 256)
-  PKV_CASE(PKV_F32, float, 32)
-  PKV_CASE(PKV_F32, float, 64)
-  PKV_CASE(PKV_F32, float, 128)
-#undef PKV_CASE
-  return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for dtype %d", D, dtype);
+size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
+
+struct WorkspaceLayout {
+  size_t tickets, ml, o, total;
+};
+
+WorkspaceLayout workspace_layout(int32_t G, int32_t D, int32_t W) {
+  WorkspaceLayout L;
+  L.tickets = kStatusBytes;
+  L.ml = L.tickets + round256(static_cast<size_t>(W) * sizeof(int32_t));
+  L.o = L.ml + round256(static_cast<size_t>(2) * W * G * 2 * sizeof(float));
+  L.total = L.o + static_cast<size_t>(2) * W * G * D * sizeof(float);
+  return L;
 }
 
 size_t workspace_bytes_for(int32_t G, int32_t D, int32_t W) {
-  const size_t ml = static_cast<size_t>(2) * W * G * 2 * sizeof(float);
-  const size_t po = static_cast<size_t>(2) * W * G * D * sizeof(float);
-  const size_t ml_al = (ml + 255) & ~static_cast<size_t>(255);
-  return kStatusBytes + ml_al + po;
+  return workspace_layout(G, D, W).total;
 }
 
-int validate(const HostArgs& h, bool need_kernels_inputs, int* warps_out) {
+int validate(const HostArgs& h, int* warps_out) {
   PKV_REQUIRE(element_bytes(h.dtype) != 0, PKV_ERR_DTYPE, "unknown dtype %d", h.dtype);
   PKV_REQUIRE(h.S >= 0 && h.S <= kMaxSeqs, PKV_ERR_UNSUPPORTED,
               "num_seqs %d outside [0, %d]", h.S, kMaxSeqs);
@@ -803,18 +1040,18 @@ int validate(const HostArgs& h, bool need_kernels_inputs, int* warps_out) {
   PKV_REQUIRE(h.workspace_bytes >= workspace_bytes_for(G, h.D, W), PKV_ERR_INVALID_ARG,
               "workspace of %zu bytes < %zu needed", h.workspace_bytes,
               workspace_bytes_for(G, h.D, W));
-  PKV_REQUIRE(h.S == 0 || (h.context_lens && h.out), PKV_ERR_INVALID_ARG, "NULL pointer");
-  PKV_REQUIRE(aligned(h.out, 16), PKV_ERR_INVALID_ARG, "out must be 16-byte aligned");
-  if (need_kernels_inputs) {
-    PKV_REQUIRE(h.NB > 0, PKV_ERR_INVALID_ARG, "num_blocks must be positive");
-    PKV_REQUIRE(static_cast<int64_t>(h.NB) * h.Hkv * kTok < (int64_t(1) << 31),
-                PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 16 >= 2^31");
-    PKV_REQUIRE(h.S == 0 || (h.q && h.k_cache && h.v_cache && h.block_tables),
-                PKV_ERR_INVALID_ARG, "NULL pointer");
-    PKV_REQUIRE(aligned(h.q, 16) && aligned(h.k_cache, 16) && aligned(h.v_cache, 16) &&
-                    aligned(h.block_tables, 4),
-                PKV_ERR_INVALID_ARG, "q and caches must be 16-byte aligned");
-  }
+  PKV_REQUIRE(h.NB > 0, PKV_ERR_INVALID_ARG, "num_blocks must be positive");
+  PKV_REQUIRE(static_cast<int64_t>(h.NB) * h.Hkv * kTok * 4 < (int64_t(1) << 31),
+              PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 64 >= 2^31");
+  PKV_REQUIRE(static_cast<int64_t>(h.S) * h.MAXB * h.Hkv * 4 +
+                      static_cast<int64_t>(h.S) * h.Hkv * 8 < (int64_t(1) << 31),
+              PKV_ERR_UNSUPPORTED, "schedule cost exceeds 2^31 quarter steps");
+  PKV_REQUIRE(h.S == 0 || (h.q && h.k_cache && h.v_cache && h.block_tables && h.context_lens &&
+                           h.out),
+              PKV_ERR_INVALID_ARG, "NULL pointer");
+  PKV_REQUIRE(aligned(h.q, 16) && aligned(h.k_cache, 16) && aligned(h.v_cache, 16) &&
+                  aligned(h.out, 16) && aligned(h.block_tables, 4),
+              PKV_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
   return PKV_OK;
 }
 
@@ -823,15 +1060,15 @@ DecodeArgs device_args(const HostArgs& h, int W) {
   const int G = h.Hq / h.Hkv;
   const int elt = element_bytes(h.dtype);
   char* ws = static_cast<char*>(h.workspace);
-  const size_t ml = static_cast<size_t>(2) * W * G * 2 * sizeof(float);
-  const size_t ml_al = (ml + 255) & ~static_cast<size_t>(255);
+  const WorkspaceLayout WL = workspace_layout(G, h.D, W);
   a.q = h.q;
   a.out = h.out;
   a.block_tables = h.block_tables;
   a.context_lens = h.context_lens;
   a.status = reinterpret_cast<int32_t*>(ws);
-  a.part_ml = reinterpret_cast<float*>(ws + kStatusBytes);
-  a.part_o = reinterpret_cast<float*>(ws + kStatusBytes + ml_al);
+  a.tickets = reinterpret_cast<int32_t*>(ws + WL.tickets);
+  a.part_ml = reinterpret_cast<float*>(ws + WL.ml);
+  a.part_o = reinterpret_cast<float*>(ws + WL.o);
   a.S = h.S;
   a.Hq = h.Hq;
   a.Hkv = h.Hkv;
@@ -841,44 +1078,56 @@ DecodeArgs device_args(const HostArgs& h, int W) {
   a.total_warps = W;
   a.q_bytes = G * h.D * elt;
   a.q_stride = (a.q_bytes + 127) & ~127;
+  a.unit_cost = G >= 4 ? PKV_UNIT_COST_LARGE_G : PKV_UNIT_COST_SMALL_G;
   a.scale_log2 = h.scale * 1.4426950408889634f;
   return a;
 }
 
 template <typename T, int D>
-int launch_partition(const HostArgs& h, int W) {
+int launch_decode(const HostArgs& h, int W) {
   using Sh = Shape<T, D>;
   int rc = ensure_smem_attr<T, D>();
   if (rc != PKV_OK) return rc;
-  const DecodeArgs a = device_args(h, W);
+  int optin = 0;
+  rc = device_smem_optin(&optin);
+  if (rc != PKV_OK) return rc;
+  DecodeArgs a = device_args(h, W);
+  // Deepest pipeline that fits the SM's shared memory.
+  const uint32_t fixed = smem_layout(Sh::kStageBytes, 0, a.q_stride, h.S).total;
+  const uint32_t per_stage = kWarps * (Sh::kStageBytes + a.q_stride + 8);
+  int stages = optin > static_cast<int>(fixed) ? static_cast<int>((optin - fixed) / per_stage) : 0;
+  stages = stages > kMaxStages ? kMaxStages : stages;
+  PKV_REQUIRE(stages >= 2, PKV_ERR_UNSUPPORTED, "pipeline does not fit in shared memory");
+  a.stages = stages;
+  const SmemLayout L = smem_layout(Sh::kStageBytes, stages, a.q_stride, h.S);
   CUtensorMap kmap, vmap;
   const int64_t rows = static_cast<int64_t>(h.NB) * h.Hkv * kTok;
-  rc = encode_cache_map(&kmap, h.k_cache, h.dtype, rows, D, Sh::kBoxCols);
+  // Single box: the cache as [rows * kSub, 128 B] half-rows, boxes of 16 * kSub
+  // half-rows (one whole tile).  Otherwise [rows, D], boxes of 16 rows x 128 B.
+  const int64_t map_rows = Sh::kSingleBox ? rows * Sh::kSub : rows;
+  const int map_cols = Sh::kSingleBox ? Sh::kBoxCols : D;
+  const int box_rows = Sh::kSingleBox ? kTok * Sh::kSub : kTok;
+  rc = encode_cache_map(&kmap, h.k_cache, h.dtype, map_rows, map_cols, Sh::kBoxCols, box_rows);
   if (rc != PKV_OK) return rc;
-  rc = encode_cache_map(&vmap, h.v_cache, h.dtype, rows, D, Sh::kBoxCols);
+  rc = encode_cache_map(&vmap, h.v_cache, h.dtype, map_rows, map_cols, Sh::kBoxCols, box_rows);
   if (rc != PKV_OK) return rc;
-  const SmemLayout L = smem_layout(Sh::kTileBytes, Sh::kStages, a.q_stride, h.S);
-  const int grid = (W + kWarps - 1) / kWarps;
-  decode_partition_kernel<T, D><<<grid, kWarps * 32, L.total, h.stream>>>(kmap, vmap, a);
-  PKV_CUDA(cudaGetLastError());
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((W + kWarps - 1) / kWarps);
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.dynamicSmemBytes = L.total;
+  cfg.stream = h.stream;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  PKV_CUDA(cudaLaunchKernelEx(&cfg, decode_attention_kernel<T, D>, kmap, vmap, a));
   return PKV_OK;
 }
 
-template <typename T, int D>
-int launch_reduce(const HostArgs& h, int W) {
-  const DecodeArgs a = device_args(h, W);
-  const SmemLayout L = reduce_smem_layout(h.S);
-  const int grid = (W + kWarps - 1) / kWarps;
-  decode_reduce_kernel<T, D><<<grid, kWarps * 32, L.total, h.stream>>>(a);
-  PKV_CUDA(cudaGetLastError());
-  return PKV_OK;
-}
-
-template <bool kPartition>
 int dispatch(const HostArgs& h, int W) {
-#define PKV_CASE(DT, TT, DD)                                                     \
-  if (h.dtype == DT && h.D == DD)                                                \
-    return kPartition ? launch_partition<TT, DD>(h, W) : launch_reduce<TT, DD>(h, W);
+#define PKV_CASE(DT, TT, DD) \
+  if (h.dtype == DT && h.D == DD) return launch_decode<TT, DD>(h, W);
   PKV_CASE(PKV_BF16, __nv_bfloat16, 64)
   PKV_CASE(PKV_BF16, __nv_bfloat16, 128)
   PKV_CASE(PKV_BF16, __nv_bfloat16, 256)
@@ -890,34 +1139,6 @@ int dispatch(const HostArgs& h, int W) {
   PKV_CASE(PKV_F32, float, 128)
 #undef PKV_CASE
   return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for dtype %d", h.D, h.dtype);
-}
-
-HostArgs make_args(const void* q, const void* k_cache, const void* v_cache,
-                   const int32_t* block_tables, int32_t MAXB, const int32_t* context_lens,
-                   int32_t S, int32_t Hq, int32_t Hkv, int32_t D, int32_t block_size, int32_t NB,
-                   float scale, void* out, void* workspace, size_t workspace_bytes,
-                   int32_t num_warps, int32_t dtype, void* stream) {
-  HostArgs h;
-  h.q = q;
-  h.k_cache = k_cache;
-  h.v_cache = v_cache;
-  h.block_tables = block_tables;
-  h.MAXB = MAXB;
-  h.context_lens = context_lens;
-  h.S = S;
-  h.Hq = Hq;
-  h.Hkv = Hkv;
-  h.D = D;
-  h.block_size = block_size;
-  h.NB = NB;
-  h.scale = scale;
-  h.out = out;
-  h.workspace = workspace;
-  h.workspace_bytes = workspace_bytes;
-  h.num_warps = num_warps;
-  h.dtype = dtype;
-  h.stream = static_cast<cudaStream_t>(stream);
-  return h;
 }
 
 }  // namespace
@@ -954,59 +1175,37 @@ int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t
   return ok();
 }
 
-int pkv_decode_attention_partition(const void* q, const void* k_cache, const void* v_cache,
-                                   const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                   const int32_t* context_lens, int32_t num_seqs,
-                                   int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
-                                   int32_t block_size, int32_t num_blocks, float scale, void* out,
-                                   void* workspace, size_t workspace_bytes, int32_t num_warps,
-                                   int32_t dtype, void* stream) {
-  const HostArgs h = make_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                               context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                               block_size, num_blocks, scale, out, workspace, workspace_bytes,
-                               num_warps, dtype, stream);
-  int W = 0;
-  int rc = validate(h, true, &W);
-  if (rc != PKV_OK) return rc;
-  if (h.S == 0) return ok();
-  rc = dispatch<true>(h, W);
-  return rc == PKV_OK ? ok() : rc;
-}
-
-int pkv_decode_attention_reduce(const int32_t* context_lens, int32_t max_blocks_per_seq,
-                                int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                                int32_t head_dim, int32_t block_size, void* out, void* workspace,
-                                size_t workspace_bytes, int32_t num_warps, int32_t dtype,
-                                void* stream) {
-  const HostArgs h = make_args(nullptr, nullptr, nullptr, nullptr, max_blocks_per_seq,
-                               context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                               block_size, 1, 1.f, out, workspace, workspace_bytes, num_warps,
-                               dtype, stream);
-  int W = 0;
-  int rc = validate(h, false, &W);
-  if (rc != PKV_OK) return rc;
-  if (h.S == 0) return ok();
-  rc = dispatch<false>(h, W);
-  return rc == PKV_OK ? ok() : rc;
-}
-
 int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache,
                          const int32_t* block_tables, int32_t max_blocks_per_seq,
                          const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                          int32_t num_blocks, float scale, void* out, void* workspace,
                          size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
-  const HostArgs h = make_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                               context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
-                               block_size, num_blocks, scale, out, workspace, workspace_bytes,
-                               num_warps, dtype, stream);
+  HostArgs h;
+  h.q = q;
+  h.k_cache = k_cache;
+  h.v_cache = v_cache;
+  h.block_tables = block_tables;
+  h.MAXB = max_blocks_per_seq;
+  h.context_lens = context_lens;
+  h.S = num_seqs;
+  h.Hq = num_q_heads;
+  h.Hkv = num_kv_heads;
+  h.D = head_dim;
+  h.block_size = block_size;
+  h.NB = num_blocks;
+  h.scale = scale;
+  h.out = out;
+  h.workspace = workspace;
+  h.workspace_bytes = workspace_bytes;
+  h.num_warps = num_warps;
+  h.dtype = dtype;
+  h.stream = static_cast<cudaStream_t>(stream);
   int W = 0;
-  int rc = validate(h, true, &W);
+  int rc = validate(h, &W);
   if (rc != PKV_OK) return rc;
   if (h.S == 0) return ok();
-  rc = dispatch<true>(h, W);
-  if (rc != PKV_OK) return rc;
-  rc = dispatch<false>(h, W);
+  rc = dispatch(h, W);
   return rc == PKV_OK ? ok() : rc;
 }
 
@@ -1081,9 +1280,11 @@ extern "C" int pkv_decode_attention_static_scratch(
   void* scratch = nullptr;
   int rc = static_scratch_address(&scratch);
   if (rc != PKV_OK) return rc;
-  // The status word is the only part of the scratch that must start at zero.
+  // The status word and the merge tickets are the parts of the scratch that must
+  // start at zero; the partial states are always written before they are read.
   if (num_seqs > 0)
-    PKV_CUDA(cudaMemsetAsync(scratch, 0, sizeof(int32_t), static_cast<cudaStream_t>(stream)));
+    PKV_CUDA(cudaMemsetAsync(scratch, 0, workspace_layout(num_q_heads / num_kv_heads, head_dim, W).ml,
+                             static_cast<cudaStream_t>(stream)));
   return pkv_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
                               num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
                               num_blocks, scale, out, scratch, PKV_STATIC_SCRATCH_BYTES, W, dtype,

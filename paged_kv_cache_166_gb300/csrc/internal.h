@@ -32,10 +32,10 @@ int cuda_fail(cudaError_t e, const char* what);
 // Number of SMs of the current device (cached per device).
 int device_sm_count(int* sms, int* device);
 
-// Encodes a 2-D TMA map over a cache viewed as [rows, head_dim] with rows of
-// head_dim elements, boxes of [16 rows x box_cols elements], 128-byte swizzle.
+// Encodes a 2-D TMA map over a cache viewed as [rows, cols] (rows contiguous,
+// cols elements each), boxes of [box_rows x box_cols elements], 128-byte swizzle.
 int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t rows,
-                     int32_t head_dim, int32_t box_cols);
+                     int32_t cols, int32_t box_cols, int32_t box_rows);
 
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;

@@ -20,6 +20,9 @@ __global__ void kv_write_kernel(const uint4* __restrict__ k, const uint4* __rest
                                 const int32_t* __restrict__ slots, int64_t total_vecs,
                                 int32_t Hkv, int32_t B, int32_t row_vecs, int64_t num_slots,
                                 uint4* __restrict__ kc, uint4* __restrict__ vc) {
+  // Let a decode-attention launch queued behind this write start its prologue now;
+  // it orders its cache reads after this grid with griddepcontrol.wait.
+  asm volatile("griddepcontrol.launch_dependents;");
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs;
        i += stride) {

@@ -77,10 +77,13 @@ def workspace_bytes(num_q_heads: int, num_kv_heads: int, head_dim: int, dtype: t
     return n.value
 
 
-def get_workspace(device: torch.device, nbytes: int) -> torch.Tensor:
-    """A zero-filled device workspace of at least ``nbytes``, cached per device and
-    stream (one workspace must not serve two launches that may overlap)."""
-    key = (device.index, torch.cuda.current_stream(device).cuda_stream)
+def get_workspace(device: torch.device, group: int, head_dim: int, num_warps: int,
+                  nbytes: int) -> torch.Tensor:
+    """A zero-filled device workspace of ``nbytes`` for one layout (group size,
+    head_dim, warp count), cached per device and stream: one workspace must not
+    serve two launches that may overlap, nor two layouts."""
+    key = (device.index, torch.cuda.current_stream(device).cuda_stream, group, head_dim,
+           num_warps)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
@@ -113,7 +116,7 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     S, Hq, D, NB, Hkv, B, MAXB = _decode_shapes(q, k_cache, v_cache, block_tables,
                                                 context_lens, out)
     need = workspace_bytes(Hq, Hkv, D, q.dtype, num_warps)
-    ws = get_workspace(dev, need) if workspace is None else workspace
+    ws = get_workspace(dev, Hq // Hkv, D, num_warps, need) if workspace is None else workspace
     if ws.numel() * ws.element_size() < need:
         raise ValueError(f"workspace smaller than the {need} bytes needed")
     N.check(N.lib().pkv_decode_attention(
@@ -121,30 +124,6 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
         context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), out.data_ptr(),
         ws.data_ptr(), ws.numel() * ws.element_size(), num_warps, dtype_code(q), _stream(dev)))
     return out
-
-
-def paged_decode_attention_partition(q, k_cache, v_cache, block_tables, context_lens, scale, out,
-                                     workspace, num_warps: int = 0) -> None:
-    """First launch of paged_decode_attention (per-warp runs + partial states)."""
-    dev = _check_cuda(q, k_cache, v_cache, block_tables, context_lens, out)
-    S, Hq, D, NB, Hkv, B, MAXB = _decode_shapes(q, k_cache, v_cache, block_tables,
-                                                context_lens, out)
-    N.check(N.lib().pkv_decode_attention_partition(
-        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(), MAXB,
-        context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), out.data_ptr(),
-        workspace.data_ptr(), workspace.numel() * workspace.element_size(), num_warps,
-        dtype_code(q), _stream(dev)))
-
-
-def paged_decode_attention_reduce(context_lens, max_blocks_per_seq: int, num_kv_heads: int,
-                                  block_size: int, out, workspace, num_warps: int = 0) -> None:
-    """Second launch of paged_decode_attention (log-sum-exp merge of split contexts)."""
-    dev = _check_cuda(context_lens, out, workspace)
-    S, Hq, D = out.shape
-    N.check(N.lib().pkv_decode_attention_reduce(
-        context_lens.data_ptr(), max_blocks_per_seq, S, Hq, num_kv_heads, D, block_size,
-        out.data_ptr(), workspace.data_ptr(), workspace.numel() * workspace.element_size(),
-        num_warps, dtype_code(out), _stream(dev)))
 
 
 def decode_status(workspace: torch.Tensor) -> int:

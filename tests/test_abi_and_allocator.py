@@ -53,7 +53,8 @@ def test_error_codes_and_messages_without_gpu():
     assert lib.pkv_decode_workspace_size(8, 1, 128, 9, 8, ctypes.byref(n)) == N.PKV_ERR_DTYPE
     assert lib.pkv_decode_workspace_size(8, 1, 96, N.PKV_BF16, 8, ctypes.byref(n)) == N.PKV_ERR_UNSUPPORTED
     assert lib.pkv_decode_workspace_size(8, 1, 128, N.PKV_BF16, 8, ctypes.byref(n)) == N.PKV_OK
-    assert n.value == 256 + 2 * 8 * 8 * 2 * 4 + 2 * 8 * 8 * 128 * 4
+    # status word, 8 tickets, m/l and accumulator partials of 2 pieces per warp
+    assert n.value == 256 + 256 + 2 * 8 * 8 * 2 * 4 + 2 * 8 * 8 * 128 * 4
     assert lib.pkv_kv_write(None, None, None, 0, None, None, 4, 2, 16, 100, N.PKV_F16, None) == N.PKV_ERR_INVALID_ARG
 
 

@@ -9,8 +9,8 @@ norm): 1e-5 for fp32, 2e-3 for fp16/bf16.  Covered:
   bench.py times (default warps), every row (13B) or sampled rows;
 * edge cases: empty contexts, lengths 1/15/16/17/31/32/33 and a full table, NaN
   in every unused slot, all group sizes, head dims and dtypes;
-* bit-identity under relabelling of physical blocks, between runs, and between
-  the fused call and its two launches;
+* bit-identity under relabelling of physical blocks and between runs; reuse of
+  one workspace across launches;
 * invalid device data flagged in the status word without a fault.
 """
 import numpy as np
@@ -80,7 +80,11 @@ def test_reduced_workloads_every_row(name, num_warps):
     got = run(b, num_warps)
     check_rows(b, seqs, got, ref)
     dev = torch.device("cuda", torch.cuda.current_device())
-    assert pkv().decode_status(pkv().get_workspace(dev, 1)) == 0
+    m = pkv()
+    ws = m.get_workspace(dev, w.group, w.head_dim, num_warps,
+                         m.workspace_bytes(w.num_q_heads, w.num_kv_heads, w.head_dim, b.q.dtype,
+                                           num_warps))
+    assert m.decode_status(ws) == 0
 
 
 def test_full_mha13b_every_row():
@@ -163,19 +167,28 @@ def test_physical_relabelling_is_bit_identical(name):
     assert torch.equal(out1, out3)          # run to run
 
 
-def test_partition_plus_reduce_equals_fused_call():
+def test_warp_counts_agree_and_workspace_is_reusable():
+    """Different cut points give the same rows within tolerance; a workspace used
+    by one launch serves the next (the merge tickets are left at zero)."""
     w, lens = REDUCED["gqa70b"]
     b = BT.decode_batch(w, lens)
-    fused = run(b, 16)
-    tables, ctx, _ = b.device_index("cuda")
+    ref = BT.oracle_rows(b, list(range(len(lens))))
+    base = run(b, 0)
     m = pkv()
     ws = torch.zeros(m.workspace_bytes(w.num_q_heads, w.num_kv_heads, w.head_dim, b.q.dtype, 16),
                      dtype=torch.uint8, device="cuda")
-    out = torch.full_like(b.q, float("nan"))
-    m.paged_decode_attention_partition(b.q, b.kc, b.vc, tables, ctx, w.scale, out, ws, 16)
-    m.paged_decode_attention_reduce(ctx, tables.shape[1], w.num_kv_heads, 16, out, ws, 16)
+    tables, ctx, _ = b.device_index("cuda")
+    outs = []
+    for _ in range(3):
+        out = torch.full_like(b.q, float("nan"))
+        m.paged_decode_attention(b.q, b.kc, b.vc, tables, ctx, w.scale, out, ws, 16)
+        outs.append(out)
     torch.cuda.synchronize()
-    assert torch.equal(out, fused)
+    assert torch.equal(outs[0], outs[1]) and torch.equal(outs[1], outs[2])
+    check_rows(b, list(range(len(lens))), base, ref)
+    check_rows(b, list(range(len(lens))), outs[0], ref)
+    tickets = ws[256:256 + 4 * 16].view(torch.int32)
+    assert torch.count_nonzero(tickets) == 0
 
 
 def test_invalid_device_data_is_flagged_not_faulted():
@@ -198,6 +211,13 @@ def test_invalid_device_data_is_flagged_not_faulted():
     assert m.decode_status(ws) & 2
     m.paged_decode_attention(b.q, b.kc, b.vc, tables, ctx, w.scale, out, ws)
     assert m.decode_status(ws) == 0
+    # the same workspace under another warp count: flagged (zero-fill first to reuse)
+    big = torch.zeros(m.workspace_bytes(w.num_q_heads, w.num_kv_heads, w.head_dim, b.q.dtype, 12),
+                      dtype=torch.uint8, device="cuda")
+    m.paged_decode_attention(b.q, b.kc, b.vc, tables, ctx, w.scale, out, big, 12)
+    assert m.decode_status(big) == 0
+    m.paged_decode_attention(b.q, b.kc, b.vc, tables, ctx, w.scale, out, big, 8)
+    assert m.decode_status(big) & 8
 
 
 def test_host_side_rejections():

@@ -1,9 +1,11 @@
 """Benchmark of one decode step of the paged KV-cache hot path on GB300.
 
-A step is one pass of the whole hot path over one batch: the cache write of
-every sequence's new token (slots from the library's block manager), then paged
-decode attention over all cached tokens, new token included (one launch; split
-contexts are merged inside it).
+A step is one pass of the whole hot path over one batch, through one call of
+the decode step: the cache write of every sequence's new token (into the slot
+the library's block manager gave its position) and paged decode attention over
+all cached tokens, new token included; split contexts are merged inside the
+attention launch.  The two launches are chained with programmatic dependent
+launch.
 
 Default workload: the 13B-shaped MHA decode batch (64 sequences, 40 query = 40
 KV heads, head_dim 128, fp16, block size 16, lognormal lengths with median 300
@@ -12,11 +14,11 @@ and sigma 1.0 clipped to [1, 2048], pool = blocks + 10% shuffled).
 value     = algorithmic KV-read bytes of decode attention / device step time
             (CUDA events on the launching stream; L2 flushed between steps).
 e2e       = the same bytes / end-to-end step time through the public API with
-            pinned host buffers: H2D of q, new K/V, slots, tables and lengths,
-            the library calls, D2H of the output.
-roofline  = the decode-attention kernel alone (timed in its own loop, L2 flushed):
-            its algorithmic bytes / its event time, against the measured HBM
-            copy bandwidth.
+            pinned host buffers: one H2D copy of the packed q, new K/V, tables and
+            lengths, the decode step, D2H of the output.
+roofline  = the decode-attention kernel, the dominant launch of a step (timed
+            in its own loop, L2 flushed): its algorithmic bytes / its event time,
+            against the measured HBM copy bandwidth.
 cpu_baseline / --impl reference = the fp64 oracle on the host cores.
 
 Under torchrun with N ranks each rank runs an independent replica of the
@@ -102,7 +104,7 @@ class ClockSampler:
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "50"],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.t = threading.Thread(target=self._read, daemon=True)
             self.t.start()
@@ -113,7 +115,10 @@ class ClockSampler:
 
     def _read(self):
         for line in self.proc.stdout:
-            self.lines.append(line.strip())
+            self.lines.append((time.perf_counter(), line.strip()))
+
+    def mark(self, name):
+        setattr(self, name, time.perf_counter())
 
     def __exit__(self, *a):
         if self.proc is not None:
@@ -124,12 +129,15 @@ class ClockSampler:
             except Exception:
                 self.proc.kill()
 
-    def summary(self):
+    def summary(self, t0=None, t1=None):
+        """Median SM clock and throttle reasons of the samples taken in [t0, t1]."""
         if not self.lines:
             return None
         sm, mx, reasons = [], [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for l in self.lines:
+        for t, l in self.lines:
+            if (t0 is not None and t < t0) or (t1 is not None and t > t1):
+                continue
             parts = [p.strip() for p in l.split(",")]
             if len(parts) < 9:
                 continue
@@ -298,12 +306,10 @@ def native(args):
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
     attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B)
-    write_bytes = kv_write_bytes(S, Hkv, D, elt)
 
     def step():
-        pkv.paged_kv_write(dev["k_new"], dev["v_new"], dev["slots"], kc, vc)
-        pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws,
-                                   args.num_warps)
+        pkv.paged_decode_step(dev["q"], dev["k_new"], dev["v_new"], kc, vc, dev["tables"],
+                              dev["ctx"], w.scale, out, ws, args.num_warps)
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -313,49 +319,73 @@ def native(args):
     if pkv.decode_status(ws) != 0:
         raise RuntimeError("device status reported an error during warm-up")
 
-    step_ms = []
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
+    starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
+    ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     with ClockSampler(local) as clocks:
+        # untimed soak of the same step so that the clock samples see this load
+        clocks.mark("t_soak")
+        t_end = time.perf_counter() + args.soak_s
+        while time.perf_counter() < t_end:
+            for _ in range(20):
+                flush.zero_()
+                step()
+            torch.cuda.synchronize()
+        torch.cuda.synchronize()
         t_wall = time.perf_counter()
-        for _ in range(args.steps):
+        for i in range(args.steps):
             flush.zero_()              # L2 flush, outside the timed events
-            e0.record(stream)
+            starts[i].record(stream)
             step()
-            e1.record(stream)
-            e1.synchronize()
-            step_ms.append(e0.elapsed_time(e1))
+            ends[i].record(stream)
         torch.cuda.synchronize()
         wall = time.perf_counter() - t_wall
+        clocks.mark("t_done")
     if world > 1:
         dist.barrier()
+    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
     ms = float(np.mean(step_ms))
 
-    # the dominant kernel alone (decode attention, one launch), for the roofline
-    part_ms = []
-    for i in range(args.warmup + args.steps):
-        flush.zero_()
-        e0.record(stream)
-        pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws,
-                                   args.num_warps)
-        e1.record(stream)
-        e1.synchronize()
-        if i >= args.warmup:
-            part_ms.append(e0.elapsed_time(e1))
-    pms = float(np.mean(part_ms))
+    # the dominant (and only) kernel of a step, alone, for the roofline; and the
+    # attention without the folded cache write, for reference
+    def kernel_ms(fn):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush.zero_()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.mean(ts))
+    pms = kernel_ms(lambda: pkv.paged_decode_attention(
+        dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws, args.num_warps))
 
-    # end to end through the public API with pinned host buffers
+    # end to end through the public API with pinned host buffers: the step's inputs
+    # packed into one pinned buffer, one H2D copy, the decode step, D2H of out
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    h2d = sum(v.numel() * v.element_size() for v in host.values())
+    names = ["q", "k_new", "v_new", "tables", "ctx"]
+    offs, total = {}, 0
+    for k in names:
+        offs[k] = total
+        total += (host[k].numel() * host[k].element_size() + 255) & ~255
+    stage_h = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    stage_d = torch.empty(total, dtype=torch.uint8, device=device)
+    views = {}
+    for k in names:
+        n = host[k].numel() * host[k].element_size()
+        stage_h[offs[k]:offs[k] + n].copy_(host[k].contiguous().view(-1).view(torch.uint8))
+        views[k] = stage_d[offs[k]:offs[k] + n].view(host[k].dtype).view(host[k].shape)
+    h2d = total
     d2h = out.numel() * out.element_size()
 
     def e2e_step():
-        for k in host:
-            dev[k].copy_(host[k], non_blocking=True)
-        pkv.paged_kv_write(dev["k_new"], dev["v_new"], dev["slots"], kc, vc)
-        pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws,
-                                   args.num_warps)
+        stage_d.copy_(stage_h, non_blocking=True)
+        pkv.paged_decode_step(views["q"], views["k_new"], views["v_new"], kc, vc, views["tables"],
+                              views["ctx"], w.scale, out, ws, args.num_warps)
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -407,7 +437,7 @@ def native(args):
                         f"block 16, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks",
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
             "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
-            "step": "paged_kv_write (1 new token/seq) + paged decode attention (one launch)",
+            "step": "paged_decode_step: cache write of 1 new token/seq + decode attention (2 launches, PDL-chained)",
             "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
             "num_warps": args.num_warps or pkv.default_num_warps(D, kc.dtype),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -416,7 +446,7 @@ def native(args):
                         "nominal_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
                         "peak_kind": peak_kind},
         "seq_tokens_per_s": round(int(lens.sum()) * world / (ms * 1e-3), 1),
-        "attention_only": {"kv_gbs": round(part_gbs, 1), "ms": round(pms, 4)},
+        "attention_kernel": {"kv_gbs": round(part_gbs, 1), "ms": round(pms, 4)},
         "roofline": {
             "bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(part_gbs / peak, 4), "traffic": traffic,
@@ -427,8 +457,9 @@ def native(args):
                 "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": 2 * args.steps,
-        "clocks": clocks.summary(),
+        "clocks": clocks.summary(clocks.t_soak, clocks.t_done),
         "wall_s_timed_loop": round(wall, 3),
+        "clocks_window": f"nvidia-smi every 50 ms over a {args.soak_s} s soak of the same step and the timed steps",
     }
     if cpu is not None:
         cs = float(np.median(cpu["seconds"]))
@@ -477,12 +508,15 @@ def reference(args):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--steps", type=int, default=500)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["native", "reference"], default="native")
     ap.add_argument("--workload", default="mha13b",
                     choices=["tiny", "mha13b", "gqa70b", "prefix", "longctx"])
     ap.add_argument("--num-warps", type=int, default=0)
+    ap.add_argument("--soak-s", type=float, default=0.6,
+                    help="seconds of untimed steps run just before the timed ones, so that the "
+                         "clock samples cover this load")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
     ap.add_argument("--ref-budget", type=float, default=5.0)
     ap.add_argument("--no-cpu-baseline", action="store_true")

@@ -172,6 +172,30 @@ int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache
                          size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream);
 
 /*
+ * pkv_decode_step — one decode step: the cache write of each sequence's new token,
+ * then pkv_decode_attention, from one call.
+ *
+ * Same arguments as pkv_decode_attention plus k_new, v_new (device [num_seqs,
+ * num_kv_heads, head_dim], contiguous, 16-byte aligned).  For every sequence s with
+ * t = context_lens[s] > 0 the new token is position t - 1 ("each decode step ->
+ * write the new token's K,V into the last block", "PagedAttention and vLLM: Virtual
+ * Memory for the KV Cache", section "L2 — Mechanism"): its K and V rows are written
+ * to slot(t - 1) of the caches, the slot read from block_tables, exactly as
+ * pkv_kv_write with that slot would; then the attention of the step runs over the
+ * updated caches.  The two launches are chained with programmatic dependent launch,
+ * so the attention's prologue overlaps the write.  Output and caches are
+ * bit-identical to pkv_kv_write followed by pkv_decode_attention with the same
+ * num_warps.  Arguments are validated before anything is written.
+ * Errors: as pkv_decode_attention.
+ */
+int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int32_t num_blocks, float scale, void* out, void* workspace,
+                    size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream);
+
+/*
  * pkv_decode_status — read and clear the device status word of a workspace.
  * Synchronises `stream`, copies the word to *status (PKV_DEV_* bits, 0 = clean)
  * and zeroes it on the device.

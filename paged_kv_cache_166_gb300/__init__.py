@@ -4,6 +4,8 @@ Public API (all device work runs in libpkv.so's sm_103a kernels):
 
 * ``paged_kv_write(k, v, slot_mapping, k_cache, v_cache)``
 * ``paged_decode_attention(q, k_cache, v_cache, block_tables, context_lens, scale, out)``
+* ``paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out)``
+  — the cache write of each sequence's new token, then the attention, from one call
 * ``paged_copy_blocks(k_cache, v_cache, src_dst_pairs)``
 * ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free)
 
@@ -16,7 +18,8 @@ from ._native import OutOfBlocks, PkvError  # noqa: F401
 def __getattr__(name):
     # torch-facing ops are imported lazily so that host-only users (the block
     # manager, the workload generators) do not need torch's CUDA runtime.
-    if name in ("paged_kv_write", "paged_decode_attention", "paged_copy_blocks",
+    if name in ("paged_kv_write", "paged_decode_attention", "paged_decode_step",
+                "paged_copy_blocks",
                 "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
         from . import ops
         return getattr(ops, name)

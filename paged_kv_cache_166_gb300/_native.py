@@ -42,6 +42,8 @@ SIGNATURES = {
     "pkv_decode_workspace_size": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "pkv_decode_attention": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,
                                             _i32, _f, _p, _p, _sz, _i32, _i32, _p]),
+    "pkv_decode_step": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32,
+                                       _i32, _i32, _f, _p, _p, _sz, _i32, _i32, _p]),
     "pkv_decode_status": (ctypes.c_int, [_p, _pi32, _p]),
     "pkv_decode_default_warps": (ctypes.c_int, [_i32, _i32, _pi32]),
     "pkv_decode_attention_static_scratch": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _i32, _i32,

@@ -70,6 +70,12 @@ namespace pkv {
 #ifndef PKV_SINGLE_BOX
 #define PKV_SINGLE_BOX 0
 #endif
+#ifndef PKV_PREFETCH_TABLES
+#define PKV_PREFETCH_TABLES 1
+#endif
+#ifndef PKV_PARALLEL_PROLOGUE
+#define PKV_PARALLEL_PROLOGUE 1
+#endif
 // Start-up cost of a (sequence, KV head) unit in quarter steps, for group sizes
 // below 4 and from 4 up (query copy, finalise, output write).
 #ifndef PKV_UNIT_COST_SMALL_G
@@ -695,6 +701,21 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   if (threadIdx.x == 0) {
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+    // The block tables are read a window at a time once the schedule is known:
+    // start pulling this CTA's slice of them into L2 now (16-byte aligned interior).
+    if (PKV_PREFETCH_TABLES) {
+      const uintptr_t t0 = reinterpret_cast<uintptr_t>(a.block_tables);
+      const uintptr_t t1 = t0 + static_cast<uintptr_t>(a.S) * a.MAXB * sizeof(int32_t);
+      const uintptr_t lo = (t0 + 15) & ~uintptr_t(15), hi = t1 & ~uintptr_t(15);
+      if (hi > lo) {
+        const uintptr_t slice = ((hi - lo) / gridDim.x + 16) & ~uintptr_t(15);
+        const uintptr_t b0 = lo + slice * blockIdx.x;
+        if (b0 < hi) {
+          const uintptr_t b1 = b0 + slice < hi ? b0 + slice : hi;
+          ptx::prefetch_l2(reinterpret_cast<const void*>(b0), static_cast<uint32_t>(b1 - b0));
+        }
+      }
+    }
     if (blockIdx.x == 0) {
       // Words 1..3 of the status area record the layout (warps, group, head_dim)
       // of the last launch; a workspace reused under another layout holds stale
@@ -822,8 +843,46 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     advance(pc, pre, S, Hkv);
   };
 
+  // Fill the ring: lanes 0..NS-1 issue the first NS steps at once, one step each.
   const int prologue = nsteps < NS ? nsteps : NS;
-  for (int m = 0; m < prologue; ++m) issue(m);
+  if (!PKV_PARALLEL_PROLOGUE) {
+    for (int m = 0; m < prologue; ++m) issue(m);
+  } else if (lane < prologue) {
+    const Cursor lc = cursor_at(pre, S, Hkv, f0 + lane);
+    const int id = ids[lane];
+    const bool need_q = (lane == 0) || (lc.j == 0);
+    const uint32_t bar = bars + 8 * lane;
+    ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
+    int32_t y;
+    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(a.NB)) {
+      y = (id * Hkv + lc.g) * kTok;
+    } else {
+      atomicOr(a.status, PKV_DEV_BAD_BLOCK_ID);
+      y = rows_total;
+    }
+    const uint32_t kt = tiles + lane * Sh::kStageBytes;
+    const uint32_t vt = kt + Sh::kTileBytes;
+    if constexpr (Sh::kSingleBox) {
+      ptx::tma_load_2d(kt, &kmap, 0, y * Sh::kSub, bar, policy);
+      ptx::tma_load_2d(vt, &vmap, 0, y * Sh::kSub, bar, policy);
+    } else {
+#pragma unroll
+      for (int c = 0; c < Sh::kSub; ++c)
+        ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
+#pragma unroll
+      for (int c = 0; c < Sh::kSub; ++c)
+        ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
+    }
+    if (need_q) {
+      const char* src = qbase + (static_cast<int64_t>(lc.s) * a.Hq + lc.g * a.G) * D * Sh::kElt;
+      ptx::bulk_load(qslot_s + lane * a.q_stride, src, a.q_bytes, bar);
+    }
+  }
+  if (PKV_PARALLEL_PROLOGUE) {
+    __syncwarp();
+    p_stage = prologue == NS ? 0 : prologue;
+    if (prologue > 0) pc = cursor_at(pre, S, Hkv, min(f0 + prologue, total - 1));
+  }
 
   using State = typename std::conditional<sizeof(T) == 2, MmaState<T, D>, FmaState<D>>::type;
   State st_;
@@ -1052,6 +1111,7 @@ int validate(const HostArgs& h, int* warps_out) {
   PKV_REQUIRE(aligned(h.q, 16) && aligned(h.k_cache, 16) && aligned(h.v_cache, 16) &&
                   aligned(h.out, 16) && aligned(h.block_tables, 4),
               PKV_ERR_INVALID_ARG, "q, caches and out must be 16-byte aligned");
+
   return PKV_OK;
 }
 
@@ -1175,12 +1235,13 @@ int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t
   return ok();
 }
 
-int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache,
-                         const int32_t* block_tables, int32_t max_blocks_per_seq,
-                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
-                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
-                         int32_t num_blocks, float scale, void* out, void* workspace,
-                         size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
+namespace {
+int decode_entry(const void* q, const void* k_cache, const void* v_cache,
+                 const int32_t* block_tables, int32_t max_blocks_per_seq,
+                 const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                 float scale, void* out, void* workspace, size_t workspace_bytes,
+                 int32_t num_warps, int32_t dtype, void* stream) {
   HostArgs h;
   h.q = q;
   h.k_cache = k_cache;
@@ -1205,6 +1266,57 @@ int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache
   int rc = validate(h, &W);
   if (rc != PKV_OK) return rc;
   if (h.S == 0) return ok();
+  rc = dispatch(h, W);
+  return rc == PKV_OK ? ok() : rc;
+}
+}  // namespace
+
+int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, float scale, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
+  return decode_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                      scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
+}
+
+int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                    void* v_cache, const int32_t* block_tables, int32_t max_blocks_per_seq,
+                    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                    int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                    int32_t num_blocks, float scale, void* out, void* workspace,
+                    size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
+  // Validate the attention arguments first, so that a refused call writes nothing.
+  HostArgs h;
+  h.q = q;
+  h.k_cache = k_cache;
+  h.v_cache = v_cache;
+  h.block_tables = block_tables;
+  h.MAXB = max_blocks_per_seq;
+  h.context_lens = context_lens;
+  h.S = num_seqs;
+  h.Hq = num_q_heads;
+  h.Hkv = num_kv_heads;
+  h.D = head_dim;
+  h.block_size = block_size;
+  h.NB = num_blocks;
+  h.scale = scale;
+  h.out = out;
+  h.workspace = workspace;
+  h.workspace_bytes = workspace_bytes;
+  h.num_warps = num_warps;
+  h.dtype = dtype;
+  h.stream = static_cast<cudaStream_t>(stream);
+  int W = 0;
+  int rc = validate(h, &W);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs == 0) return ok();
+  rc = launch_decode_append(k_new, v_new, block_tables, max_blocks_per_seq, context_lens,
+                            num_seqs, k_cache, v_cache, num_blocks, num_kv_heads, block_size,
+                            head_dim, dtype, stream);
+  if (rc != PKV_OK) return rc;
   rc = dispatch(h, W);
   return rc == PKV_OK ? ok() : rc;
 }

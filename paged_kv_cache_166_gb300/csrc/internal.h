@@ -37,6 +37,13 @@ int device_sm_count(int* sms, int* device);
 int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t rows,
                      int32_t cols, int32_t box_cols, int32_t box_rows);
 
+// Launches the decode-step cache write: for every sequence s with t = ctx[s] > 0,
+// the rows k_new[s], v_new[s] go to slot(t - 1) of its block table (kv_ops.cu).
+int launch_decode_append(const void* k_new, const void* v_new, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                         void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                         int32_t block_size, int32_t head_dim, int32_t dtype, void* stream);
+
 inline bool aligned(const void* p, uintptr_t a) {
   return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0;
 }

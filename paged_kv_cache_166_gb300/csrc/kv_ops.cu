@@ -58,6 +58,34 @@ __global__ void copy_blocks_kernel(uint4* __restrict__ kc, uint4* __restrict__ v
   }
 }
 
+// Decode-step cache write: sequence s's new token is its position t - 1, t = ctx[s];
+// its slot comes from the block table, slot = table[s][(t-1) / B] * B + (t-1) % B
+// ("What is paged attention?", section "How it works"), and its rows of every KV
+// head are copied there.  Sequences with t <= 0 or t > max_blocks * B, and slots
+// outside the pool, write nothing.
+__global__ void decode_append_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v,
+                                     const int32_t* __restrict__ tables, int32_t MAXB,
+                                     const int32_t* __restrict__ ctx, int64_t total_vecs,
+                                     int32_t Hkv, int32_t B, int32_t row_vecs, int32_t NB,
+                                     uint4* __restrict__ kc, uint4* __restrict__ vc) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs;
+       i += stride) {
+    const int64_t th = i / row_vecs;
+    const int32_t c = static_cast<int32_t>(i - th * row_vecs);
+    const int64_t s = th / Hkv;
+    const int32_t h = static_cast<int32_t>(th - s * Hkv);
+    const int32_t t = __ldg(ctx + s);
+    if (t <= 0 || t > MAXB * B) continue;
+    const int32_t b = __ldg(tables + s * MAXB + (t - 1) / B);
+    if (b < 0 || b >= NB) continue;
+    const int64_t dst = ((static_cast<int64_t>(b) * Hkv + h) * B + (t - 1) % B) * row_vecs + c;
+    kc[dst] = __ldg(k + i);
+    vc[dst] = __ldg(v + i);
+  }
+}
+
 int grid_for(int64_t work, int threads) {
   int sms = 0, dev = 0;
   if (device_sm_count(&sms, &dev) != PKV_OK) sms = 132;
@@ -67,6 +95,29 @@ int grid_for(int64_t work, int threads) {
 }
 
 }  // namespace
+
+int launch_decode_append(const void* k_new, const void* v_new, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                         void* k_cache, void* v_cache, int32_t num_blocks, int32_t num_kv_heads,
+                         int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
+  const int elt = element_bytes(dtype);
+  PKV_REQUIRE(elt != 0, PKV_ERR_DTYPE, "unknown dtype %d", dtype);
+  PKV_REQUIRE(k_new && v_new, PKV_ERR_INVALID_ARG, "NULL k_new / v_new");
+  PKV_REQUIRE(aligned(k_new, 16) && aligned(v_new, 16), PKV_ERR_INVALID_ARG,
+              "k_new and v_new must be 16-byte aligned");
+  PKV_REQUIRE((static_cast<int64_t>(head_dim) * elt) % 16 == 0, PKV_ERR_INVALID_ARG,
+              "head_dim * element size must be a multiple of 16 bytes");
+  const int32_t row_vecs = static_cast<int32_t>(static_cast<int64_t>(head_dim) * elt / 16);
+  const int64_t total = static_cast<int64_t>(num_seqs) * num_kv_heads * row_vecs;
+  const int threads = 256;
+  decode_append_kernel<<<grid_for(total, threads), threads, 0, static_cast<cudaStream_t>(stream)>>>(
+      static_cast<const uint4*>(k_new), static_cast<const uint4*>(v_new), block_tables,
+      max_blocks_per_seq, context_lens, total, num_kv_heads, block_size, row_vecs, num_blocks,
+      static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
+  PKV_CUDA(cudaGetLastError());
+  return PKV_OK;
+}
+
 }  // namespace pkv
 
 using namespace pkv;

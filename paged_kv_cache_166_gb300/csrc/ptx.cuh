@@ -82,6 +82,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       : "memory");
 }
 
+// Bulk prefetch of global memory into L2 (16-byte aligned, size a multiple of 16).
+__device__ __forceinline__ void prefetch_l2(const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src), "r"(bytes) : "memory");
+}
+
 // L2 policy: lines of this access are the first evicted (read-once stream).
 __device__ __forceinline__ uint64_t policy_evict_first() {
   uint64_t p;

@@ -126,6 +126,32 @@ def paged_decode_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torc
     return out
 
 
+def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                      k_cache: torch.Tensor, v_cache: torch.Tensor, block_tables: torch.Tensor,
+                      context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                      workspace: Optional[torch.Tensor] = None, num_warps: int = 0) -> torch.Tensor:
+    """One decode step: write each sequence's new token (k_new, v_new [S, Hkv, D],
+    position context_lens[s] - 1, slot from the block table) into the caches, then
+    attend over them (two launches chained with programmatic dependent launch)."""
+    dev = _check_cuda(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, out)
+    S, Hq, D, NB, Hkv, B, MAXB = _decode_shapes(q, k_cache, v_cache, block_tables,
+                                                context_lens, out)
+    if k_new.shape != (S, Hkv, D) or v_new.shape != (S, Hkv, D):
+        raise ValueError("k_new and v_new must be [S, Hkv, D]")
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise TypeError("k_new and v_new must share the dtype of q")
+    need = workspace_bytes(Hq, Hkv, D, q.dtype, num_warps)
+    ws = get_workspace(dev, Hq // Hkv, D, num_warps, need) if workspace is None else workspace
+    if ws.numel() * ws.element_size() < need:
+        raise ValueError(f"workspace smaller than the {need} bytes needed")
+    N.check(N.lib().pkv_decode_step(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(),
+        block_tables.data_ptr(), MAXB, context_lens.data_ptr(), S, Hq, Hkv, D, B, NB,
+        float(scale), out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), num_warps,
+        dtype_code(q), _stream(dev)))
+    return out
+
+
 def decode_status(workspace: torch.Tensor) -> int:
     """Reads and clears the device status bits the decode kernels recorded."""
     v = ctypes.c_int32(0)

@@ -11,7 +11,9 @@ norm): 1e-5 for fp32, 2e-3 for fp16/bf16.  Covered:
   in every unused slot, all group sizes, head dims and dtypes;
 * bit-identity under relabelling of physical blocks and between runs; reuse of
   one workspace across launches;
-* invalid device data flagged in the status word without a fault.
+* invalid device data flagged in the status word without a fault;
+* the decode step with the cache write folded in: bit-identical to the write
+  followed by the attention (output and caches), and against the oracle.
 """
 import numpy as np
 import pytest
@@ -235,3 +237,57 @@ def test_host_side_rejections():
     q4 = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(m.PkvError):          # block size 8 is not supported by the kernels
         m.paged_decode_attention(q4, kc8, kc8, t, c, 0.1, torch.empty_like(q4))
+
+
+# ---- the decode step with the cache write folded into the attention launch ----
+
+def run_step(b: BT.Batch, num_warps=0):
+    tables, ctx, _ = b.device_index("cuda")
+    out = torch.full_like(b.q, float("nan"))
+    pkv().paged_decode_step(b.q, b.k_new, b.v_new, b.kc, b.vc, tables, ctx, b.w.scale, out,
+                            num_warps=num_warps)
+    torch.cuda.synchronize()
+    return out
+
+
+def clone_caches(b: BT.Batch) -> BT.Batch:
+    import dataclasses
+    return dataclasses.replace(b, kc=b.kc.clone(), vc=b.vc.clone())
+
+
+@pytest.mark.parametrize("name", list(REDUCED))
+@pytest.mark.parametrize("num_warps", [0, 3, 61])
+def test_decode_step_equals_write_then_attend(name, num_warps):
+    """Fused step: same output bits and same cache bits as the two launches."""
+    w, lens = REDUCED[name]
+    b = BT.decode_batch(w, lens)
+    b2 = clone_caches(b)
+    fused = run_step(b, num_warps)
+    separate = run(b2, num_warps)
+    assert torch.equal(fused, separate)
+    assert torch.equal(b.kc.view(torch.int16 if b.kc.element_size() == 2 else torch.int32),
+                       b2.kc.view(torch.int16 if b2.kc.element_size() == 2 else torch.int32))
+    assert torch.equal(b.vc.view(torch.int16 if b.vc.element_size() == 2 else torch.int32),
+                       b2.vc.view(torch.int16 if b2.vc.element_size() == 2 else torch.int32))
+
+
+@pytest.mark.parametrize("dtype,D,G", [("bf16", 128, 8), ("f16", 64, 1), ("f32", 64, 2),
+                                       ("bf16", 256, 4)])
+def test_decode_step_edge_lengths_against_oracle(dtype, D, G):
+    import dataclasses
+    w = dataclasses.replace(W.WORKLOADS["tiny"], dtype=dtype, head_dim=D, num_kv_heads=3,
+                            num_q_heads=3 * G, fixed_pool_blocks=0, seed=23)
+    lens = np.array([0, 1, 15, 16, 17, 31, 32, 33, 0, 160, 2])
+    b = BT.decode_batch(w, lens)
+    seqs = list(range(len(lens)))
+    ref = BT.oracle_rows(b, seqs)
+    got = run_step(b, 2)
+    check_rows(b, seqs, got, ref)
+    assert torch.all(got[torch.from_numpy(lens == 0).cuda()] == 0)
+
+
+def test_decode_step_full_mha13b_every_row():
+    b = BT.decode_batch(W.WORKLOADS["mha13b"])
+    seqs = list(range(len(b.lens)))
+    ref = BT.oracle_rows(b, seqs)
+    check_rows(b, seqs, run_step(b), ref)

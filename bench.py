@@ -72,6 +72,24 @@ def measured_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(values, device=None):
+    """Element-wise maximum of `values` over all ranks of the default process
+    group (the values themselves without one)."""
+    import torch
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t.cpu()]
+
+
+def whole_job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
+    """Throughput of the whole job: every rank moves bytes_per_rank in its step,
+    the job's step lasts as long as its slowest rank (ms)."""
+    return bytes_per_rank * world / (ms * 1e-3) / 1e9
+
+
 def profile_traffic(kernel_tag: str):
     """Per-launch DRAM bytes from the committed ncu summary of this kernel, if the
     kernel source is unchanged since it was captured."""
@@ -405,18 +423,14 @@ def native(args):
     if status:
         raise RuntimeError(f"device status {status} after the timed steps")
 
-    if world > 1:
-        t = torch.tensor([ms, e2e], dtype=torch.float64, device=device)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms, e2e = float(t[0]), float(t[1])
+    ms, e2e = max_over_ranks([ms, e2e], device)
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
     peak, peak_kind = measured_peak()
-    total_bytes = attn_bytes * world
-    gbs = total_bytes / (ms * 1e-3) / 1e9
+    gbs = whole_job_gbs(attn_bytes, world, ms)
     part_gbs = attn_bytes / (pms * 1e-3) / 1e9
     traffic = profile_traffic(f"decode_attention_{args.workload}")
     line = {
@@ -453,7 +467,7 @@ def native(args):
             "kernel": "decode_attention_kernel", "bytes_per_launch": attn_bytes,
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         },
-        "e2e": {"value": round(total_bytes / (e2e * 1e-3) / 1e9, 1), "unit": "GB/s",
+        "e2e": {"value": round(whole_job_gbs(attn_bytes, world, e2e), 1), "unit": "GB/s",
                 "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": int(h2d),
                 "d2h_bytes_per_step": int(d2h)},
         "gpu_launches": 2 * args.steps,

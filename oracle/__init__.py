@@ -21,6 +21,10 @@ written from the pages that describe PagedAttention:
   "The OS-Inspired Insight" and "Walking Through the Lifecycle").
 * ``kv_bytes``         — the KV-cache size formula and block arithmetic
   ("PagedAttention and vLLM: Virtual Memory for the KV Cache", summary FAQ).
+* ``fp8``              — the fp8 (E4M3) quantised KV cache: code table, the
+  quantising cache write and attention over the dequantised values
+  ("PagedAttention — how vLLM stopped wasting 80%...", FAQ "How does this
+  relate to quantization?").
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against values the
 pages print, library routines on special cases, closed forms and invariants.

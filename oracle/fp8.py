@@ -19,10 +19,14 @@ bytes per element").  They fix no format.  The reading taken here:
   +-448 beyond the range; NaN gives the code 0x7F;
 * it reads back as ``decode(code) * scale``.
 
-Layouts: the K cache keeps ``[num_blocks, num_kv_heads, B, head_dim]``; the V
-cache stores each (block, KV head) tile transposed, ``[num_blocks, num_kv_heads,
-head_dim, B]``.  Attention over the fp8 cache is the fp64 decode attention
-(the definition ``paged_attention`` follows) over the dequantised values.
+Layouts (block size 16): the K cache keeps ``[num_blocks, num_kv_heads, 16,
+head_dim]``; the V cache stores each (block, KV head) tile transposed,
+``[num_blocks, num_kv_heads, head_dim, 16]``, and inside each 16-byte head_dim
+row token ``t`` sits at byte ``V_POS[t]`` — the order ``0 1 8 9 2 3 10 11 4 5
+12 13 6 7 14 15`` (byte ``j`` holds token ``V_TOKEN[j]``), which a tensor-core
+kernel reads in the token pairs of its score fragments.  Attention over the fp8
+cache is the fp64 decode attention (the definition ``paged_attention`` follows)
+over the dequantised values.
 """
 from __future__ import annotations
 
@@ -30,6 +34,10 @@ import numpy as np
 
 MAX_FINITE = 448.0
 NAN_CODE = 0x7F
+BLOCK = 16
+# byte j of a V head_dim row holds token V_TOKEN[j]; token t sits at byte V_POS[t]
+V_TOKEN = np.array([0, 1, 8, 9, 2, 3, 10, 11, 4, 5, 12, 13, 6, 7, 14, 15])
+V_POS = np.argsort(V_TOKEN)
 
 
 def decode(codes) -> np.ndarray:
@@ -73,10 +81,11 @@ def quantize(x, scale) -> np.ndarray:
 def kv_write_fp8(k, v, slot_mapping, k_scale, v_scale, k_cache: np.ndarray,
                  v_cache: np.ndarray) -> None:
     """Quantise and scatter ``k, v [T, Hkv, D]`` into the fp8 caches in place:
-    ``K8[s // B, h, s % B, :] = quantize(k[i, h, :], k_scale[h])`` and
-    ``V8[s // B, h, :, s % B] = quantize(v[i, h, :], v_scale[h])`` (V tiles are
-    stored transposed); negative slots are padding and skipped."""
+    ``K8[s // 16, h, s % 16, :] = quantize(k[i, h, :], k_scale[h])`` and
+    ``V8[s // 16, h, :, V_POS[s % 16]] = quantize(v[i, h, :], v_scale[h])``;
+    negative slots are padding and skipped."""
     B = k_cache.shape[2]
+    assert B == BLOCK and v_cache.shape[3] == BLOCK
     ks = np.asarray(k_scale, dtype=np.float32)[:, None]
     vs = np.asarray(v_scale, dtype=np.float32)[:, None]
     k32 = np.asarray(k, dtype=np.float32)
@@ -85,7 +94,7 @@ def kv_write_fp8(k, v, slot_mapping, k_scale, v_scale, k_cache: np.ndarray,
         if s < 0:
             continue
         k_cache[s // B, :, s % B, :] = quantize(k32[i], ks)
-        v_cache[s // B, :, :, s % B] = quantize(v32[i], vs)
+        v_cache[s // B, :, :, V_POS[s % B]] = quantize(v32[i], vs)
 
 
 def gather_fp8(k_cache, v_cache, k_scale, v_scale, block_table_row, t: int, kv_head: int):
@@ -98,7 +107,7 @@ def gather_fp8(k_cache, v_cache, k_scale, v_scale, block_table_row, t: int, kv_h
     ks = np.float64(np.float32(k_scale[kv_head]))
     vs = np.float64(np.float32(v_scale[kv_head]))
     k = decode(np.asarray(k_cache)[phys, kv_head, off, :]) * ks
-    v = decode(np.asarray(v_cache)[phys, kv_head, :, off]) * vs
+    v = decode(np.asarray(v_cache)[phys, kv_head, :, V_POS[off]]) * vs
     return k, v
 
 

@@ -19,7 +19,8 @@ fp32 scale per KV head, round to nearest even, saturating.
   scales), attention over the fp8 pool equals torch's fp64 SDPA on the
   contiguous values; dequantisation error stays within half a code step.
 * Layout: a written token lands at [block, head, offset, :] in K and at
-  [block, head, :, offset] in V; padding slots are skipped.
+  [block, head, :, byte of offset] in V (the byte order is a permutation of
+  the 16 tokens); padding slots are skipped.
 """
 import numpy as np
 import pytest
@@ -95,17 +96,24 @@ def test_quantize_error_within_half_a_step():
     assert np.all(np.abs(back - x) <= bound * (1 + 1e-12))
 
 
-def test_write_layout_and_padding():
-    NB, Hkv, B, D = 4, 2, 4, 8
+def test_v_byte_order_is_a_permutation():
+    assert sorted(fp8.V_TOKEN.tolist()) == list(range(16))
+    assert np.array_equal(fp8.V_TOKEN[fp8.V_POS], np.arange(16))
+
+
+@pytest.mark.parametrize("slot", [0, 9, 18, 31])
+def test_write_layout_and_padding(slot):
+    NB, Hkv, B, D = 3, 2, 16, 8
     kc = np.zeros((NB, Hkv, B, D), np.uint8)
     vc = np.zeros((NB, Hkv, D, B), np.uint8)
     k = np.full((2, Hkv, D), 1.0, np.float32)
     v = np.full((2, Hkv, D), 2.0, np.float32)
     k[1] = -1.0
-    fp8.kv_write_fp8(k, v, [9, -1], [1.0, 0.5], [1.0, 4.0], kc, vc)
-    blk, off = 9 // B, 9 % B
+    fp8.kv_write_fp8(k, v, [slot, -1], [1.0, 0.5], [1.0, 4.0], kc, vc)
+    blk, off = slot // B, slot % B
     assert np.all(kc[blk, 0, off] == 0x38) and np.all(kc[blk, 1, off] == 0x40)  # 1.0, 2.0
-    assert np.all(vc[blk, 0, :, off] == 0x40) and np.all(vc[blk, 1, :, off] == 0x30)  # 2.0, 0.5
+    byte = int(fp8.V_POS[off])
+    assert np.all(vc[blk, 0, :, byte] == 0x40) and np.all(vc[blk, 1, :, byte] == 0x30)  # 2.0, 0.5
     assert np.count_nonzero(kc) == Hkv * D and np.count_nonzero(vc) == Hkv * D
 
 
@@ -125,9 +133,11 @@ def test_attention_on_representable_values_matches_sdpa(Hq, Hkv, D, lens):
     kf, vf, tables = _paged_pool(5, Ks, Vs, B)
     kf = np.nan_to_num(kf)
     vf = np.nan_to_num(vf)
-    # quantise the pool (the values are exactly representable), V tiles transposed
+    # quantise the pool (the values are exactly representable); V tiles transposed,
+    # tokens in the V byte order
     k8 = fp8.quantize(kf, k_scale[None, :, None, None])
-    v8 = np.ascontiguousarray(np.swapaxes(fp8.quantize(vf, v_scale[None, :, None, None]), 2, 3))
+    vt = np.swapaxes(fp8.quantize(vf, v_scale[None, :, None, None]), 2, 3)
+    v8 = np.ascontiguousarray(vt[..., fp8.V_TOKEN])
     scale = float(np.float32(1 / np.sqrt(D)))
     got = fp8.paged_attention_fp8(q, k8, v8, k_scale, v_scale, tables, np.array(lens), scale)
     ref = _sdpa(q, Ks, Vs, scale, Hq // Hkv)

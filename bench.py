@@ -49,13 +49,15 @@ FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
-def attention_bytes(lens, Hq, Hkv, D, elt, B=16) -> int:
+def attention_bytes(lens, Hq, Hkv, D, elt, B=16, q_elt=None) -> int:
     """Algorithmic bytes decode attention must move: K and V rows of the cached
-    tokens (no padded block tails), the int32 table entries, the context length,
-    one query and one output row per query head."""
+    tokens (no padded block tails, `elt` bytes per element), the int32 table
+    entries, the context length, one query and one output row per query head
+    (`q_elt` bytes per element, default `elt`)."""
     lens = np.asarray(lens, dtype=np.int64)
     nb = (lens + B - 1) // B
-    return int((2 * lens * Hkv * D * elt + 4 * nb + 4 + 2 * Hq * D * elt).sum())
+    q_elt = elt if q_elt is None else q_elt
+    return int((2 * lens * Hkv * D * elt + 4 * nb + 4 + 2 * Hq * D * q_elt).sum())
 
 
 def kv_write_bytes(num_tokens, Hkv, D, elt) -> int:
@@ -176,7 +178,7 @@ class ClockSampler:
 # --------------------------------------------------------------------------------------
 # workload construction through the library (block manager -> tables, slots)
 # --------------------------------------------------------------------------------------
-def build_batch(name: str, device, rank: int = 0):
+def build_batch(name: str, device, rank: int = 0, kv: str = "native"):
     import torch
     from paged_kv_cache_166_gb300 import BlockAllocator
     from paged_kv_cache_166_gb300 import workloads as W
@@ -199,10 +201,18 @@ def build_batch(name: str, device, rank: int = 0):
     tables, ctx = alloc.export_tables(sids, maxb)
     dt = W.torch_dtype(w.dtype)
     S, Hq, Hkv, D = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim
-    kc = torch.empty((NB, Hkv, B, D), dtype=dt, device=device)
-    vc = torch.empty_like(kc)
-    W.fill_normal_(kc, seed, W.STREAM_K_POOL)
-    W.fill_normal_(vc, seed, W.STREAM_V_POOL)
+    if kv == "fp8":
+        # E4M3 codes of N(0,1) draws with per-KV-head scales; V tiles transposed
+        kc = torch.empty((NB, Hkv, B, D), dtype=torch.uint8, device=device)
+        vc = torch.empty((NB, Hkv, D, B), dtype=torch.uint8, device=device)
+        k_scale, v_scale = W.fp8_scales(Hkv, seed), W.fp8_scales(Hkv, seed + 1)
+        W.fill_fp8_codes_(kc, k_scale, seed, W.STREAM_K_POOL)
+        W.fill_fp8_codes_(vc, v_scale, seed, W.STREAM_V_POOL)
+    else:
+        kc = torch.empty((NB, Hkv, B, D), dtype=dt, device=device)
+        vc = torch.empty_like(kc)
+        W.fill_normal_(kc, seed, W.STREAM_K_POOL)
+        W.fill_normal_(vc, seed, W.STREAM_V_POOL)
     host = {
         "q": W.normal_tensor((S, Hq, D), w.dtype, seed, W.STREAM_Q, "cpu"),
         "k_new": W.normal_tensor((S, Hkv, D), w.dtype, seed, W.STREAM_K_NEW, "cpu"),
@@ -213,6 +223,9 @@ def build_batch(name: str, device, rank: int = 0):
     }
     host = {k: v.pin_memory() for k, v in host.items()}
     dev = {k: v.to(device) for k, v in host.items()}
+    if kv == "fp8":
+        dev["k_scale"] = torch.from_numpy(k_scale).to(device)
+        dev["v_scale"] = torch.from_numpy(v_scale).to(device)
     return w, lens, NB, kc, vc, host, dev
 
 
@@ -307,27 +320,46 @@ def native(args):
     device = torch.device("cuda", local)
 
     # the oracle pool is spawned before the first GPU call of this process
-    cpu = time_oracle(args.workload, budget_s=args.cpu_budget) if (rank == 0 and world == 1 and
-                                                                     not args.no_cpu_baseline) else None
+    cpu = time_oracle(args.workload, budget_s=args.cpu_budget) if (
+        rank == 0 and world == 1 and not args.no_cpu_baseline and args.kv == "native") else None
 
     import __graft_entry__
     __graft_entry__.build()
     import paged_kv_cache_166_gb300 as pkv
 
-    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, rank)
+    fp8 = args.kv == "fp8"
+    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, rank, args.kv)
     S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     elt = kc.element_size()
+    q_elt = dev["q"].element_size()
     MAXB = dev["tables"].shape[1]
     out = torch.empty_like(dev["q"])
-    ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, kc.dtype, args.num_warps), dtype=torch.uint8,
-                     device=device)
+    ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, "fp8" if fp8 else dev["q"].dtype,
+                                         args.num_warps),
+                     dtype=torch.uint8, device=device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
     stream = torch.cuda.current_stream(device)
-    attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B)
+    attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B, q_elt)
+
+    def decode_step(q, k_new, v_new, tables, ctx):
+        if fp8:
+            pkv.paged_decode_step_fp8(q, k_new, v_new, kc, vc, dev["k_scale"], dev["v_scale"],
+                                      tables, ctx, w.scale, out, ws, args.num_warps)
+        else:
+            pkv.paged_decode_step(q, k_new, v_new, kc, vc, tables, ctx, w.scale, out, ws,
+                                  args.num_warps)
+
+    def attention():
+        if fp8:
+            pkv.paged_decode_attention_fp8(dev["q"], kc, vc, dev["k_scale"], dev["v_scale"],
+                                           dev["tables"], dev["ctx"], w.scale, out, ws,
+                                           args.num_warps)
+        else:
+            pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out,
+                                       ws, args.num_warps)
 
     def step():
-        pkv.paged_decode_step(dev["q"], dev["k_new"], dev["v_new"], kc, vc, dev["tables"],
-                              dev["ctx"], w.scale, out, ws, args.num_warps)
+        decode_step(dev["q"], dev["k_new"], dev["v_new"], dev["tables"], dev["ctx"])
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
@@ -379,8 +411,7 @@ def native(args):
             if i >= args.warmup:
                 ts.append(e0.elapsed_time(e1))
         return float(np.mean(ts))
-    pms = kernel_ms(lambda: pkv.paged_decode_attention(
-        dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out, ws, args.num_warps))
+    pms = kernel_ms(attention)
 
     # end to end through the public API with pinned host buffers: the step's inputs
     # packed into one pinned buffer, one H2D copy, the decode step, D2H of out
@@ -402,8 +433,7 @@ def native(args):
 
     def e2e_step():
         stage_d.copy_(stage_h, non_blocking=True)
-        pkv.paged_decode_step(views["q"], views["k_new"], views["v_new"], kc, vc, views["tables"],
-                              views["ctx"], w.scale, out, ws, args.num_warps)
+        decode_step(views["q"], views["k_new"], views["v_new"], views["tables"], views["ctx"])
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
@@ -432,7 +462,8 @@ def native(args):
     peak, peak_kind = measured_peak()
     gbs = whole_job_gbs(attn_bytes, world, ms)
     part_gbs = attn_bytes / (pms * 1e-3) / 1e9
-    traffic = profile_traffic(f"decode_attention_{args.workload}")
+    tag = f"decode_attention_fp8_{args.workload}" if fp8 else f"decode_attention_{args.workload}"
+    traffic = profile_traffic(tag)
     line = {
         "metric": METRIC,
         "value": round(gbs, 1),
@@ -444,16 +475,20 @@ def native(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": w.dtype,
+        "dtype": f"e4m3 KV, {w.dtype} q" if fp8 else w.dtype,
         "data": "synthetic",
         "config": {
             "workload": f"{w.name}: {S} seqs, {Hq} q / {Hkv} kv heads, head_dim {D}, {w.dtype}, "
-                        f"block 16, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks",
+                        f"block 16, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks"
+                        + (", fp8 (E4M3) KV cache with per-KV-head scales" if fp8 else ""),
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
             "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
-            "step": "paged_decode_step: cache write of 1 new token/seq + decode attention (2 launches, PDL-chained)",
+            "step": ("paged_decode_step_fp8: quantising cache write of 1 new token/seq + decode attention "
+                     "(2 launches, PDL-chained)") if fp8 else
+                    "paged_decode_step: cache write of 1 new token/seq + decode attention (2 launches, PDL-chained)",
+            "kv_cache": "fp8 e4m3" if fp8 else w.dtype,
             "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
-            "num_warps": args.num_warps or pkv.default_num_warps(D, kc.dtype),
+            "num_warps": args.num_warps or pkv.default_num_warps(D, "fp8" if fp8 else dev["q"].dtype),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "pct_of_peak": {"measured_copy": round(100 * gbs / peak, 1),
@@ -464,7 +499,8 @@ def native(args):
         "roofline": {
             "bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(part_gbs / peak, 4), "traffic": traffic,
-            "kernel": "decode_attention_kernel", "bytes_per_launch": attn_bytes,
+            "kernel": "decode_attention_kernel" + (" (fp8 cache)" if fp8 else ""),
+            "bytes_per_launch": attn_bytes,
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         },
         "e2e": {"value": round(whole_job_gbs(attn_bytes, world, e2e), 1), "unit": "GB/s",
@@ -528,6 +564,8 @@ def main():
     ap.add_argument("--workload", default="mha13b",
                     choices=["tiny", "mha13b", "gqa70b", "prefix", "longctx"])
     ap.add_argument("--num-warps", type=int, default=0)
+    ap.add_argument("--kv", choices=["native", "fp8"], default="native",
+                    help="cache element type: the workload's dtype, or fp8 E4M3 with per-head scales")
     ap.add_argument("--soak-s", type=float, default=0.6,
                     help="seconds of untimed steps run just before the timed ones, so that the "
                          "clock samples cover this load")

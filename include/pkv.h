@@ -30,7 +30,8 @@
  *     ("What is paged attention?", section "How it works").  Token slot s lives at
  *     cache[s / block_size, :, s % block_size, :].
  *   - dtype codes: PKV_F32, PKV_F16, PKV_BF16; q, out, k, v and the caches share
- *     one dtype.  Index tensors are int32.
+ *     one dtype, except on the fp8 entry points (section "fp8 KV cache").  Index
+ *     tensors are int32.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -52,7 +53,12 @@ enum pkv_status {
   PKV_ERR_DEVICE = -6        /* a kernel reported a device-side error (see pkv_decode_status) */
 };
 
-enum pkv_dtype { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2 };
+enum pkv_dtype {
+  PKV_F32 = 0,
+  PKV_F16 = 1,
+  PKV_BF16 = 2,
+  PKV_FP8_E4M3 = 3 /* 8-bit quantised cache elements; only where an entry point says so */
+};
 
 /* Device-side status bits recorded by the decode kernels in the workspace. */
 enum pkv_device_status {
@@ -117,6 +123,8 @@ int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int3
  * workspace again before reuse.
  * One workspace must not be used by two launches that may run concurrently.
  */
+/* dtype PKV_FP8_E4M3 sizes the workspace of pkv_decode_attention_fp8 and
+ * pkv_decode_step_fp8 (whose default warp count differs). */
 int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                               int32_t dtype, int32_t num_warps, size_t* bytes);
 
@@ -203,6 +211,7 @@ int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k
 int pkv_decode_status(void* workspace, int32_t* status, void* stream);
 
 /* Number of worker warps the default launch uses on the current device. */
+/* (dtype PKV_FP8_E4M3: the default of attention over the fp8 cache.) */
 int pkv_decode_default_warps(int32_t head_dim, int32_t dtype, int32_t* num_warps);
 
 /*
@@ -246,6 +255,93 @@ int pkv_decode_attention_static_scratch(const void* q, const void* k_cache, cons
                                         void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* fp8 KV cache                                                               */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * A quantised KV cache stores K and V in 8 bits instead of 16, halving the bytes
+ * per cached token; the pages call it orthogonal to paging and composable with
+ * it ("PagedAttention — how vLLM stopped wasting 80% of your GPU memory", FAQ
+ * "How does this relate to quantization?").  They fix no format; this library
+ * uses:
+ *   - elements: fp8 E4M3 (1 sign, 4 exponent bits with bias 7, 3 mantissa bits,
+ *     subnormals, no infinity, largest finite 448, S.1111.111 is NaN);
+ *   - scales: one fp32 scale per KV head for K (k_scale[num_kv_heads]) and one
+ *     for V (v_scale[...]), both device arrays; an element reads back as
+ *     code * scale;
+ *   - quantisation on write: code = E4M3(x / scale), x widened to fp32, the
+ *     quotient a correctly rounded fp32 division, then rounded to the nearest
+ *     E4M3 value with ties to an even code and saturated to +-448 (NaN stays NaN);
+ *   - layouts (block_size 16):
+ *       k_cache [num_blocks, num_kv_heads, 16, head_dim] uint8 (as above);
+ *       v_cache [num_blocks, num_kv_heads, head_dim, 16] uint8: each (block, KV
+ *       head) tile transposed, and within each 16-byte head_dim row token t of
+ *       the block at byte V_POS[t], the byte order being the tokens
+ *       0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15 (byte j holds the j-th of these).
+ *   pkv_copy_blocks copies fp8 blocks with dtype PKV_FP8_E4M3 and
+ *   block_elems = num_kv_heads * 16 * head_dim.
+ */
+
+/*
+ * pkv_kv_write_fp8 — quantise new tokens' K and V and scatter them into the fp8
+ * caches: for i < num_tokens, h < num_kv_heads with s = slot_mapping[i] >= 0,
+ *   k_cache[s / 16, h, s % 16, :]          = E4M3(k[i, h, :] / k_scale[h])
+ *   v_cache[s / 16, h, :, V_POS[s % 16]]   = E4M3(v[i, h, :] / v_scale[h])
+ * k, v          device [num_tokens, num_kv_heads, head_dim] in `dtype`
+ *               (PKV_F32, PKV_F16 or PKV_BF16), contiguous, 16-byte aligned.
+ * slot_mapping, num_blocks, block_size (must be 16): as pkv_kv_write.
+ * k_scale, v_scale  device float [num_kv_heads], positive and finite.
+ * Requirements: head_dim a multiple of 16; caches 16-byte aligned.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+int pkv_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
+                     int32_t num_tokens, void* k_cache, void* v_cache, const float* k_scale,
+                     const float* v_scale, int32_t num_blocks, int32_t num_kv_heads,
+                     int32_t block_size, int32_t head_dim, int32_t dtype, void* stream);
+
+/*
+ * pkv_decode_attention_fp8 — pkv_decode_attention over fp8 caches: the same
+ * attention with K[slot, g, :] = code * k_scale[g] and V likewise, computed as
+ *   scores = (scale * k_scale[g]) * q . code_k,  out = v_scale[g] * softmax . code_v.
+ * q and out are `dtype` (PKV_F16 or PKV_BF16); the cache codes are widened
+ * exactly to f16 for the tensor-core contractions, q is converted to f16 (exact
+ * for values of magnitude in [2^-14, 65504]; |q| must stay below 65504), and
+ * scores, softmax and accumulation are fp32.  The workspace, num_warps,
+ * determinism, status reporting and the programmatic-launch chaining are those
+ * of pkv_decode_attention; size the workspace with pkv_decode_workspace_size
+ * for dtype PKV_FP8_E4M3 and the same head shape and num_warps (one CTA of 8
+ * worker warps per SM by default: the 4 KB fp8 stages leave room for them).
+ * Supported: block_size 16, head_dim 128 or 256, G in {1, 2, 4, 8}.
+ * Errors: as pkv_decode_attention.
+ */
+int pkv_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int32_t num_blocks, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, int32_t num_warps, int32_t dtype,
+                             void* stream);
+
+/*
+ * pkv_decode_step_fp8 — one decode step over fp8 caches: each sequence's new
+ * token (k_new, v_new [num_seqs, num_kv_heads, head_dim] in `dtype`, position
+ * t - 1 for t = context_lens[s] > 0, slot from its block table) is quantised
+ * into the caches exactly as pkv_kv_write_fp8 would, then
+ * pkv_decode_attention_fp8 runs; the two launches are chained with programmatic
+ * dependent launch.  Output and caches are bit-identical to pkv_kv_write_fp8
+ * followed by pkv_decode_attention_fp8.
+ * Errors: as pkv_decode_attention_fp8.
+ */
+int pkv_decode_step_fp8(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const float* k_scale, const float* v_scale,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int32_t num_blocks, float scale, void* out, void* workspace,
+                        size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Copy-on-write block copy                                                   */
 /* ------------------------------------------------------------------------- */
 
@@ -260,7 +356,8 @@ int pkv_decode_attention_static_scratch(const void* q, const void* k_cache, cons
  * Parallel Sampling").  Pairs with an id outside [0, num_blocks) are skipped.
  * A dst that is also some pair's src, or two pairs with one dst: unspecified.
  * src_dst_pairs is device int32 [num_pairs, 2].  block_elems * element size
- * must be a multiple of 16 bytes and both caches 16-byte aligned.
+ * must be a multiple of 16 bytes and both caches 16-byte aligned.  dtype may
+ * be PKV_FP8_E4M3 for fp8 caches (one byte per element).
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_CUDA.
  */
 int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int32_t num_pairs,

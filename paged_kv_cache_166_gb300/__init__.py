@@ -7,6 +7,8 @@ Public API (all device work runs in libpkv.so's sm_103a kernels):
 * ``paged_decode_step(q, k_new, v_new, k_cache, v_cache, block_tables, context_lens, scale, out)``
   — the cache write of each sequence's new token, then the attention, from one call
 * ``paged_copy_blocks(k_cache, v_cache, src_dst_pairs)``
+* fp8 (E4M3) cache with per-KV-head scales: ``paged_kv_write_fp8``,
+  ``paged_decode_attention_fp8``, ``paged_decode_step_fp8``
 * ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free)
 
 The library is loaded on first use; importing this package needs no GPU.
@@ -19,7 +21,8 @@ def __getattr__(name):
     # torch-facing ops are imported lazily so that host-only users (the block
     # manager, the workload generators) do not need torch's CUDA runtime.
     if name in ("paged_kv_write", "paged_decode_attention", "paged_decode_step",
-                "paged_copy_blocks",
+                "paged_copy_blocks", "paged_kv_write_fp8", "paged_decode_attention_fp8",
+                "paged_decode_step_fp8",
                 "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
         from . import ops
         return getattr(ops, name)

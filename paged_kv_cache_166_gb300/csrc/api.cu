@@ -67,26 +67,34 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 }  // namespace
 
-int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t rows,
-                     int32_t cols, int32_t box_cols, int32_t box_rows) {
+int encode_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType type, int elt_bytes,
+                  int64_t rows, int32_t cols, int32_t box_cols, int32_t box_rows,
+                  CUtensorMapSwizzle swizzle) {
   auto fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * elt_bytes};
+  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t estr[2] = {1u, 1u};
+  CUresult r = fn(map, type, 2, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
+  return PKV_OK;
+}
+
+int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t rows,
+                     int32_t cols, int32_t box_cols, int32_t box_rows) {
   CUtensorMapDataType dt;
   switch (dtype) {
     case PKV_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
     case PKV_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
     case PKV_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
+    case PKV_FP8_E4M3: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
     default: return fail(PKV_ERR_DTYPE, "unknown dtype %d", dtype);
   }
-  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
-  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * element_bytes(dtype)};
-  const cuuint32_t box[2] = {static_cast<cuuint32_t>(box_cols), static_cast<cuuint32_t>(box_rows)};
-  const cuuint32_t estr[2] = {1u, 1u};
-  CUresult r = fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
-                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
-                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
-  if (r != CUDA_SUCCESS) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled failed (%d)", (int)r);
-  return PKV_OK;
+  return encode_map_2d(map, base, dt, element_bytes(dtype), rows, cols, box_cols, box_rows,
+                       CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
 }  // namespace pkv

@@ -45,6 +45,7 @@
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -60,8 +61,19 @@ namespace pkv {
 #ifndef PKV_WARPS_PER_CTA
 #define PKV_WARPS_PER_CTA 4
 #endif
+// fp8 stages are half the size (and hold no query rows): more warps fit, and hide
+// each other's latency; at head_dim 256 the register budget allows fewer.
+#ifndef PKV_WARPS_PER_CTA_FP8
+#define PKV_WARPS_PER_CTA_FP8 16
+#endif
+#ifndef PKV_WARPS_PER_CTA_FP8_WIDE
+#define PKV_WARPS_PER_CTA_FP8_WIDE 8
+#endif
 #ifndef PKV_MAX_STAGES
 #define PKV_MAX_STAGES 8
+#endif
+#ifndef PKV_MAX_STAGES_FP8
+#define PKV_MAX_STAGES_FP8 12
 #endif
 #ifndef PKV_EARLY_RELEASE
 #define PKV_EARLY_RELEASE 0
@@ -72,6 +84,10 @@ namespace pkv {
 #endif
 #ifndef PKV_PREFETCH_TABLES
 #define PKV_PREFETCH_TABLES 1
+#endif
+// Skip the accumulator rescale of a step whose running maxima did not change.
+#ifndef PKV_RESCALE_SKIP
+#define PKV_RESCALE_SKIP 0
 #endif
 #ifndef PKV_PARALLEL_PROLOGUE
 #define PKV_PARALLEL_PROLOGUE 1
@@ -88,8 +104,15 @@ namespace pkv {
 constexpr int kTok = 16;                 // tokens per cache block (kernel requirement)
 constexpr int kSwizzleRow = 128;         // bytes per swizzled shared-memory row
 constexpr int kSubTile = kTok * kSwizzleRow;  // one swizzled [16 x 128 B] sub-tile
-constexpr int kWarps = PKV_WARPS_PER_CTA;     // worker warps per CTA
+constexpr int kWarps = PKV_WARPS_PER_CTA;     // worker warps per CTA (16/32-bit caches)
+constexpr int kWarpsFp8 = PKV_WARPS_PER_CTA_FP8;  // the same for the fp8 cache, head_dim 128
+constexpr int kWarpsFp8Wide = PKV_WARPS_PER_CTA_FP8_WIDE;  // ... and head_dim 256
+
+__host__ __device__ constexpr int fp8_warps_per_cta(int D) {
+  return D <= 128 ? kWarpsFp8 : kWarpsFp8Wide;
+}
 constexpr int kMaxStages = PKV_MAX_STAGES;    // per-warp pipeline depth limit
+constexpr int kMaxStagesFp8 = PKV_MAX_STAGES_FP8;  // the same for 4 KB fp8 stages
 constexpr int kMaxSeqs = 2048;
 constexpr int kMaxGroup = 8;
 constexpr uint64_t kWaitLimitNs = 1000000000ull;  // 1 s per wait before giving up
@@ -104,6 +127,8 @@ struct DecodeArgs {
   float* part_o;     // [2 * total_warps, G, D]  (unnormalised accumulator)
   int32_t* tickets;  // [total_warps], zero between launches
   int32_t* status;
+  const float* k_scale;  // fp8 cache: per-KV-head scales (else NULL)
+  const float* v_scale;
   int32_t S, Hq, Hkv, G, MAXB, NB;
   int32_t total_warps;
   int32_t stages;    // per-warp pipeline depth
@@ -113,17 +138,31 @@ struct DecodeArgs {
   float scale_log2;  // scale * log2(e)
 };
 
-template <typename T, int D>
+// Cache element tag of the fp8 (E4M3) cache; q and out stay 16-bit there.
+struct E4M3 {};
+template <typename C>
+struct CacheBytes {
+  static constexpr int value = sizeof(C);
+};
+template <>
+struct CacheBytes<E4M3> {
+  static constexpr int value = 1;
+};
+
+template <typename C, int D>
 struct Shape {
-  static constexpr int kElt = sizeof(T);
+  static constexpr bool kFp8 = std::is_same<C, E4M3>::value;
+  static constexpr int kElt = CacheBytes<C>::value;
+  static constexpr int kWarpsPerCta = kFp8 ? fp8_warps_per_cta(D) : kWarps;
   static constexpr int kTileBytes = kTok * D * kElt;
   static constexpr int kSub = D * kElt / kSwizzleRow;     // sub-tiles per tile
   static constexpr int kBoxCols = kSwizzleRow / kElt;      // elements per sub-tile row
   static constexpr int kStageBytes = 2 * kTileBytes;       // K and V tile
   // fp16/bf16 tiles up to head_dim 128 fit in registers: release the stage early
   static constexpr bool kEarlyRelease = PKV_EARLY_RELEASE && (kElt == 2) && (D <= 128);
+  // fp8: K in kSub boxes of [16 rows x 128 B]; V (stored [D x 16 B]) in one box
   // one box per tile: rows of the tile are viewed as kSub half-rows of 128 B
-  static constexpr bool kSingleBox = PKV_SINGLE_BOX && (kSub <= 2);
+  static constexpr bool kSingleBox = PKV_SINGLE_BOX && !kFp8 && (kSub <= 2);
   static_assert(kSub * kSwizzleRow == D * kElt, "head_dim * elt must be a multiple of 128 B");
 };
 
@@ -132,18 +171,18 @@ struct SmemLayout {
 };
 
 __host__ __device__ inline SmemLayout smem_layout(int stage_bytes, int stages, int q_stride,
-                                                  int S) {
+                                                  int S, int nw) {
   SmemLayout L;
   uint32_t off = 0;
   L.tiles = off;
-  off += kWarps * stages * stage_bytes;
+  off += nw * stages * stage_bytes;
   L.q = off;
-  off += kWarps * stages * q_stride;
+  off += nw * stages * q_stride;
   off = (off + 15u) & ~15u;
   L.bars = off;
-  off += kWarps * stages * 8;
+  off += nw * stages * 8;
   L.ids = off;
-  off += kWarps * 64 * 4;
+  off += nw * 64 * 4;
   L.ctx = off;
   off += S * 4;
   L.pre = off;
@@ -404,12 +443,14 @@ struct MmaState {
     l1 = l1 * al1 + (p1 + p3);
     m0 = mn0;
     m1 = mn1;
+    if (!PKV_RESCALE_SKIP || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
 #pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      o[mt][0] *= al0;
-      o[mt][1] *= al1;
-      o[mt][2] *= al0;
-      o[mt][3] *= al1;
+      for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
     }
     // transpose the (tokens x heads) halves in registers
     pb0 = ptx::movmatrix_trans(ptx::pack2<T>(p0, p1));
@@ -509,6 +550,200 @@ struct MmaState {
       if (h1 < G) {
         po[h1 * D + mt * 16 + gid] = o[mt][1];
         po[h1 * D + mt * 16 + gid + 8] = o[mt][3];
+      }
+    }
+    if (gid == 0) {
+      if (h0 < G) { pml[h0 * 2] = m0; pml[h0 * 2 + 1] = l0; }
+      if (h1 < G) { pml[h1 * 2] = m1; pml[h1 * 2 + 1] = l1; }
+    }
+  }
+};
+
+// fp8 (E4M3) tiles.  K: [16 tokens x D bytes] in 128-byte swizzled sub-tiles.
+// V: stored transposed, [D x 16 bytes] unswizzled, each 16-byte row holding the
+// 16 tokens in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15.  Operand
+// fragments come from ldmatrix on bytes: a lane's 32-bit word holds 4 consecutive
+// bytes of one row, widened exactly to two f16 pairs (hardware conversion), and
+// the contractions run on the f16 tensor cores with fp32 accumulation:
+//   scores: the MMA's k index maps to head_dim as k = 2i, 2i+1 -> d = 4i, 4i+1
+//     and k = 2i+8, 2i+9 -> d = 4i+2, 4i+3 (within each 16-wide step); q is loaded
+//     in the same order, so the dot products are unchanged;
+//   P.V:    a V word holds tokens 2i, 2i+1, 2i+8, 2i+9 of one head_dim row, the
+//     token order in which P^T comes out of movmatrix, so P needs no reshuffle.
+// q (f16 or bf16) is converted to f16; k_scale folds into the score scale and
+// v_scale multiplies the accumulator when it is written.
+template <typename T, int D>
+struct Fp8State {
+  static constexpr int KS = D / 16;
+  static constexpr int kSub = D / kSwizzleRow;
+  float o[KS][4];   // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
+  uint32_t qb[KS][2];
+  float m0, m1, l0, l1;
+  float sl2, vs;    // score scale (log2 units, k_scale folded in), v_scale
+
+  static __device__ __forceinline__ uint32_t widen(uint32_t two_codes) {
+    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
+        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
+    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  }
+
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int i = 0; i < KS; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+    m0 = m1 = -INFINITY;
+    l0 = l1 = 0.f;
+  }
+
+  __device__ __forceinline__ void set_scales(float k_scale, float v_scale, float scale_log2) {
+    sl2 = scale_log2 * k_scale;
+    vs = v_scale;
+  }
+
+  // The G query rows of the unit, read from global memory (8 bytes per lane and
+  // step: head gid, elements 16 ks + 4 tig .. + 3) and converted to f16.
+  __device__ __forceinline__ void load_q_rows(const T* rows, int G, int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+    const T* row = rows + gid * D + 4 * tig;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      if (gid < G) {
+        const uint2 u = __ldg(reinterpret_cast<const uint2*>(row + ks * 16));
+        const T* p = reinterpret_cast<const T*>(&u);
+        qb[ks][0] = ptx::pack2<__half>(ptx::to_float(p[0]), ptx::to_float(p[1]));
+        qb[ks][1] = ptx::pack2<__half>(ptx::to_float(p[2]), ptx::to_float(p[3]));
+      } else {
+        qb[ks][0] = qb[ks][1] = 0u;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void step_smem(uint32_t ktile, uint32_t vtile, int valid,
+                                            float /*scale_log2*/, int lane) {
+    const int gid = lane >> 2, tig = lane & 3, mi = lane >> 3, r = lane & 7;
+    float c0[4] = {0.f, 0.f, 0.f, 0.f}, c1[4] = {0.f, 0.f, 0.f, 0.f};
+    // ldmatrix of K: matrices {tok 0-7, chunk 2p}, {tok 8-15, 2p}, {0-7, 2p+1}, {8-15, 2p+1}
+    const int krow = r + (mi & 1) * 8;
+#pragma unroll
+    for (int p = 0; p < KS / 2; ++p) {
+      uint32_t w[4], a[4];
+      ptx::ldsm_x4(ktile + tile_offset<kSub, false>(krow, 2 * p + (mi >> 1)), w);
+      a[0] = widen(w[0]);
+      a[1] = widen(w[1]);
+      a[2] = widen(w[0] >> 16);
+      a[3] = widen(w[1] >> 16);
+      ptx::mma_16816<__half>(c0, a, qb[2 * p][0], qb[2 * p][1]);
+      a[0] = widen(w[2]);
+      a[1] = widen(w[3]);
+      a[2] = widen(w[2] >> 16);
+      a[3] = widen(w[3] >> 16);
+      ptx::mma_16816<__half>(c1, a, qb[2 * p + 1][0], qb[2 * p + 1][1]);
+    }
+    float x[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) x[i] = (c0[i] + c1[i]) * sl2;
+    if (valid < kTok) {
+      if (gid >= valid) x[0] = x[1] = -INFINITY;
+      if (gid + 8 >= valid) x[2] = x[3] = -INFINITY;
+    }
+    // online softmax, P^T as the f16 B operand
+    float mx0 = fmaxf(x[0], x[2]), mx1 = fmaxf(x[1], x[3]);
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      mx0 = fmaxf(mx0, __shfl_xor_sync(0xffffffffu, mx0, off));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
+    }
+    const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
+    const float p0 = exp2f(x[0] - mn0), p1 = exp2f(x[1] - mn1);
+    const float p2 = exp2f(x[2] - mn0), p3 = exp2f(x[3] - mn1);
+    l0 = l0 * al0 + (p0 + p2);
+    l1 = l1 * al1 + (p1 + p3);
+    m0 = mn0;
+    m1 = mn1;
+    // once the running maxima settle, whole steps leave them unchanged (al == 1)
+    if (__any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) {
+        o[mt][0] *= al0;
+        o[mt][1] *= al1;
+        o[mt][2] *= al0;
+        o[mt][3] *= al1;
+      }
+    }
+    const uint32_t pb0 = ptx::movmatrix_trans(ptx::pack2<__half>(p0, p1));
+    const uint32_t pb1 = ptx::movmatrix_trans(ptx::pack2<__half>(p2, p3));
+    // masks of the V lanes: a word's f16 pairs hold tokens (2 tig, 2 tig + 1) and
+    // (2 tig + 8, 2 tig + 9); rows past the context may hold anything, NaN included
+    const bool partial = valid < kTok;
+    const uint32_t mlo =
+        (2 * tig < valid ? 0x0000ffffu : 0u) | (2 * tig + 1 < valid ? 0xffff0000u : 0u);
+    const uint32_t mhi =
+        (2 * tig + 8 < valid ? 0x0000ffffu : 0u) | (2 * tig + 9 < valid ? 0xffff0000u : 0u);
+    // ldmatrix of V^T: matrix j holds head_dim rows 32p + 8j .. 32p + 8j + 7
+#pragma unroll
+    for (int p = 0; p < KS / 2; ++p) {
+      uint32_t w[4], a[4];
+      ptx::ldsm_x4(vtile + (32 * p + 8 * mi + r) * 16, w);
+      a[0] = widen(w[0]);
+      a[1] = widen(w[1]);
+      a[2] = widen(w[0] >> 16);
+      a[3] = widen(w[1] >> 16);
+      if (partial) {
+        a[0] &= mlo;
+        a[1] &= mlo;
+        a[2] &= mhi;
+        a[3] &= mhi;
+      }
+      ptx::mma_16816<__half>(o[2 * p], a, pb0, pb1);
+      a[0] = widen(w[2]);
+      a[1] = widen(w[3]);
+      a[2] = widen(w[2] >> 16);
+      a[3] = widen(w[3] >> 16);
+      if (partial) {
+        a[0] &= mlo;
+        a[1] &= mlo;
+        a[2] &= mhi;
+        a[3] &= mhi;
+      }
+      ptx::mma_16816<__half>(o[2 * p + 1], a, pb0, pb1);
+    }
+  }
+
+  __device__ __forceinline__ void reduce_sums() {
+#pragma unroll
+    for (int off = 4; off < 32; off <<= 1) {
+      l0 += __shfl_xor_sync(0xffffffffu, l0, off);
+      l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    }
+  }
+
+  __device__ __forceinline__ void write_out(T* out_rows, int G, int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+    const float i0 = vs / l0, i1 = vs / l1;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      const uint32_t lo = ptx::movmatrix_trans(ptx::pack2<T>(o[mt][0] * i0, o[mt][1] * i1));
+      const uint32_t hi = ptx::movmatrix_trans(ptx::pack2<T>(o[mt][2] * i0, o[mt][3] * i1));
+      if (gid < G) {
+        T* row = out_rows + gid * D + mt * 16 + 2 * tig;
+        *reinterpret_cast<uint32_t*>(row) = lo;
+        *reinterpret_cast<uint32_t*>(row + 8) = hi;
+      }
+    }
+  }
+
+  __device__ __forceinline__ void write_partial(float* po, float* pml, int G, int lane) {
+    const int gid = lane >> 2, tig = lane & 3;
+    const int h0 = 2 * tig, h1 = 2 * tig + 1;
+#pragma unroll
+    for (int mt = 0; mt < KS; ++mt) {
+      if (h0 < G) {
+        po[h0 * D + mt * 16 + gid] = o[mt][0] * vs;
+        po[h0 * D + mt * 16 + gid + 8] = o[mt][2] * vs;
+      }
+      if (h1 < G) {
+        po[h1 * D + mt * 16 + gid] = o[mt][1] * vs;
+        po[h1 * D + mt * 16 + gid + 8] = o[mt][3] * vs;
       }
     }
     if (gid == 0) {
@@ -691,11 +926,11 @@ struct CutUnit {
 // ---------------------------------------------------------------------------------
 // The decode kernel: one persistent pass of every worker warp over its run.
 // ---------------------------------------------------------------------------------
-template <typename T, int D>
-__global__ void __launch_bounds__(kWarps * 32, 1)
+template <typename T, typename C, int D>
+__global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     decode_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
-  using Sh = Shape<T, D>;
+  using Sh = Shape<C, D>;
   const int NS = a.stages;
   extern __shared__ uint8_t smem_raw[];
   if (threadIdx.x == 0) {
@@ -732,7 +967,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base_s = (raw + 1023u) & ~1023u;
   uint8_t* const base = smem_raw + (base_s - raw);
-  const SmemLayout L = smem_layout(Sh::kStageBytes, NS, a.q_stride, a.S);
+  const SmemLayout L = smem_layout(Sh::kStageBytes, NS, a.q_stride, a.S, Sh::kWarpsPerCta);
   int32_t* const ctx_s = reinterpret_cast<int32_t*>(base + L.ctx);
   int32_t* const pre = reinterpret_cast<int32_t*>(base + L.pre);
   int32_t* const prew = reinterpret_cast<int32_t*>(base + L.prew);
@@ -740,7 +975,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
                  reinterpret_cast<int32_t*>(base + L.scratch), a.status);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int gw = blockIdx.x * kWarps + warp;
+  const int gw = blockIdx.x * Sh::kWarpsPerCta + warp;
   const int S = a.S, Hkv = a.Hkv, MAXB = a.MAXB;
   const int total = pre[S];
   const int W = a.total_warps;
@@ -810,7 +1045,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     }
     if (lane == 0) {
       const int id = ids[((m >> 5) & 1) * 32 + (m & 31)];
-      const bool need_q = (m == 0) || (pc.j == 0);
+      const bool need_q = !Sh::kFp8 && ((m == 0) || (pc.j == 0));
       const uint32_t bar = bars + 8 * p_stage;
       ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
       int32_t y;
@@ -829,13 +1064,17 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
         for (int c = 0; c < Sh::kSub; ++c)
           ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
+        if constexpr (Sh::kFp8) {
+          ptx::tma_load_2d(vt, &vmap, 0, (y / kTok) * (D / 8), bar, policy);
+        } else {
 #pragma unroll
-        for (int c = 0; c < Sh::kSub; ++c)
-          ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
+          for (int c = 0; c < Sh::kSub; ++c)
+            ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
+        }
       }
       if (need_q) {
         const char* src =
-            qbase + (static_cast<int64_t>(pc.s) * a.Hq + pc.g * a.G) * D * Sh::kElt;
+            qbase + (static_cast<int64_t>(pc.s) * a.Hq + pc.g * a.G) * D * sizeof(T);
         ptx::bulk_load(qslot_s + p_stage * a.q_stride, src, a.q_bytes, bar);
       }
     }
@@ -850,7 +1089,7 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
   } else if (lane < prologue) {
     const Cursor lc = cursor_at(pre, S, Hkv, f0 + lane);
     const int id = ids[lane];
-    const bool need_q = (lane == 0) || (lc.j == 0);
+    const bool need_q = !Sh::kFp8 && ((lane == 0) || (lc.j == 0));
     const uint32_t bar = bars + 8 * lane;
     ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
     int32_t y;
@@ -869,12 +1108,16 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
 #pragma unroll
       for (int c = 0; c < Sh::kSub; ++c)
         ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
+      if constexpr (Sh::kFp8) {
+        ptx::tma_load_2d(vt, &vmap, 0, (y / kTok) * (D / 8), bar, policy);
+      } else {
 #pragma unroll
-      for (int c = 0; c < Sh::kSub; ++c)
-        ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
+        for (int c = 0; c < Sh::kSub; ++c)
+          ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
+      }
     }
     if (need_q) {
-      const char* src = qbase + (static_cast<int64_t>(lc.s) * a.Hq + lc.g * a.G) * D * Sh::kElt;
+      const char* src = qbase + (static_cast<int64_t>(lc.s) * a.Hq + lc.g * a.G) * D * sizeof(T);
       ptx::bulk_load(qslot_s + lane * a.q_stride, src, a.q_bytes, bar);
     }
   }
@@ -884,7 +1127,9 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
     if (prologue > 0) pc = cursor_at(pre, S, Hkv, min(f0 + prologue, total - 1));
   }
 
-  using State = typename std::conditional<sizeof(T) == 2, MmaState<T, D>, FmaState<D>>::type;
+  using State = typename std::conditional<
+      Sh::kFp8, Fp8State<T, D>,
+      typename std::conditional<sizeof(T) == 2, MmaState<T, D>, FmaState<D>>::type>::type;
   State st_;
   Cursor cc = cursor_at(pre, S, Hkv, f0);
   int first_j = cc.j;
@@ -909,8 +1154,15 @@ __global__ void __launch_bounds__(kWarps * 32, 1)
       return;
     }
     if (n == 0 || cc.j == 0) {
-      st_.load_q(qslot + c_stage * a.q_stride, a.G, lane);
+      if constexpr (Sh::kFp8) {
+        st_.load_q_rows(reinterpret_cast<const T*>(a.q) +
+                            (static_cast<int64_t>(cc.s) * a.Hq + cc.g * a.G) * D,
+                        a.G, lane);
+      } else {
+        st_.load_q(qslot + c_stage * a.q_stride, a.G, lane);
+      }
       st_.reset();
+      if constexpr (Sh::kFp8) st_.set_scales(a.k_scale[cc.g], a.v_scale[cc.g], a.scale_log2);
       first_j = cc.j;
     }
     const int valid = (cc.j == cc.nb - 1) ? ctx_s[cc.s] - cc.j * kTok : kTok;
@@ -994,12 +1246,16 @@ struct HostArgs {
   void* workspace;
   size_t workspace_bytes;
   int32_t num_warps;
-  int32_t dtype;
+  int32_t dtype;  // of q and out (and of the caches unless fp8)
   cudaStream_t stream;
+  bool fp8 = false;  // E4M3 caches with per-KV-head scales
+  const float* k_scale = nullptr;
+  const float* v_scale = nullptr;
 };
 
 bool supported_head_dim(int32_t dtype, int32_t D) {
   if (dtype == PKV_F32) return D == 32 || D == 64 || D == 128;
+  if (dtype == PKV_FP8_E4M3) return D == 128 || D == 256;
   return D == 64 || D == 128 || D == 256;
 }
 
@@ -1021,7 +1277,7 @@ int device_smem_optin(int* bytes) {
   return PKV_OK;
 }
 
-template <typename T, int D>
+template <typename T, typename C, int D>
 int ensure_smem_attr() {
   // Raise the dynamic shared-memory limit once per device for this instantiation.
   static std::once_flag flags[64];
@@ -1033,7 +1289,7 @@ int ensure_smem_attr() {
   int rc = device_smem_optin(&optin);
   if (rc != PKV_OK) return rc;
   std::call_once(flags[dev], [&] {
-    results[dev] = cudaFuncSetAttribute(decode_attention_kernel<T, D>,
+    results[dev] = cudaFuncSetAttribute(decode_attention_kernel<T, C, D>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   });
   if (results[dev] != cudaSuccess)
@@ -1041,15 +1297,16 @@ int ensure_smem_attr() {
   return PKV_OK;
 }
 
-// One CTA of kWarps warps per SM (the kernel sizes its pipeline to fill the SM's
-// shared memory), so the default warp count is SMs x kWarps.
+// One CTA per SM (the kernel sizes its pipeline to fill the SM's shared memory),
+// so the default warp count is SMs x warps per CTA.  dtype PKV_FP8_E4M3 stands for
+// attention over the fp8 cache.
 int default_warps(int32_t dtype, int32_t D) {
   if (!supported_head_dim(dtype, D))
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for dtype %d", D, dtype);
   int sms = 0, dev = 0;
   int rc = device_sm_count(&sms, &dev);
   if (rc != PKV_OK) return rc;
-  return sms * kWarps;
+  return sms * (dtype == PKV_FP8_E4M3 ? fp8_warps_per_cta(D) : kWarps);
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -1073,6 +1330,19 @@ size_t workspace_bytes_for(int32_t G, int32_t D, int32_t W) {
 
 int validate(const HostArgs& h, int* warps_out) {
   PKV_REQUIRE(element_bytes(h.dtype) != 0, PKV_ERR_DTYPE, "unknown dtype %d", h.dtype);
+  if (h.fp8) {
+    PKV_REQUIRE(h.dtype == PKV_F16 || h.dtype == PKV_BF16, PKV_ERR_DTYPE,
+                "q dtype %d: attention over the fp8 cache takes f16 or bf16 q", h.dtype);
+    PKV_REQUIRE(h.D == 128 || h.D == 256, PKV_ERR_UNSUPPORTED,
+                "head_dim %d unsupported for the fp8 cache (128 or 256)", h.D);
+    PKV_REQUIRE(h.S == 0 || (h.k_scale && h.v_scale), PKV_ERR_INVALID_ARG,
+                "NULL k_scale / v_scale");
+    PKV_REQUIRE(static_cast<int64_t>(h.NB) * h.Hkv * h.D < (int64_t(1) << 31),
+                PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * head_dim >= 2^31");
+  } else {
+    PKV_REQUIRE(h.dtype != PKV_FP8_E4M3, PKV_ERR_DTYPE,
+                "fp8 caches are read by pkv_decode_attention_fp8");
+  }
   PKV_REQUIRE(h.S >= 0 && h.S <= kMaxSeqs, PKV_ERR_UNSUPPORTED,
               "num_seqs %d outside [0, %d]", h.S, kMaxSeqs);
   PKV_REQUIRE(h.Hq > 0 && h.Hkv > 0 && h.Hq % h.Hkv == 0, PKV_ERR_INVALID_ARG,
@@ -1090,7 +1360,7 @@ int validate(const HostArgs& h, int* warps_out) {
   PKV_REQUIRE(h.num_warps >= 0, PKV_ERR_INVALID_ARG, "negative num_warps");
   int W = h.num_warps;
   if (W == 0) {
-    W = default_warps(h.dtype, h.D);
+    W = default_warps(h.fp8 ? PKV_FP8_E4M3 : h.dtype, h.D);
     if (W < 0) return W;
   }
   *warps_out = W;
@@ -1140,28 +1410,44 @@ DecodeArgs device_args(const HostArgs& h, int W) {
   a.q_stride = (a.q_bytes + 127) & ~127;
   a.unit_cost = G >= 4 ? PKV_UNIT_COST_LARGE_G : PKV_UNIT_COST_SMALL_G;
   a.scale_log2 = h.scale * 1.4426950408889634f;
+  a.k_scale = h.k_scale;
+  a.v_scale = h.v_scale;
   return a;
 }
 
-template <typename T, int D>
+template <typename T, typename C, int D>
 int launch_decode(const HostArgs& h, int W) {
-  using Sh = Shape<T, D>;
-  int rc = ensure_smem_attr<T, D>();
+  using Sh = Shape<C, D>;
+  int rc = ensure_smem_attr<T, C, D>();
   if (rc != PKV_OK) return rc;
   int optin = 0;
   rc = device_smem_optin(&optin);
   if (rc != PKV_OK) return rc;
   DecodeArgs a = device_args(h, W);
+  if constexpr (Sh::kFp8) a.q_stride = 0;  // the fp8 path reads q rows straight into registers
   // Deepest pipeline that fits the SM's shared memory.
-  const uint32_t fixed = smem_layout(Sh::kStageBytes, 0, a.q_stride, h.S).total;
-  const uint32_t per_stage = kWarps * (Sh::kStageBytes + a.q_stride + 8);
+  const uint32_t fixed = smem_layout(Sh::kStageBytes, 0, a.q_stride, h.S, Sh::kWarpsPerCta).total;
+  const uint32_t per_stage = Sh::kWarpsPerCta * (Sh::kStageBytes + a.q_stride + 8);
   int stages = optin > static_cast<int>(fixed) ? static_cast<int>((optin - fixed) / per_stage) : 0;
-  stages = stages > kMaxStages ? kMaxStages : stages;
+  const int max_stages = Sh::kFp8 ? kMaxStagesFp8 : kMaxStages;
+  stages = stages > max_stages ? max_stages : stages;
   PKV_REQUIRE(stages >= 2, PKV_ERR_UNSUPPORTED, "pipeline does not fit in shared memory");
   a.stages = stages;
-  const SmemLayout L = smem_layout(Sh::kStageBytes, stages, a.q_stride, h.S);
+  const SmemLayout L = smem_layout(Sh::kStageBytes, stages, a.q_stride, h.S, Sh::kWarpsPerCta);
   CUtensorMap kmap, vmap;
   const int64_t rows = static_cast<int64_t>(h.NB) * h.Hkv * kTok;
+  if constexpr (Sh::kFp8) {
+    // K: [rows, D] bytes, boxes of 16 rows x 128 B, swizzled.  V: each transposed
+    // [D x 16 B] tile is 16 D contiguous bytes, viewed as D/8 rows of 128 B so that
+    // one unswizzled box of D/8 rows moves it (the bytes land in the same order).
+    rc = encode_map_2d(&kmap, h.k_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, rows, D,
+                       Sh::kBoxCols, kTok, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != PKV_OK) return rc;
+    rc = encode_map_2d(&vmap, h.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
+                       static_cast<int64_t>(h.NB) * h.Hkv * (D / 8), kSwizzleRow, kSwizzleRow,
+                       D / 8, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != PKV_OK) return rc;
+  } else {
   // Single box: the cache as [rows * kSub, 128 B] half-rows, boxes of 16 * kSub
   // half-rows (one whole tile).  Otherwise [rows, D], boxes of 16 rows x 128 B.
   const int64_t map_rows = Sh::kSingleBox ? rows * Sh::kSub : rows;
@@ -1171,9 +1457,10 @@ int launch_decode(const HostArgs& h, int W) {
   if (rc != PKV_OK) return rc;
   rc = encode_cache_map(&vmap, h.v_cache, h.dtype, map_rows, map_cols, Sh::kBoxCols, box_rows);
   if (rc != PKV_OK) return rc;
+  }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3((W + kWarps - 1) / kWarps);
-  cfg.blockDim = dim3(kWarps * 32);
+  cfg.gridDim = dim3((W + Sh::kWarpsPerCta - 1) / Sh::kWarpsPerCta);
+  cfg.blockDim = dim3(Sh::kWarpsPerCta * 32);
   cfg.dynamicSmemBytes = L.total;
   cfg.stream = h.stream;
   cudaLaunchAttribute attr[1];
@@ -1181,13 +1468,23 @@ int launch_decode(const HostArgs& h, int W) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  PKV_CUDA(cudaLaunchKernelEx(&cfg, decode_attention_kernel<T, D>, kmap, vmap, a));
+  PKV_CUDA(cudaLaunchKernelEx(&cfg, decode_attention_kernel<T, C, D>, kmap, vmap, a));
   return PKV_OK;
 }
 
 int dispatch(const HostArgs& h, int W) {
+  if (h.fp8) {
+#define PKV_CASE8(DT, TT, DD) \
+  if (h.dtype == DT && h.D == DD) return launch_decode<TT, E4M3, DD>(h, W);
+    PKV_CASE8(PKV_BF16, __nv_bfloat16, 128)
+    PKV_CASE8(PKV_BF16, __nv_bfloat16, 256)
+    PKV_CASE8(PKV_F16, __half, 128)
+    PKV_CASE8(PKV_F16, __half, 256)
+#undef PKV_CASE8
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for the fp8 cache", h.D);
+  }
 #define PKV_CASE(DT, TT, DD) \
-  if (h.dtype == DT && h.D == DD) return launch_decode<TT, DD>(h, W);
+  if (h.dtype == DT && h.D == DD) return launch_decode<TT, TT, DD>(h, W);
   PKV_CASE(PKV_BF16, __nv_bfloat16, 64)
   PKV_CASE(PKV_BF16, __nv_bfloat16, 128)
   PKV_CASE(PKV_BF16, __nv_bfloat16, 256)
@@ -1236,12 +1533,12 @@ int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t
 }
 
 namespace {
-int decode_entry(const void* q, const void* k_cache, const void* v_cache,
-                 const int32_t* block_tables, int32_t max_blocks_per_seq,
-                 const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
-                 int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
-                 float scale, void* out, void* workspace, size_t workspace_bytes,
-                 int32_t num_warps, int32_t dtype, void* stream) {
+HostArgs host_args(const void* q, const void* k_cache, const void* v_cache,
+                   const int32_t* block_tables, int32_t max_blocks_per_seq,
+                   const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                   int32_t num_kv_heads, int32_t head_dim, int32_t block_size, int32_t num_blocks,
+                   float scale, void* out, void* workspace, size_t workspace_bytes,
+                   int32_t num_warps, int32_t dtype, void* stream) {
   HostArgs h;
   h.q = q;
   h.k_cache = k_cache;
@@ -1262,6 +1559,10 @@ int decode_entry(const void* q, const void* k_cache, const void* v_cache,
   h.num_warps = num_warps;
   h.dtype = dtype;
   h.stream = static_cast<cudaStream_t>(stream);
+  return h;
+}
+
+int decode_entry(const HostArgs& h) {
   int W = 0;
   int rc = validate(h, &W);
   if (rc != PKV_OK) return rc;
@@ -1277,9 +1578,10 @@ int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache
                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                          int32_t num_blocks, float scale, void* out, void* workspace,
                          size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
-  return decode_entry(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                      num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                      scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
+  return decode_entry(host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                                context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                                block_size, num_blocks, scale, out, workspace, workspace_bytes,
+                                num_warps, dtype, stream));
 }
 
 int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -1289,26 +1591,10 @@ int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k
                     int32_t num_blocks, float scale, void* out, void* workspace,
                     size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
   // Validate the attention arguments first, so that a refused call writes nothing.
-  HostArgs h;
-  h.q = q;
-  h.k_cache = k_cache;
-  h.v_cache = v_cache;
-  h.block_tables = block_tables;
-  h.MAXB = max_blocks_per_seq;
-  h.context_lens = context_lens;
-  h.S = num_seqs;
-  h.Hq = num_q_heads;
-  h.Hkv = num_kv_heads;
-  h.D = head_dim;
-  h.block_size = block_size;
-  h.NB = num_blocks;
-  h.scale = scale;
-  h.out = out;
-  h.workspace = workspace;
-  h.workspace_bytes = workspace_bytes;
-  h.num_warps = num_warps;
-  h.dtype = dtype;
-  h.stream = static_cast<cudaStream_t>(stream);
+  const HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                               context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, num_blocks, scale, out, workspace, workspace_bytes,
+                               num_warps, dtype, stream);
   int W = 0;
   int rc = validate(h, &W);
   if (rc != PKV_OK) return rc;
@@ -1316,6 +1602,48 @@ int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k
   rc = launch_decode_append(k_new, v_new, block_tables, max_blocks_per_seq, context_lens,
                             num_seqs, k_cache, v_cache, num_blocks, num_kv_heads, block_size,
                             head_dim, dtype, stream);
+  if (rc != PKV_OK) return rc;
+  rc = dispatch(h, W);
+  return rc == PKV_OK ? ok() : rc;
+}
+
+int pkv_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
+                             const float* k_scale, const float* v_scale,
+                             const int32_t* block_tables, int32_t max_blocks_per_seq,
+                             const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                             int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                             int32_t num_blocks, float scale, void* out, void* workspace,
+                             size_t workspace_bytes, int32_t num_warps, int32_t dtype,
+                             void* stream) {
+  HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                         scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
+  h.fp8 = true;
+  h.k_scale = k_scale;
+  h.v_scale = v_scale;
+  return decode_entry(h);
+}
+
+int pkv_decode_step_fp8(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                        void* v_cache, const float* k_scale, const float* v_scale,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                        int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                        int32_t num_blocks, float scale, void* out, void* workspace,
+                        size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
+  HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                         scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
+  h.fp8 = true;
+  h.k_scale = k_scale;
+  h.v_scale = v_scale;
+  int W = 0;
+  int rc = validate(h, &W);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs == 0) return ok();
+  rc = launch_kv_write_fp8(k_new, v_new, nullptr, block_tables, max_blocks_per_seq, context_lens,
+                           num_seqs, k_cache, v_cache, k_scale, v_scale, num_blocks,
+                           num_kv_heads, head_dim, dtype, stream);
   if (rc != PKV_OK) return rc;
   rc = dispatch(h, W);
   return rc == PKV_OK ? ok() : rc;

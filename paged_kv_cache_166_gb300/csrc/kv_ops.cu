@@ -2,6 +2,9 @@
 // copy-on-write.  Both are pure data movement in 16-byte vectors: each thread
 // moves one 16-byte piece of one row, so a warp covers contiguous bytes of a
 // [head_dim] row on both sides.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_fp8.h>
 #include <cuda_runtime.h>
 
 #include <cstdint>
@@ -86,6 +89,112 @@ __global__ void decode_append_kernel(const uint4* __restrict__ k, const uint4* _
   }
 }
 
+// ---- fp8 (E4M3) quantising cache write --------------------------------------------
+// Byte of token t (0..15) inside a 16-byte head_dim row of an fp8 V tile: the
+// tokens are stored in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15.
+__device__ __forceinline__ int fp8_v_pos(int t) {
+  return t < 8 ? 4 * (t >> 1) + (t & 1) : 4 * ((t - 8) >> 1) + 2 + (t & 1);
+}
+
+// 16 consecutive input elements widened to fp32 (16-byte aligned source).
+__device__ __forceinline__ void load16(const float* p, float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const float4 f = __ldg(reinterpret_cast<const float4*>(p) + i);
+    x[4 * i] = f.x;
+    x[4 * i + 1] = f.y;
+    x[4 * i + 2] = f.z;
+    x[4 * i + 3] = f.w;
+  }
+}
+__device__ __forceinline__ void load16(const __half* p, float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
+      x[8 * i + 2 * j] = f.x;
+      x[8 * i + 2 * j + 1] = f.y;
+    }
+  }
+}
+__device__ __forceinline__ void load16(const __nv_bfloat16* p, float (&x)[16]) {
+#pragma unroll
+  for (int i = 0; i < 2; ++i) {
+    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + i);
+    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
+      x[8 * i + 2 * j] = f.x;
+      x[8 * i + 2 * j + 1] = f.y;
+    }
+  }
+}
+
+// E4M3 codes of x[i] / scale, i < 16: the quotient a correctly rounded fp32
+// division, then round to nearest even with saturation to +-448 (the hardware
+// conversion); byte i of the result is element i.
+__device__ __forceinline__ uint4 quantize16(const float (&x)[16], float scale) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 8; ++j) {
+    const float2 q = make_float2(__fdiv_rn(x[2 * j], scale), __fdiv_rn(x[2 * j + 1], scale));
+    const uint32_t pair = __nv_cvt_float2_to_fp8x2(q, __NV_SATFINITE, __NV_E4M3);
+    w[j >> 1] |= (pair & 0xffffu) << (16 * (j & 1));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+// Token i (or sequence i's new token, when slots is NULL: position ctx[i] - 1 of
+// its block table) for KV head h, elements [16 c, 16 c + 16) of the row:
+//   K8[slot / 16, h, slot % 16, 16c + e]       = E4M3(k[i, h, 16c + e] / k_scale[h])
+//   V8[slot / 16, h, 16c + e, V_POS[slot % 16]] = E4M3(v[i, h, 16c + e] / v_scale[h])
+template <typename Tin>
+__global__ void kv_write_fp8_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
+                                    const int32_t* __restrict__ slots,
+                                    const int32_t* __restrict__ tables, int32_t MAXB,
+                                    const int32_t* __restrict__ ctx, int64_t total, int32_t Hkv,
+                                    int32_t D, int32_t NB, const float* __restrict__ ks,
+                                    const float* __restrict__ vs, uint8_t* __restrict__ kc,
+                                    uint8_t* __restrict__ vc) {
+  asm volatile("griddepcontrol.launch_dependents;");
+  const int groups = D / 16;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t th = i / groups;
+    const int32_t c = static_cast<int32_t>(i - th * groups);
+    const int64_t t = th / Hkv;
+    const int32_t h = static_cast<int32_t>(th - t * Hkv);
+    int32_t slot;
+    if (slots != nullptr) {
+      slot = __ldg(slots + t);
+      if (slot < 0 || slot >= NB * 16) continue;
+    } else {
+      const int32_t n = __ldg(ctx + t);
+      if (n <= 0 || n > MAXB * 16) continue;
+      const int32_t b = __ldg(tables + t * MAXB + (n - 1) / 16);
+      if (b < 0 || b >= NB) continue;
+      slot = b * 16 + (n - 1) % 16;
+    }
+    const int64_t tile = static_cast<int64_t>(slot / 16) * Hkv + h;
+    const int32_t off = slot % 16;
+    const int64_t src = th * D + 16 * c;
+    float x[16];
+    load16(k + src, x);
+    *reinterpret_cast<uint4*>(kc + (tile * 16 + off) * D + 16 * c) = quantize16(x, __ldg(ks + h));
+    load16(v + src, x);
+    const uint4 q = quantize16(x, __ldg(vs + h));
+    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
+    uint8_t* const col = vc + (tile * D + 16 * c) * 16 + fp8_v_pos(off);
+#pragma unroll
+    for (int e = 0; e < 16; ++e) col[e * 16] = static_cast<uint8_t>(w[e >> 2] >> (8 * (e & 3)));
+  }
+}
+
 int grid_for(int64_t work, int threads) {
   int sms = 0, dev = 0;
   if (device_sm_count(&sms, &dev) != PKV_OK) sms = 132;
@@ -95,6 +204,45 @@ int grid_for(int64_t work, int threads) {
 }
 
 }  // namespace
+
+int launch_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
+                        const int32_t* block_tables, int32_t max_blocks_per_seq,
+                        const int32_t* context_lens, int32_t num_tokens, void* k_cache,
+                        void* v_cache, const float* k_scale, const float* v_scale,
+                        int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
+                        int32_t dtype, void* stream) {
+  PKV_REQUIRE(dtype == PKV_F32 || dtype == PKV_F16 || dtype == PKV_BF16, PKV_ERR_DTYPE,
+              "input dtype %d is not f32, f16 or bf16", dtype);
+  PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && num_kv_heads > 0 && head_dim > 0 &&
+                  head_dim % 16 == 0,
+              PKV_ERR_INVALID_ARG, "bad sizes (head_dim must be a positive multiple of 16)");
+  PKV_REQUIRE(static_cast<int64_t>(num_blocks) * 16 < (int64_t(1) << 31), PKV_ERR_INVALID_ARG,
+              "num_blocks * 16 must be < 2^31");
+  if (num_tokens == 0) return PKV_OK;
+  PKV_REQUIRE(k && v && k_cache && v_cache && k_scale && v_scale, PKV_ERR_INVALID_ARG,
+              "NULL pointer");
+  PKV_REQUIRE(slot_mapping || (block_tables && context_lens), PKV_ERR_INVALID_ARG,
+              "NULL slot mapping / block tables");
+  PKV_REQUIRE(aligned(k, 16) && aligned(v, 16) && aligned(k_cache, 16) && aligned(v_cache, 16),
+              PKV_ERR_INVALID_ARG, "k, v and caches must be 16-byte aligned");
+  const int64_t total = static_cast<int64_t>(num_tokens) * num_kv_heads * (head_dim / 16);
+  const int threads = 256;
+  const dim3 grid(grid_for(total, threads));
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  auto* kc = static_cast<uint8_t*>(k_cache);
+  auto* vc = static_cast<uint8_t*>(v_cache);
+#define PKV_FP8_WRITE(TT)                                                                   \
+  kv_write_fp8_kernel<TT><<<grid, threads, 0, st>>>(                                        \
+      static_cast<const TT*>(k), static_cast<const TT*>(v), slot_mapping, block_tables,     \
+      max_blocks_per_seq, context_lens, total, num_kv_heads, head_dim, num_blocks, k_scale, \
+      v_scale, kc, vc)
+  if (dtype == PKV_F32) PKV_FP8_WRITE(float);
+  else if (dtype == PKV_F16) PKV_FP8_WRITE(__half);
+  else PKV_FP8_WRITE(__nv_bfloat16);
+#undef PKV_FP8_WRITE
+  PKV_CUDA(cudaGetLastError());
+  return PKV_OK;
+}
 
 int launch_decode_append(const void* k_new, const void* v_new, const int32_t* block_tables,
                          int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
@@ -129,6 +277,8 @@ int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int3
                  int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
   const int elt = element_bytes(dtype);
   PKV_REQUIRE(elt != 0, PKV_ERR_DTYPE, "unknown dtype %d", dtype);
+  PKV_REQUIRE(dtype != PKV_FP8_E4M3, PKV_ERR_DTYPE,
+              "fp8 caches are written by pkv_kv_write_fp8 (quantising, V tiles transposed)");
   PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && num_kv_heads > 0 && block_size > 0 &&
                   head_dim > 0,
               PKV_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0)");
@@ -149,6 +299,19 @@ int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int3
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache));
   PKV_CUDA(cudaGetLastError());
   return ok();
+}
+
+int pkv_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
+                     int32_t num_tokens, void* k_cache, void* v_cache, const float* k_scale,
+                     const float* v_scale, int32_t num_blocks, int32_t num_kv_heads,
+                     int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
+  PKV_REQUIRE(block_size == 16, PKV_ERR_UNSUPPORTED, "fp8 caches use block_size 16, not %d",
+              block_size);
+  PKV_REQUIRE(num_tokens == 0 || slot_mapping, PKV_ERR_INVALID_ARG, "NULL slot_mapping");
+  const int rc = launch_kv_write_fp8(k, v, slot_mapping, nullptr, 0, nullptr, num_tokens, k_cache,
+                                     v_cache, k_scale, v_scale, num_blocks, num_kv_heads,
+                                     head_dim, dtype, stream);
+  return rc == PKV_OK ? ok() : rc;
 }
 
 int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int32_t num_pairs,

@@ -63,27 +63,32 @@ def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
                                  dtype_code(k), _stream(dev)))
 
 
-def default_num_warps(head_dim: int, dtype: torch.dtype) -> int:
+def default_num_warps(head_dim: int, dtype) -> int:
+    """Default worker warps; ``dtype`` as in ``workspace_bytes``."""
+    code = N.PKV_FP8_E4M3 if dtype == "fp8" else _DTYPES[dtype]
     n = ctypes.c_int32(0)
-    N.check(N.lib().pkv_decode_default_warps(head_dim, _DTYPES[dtype], ctypes.byref(n)))
+    N.check(N.lib().pkv_decode_default_warps(head_dim, code, ctypes.byref(n)))
     return n.value
 
 
-def workspace_bytes(num_q_heads: int, num_kv_heads: int, head_dim: int, dtype: torch.dtype,
+def workspace_bytes(num_q_heads: int, num_kv_heads: int, head_dim: int, dtype,
                     num_warps: int = 0) -> int:
+    """Decode workspace bytes; ``dtype`` is q's torch dtype, or "fp8" for
+    attention over the fp8 cache."""
+    code = N.PKV_FP8_E4M3 if dtype == "fp8" else _DTYPES[dtype]
     n = ctypes.c_size_t(0)
-    N.check(N.lib().pkv_decode_workspace_size(num_q_heads, num_kv_heads, head_dim,
-                                              _DTYPES[dtype], num_warps, ctypes.byref(n)))
+    N.check(N.lib().pkv_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, code,
+                                              num_warps, ctypes.byref(n)))
     return n.value
 
 
 def get_workspace(device: torch.device, group: int, head_dim: int, num_warps: int,
-                  nbytes: int) -> torch.Tensor:
+                  nbytes: int, kind: str = "") -> torch.Tensor:
     """A zero-filled device workspace of ``nbytes`` for one layout (group size,
-    head_dim, warp count), cached per device and stream: one workspace must not
-    serve two launches that may overlap, nor two layouts."""
+    head_dim, warp count, cache kind), cached per device and stream: one workspace
+    must not serve two launches that may overlap, nor two layouts."""
     key = (device.index, torch.cuda.current_stream(device).cuda_stream, group, head_dim,
-           num_warps)
+           num_warps, kind)
     ws = _WORKSPACES.get(key)
     if ws is None or ws.numel() < nbytes:
         ws = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
@@ -152,6 +157,115 @@ def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     return out
 
 
+def _fp8_caches(k_cache, v_cache):
+    """(k_cache, v_cache) as uint8 views: fp8 caches may be uint8 or float8_e4m3fn."""
+    out = []
+    for c in (k_cache, v_cache):
+        if c.dtype == getattr(torch, "float8_e4m3fn", None):
+            c = c.view(torch.uint8)
+        if c.dtype != torch.uint8:
+            raise TypeError("fp8 caches must be uint8 or float8_e4m3fn tensors")
+        out.append(c)
+    return out
+
+
+def _check_scales(k_scale, v_scale, Hkv):
+    for t in (k_scale, v_scale):
+        if t.dtype != torch.float32 or t.shape != (Hkv,):
+            raise ValueError(f"scales must be float32 [{Hkv}]")
+
+
+def paged_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                       k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                       v_scale: torch.Tensor) -> None:
+    """Quantise k, v [T, Hkv, D] to fp8 (E4M3, per-KV-head scales) and scatter them:
+    k_cache [NB, Hkv, 16, D], v_cache [NB, Hkv, D, 16] (uint8)."""
+    kc, vc = _fp8_caches(k_cache, v_cache)
+    dev = _check_cuda(k, v, slot_mapping, kc, vc, k_scale, v_scale)
+    _check_index(slot_mapping, "slot_mapping")
+    if k.shape != v.shape or k.dim() != 3 or kc.dim() != 4 or vc.dim() != 4:
+        raise ValueError("expected k, v [T, Hkv, D], k_cache [NB, Hkv, 16, D], v_cache [NB, Hkv, D, 16]")
+    T, Hkv, D = k.shape
+    NB, B = kc.shape[0], kc.shape[2]
+    if kc.shape != (NB, Hkv, B, D) or vc.shape != (NB, Hkv, D, B) or slot_mapping.shape != (T,):
+        raise ValueError("shape mismatch between tokens, slots and fp8 caches")
+    _check_scales(k_scale, v_scale, Hkv)
+    if k.dtype != v.dtype:
+        raise TypeError("k and v must share a dtype")
+    N.check(N.lib().pkv_kv_write_fp8(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
+                                     kc.data_ptr(), vc.data_ptr(), k_scale.data_ptr(),
+                                     v_scale.data_ptr(), NB, Hkv, B, D, dtype_code(k),
+                                     _stream(dev)))
+
+
+def _fp8_shapes(q, kc, vc, block_tables, context_lens, out):
+    if q.dim() != 3 or kc.dim() != 4 or vc.dim() != 4:
+        raise ValueError("expected q [S, Hq, D], k_cache [NB, Hkv, 16, D], v_cache [NB, Hkv, D, 16]")
+    S, Hq, D = q.shape
+    NB, Hkv, B, D2 = kc.shape
+    if D2 != D or vc.shape != (NB, Hkv, D, B) or out.shape != q.shape:
+        raise ValueError("head_dim mismatch, v_cache not [NB, Hkv, D, 16] or out shape != q shape")
+    if block_tables.dim() != 2 or block_tables.shape[0] != S or context_lens.shape != (S,):
+        raise ValueError("block_tables must be [S, max_blocks] and context_lens [S]")
+    if q.dtype != out.dtype:
+        raise TypeError("q and out must share a dtype")
+    _check_index(block_tables, "block_tables")
+    _check_index(context_lens, "context_lens")
+    return S, Hq, D, NB, Hkv, B, block_tables.shape[1]
+
+
+def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                               k_scale: torch.Tensor, v_scale: torch.Tensor,
+                               block_tables: torch.Tensor, context_lens: torch.Tensor,
+                               scale: float, out: torch.Tensor,
+                               workspace: Optional[torch.Tensor] = None,
+                               num_warps: int = 0) -> torch.Tensor:
+    """Decode attention of q [S, Hq, D] (f16/bf16) over fp8 caches; writes and returns out."""
+    kc, vc = _fp8_caches(k_cache, v_cache)
+    dev = _check_cuda(q, kc, vc, k_scale, v_scale, block_tables, context_lens, out)
+    S, Hq, D, NB, Hkv, B, MAXB = _fp8_shapes(q, kc, vc, block_tables, context_lens, out)
+    _check_scales(k_scale, v_scale, Hkv)
+    need = workspace_bytes(Hq, Hkv, D, "fp8", num_warps)
+    ws = get_workspace(dev, Hq // Hkv, D, num_warps, need, "fp8") if workspace is None else workspace
+    if ws.numel() * ws.element_size() < need:
+        raise ValueError(f"workspace smaller than the {need} bytes needed")
+    N.check(N.lib().pkv_decode_attention_fp8(
+        q.data_ptr(), kc.data_ptr(), vc.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
+        block_tables.data_ptr(), MAXB, context_lens.data_ptr(), S, Hq, Hkv, D, B, NB,
+        float(scale), out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), num_warps,
+        dtype_code(q), _stream(dev)))
+    return out
+
+
+def paged_decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                          k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                          v_scale: torch.Tensor, block_tables: torch.Tensor,
+                          context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                          workspace: Optional[torch.Tensor] = None,
+                          num_warps: int = 0) -> torch.Tensor:
+    """One decode step over fp8 caches: quantise and write each sequence's new token
+    (position context_lens[s] - 1), then attend (two launches, programmatic
+    dependent launch)."""
+    kc, vc = _fp8_caches(k_cache, v_cache)
+    dev = _check_cuda(q, k_new, v_new, kc, vc, k_scale, v_scale, block_tables, context_lens, out)
+    S, Hq, D, NB, Hkv, B, MAXB = _fp8_shapes(q, kc, vc, block_tables, context_lens, out)
+    _check_scales(k_scale, v_scale, Hkv)
+    if k_new.shape != (S, Hkv, D) or v_new.shape != (S, Hkv, D):
+        raise ValueError("k_new and v_new must be [S, Hkv, D]")
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise TypeError("k_new and v_new must share the dtype of q")
+    need = workspace_bytes(Hq, Hkv, D, "fp8", num_warps)
+    ws = get_workspace(dev, Hq // Hkv, D, num_warps, need, "fp8") if workspace is None else workspace
+    if ws.numel() * ws.element_size() < need:
+        raise ValueError(f"workspace smaller than the {need} bytes needed")
+    N.check(N.lib().pkv_decode_step_fp8(
+        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+        k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(), MAXB,
+        context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), out.data_ptr(),
+        ws.data_ptr(), ws.numel() * ws.element_size(), num_warps, dtype_code(q), _stream(dev)))
+    return out
+
+
 def decode_status(workspace: torch.Tensor) -> int:
     """Reads and clears the device status bits the decode kernels recorded."""
     v = ctypes.c_int32(0)
@@ -170,6 +284,8 @@ def paged_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
         raise ValueError("src_dst_pairs must hold pairs")
     NB = k_cache.shape[0]
     block_elems = k_cache[0].numel()
+    fp8 = k_cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None))
+    code = N.PKV_FP8_E4M3 if fp8 else dtype_code(k_cache)
     N.check(N.lib().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
-                                    src_dst_pairs.data_ptr(), n, NB, block_elems,
-                                    dtype_code(k_cache), _stream(dev)))
+                                    src_dst_pairs.data_ptr(), n, NB, block_elems, code,
+                                    _stream(dev)))

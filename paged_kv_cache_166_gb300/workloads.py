@@ -29,6 +29,7 @@ STREAM_V_POOL = 4
 STREAM_K_NEW = 5
 STREAM_V_NEW = 6
 STREAM_SUFFIX = 7
+STREAM_SCALES = 8
 
 
 @dataclasses.dataclass(frozen=True)
@@ -171,6 +172,32 @@ def fill_normal_(t, seed: int, stream: int, chunk_rows: int = 4096):
         x = torch.randn((r1 - r0,) + tuple(t.shape[1:]), generator=gen, device=t.device,
                         dtype=torch.float32)
         t[r0:r1].copy_(x)
+    return t
+
+
+def fp8_scales(num_kv_heads: int, seed: int) -> np.ndarray:
+    """Per-KV-head fp32 scales for an fp8 cache of N(0,1) data: a seeded value in
+    [3, 6] / 448 per head, so that 3 to 6 standard deviations reach the largest
+    E4M3 magnitude."""
+    return (rng(seed, STREAM_SCALES).uniform(3.0, 6.0, num_kv_heads) / 448.0).astype(np.float32)
+
+
+def fill_fp8_codes_(t, scales, seed: int, stream: int, chunk_rows: int = 4096):
+    """Fill a uint8 fp8 cache ([NB, Hkv, ...], head axis 1) with the E4M3 codes of
+    N(0,1) draws divided by the head's scale and clipped to +-448, chunked along
+    dim 0.  The codes come from torch's float8_e4m3fn cast of the draws: synthetic
+    input only (never a NaN code)."""
+    import torch
+    gen = torch.Generator(device=t.device)
+    gen.manual_seed(int(seed) * 1000003 + int(stream))
+    inv = (1.0 / torch.as_tensor(np.asarray(scales, dtype=np.float32), device=t.device))
+    inv = inv.view((1, -1) + (1,) * (t.dim() - 2))
+    n = t.shape[0]
+    for r0 in range(0, n, chunk_rows):
+        r1 = min(n, r0 + chunk_rows)
+        x = torch.randn((r1 - r0,) + tuple(t.shape[1:]), generator=gen, device=t.device,
+                        dtype=torch.float32)
+        t[r0:r1].copy_((x * inv).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8))
     return t
 
 

@@ -85,6 +85,11 @@ namespace pkv {
 #ifndef PKV_PREFETCH_TABLES
 #define PKV_PREFETCH_TABLES 1
 #endif
+// fp8 cache: widen codes to f16 with integer ops (value * 2^-8) instead of the
+// conversion instruction.
+#ifndef PKV_FP8_WIDEN_ALU
+#define PKV_FP8_WIDEN_ALU 1
+#endif
 // Skip the accumulator rescale of a step whose running maxima did not change.
 #ifndef PKV_RESCALE_SKIP
 #define PKV_RESCALE_SKIP 0
@@ -581,11 +586,30 @@ struct Fp8State {
   float m0, m1, l0, l1;
   float sl2, vs;    // score scale (log2 units, k_scale folded in), v_scale
 
+#if PKV_FP8_WIDEN_ALU
+  // Bytes 0-1 (widen) or 2-3 (widen_hi) of w as an f16 pair holding value * 2^-8:
+  // the E4M3 exponent and mantissa bits shifted left by 7 are exactly the f16 bits
+  // of value * 2^-8 (subnormals included), and the sign moves from bit 14 to 15.
+  static __device__ __forceinline__ uint32_t spread(uint32_t pair16) {
+    const uint32_t y = pair16 << 7;
+    return y + (y & 0x40004000u);
+  }
+  static __device__ __forceinline__ uint32_t widen(uint32_t w) {
+    return spread(__byte_perm(w, 0u, 0x4140));
+  }
+  static __device__ __forceinline__ uint32_t widen_hi(uint32_t w) {
+    return spread(__byte_perm(w, 0u, 0x4342));
+  }
+  static constexpr float kWidenScale = 256.f;
+#else
   static __device__ __forceinline__ uint32_t widen(uint32_t two_codes) {
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
         static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
   }
+  static __device__ __forceinline__ uint32_t widen_hi(uint32_t w) { return widen(w >> 16); }
+  static constexpr float kWidenScale = 1.f;
+#endif
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -595,8 +619,8 @@ struct Fp8State {
   }
 
   __device__ __forceinline__ void set_scales(float k_scale, float v_scale, float scale_log2) {
-    sl2 = scale_log2 * k_scale;
-    vs = v_scale;
+    sl2 = scale_log2 * (k_scale * kWidenScale);
+    vs = v_scale * kWidenScale;
   }
 
   // The G query rows of the unit, read from global memory (8 bytes per lane and
@@ -629,13 +653,13 @@ struct Fp8State {
       ptx::ldsm_x4(ktile + tile_offset<kSub, false>(krow, 2 * p + (mi >> 1)), w);
       a[0] = widen(w[0]);
       a[1] = widen(w[1]);
-      a[2] = widen(w[0] >> 16);
-      a[3] = widen(w[1] >> 16);
+      a[2] = widen_hi(w[0]);
+      a[3] = widen_hi(w[1]);
       ptx::mma_16816<__half>(c0, a, qb[2 * p][0], qb[2 * p][1]);
       a[0] = widen(w[2]);
       a[1] = widen(w[3]);
-      a[2] = widen(w[2] >> 16);
-      a[3] = widen(w[3] >> 16);
+      a[2] = widen_hi(w[2]);
+      a[3] = widen_hi(w[3]);
       ptx::mma_16816<__half>(c1, a, qb[2 * p + 1][0], qb[2 * p + 1][1]);
     }
     float x[4];
@@ -686,8 +710,8 @@ struct Fp8State {
       ptx::ldsm_x4(vtile + (32 * p + 8 * mi + r) * 16, w);
       a[0] = widen(w[0]);
       a[1] = widen(w[1]);
-      a[2] = widen(w[0] >> 16);
-      a[3] = widen(w[1] >> 16);
+      a[2] = widen_hi(w[0]);
+      a[3] = widen_hi(w[1]);
       if (partial) {
         a[0] &= mlo;
         a[1] &= mlo;
@@ -697,8 +721,8 @@ struct Fp8State {
       ptx::mma_16816<__half>(o[2 * p], a, pb0, pb1);
       a[0] = widen(w[2]);
       a[1] = widen(w[3]);
-      a[2] = widen(w[2] >> 16);
-      a[3] = widen(w[3] >> 16);
+      a[2] = widen_hi(w[2]);
+      a[3] = widen_hi(w[3]);
       if (partial) {
         a[0] &= mlo;
         a[1] &= mlo;

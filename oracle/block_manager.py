@@ -38,6 +38,16 @@ The rules, in the pages' order:
 * ``free`` returns every block of the sequence's table, decrementing in reverse
   table order (the order is open on the pages; reverse order makes the worked
   example's request C receive P0 then P1, as the example states).
+* Preemption by swapping ("PagedAttention — how vLLM stopped wasting 80%...",
+  section "Preemption: what happens when memory runs out anyway": copy the
+  preempted sequence's blocks out to CPU RAM, and back into freshly allocated
+  GPU blocks when it resumes; "PagedAttention and vLLM: Virtual Memory for the
+  KV Cache", section "L3": preemption is all-or-nothing per sequence):
+  ``swap_out`` returns the sequence's table (the blocks whose contents go to
+  host memory, in logical order) and gives every block back as ``free`` does,
+  keeping the sequence's length; ``swap_in`` gives it ``ceil(length / B)``
+  newly allocated blocks, all or nothing, in logical order.  A swapped-out
+  sequence cannot be appended to, forked or exported until it is swapped in.
 
 Sequence ids are handed out 0, 1, 2, ... and never reused.
 """
@@ -68,6 +78,7 @@ class BlockManager:
         self.refcount: List[int] = [0] * num_blocks
         self.tables: dict = {}
         self.lengths: dict = {}
+        self.swapped: set = set()
         self._next_seq = 0
 
     # --- free list and refcounts -------------------------------------------------
@@ -102,7 +113,7 @@ class BlockManager:
         return sid
 
     def fork(self, parent: int) -> int:
-        self._check_seq(parent)
+        self._check_resident(parent)
         child = self.create()
         self.tables[child] = list(self.tables[parent])
         self.lengths[child] = self.lengths[parent]
@@ -116,10 +127,35 @@ class BlockManager:
             self.decref(b)
         del self.tables[sid]
         del self.lengths[sid]
+        self.swapped.discard(sid)
+
+    def swap_out(self, sid: int) -> List[int]:
+        """Preempt ``sid``: its table (blocks to copy to host, logical order); every
+        block is given back (reverse order); the length is kept."""
+        self._check_resident(sid)
+        table = list(self.tables[sid])
+        for b in reversed(table):
+            self.decref(b)
+        self.tables[sid] = []
+        self.swapped.add(sid)
+        return table
+
+    def swap_in(self, sid: int) -> List[int]:
+        """Resume ``sid``: ``ceil(length / B)`` fresh blocks (all or nothing)."""
+        self._check_seq(sid)
+        if sid not in self.swapped:
+            raise InvalidOperation(f"sequence {sid} is not swapped out")
+        n = -(-self.lengths[sid] // self.block_size)
+        if n > self.num_free():
+            raise OutOfBlocks("pool cannot hold the swapped-in sequence")
+        table = [self.alloc() for _ in range(n)]
+        self.tables[sid] = table
+        self.swapped.discard(sid)
+        return table
 
     def blocks_needed(self, sid: int, n: int) -> int:
         """Blocks an append of ``n`` tokens would take from the free list."""
-        self._check_seq(sid)
+        self._check_resident(sid)
         B = self.block_size
         t = self.lengths[sid]
         table = self.tables[sid]
@@ -162,7 +198,7 @@ class BlockManager:
         tab = np.zeros((len(seqs), max_blocks), dtype=np.int32)
         ctx = np.zeros(len(seqs), dtype=np.int32)
         for r, sid in enumerate(seqs):
-            self._check_seq(sid)
+            self._check_resident(sid)
             t = self.tables[sid]
             if len(t) > max_blocks:
                 raise InvalidOperation("table longer than max_blocks")
@@ -173,3 +209,8 @@ class BlockManager:
     def _check_seq(self, sid: int) -> None:
         if sid not in self.tables:
             raise InvalidOperation(f"unknown sequence {sid}")
+
+    def _check_resident(self, sid: int) -> None:
+        self._check_seq(sid)
+        if sid in self.swapped:
+            raise InvalidOperation(f"sequence {sid} is swapped out")

@@ -15,6 +15,11 @@ TEST INFRASTRUCTURE (see ``oracle/__init__.py``): never imported by the library.
   from ``src`` to ``dst`` ("allocates a new physical block, copies the
   content", same page, section "Copy-on-Write for Beam Search and Parallel
   Sampling").
+* ``swap_out_blocks`` / ``swap_in_blocks``: preemption by swapping copies a
+  sequence's blocks out to host memory and back into freshly allocated blocks
+  ("PagedAttention — how vLLM stopped wasting 80%...", section "Preemption:
+  what happens when memory runs out anyway"): the host buffer holds the blocks
+  in the order of the id list, each block whole (every KV head and slot).
 """
 from __future__ import annotations
 
@@ -36,3 +41,17 @@ def copy_blocks(k_cache: np.ndarray, v_cache: np.ndarray, src_dst_pairs) -> None
     for src, dst in np.asarray(src_dst_pairs, dtype=np.int64).reshape(-1, 2).tolist():
         k_cache[dst] = k_cache[src]
         v_cache[dst] = v_cache[src]
+
+
+def swap_out_blocks(k_cache: np.ndarray, v_cache: np.ndarray, block_ids):
+    """Host copies ``[n, ...]`` of the K and V blocks ``block_ids``, in that order."""
+    ids = np.asarray(block_ids, dtype=np.int64)
+    return k_cache[ids].copy(), v_cache[ids].copy()
+
+
+def swap_in_blocks(host_k: np.ndarray, host_v: np.ndarray, block_ids, k_cache: np.ndarray,
+                   v_cache: np.ndarray) -> None:
+    """Block ``block_ids[i]`` of each cache becomes host block ``i``."""
+    for i, b in enumerate(np.asarray(block_ids, dtype=np.int64).tolist()):
+        k_cache[b] = host_k[i]
+        v_cache[b] = host_v[i]

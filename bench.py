@@ -524,6 +524,82 @@ def native(args):
         dist.destroy_process_group()
 
 
+def swap_bench(args):
+    """Preemption by swapping: the blocks of a quarter of the workload's context
+    (whole sequences, longest first) copied to page-locked host memory and back,
+    timed with CUDA events; against a plain copy of the same bytes between one
+    contiguous device buffer and one pinned host buffer (the link's copy rate)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_166_gb300 as pkv
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, 0, args.kv)
+    B = w.block_size
+    nb = (lens + B - 1) // B
+    tables = host["tables"].numpy()
+    order = np.argsort(-lens)
+    picked, total = [], 0
+    for s_ in order:
+        if total >= nb.sum() // 4:
+            break
+        picked.append(int(s_))
+        total += int(nb[s_])
+    ids = np.concatenate([tables[s_, :nb[s_]] for s_ in picked]).astype(np.int32)
+    n = len(ids)
+    ids_d = torch.from_numpy(ids).to(device)
+    hk = torch.empty((n,) + tuple(kc.shape[1:]), dtype=kc.dtype).pin_memory()
+    hv = torch.empty((n,) + tuple(vc.shape[1:]), dtype=vc.dtype).pin_memory()
+    block_bytes = kc[0].numel() * kc.element_size()
+    moved = 2 * n * block_bytes                      # K and V, one direction
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    t_out = timed(lambda: pkv.paged_swap_out(kc, vc, ids_d, hk, hv))
+    t_in = timed(lambda: pkv.paged_swap_in(hk, hv, ids_d, kc, vc))
+    # the link's copy rate for the same bytes: contiguous device <-> pinned host
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=device)
+    hbuf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    c_out = timed(lambda: hbuf.copy_(dbuf, non_blocking=True))
+    c_in = timed(lambda: dbuf.copy_(hbuf, non_blocking=True))
+    gbs = lambda ms: moved / (ms * 1e-3) / 1e9
+    value = 2 * moved / ((t_out + t_in) * 1e-3) / 1e9
+    peak = 2 * moved / ((c_out + c_in) * 1e-3) / 1e9
+    line = {
+        "metric": "swap GB/s: a sequence set's K/V blocks to pinned host memory and back",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_out + t_in, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if args.kv == "fp8" else w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: {len(picked)} longest sequences, {n} blocks of "
+                               f"{block_bytes} B per cache ({2 * n * block_bytes / 1e6:.1f} MB "
+                               "each way)", "op": "paged_swap_out then paged_swap_in"},
+        "swap_out": {"ms": round(t_out, 4), "gbs": round(gbs(t_out), 1)},
+        "swap_in": {"ms": round(t_in, 4), "gbs": round(gbs(t_in), 1)},
+        "roofline": {"bound": "link", "achieved": round(value, 1), "peak": round(peak, 1),
+                     "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
+                     "peak_source": "measured in this run: contiguous cudaMemcpyAsync of the "
+                                    "same bytes device->pinned host and back",
+                     "copy_out_gbs": round(gbs(c_out), 1), "copy_in_gbs": round(gbs(c_in), 1)},
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -564,6 +640,8 @@ def main():
     ap.add_argument("--workload", default="mha13b",
                     choices=["tiny", "mha13b", "gqa70b", "prefix", "longctx"])
     ap.add_argument("--num-warps", type=int, default=0)
+    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
+                    help="decode: the decode step (default); swap: blocks to host and back")
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="cache element type: the workload's dtype, or fp8 E4M3 with per-head scales")
     ap.add_argument("--soak-s", type=float, default=0.6,
@@ -576,6 +654,9 @@ def main():
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps
     if args.workload == "prefix":
         ap.error("the shared-prefix workload is a parity case; bench the decode batches")
+    if args.op == "swap":
+        swap_bench(args)
+        return
     (reference if args.impl == "reference" else native)(args)
 
 

@@ -364,6 +364,36 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, 
                     int32_t num_blocks, int64_t block_elems, int32_t dtype, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* Swapping blocks to host memory                                             */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * pkv_swap_out_blocks — copy whole blocks, K and V, to host memory: host block i
+ * (bytes [i*block_bytes, (i+1)*block_bytes) of host_k and of host_v) becomes a
+ * copy of cache block block_ids[i], for i < num_ids.  pkv_swap_in_blocks — the
+ * reverse: cache block block_ids[i] becomes host block i.  These are the data
+ * copies of preemption by swapping (see pkv_seq_swap_out / pkv_seq_swap_in).
+ * The kernel reads or writes the host buffers directly over the CPU-GPU link.
+ * block_ids    device int32 [num_ids]; ids outside [0, num_blocks) are skipped.
+ * block_bytes  bytes of one block of one cache (num_kv_heads * block_size *
+ *              head_dim * element size), a multiple of 16.
+ * host_k, host_v  page-locked (or managed) host memory of at least
+ *              num_ids * block_bytes bytes each, 16-byte aligned; other host
+ *              memory is refused with PKV_ERR_INVALID_ARG before any work is
+ *              queued.  The caller keeps the buffers alive until the stream has
+ *              passed the copy.
+ * k_cache, v_cache  device caches, 16-byte aligned (any element type and layout:
+ *              blocks are moved as bytes).
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.
+ */
+int pkv_swap_out_blocks(const void* k_cache, const void* v_cache, const int32_t* block_ids,
+                        int32_t num_ids, int32_t num_blocks, int64_t block_bytes, void* host_k,
+                        void* host_v, void* stream);
+int pkv_swap_in_blocks(const void* host_k, const void* host_v, const int32_t* block_ids,
+                       int32_t num_ids, int32_t num_blocks, int64_t block_bytes, void* k_cache,
+                       void* v_cache, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Host block manager                                                         */
 /* ------------------------------------------------------------------------- */
 /*
@@ -400,6 +430,28 @@ int pkv_num_free_blocks(pkv_allocator_t* a, int32_t* num_free);
 int pkv_seq_create(pkv_allocator_t* a, int32_t* seq);
 int pkv_seq_fork(pkv_allocator_t* a, int32_t parent, int32_t* child);
 int pkv_seq_free(pkv_allocator_t* a, int32_t seq);
+
+/*
+ * Preemption by swapping ("PagedAttention — how vLLM stopped wasting 80% of
+ * your GPU memory", section "Preemption: what happens when memory runs out
+ * anyway": copy the preempted sequence's blocks out to CPU RAM, and back into
+ * freshly allocated GPU blocks when it resumes; all or nothing per sequence).
+ *
+ * pkv_seq_swap_out — writes the sequence's table (physical ids in logical order,
+ * *n of them; ids_out must hold them all) and gives every block back in reverse
+ * table order, as pkv_seq_free does; the sequence keeps its length and is
+ * swapped out: append, fork, blocks_needed, export and swap_out refuse it until
+ * pkv_seq_swap_in.  Copy the blocks' contents to host memory with
+ * pkv_swap_out_blocks before any of the returned ids is reused.
+ * pkv_seq_swap_in — gives a swapped-out sequence ceil(length / block_size)
+ * freshly allocated blocks, written to ids_out in logical order (PKV_ERR_OUT_OF_BLOCKS
+ * with the state unchanged if the pool cannot supply them all); restore their
+ * contents with pkv_swap_in_blocks.
+ */
+int pkv_seq_swap_out(pkv_allocator_t* a, int32_t seq, int32_t* ids_out, int32_t capacity,
+                     int32_t* n);
+int pkv_seq_swap_in(pkv_allocator_t* a, int32_t seq, int32_t* ids_out, int32_t capacity,
+                    int32_t* n);
 
 /* Blocks an append of n_tokens would take from the free list (CoW copy included). */
 int pkv_seq_blocks_needed(pkv_allocator_t* a, int32_t seq, int32_t n_tokens, int32_t* needed);

@@ -9,6 +9,8 @@ Public API (all device work runs in libpkv.so's sm_103a kernels):
 * ``paged_copy_blocks(k_cache, v_cache, src_dst_pairs)``
 * fp8 (E4M3) cache with per-KV-head scales: ``paged_kv_write_fp8``,
   ``paged_decode_attention_fp8``, ``paged_decode_step_fp8``
+* ``paged_swap_out`` / ``paged_swap_in`` — blocks to and from pinned host memory
+  (preemption by swapping, with ``BlockAllocator.swap_out`` / ``swap_in``)
 * ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free)
 
 The library is loaded on first use; importing this package needs no GPU.
@@ -22,7 +24,7 @@ def __getattr__(name):
     # manager, the workload generators) do not need torch's CUDA runtime.
     if name in ("paged_kv_write", "paged_decode_attention", "paged_decode_step",
                 "paged_copy_blocks", "paged_kv_write_fp8", "paged_decode_attention_fp8",
-                "paged_decode_step_fp8",
+                "paged_decode_step_fp8", "paged_swap_out", "paged_swap_in",
                 "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
         from . import ops
         return getattr(ops, name)

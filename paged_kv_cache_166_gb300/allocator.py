@@ -93,6 +93,22 @@ class BlockAllocator:
         cows = [(int(pair[0]), int(pair[1]))] if ncow.value else []
         return slots[:n], cows
 
+    def swap_out(self, seq: int) -> List[int]:
+        """Preempt by swapping: the sequence's block ids (logical order), all given
+        back to the pool; copy their contents out (paged_swap_out) before reuse."""
+        buf = np.empty(max(len(self.table(seq)), 1), dtype=np.int32)
+        n = ctypes.c_int32(0)
+        N.check(self._lib.pkv_seq_swap_out(self._h, seq, _ptr(buf), len(buf), ctypes.byref(n)))
+        return buf[:n.value].tolist()
+
+    def swap_in(self, seq: int) -> List[int]:
+        """Resume a swapped-out sequence: its fresh block ids (logical order)."""
+        B = self.block_size
+        buf = np.empty(max(-(-self.length(seq) // B), 1), dtype=np.int32)
+        n = ctypes.c_int32(0)
+        N.check(self._lib.pkv_seq_swap_in(self._h, seq, _ptr(buf), len(buf), ctypes.byref(n)))
+        return buf[:n.value].tolist()
+
     def length(self, seq: int) -> int:
         return self._out(self._lib.pkv_seq_len, seq)
 

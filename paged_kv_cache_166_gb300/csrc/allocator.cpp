@@ -9,7 +9,12 @@
 //   * a sequence's block table maps logical block j to a physical id;
 //   * position p needs a new block when p % B == 0; a write into a shared
 //     (refcount > 1) partial last block first moves the writer onto a private
-//     copy; slot(p) = table[p / B] * B + p % B.
+//     copy; slot(p) = table[p / B] * B + p % B;
+//   * preemption by swapping ("PagedAttention — how vLLM stopped wasting 80% of
+//     your GPU memory", section "Preemption: what happens when memory runs out
+//     anyway"): swap-out hands back the sequence's blocks (their contents go to
+//     host memory) and keeps its length; swap-in gives it ceil(len / B) fresh
+//     blocks, all or nothing.
 // Every public call validates first and mutates only once it cannot fail, so a
 // failing call leaves the state unchanged.
 #include <cstdint>
@@ -29,6 +34,7 @@ struct pkv_allocator {
     std::vector<int32_t> table;
     int32_t len = 0;
     bool live = false;
+    bool swapped = false;  // blocks handed back by swap-out, not yet swapped in
   };
   std::vector<Seq> seqs;             // indexed by sequence id
 
@@ -37,6 +43,7 @@ struct pkv_allocator {
   bool live_seq(int32_t s) const {
     return s >= 0 && s < static_cast<int32_t>(seqs.size()) && seqs[s].live;
   }
+  bool resident_seq(int32_t s) const { return live_seq(s) && !seqs[s].swapped; }
 
   int32_t pop() {
     int32_t b = free_stack.back();
@@ -143,7 +150,8 @@ int pkv_seq_create(pkv_allocator_t* a, int32_t* seq) {
 
 int pkv_seq_fork(pkv_allocator_t* a, int32_t parent, int32_t* child) {
   PKV_REQUIRE(a && child, PKV_ERR_INVALID_ARG, "NULL argument");
-  PKV_REQUIRE(a->live_seq(parent), PKV_ERR_INVALID_ARG, "unknown sequence %d", parent);
+  PKV_REQUIRE(a->resident_seq(parent), PKV_ERR_INVALID_ARG,
+              "unknown or swapped-out sequence %d", parent);
   a->seqs.emplace_back();
   auto& c = a->seqs.back();
   const auto& p = a->seqs[parent];
@@ -164,12 +172,50 @@ int pkv_seq_free(pkv_allocator_t* a, int32_t seq) {
   s.table.shrink_to_fit();
   s.len = 0;
   s.live = false;
+  s.swapped = false;
+  return pkv::ok();
+}
+
+int pkv_seq_swap_out(pkv_allocator_t* a, int32_t seq, int32_t* ids_out, int32_t capacity,
+                     int32_t* n) {
+  PKV_REQUIRE(a && n, PKV_ERR_INVALID_ARG, "NULL argument");
+  PKV_REQUIRE(a->resident_seq(seq), PKV_ERR_INVALID_ARG, "unknown or swapped-out sequence %d",
+              seq);
+  auto& s = a->seqs[seq];
+  const int32_t m = static_cast<int32_t>(s.table.size());
+  PKV_REQUIRE(m == 0 || (ids_out && capacity >= m), PKV_ERR_INVALID_ARG,
+              "ids_out holds %d ids, the sequence has %d blocks", capacity, m);
+  if (m) std::memcpy(ids_out, s.table.data(), sizeof(int32_t) * m);
+  for (auto it = s.table.rbegin(); it != s.table.rend(); ++it) a->decref(*it);
+  s.table.clear();
+  s.swapped = true;
+  *n = m;
+  return pkv::ok();
+}
+
+int pkv_seq_swap_in(pkv_allocator_t* a, int32_t seq, int32_t* ids_out, int32_t capacity,
+                    int32_t* n) {
+  PKV_REQUIRE(a && n, PKV_ERR_INVALID_ARG, "NULL argument");
+  PKV_REQUIRE(a->live_seq(seq) && a->seqs[seq].swapped, PKV_ERR_INVALID_ARG,
+              "sequence %d is not swapped out", seq);
+  auto& s = a->seqs[seq];
+  const int64_t B = a->block_size;
+  const int32_t m = static_cast<int32_t>((s.len + B - 1) / B);
+  PKV_REQUIRE(m == 0 || (ids_out && capacity >= m), PKV_ERR_INVALID_ARG,
+              "ids_out holds %d ids, the sequence needs %d blocks", capacity, m);
+  PKV_REQUIRE(static_cast<size_t>(m) <= a->free_stack.size(), PKV_ERR_OUT_OF_BLOCKS,
+              "swap-in needs %d blocks, %zu free", m, a->free_stack.size());
+  s.table.resize(m);
+  for (int32_t j = 0; j < m; ++j) s.table[j] = ids_out[j] = a->pop();
+  s.swapped = false;
+  *n = m;
   return pkv::ok();
 }
 
 int pkv_seq_blocks_needed(pkv_allocator_t* a, int32_t seq, int32_t n, int32_t* needed) {
   PKV_REQUIRE(a && needed, PKV_ERR_INVALID_ARG, "NULL argument");
-  PKV_REQUIRE(a->live_seq(seq), PKV_ERR_INVALID_ARG, "unknown sequence %d", seq);
+  PKV_REQUIRE(a->resident_seq(seq), PKV_ERR_INVALID_ARG, "unknown or swapped-out sequence %d",
+              seq);
   PKV_REQUIRE(n >= 0, PKV_ERR_INVALID_ARG, "negative token count");
   *needed = static_cast<int32_t>(a->needed(a->seqs[seq], n));
   return pkv::ok();
@@ -178,7 +224,8 @@ int pkv_seq_blocks_needed(pkv_allocator_t* a, int32_t seq, int32_t n, int32_t* n
 int pkv_seq_append(pkv_allocator_t* a, int32_t seq, int32_t n, int32_t* slots_out,
                    int32_t* cow_pair_out, int32_t* n_cow) {
   PKV_REQUIRE(a && n_cow, PKV_ERR_INVALID_ARG, "NULL argument");
-  PKV_REQUIRE(a->live_seq(seq), PKV_ERR_INVALID_ARG, "unknown sequence %d", seq);
+  PKV_REQUIRE(a->resident_seq(seq), PKV_ERR_INVALID_ARG, "unknown or swapped-out sequence %d",
+              seq);
   PKV_REQUIRE(n >= 0, PKV_ERR_INVALID_ARG, "negative token count");
   PKV_REQUIRE(n == 0 || slots_out, PKV_ERR_INVALID_ARG, "slots_out is NULL");
   auto& s = a->seqs[seq];
@@ -238,7 +285,8 @@ int pkv_export_tables(pkv_allocator_t* a, const int32_t* seqs, int32_t num, int3
               "NULL argument");
   PKV_REQUIRE(num >= 0 && max_blocks >= 0, PKV_ERR_INVALID_ARG, "negative size");
   for (int32_t r = 0; r < num; ++r) {
-    PKV_REQUIRE(a->live_seq(seqs[r]), PKV_ERR_INVALID_ARG, "unknown sequence %d", seqs[r]);
+    PKV_REQUIRE(a->resident_seq(seqs[r]), PKV_ERR_INVALID_ARG,
+                "unknown or swapped-out sequence %d", seqs[r]);
     PKV_REQUIRE(a->seqs[seqs[r]].table.size() <= static_cast<size_t>(max_blocks),
                 PKV_ERR_INVALID_ARG, "table of sequence %d has %zu blocks > max_blocks %d",
                 seqs[r], a->seqs[seqs[r]].table.size(), max_blocks);

@@ -195,6 +195,36 @@ __global__ void kv_write_fp8_kernel(const Tin* __restrict__ k, const Tin* __rest
   }
 }
 
+// Preemption by swapping ("PagedAttention — how vLLM stopped wasting 80% of your
+// GPU memory", section "Preemption: what happens when memory runs out anyway"):
+// out: host block i = cache block ids[i];  in: cache block ids[i] = host block i,
+// for K and V, whole blocks, 16-byte vectors.  Host buffers are page-locked host
+// memory the kernel reads or writes directly (over the CPU-GPU link).  Ids
+// outside [0, NB) are skipped.
+__global__ void swap_blocks_kernel(const uint4* __restrict__ src_k, const uint4* __restrict__ src_v,
+                                   uint4* __restrict__ dst_k, uint4* __restrict__ dst_v,
+                                   const int32_t* __restrict__ ids, int32_t n, int32_t NB,
+                                   int64_t block_vecs, bool to_host) {
+  const int64_t total = static_cast<int64_t>(n) * block_vecs;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int64_t p = i / block_vecs;
+    const int64_t c = i - p * block_vecs;
+    const int32_t b = __ldg(ids + p);
+    if (b < 0 || b >= NB) continue;
+    const int64_t cache_at = static_cast<int64_t>(b) * block_vecs + c;
+    const int64_t host_at = p * block_vecs + c;
+    if (to_host) {
+      dst_k[host_at] = __ldcs(src_k + cache_at);
+      dst_v[host_at] = __ldcs(src_v + cache_at);
+    } else {
+      dst_k[cache_at] = __ldcs(src_k + host_at);
+      dst_v[cache_at] = __ldcs(src_v + host_at);
+    }
+  }
+}
+
 int grid_for(int64_t work, int threads) {
   int sms = 0, dev = 0;
   if (device_sm_count(&sms, &dev) != PKV_OK) sms = 132;
@@ -240,6 +270,53 @@ int launch_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mappin
   else if (dtype == PKV_F16) PKV_FP8_WRITE(__half);
   else PKV_FP8_WRITE(__nv_bfloat16);
 #undef PKV_FP8_WRITE
+  PKV_CUDA(cudaGetLastError());
+  return PKV_OK;
+}
+
+// Device address of a page-locked (or managed) host buffer, or an error if the
+// device cannot address it.
+int host_buffer_device_ptr(const void* host, void** dev_ptr) {
+  cudaPointerAttributes attr{};
+  PKV_CUDA(cudaPointerGetAttributes(&attr, host));
+  PKV_REQUIRE(attr.type == cudaMemoryTypeHost || attr.type == cudaMemoryTypeManaged,
+              PKV_ERR_INVALID_ARG,
+              "host buffer %p is not page-locked or managed memory (type %d)", host,
+              static_cast<int>(attr.type));
+  PKV_REQUIRE(attr.devicePointer != nullptr, PKV_ERR_INVALID_ARG,
+              "host buffer %p is not mapped into the device address space", host);
+  *dev_ptr = attr.devicePointer;
+  return PKV_OK;
+}
+
+int launch_swap(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
+                const int32_t* ids, int32_t n, int32_t NB, int64_t block_bytes, bool to_host,
+                void* stream) {
+  PKV_REQUIRE(n >= 0 && NB > 0 && block_bytes > 0 && block_bytes % 16 == 0, PKV_ERR_INVALID_ARG,
+              "bad sizes (block_bytes must be a positive multiple of 16)");
+  if (n == 0) return PKV_OK;
+  PKV_REQUIRE(src_k && src_v && dst_k && dst_v && ids, PKV_ERR_INVALID_ARG, "NULL pointer");
+  PKV_REQUIRE(aligned(src_k, 16) && aligned(src_v, 16) && aligned(dst_k, 16) && aligned(dst_v, 16),
+              PKV_ERR_INVALID_ARG, "caches and host buffers must be 16-byte aligned");
+  const void* hk = to_host ? dst_k : src_k;
+  const void* hv = to_host ? dst_v : src_v;
+  void *dk = nullptr, *dv = nullptr;
+  int rc = host_buffer_device_ptr(hk, &dk);
+  if (rc != PKV_OK) return rc;
+  rc = host_buffer_device_ptr(hv, &dv);
+  if (rc != PKV_OK) return rc;
+  const int64_t block_vecs = block_bytes / 16;
+  const int threads = 256;
+  cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (to_host) {
+    swap_blocks_kernel<<<grid_for(n * block_vecs, threads), threads, 0, st>>>(
+        static_cast<const uint4*>(src_k), static_cast<const uint4*>(src_v),
+        static_cast<uint4*>(dk), static_cast<uint4*>(dv), ids, n, NB, block_vecs, true);
+  } else {
+    swap_blocks_kernel<<<grid_for(n * block_vecs, threads), threads, 0, st>>>(
+        static_cast<const uint4*>(dk), static_cast<const uint4*>(dv), static_cast<uint4*>(dst_k),
+        static_cast<uint4*>(dst_v), ids, n, NB, block_vecs, false);
+  }
   PKV_CUDA(cudaGetLastError());
   return PKV_OK;
 }
@@ -311,6 +388,22 @@ int pkv_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
   const int rc = launch_kv_write_fp8(k, v, slot_mapping, nullptr, 0, nullptr, num_tokens, k_cache,
                                      v_cache, k_scale, v_scale, num_blocks, num_kv_heads,
                                      head_dim, dtype, stream);
+  return rc == PKV_OK ? ok() : rc;
+}
+
+int pkv_swap_out_blocks(const void* k_cache, const void* v_cache, const int32_t* block_ids,
+                        int32_t num_ids, int32_t num_blocks, int64_t block_bytes, void* host_k,
+                        void* host_v, void* stream) {
+  const int rc = launch_swap(k_cache, v_cache, host_k, host_v, block_ids, num_ids, num_blocks,
+                             block_bytes, true, stream);
+  return rc == PKV_OK ? ok() : rc;
+}
+
+int pkv_swap_in_blocks(const void* host_k, const void* host_v, const int32_t* block_ids,
+                       int32_t num_ids, int32_t num_blocks, int64_t block_bytes, void* k_cache,
+                       void* v_cache, void* stream) {
+  const int rc = launch_swap(host_k, host_v, k_cache, v_cache, block_ids, num_ids, num_blocks,
+                             block_bytes, false, stream);
   return rc == PKV_OK ? ok() : rc;
 }
 

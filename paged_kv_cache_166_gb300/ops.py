@@ -266,6 +266,42 @@ def paged_decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     return out
 
 
+def _swap_args(k_cache, v_cache, block_ids, host_k, host_v):
+    dev = _check_cuda(k_cache, v_cache, block_ids)
+    _check_index(block_ids, "block_ids")
+    if block_ids.dim() != 1:
+        raise ValueError("block_ids must be [n]")
+    n = block_ids.shape[0]
+    block_bytes = k_cache[0].numel() * k_cache.element_size()
+    if v_cache.shape[0] != k_cache.shape[0] or v_cache[0].numel() * v_cache.element_size() != block_bytes:
+        raise ValueError("K and V caches must hold blocks of the same size")
+    for h in (host_k, host_v):
+        if h.is_cuda or not h.is_pinned() or not h.is_contiguous():
+            raise ValueError("host buffers must be contiguous page-locked (pinned) CPU tensors")
+        if h.numel() * h.element_size() < n * block_bytes:
+            raise ValueError(f"host buffer smaller than {n} blocks of {block_bytes} bytes")
+    return dev, n, block_bytes
+
+
+def paged_swap_out(k_cache: torch.Tensor, v_cache: torch.Tensor, block_ids: torch.Tensor,
+                   host_k: torch.Tensor, host_v: torch.Tensor) -> None:
+    """Copy cache blocks block_ids (device int32 [n]) to pinned host buffers: host
+    block i = cache block block_ids[i], K and V."""
+    dev, n, bb = _swap_args(k_cache, v_cache, block_ids, host_k, host_v)
+    N.check(N.lib().pkv_swap_out_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
+                                        block_ids.data_ptr(), n, k_cache.shape[0], bb,
+                                        host_k.data_ptr(), host_v.data_ptr(), _stream(dev)))
+
+
+def paged_swap_in(host_k: torch.Tensor, host_v: torch.Tensor, block_ids: torch.Tensor,
+                  k_cache: torch.Tensor, v_cache: torch.Tensor) -> None:
+    """Copy pinned host blocks back: cache block block_ids[i] = host block i."""
+    dev, n, bb = _swap_args(k_cache, v_cache, block_ids, host_k, host_v)
+    N.check(N.lib().pkv_swap_in_blocks(host_k.data_ptr(), host_v.data_ptr(),
+                                       block_ids.data_ptr(), n, k_cache.shape[0], bb,
+                                       k_cache.data_ptr(), v_cache.data_ptr(), _stream(dev)))
+
+
 def decode_status(workspace: torch.Tensor) -> int:
     """Reads and clears the device status bits the decode kernels recorded."""
     v = ctypes.c_int32(0)

@@ -88,6 +88,22 @@ class Pair:
         self.c.free(s)
         self.o.free(s)
 
+    def swap_out(self, s):
+        a, b = self.c.swap_out(s), self.o.swap_out(s)
+        assert a == b
+        return a
+
+    def swap_in(self, s):
+        try:
+            b = self.o.swap_in(s)
+        except OracleOOB:
+            with pytest.raises(N.OutOfBlocks):
+                self.c.swap_in(s)
+            return None
+        a = self.c.swap_in(s)
+        assert a == b
+        return a
+
     def append(self, s, n):
         need = self.o.blocks_needed(s, n)
         assert self.c.blocks_needed(s, n) == need
@@ -164,18 +180,31 @@ def test_random_operations_bit_exact(seed):
     B = int(r.choice([1, 2, 4, 16]))
     NB = int(r.integers(8, 96))
     p = Pair(NB, B, r.permutation(NB).astype(np.int32))
-    live = []
-    for _ in range(500):
-        op = r.integers(0, 10)
+    live, swapped = [], []
+    for _ in range(600):
+        op = r.integers(0, 12)
         if op < 2 or not live:
             live.append(p.create())
         elif op < 7:
             p.append(live[r.integers(len(live))], int(r.integers(0, 3 * B + 2)))
         elif op < 8:
             live.append(p.fork(live[r.integers(len(live))]))
-        else:
+        elif op < 9:
             p.free(live.pop(r.integers(len(live))))
+        elif op < 10:
+            swapped.append(live.pop(r.integers(len(live))))
+            p.swap_out(swapped[-1])
+        elif swapped:
+            s = swapped[r.integers(len(swapped))]
+            if p.swap_in(s) is not None:
+                swapped.remove(s)
+                live.append(s)
         p.compare()
+    for s in swapped:  # swapped-out sequences refuse resident operations
+        with pytest.raises(N.PkvError):
+            p.c.append(s, 1)
+        with pytest.raises(N.PkvError):
+            p.c.fork(s)
 
 
 def test_export_tables_matches_oracle():

@@ -21,6 +21,9 @@ written from the pages that describe PagedAttention:
   "The OS-Inspired Insight" and "Walking Through the Lifecycle").
 * ``kv_bytes``         — the KV-cache size formula and block arithmetic
   ("PagedAttention and vLLM: Virtual Memory for the KV Cache", summary FAQ).
+* ``prefill``          — paged (chunked) prefill attention: a chunk of queries
+  attending causally through the block table ("PagedAttention: How vLLM
+  Borrowed Virtual Memory...", section "Walking Through the Lifecycle").
 * ``fp8``              — the fp8 (E4M3) quantised KV cache: code table, the
   quantising cache write and attention over the dequantised values
   ("PagedAttention — how vLLM stopped wasting 80%...", FAQ "How does this

@@ -600,6 +600,79 @@ def swap_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def prefill_bench(args):
+    """Paged prefill: every sequence's prompt processed in one causal pass (or, with
+    --chunk C, its last C positions as a chunk over the rest of its context) over
+    a paged cache of the workload's shape; TFLOP/s of the causal attention (4 * D
+    flops per query head and visible key) against the measured bf16 tensor peak."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_166_gb300 as pkv
+    from paged_kv_cache_166_gb300 import BlockAllocator
+    from paged_kv_cache_166_gb300 import workloads as W
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = W.WORKLOADS[args.workload]
+    dt = "bf16" if w.dtype == "f32" else w.dtype
+    S, P = args.prefill_seqs, args.prefill_len
+    C = args.chunk or P
+    B, Hq, Hkv, D = w.block_size, w.num_q_heads, w.num_kv_heads, w.head_dim
+    NB = S * (-(-P // B)) + 1
+    alloc = BlockAllocator(NB, B, W.pool_order(NB, w.seed))
+    sids = [alloc.create() for _ in range(S)]
+    for s_ in sids:
+        alloc.append(s_, P)
+    tables, ctx = alloc.export_tables(sids, -(-P // B))
+    kc = torch.empty((NB, Hkv, B, D), dtype=W.torch_dtype(dt), device=device)
+    vc = torch.empty_like(kc)
+    W.fill_normal_(kc, w.seed, W.STREAM_K_POOL)
+    W.fill_normal_(vc, w.seed, W.STREAM_V_POOL)
+    q = W.normal_tensor((S * C, Hq, D), dt, w.seed, W.STREAM_Q, device)
+    out = torch.empty_like(q)
+    qstart = torch.arange(0, S * C + 1, C, dtype=torch.int32, device=device)
+    tab_d, ctx_d = torch.from_numpy(tables).to(device), torch.from_numpy(ctx).to(device)
+    # visible keys: query i of a chunk sees P - C + i + 1 positions
+    pairs = S * sum(P - C + i + 1 for i in range(C))
+    flops = 4.0 * D * Hq * pairs
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    ts = []
+    for i in range(args.warmup + args.steps):
+        flush.zero_()
+        e0.record(stream)
+        pkv.paged_prefill_attention(q, kc, vc, tab_d, ctx_d, qstart, w.scale, out)
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            ts.append(e0.elapsed_time(e1))
+    ms = float(np.median(ts))
+    tflops = flops / (ms * 1e-3) / 1e12
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            peak, kind = float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        peak, kind = 1900.0, "fallback"
+    line = {
+        "metric": "paged prefill attention TFLOP/s (causal, 4*D flops per query head and key)",
+        "value": round(tflops, 1), "unit": "TFLOP/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": f"{w.name} shape: {S} sequences x {P}-token context, chunk of {C} "
+                               f"queries each, {Hq} q / {Hkv} kv heads, head_dim {D}, {dt}",
+                   "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)"},
+        "tokens_per_s": round(S * C / (ms * 1e-3), 1),
+        "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "kernel": "prefill_attention_kernel (mma.sync m16n8k16)",
+                     "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({kind}; dense cuBLAS)"},
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -640,8 +713,12 @@ def main():
     ap.add_argument("--workload", default="mha13b",
                     choices=["tiny", "mha13b", "gqa70b", "prefix", "longctx"])
     ap.add_argument("--num-warps", type=int, default=0)
-    ap.add_argument("--op", choices=["decode", "swap"], default="decode",
-                    help="decode: the decode step (default); swap: blocks to host and back")
+    ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
+                    help="decode: the decode step (default); swap: blocks to host and back; "
+                         "prefill: causal prefill attention")
+    ap.add_argument("--prefill-seqs", type=int, default=16)
+    ap.add_argument("--prefill-len", type=int, default=2048)
+    ap.add_argument("--chunk", type=int, default=0, help="prefill chunk (0: the whole prompt)")
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="cache element type: the workload's dtype, or fp8 E4M3 with per-head scales")
     ap.add_argument("--soak-s", type=float, default=0.6,
@@ -656,6 +733,9 @@ def main():
         ap.error("the shared-prefix workload is a parity case; bench the decode batches")
     if args.op == "swap":
         swap_bench(args)
+        return
+    if args.op == "prefill":
+        prefill_bench(args)
         return
     (reference if args.impl == "reference" else native)(args)
 

@@ -255,6 +255,43 @@ int pkv_decode_attention_static_scratch(const void* q, const void* k_cache, cons
                                         void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* Paged prefill attention                                                    */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * pkv_prefill_attention — causal attention of a chunk of new prompt tokens per
+ * sequence over the paged cache (prefill, or chunked prefill: "PagedAttention: How
+ * vLLM Borrowed Virtual Memory...", section "Walking Through the Lifecycle",
+ * Prefill, and section "RadixAttention ..." on chunked prefill).
+ *
+ * Sequence s has t = context_lens[s] tokens in the cache — its chunk included,
+ * written before this call (pkv_kv_write) — and c = query_start[s+1] -
+ * query_start[s] queries, the last c positions: query row query_start[s] + i is
+ * at position p = t - c + i and, for query head h of KV group g = h / G, attends
+ * to every position j <= p:
+ *   out[row, h] = softmax_j(scale * q[row, h] . K[slot(j), g]) . V[slot(j), g].
+ * A whole-prompt prefill is c = t.
+ *
+ * q, out        device [T, num_q_heads, head_dim] (T = query_start[num_seqs]),
+ *               f16 or bf16, contiguous; only the T rows are written.
+ * block_tables, context_lens, caches: as pkv_decode_attention.
+ * query_start   device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0.
+ * status        device int32 word or NULL: PKV_DEV_* bits are ORed into it
+ *               (lengths out of range are clamped, bad block ids read as zeros,
+ *               a wait that timed out abandons the launch).
+ * Supported: block_size 16, head_dim 64 or 128, G in {1, 2, 4, 8},
+ * num_seqs <= 2048.  Computed on the tensor cores (bf16/f16 inputs, fp32
+ * accumulation and softmax); results depend only on the values and lengths.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+int pkv_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* context_lens, const int32_t* query_start,
+                          int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                          int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                          void* out, int32_t* status, int32_t dtype, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* fp8 KV cache                                                               */
 /* ------------------------------------------------------------------------- */
 

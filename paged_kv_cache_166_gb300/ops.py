@@ -266,6 +266,39 @@ def paged_decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     return out
 
 
+def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                            block_tables: torch.Tensor, context_lens: torch.Tensor,
+                            query_start: torch.Tensor, scale: float, out: torch.Tensor,
+                            status: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """Causal attention of each sequence's chunk of queries q [T, Hq, D] (rows
+    query_start[s]..query_start[s+1]-1, the last positions of context_lens[s]) over
+    the paged caches; writes and returns out."""
+    dev = _check_cuda(q, k_cache, v_cache, block_tables, context_lens, query_start, out)
+    if q.dim() != 3 or k_cache.dim() != 4 or k_cache.shape != v_cache.shape or out.shape != q.shape:
+        raise ValueError("expected q, out [T, Hq, D] and caches [NB, Hkv, B, D]")
+    T, Hq, D = q.shape
+    NB, Hkv, B, D2 = k_cache.shape
+    S = context_lens.shape[0]
+    if D2 != D or block_tables.dim() != 2 or block_tables.shape[0] != S or query_start.shape != (S + 1,):
+        raise ValueError("block_tables [S, max_blocks], context_lens [S], query_start [S + 1]")
+    for t, n in ((block_tables, "block_tables"), (context_lens, "context_lens"),
+                 (query_start, "query_start")):
+        _check_index(t, n)
+    if not (q.dtype == k_cache.dtype == v_cache.dtype == out.dtype):
+        raise TypeError("q, caches and out must share a dtype")
+    st = 0
+    if status is not None:
+        _check_cuda(status)
+        if status.dtype != torch.int32 or status.numel() < 1:
+            raise ValueError("status must be a device int32 tensor")
+        st = status.data_ptr()
+    N.check(N.lib().pkv_prefill_attention(
+        q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
+        block_tables.shape[1], context_lens.data_ptr(), query_start.data_ptr(), S, Hq, Hkv, D, B,
+        NB, float(scale), out.data_ptr(), st or None, dtype_code(q), _stream(dev)))
+    return out
+
+
 def _swap_args(k_cache, v_cache, block_ids, host_k, host_v):
     dev = _check_cuda(k_cache, v_cache, block_ids)
     _check_index(block_ids, "block_ids")

@@ -1,0 +1,109 @@
+"""GPU parity of paged (chunked) prefill attention against the fp64 oracle.
+
+Row tolerance as for decode (2e-3 of the oracle row's L2 norm, f16/bf16).
+Covered: whole-prompt prefills of lengths 1 to several hundred, chunks of 1 to
+65 queries at the end of longer contexts, an empty chunk, every group size
+{1, 2, 4, 8}, head_dim 64 and 128, f16 and bf16; NaN in every cache slot no
+query may read (block tails past the context, unused blocks); a clean status
+word; rows outside the chunks left untouched.
+"""
+import numpy as np
+import pytest
+import torch
+
+import batches as BT
+from oracle import prefill as opf
+from oracle.block_manager import BlockManager
+from paged_kv_cache_166_gb300 import workloads as W
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    import __graft_entry__
+    __graft_entry__.build()
+
+
+def pkv():
+    import paged_kv_cache_166_gb300 as m
+    return m
+
+
+def case(dtype, Hq, Hkv, D, lens, chunks, seed=11):
+    B = 16
+    NB = int(sum(-(-t // B) for t in lens)) + 7
+    mgr = BlockManager(NB, B, W.pool_order(NB, seed))
+    sids = [mgr.create() for _ in lens]
+    for s, t in zip(sids, lens):
+        mgr.append(s, int(t))
+    maxb = max(1, max(len(mgr.tables[s]) for s in sids))
+    tables, ctx = mgr.export_tables(sids, maxb)
+    tdt = W.torch_dtype(dtype)
+    kc = torch.empty((NB, Hkv, B, D), dtype=tdt, device="cuda")
+    vc = torch.empty_like(kc)
+    W.fill_normal_(kc, seed, W.STREAM_K_POOL)
+    W.fill_normal_(vc, seed, W.STREAM_V_POOL)
+    # NaN in every slot no query may read
+    used = np.zeros((NB, B), dtype=bool)
+    for s, t in enumerate(lens):
+        for p in range(t):
+            used[tables[s, p // B], p % B] = True
+    m = torch.from_numpy(~used).cuda().view(NB, 1, B, 1).expand_as(kc)
+    kc[m] = float("nan")
+    vc[m] = float("nan")
+    qstart = np.concatenate([[0], np.cumsum(chunks)]).astype(np.int32)
+    q = W.normal_tensor((int(qstart[-1]) + 3, Hq, D), dtype, seed, W.STREAM_Q, "cuda")
+    return kc, vc, q, tables, ctx, qstart
+
+
+CASES = [
+    ("f16", 8, 8, 128, (1, 15, 16, 17, 100, 333), None),
+    ("bf16", 64, 8, 128, (40, 700, 129), (40, 65, 1)),
+    ("bf16", 16, 4, 64, (33, 64, 500, 31), (7, 64, 0, 31)),
+    ("f16", 8, 4, 128, (1000, 17), (200, 17)),
+    ("bf16", 8, 1, 128, (300, 96), (300, 33)),
+]
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,lens,chunks", CASES)
+def test_prefill_matches_oracle(dtype, Hq, Hkv, D, lens, chunks):
+    chunks = lens if chunks is None else chunks
+    kc, vc, q, tables, ctx, qstart = case(dtype, Hq, Hkv, D, lens, chunks)
+    T = int(qstart[-1])
+    ref = opf.paged_prefill_attention(BT.np64(q[:T]), BT.np64(kc), BT.np64(vc), tables, ctx,
+                                      qstart, 1 / np.sqrt(D))
+    out = torch.full_like(q, 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(ctx).cuda(), torch.from_numpy(qstart).cuda(),
+                                  1 / np.sqrt(D), out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = BT.np64(out)
+    assert np.all(got[T:] == 7.0)                        # rows past the chunks untouched
+    err = BT.row_errors(got[:T], ref)
+    assert np.isfinite(got[:T]).all()
+    assert err.max() <= BT.tolerance(dtype), f"row error {err.max():.3e}"
+
+
+def test_prefill_last_query_agrees_with_decode_kernel():
+    """The last query of each chunk is a decode query at the same context."""
+    dtype, Hq, Hkv, D = "bf16", 32, 4, 128
+    lens, chunks = (257, 40, 1025), (17, 40, 5)
+    kc, vc, q, tables, ctx, qstart = case(dtype, Hq, Hkv, D, lens, chunks, seed=12)
+    T = int(qstart[-1])
+    out = torch.empty_like(q)
+    pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(ctx).cuda(), torch.from_numpy(qstart).cuda(),
+                                  0.1, out)
+    last = torch.from_numpy(qstart[1:] - 1).long().cuda()
+    dec = torch.empty_like(q[last])
+    pkv().paged_decode_attention(q[last].contiguous(), kc, vc, torch.from_numpy(tables).cuda(),
+                                 torch.from_numpy(ctx).cuda(), 0.1, dec)
+    torch.cuda.synchronize()
+    ref = BT.np64(dec)
+    err = BT.row_errors(BT.np64(out[last]), ref)
+    assert err.max() <= 2 * BT.tolerance(dtype)

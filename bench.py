@@ -178,12 +178,15 @@ class ClockSampler:
 # --------------------------------------------------------------------------------------
 # workload construction through the library (block manager -> tables, slots)
 # --------------------------------------------------------------------------------------
-def build_batch(name: str, device, rank: int = 0, kv: str = "native"):
+def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size: int = 0):
     import torch
     from paged_kv_cache_166_gb300 import BlockAllocator
     from paged_kv_cache_166_gb300 import workloads as W
 
     w = W.WORKLOADS[name]
+    if block_size and block_size != w.block_size:
+        import dataclasses
+        w = dataclasses.replace(w, block_size=block_size)
     seed = w.seed + 1000 * rank
     lens = W.context_lengths(w)
     if rank:
@@ -328,7 +331,8 @@ def native(args):
     import paged_kv_cache_166_gb300 as pkv
 
     fp8 = args.kv == "fp8"
-    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, rank, args.kv)
+    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, rank, args.kv,
+                                                 args.block_size)
     S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     elt = kc.element_size()
     q_elt = dev["q"].element_size()
@@ -479,7 +483,7 @@ def native(args):
         "data": "synthetic",
         "config": {
             "workload": f"{w.name}: {S} seqs, {Hq} q / {Hkv} kv heads, head_dim {D}, {w.dtype}, "
-                        f"block 16, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks"
+                        f"block {B}, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks"
                         + (", fp8 (E4M3) KV cache with per-KV-head scales" if fp8 else ""),
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
             "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
@@ -719,6 +723,8 @@ def main():
     ap.add_argument("--prefill-seqs", type=int, default=16)
     ap.add_argument("--prefill-len", type=int, default=2048)
     ap.add_argument("--chunk", type=int, default=0, help="prefill chunk (0: the whole prompt)")
+    ap.add_argument("--block-size", type=int, default=0, choices=[0, 8, 16, 32],
+                    help="cache block size (0: the workload's, 16)")
     ap.add_argument("--kv", choices=["native", "fp8"], default="native",
                     help="cache element type: the workload's dtype, or fp8 E4M3 with per-head scales")
     ap.add_argument("--soak-s", type=float, default=0.6,

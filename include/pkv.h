@@ -164,9 +164,11 @@ int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t
  *               zero-filled before first use.
  * num_warps     worker warps (0 = device default); pass the same value given to
  *               pkv_decode_workspace_size.
- * Supported: block_size 16; dtype F16/BF16 with head_dim 64, 128 or 256, or F32
- * with head_dim 32, 64 or 128; G in {1, 2, 4, 8}; num_seqs <= 2048;
- * num_blocks*num_kv_heads*16 < 2^31; num_seqs*max_blocks_per_seq*num_kv_heads < 2^31.
+ * Supported: block_size 8, 16 or 32 (the kernels work in 16-token steps: half a
+ * 32-token block, or two 8-token blocks; results do not depend on the block
+ * size); dtype F16/BF16 with head_dim 64, 128 or 256, or F32 with head_dim 32,
+ * 64 or 128; G in {1, 2, 4, 8}; num_seqs <= 2048;
+ * num_blocks*num_kv_heads*block_size*4 < 2^31; num_seqs*max_blocks_per_seq*num_kv_heads < 2^31.
  * Invalid device data (a context length outside [0, max_blocks_per_seq*16], a
  * block id outside [0, num_blocks)) never faults: it is clamped or read as zeros
  * and recorded in the workspace status word (see pkv_decode_status).

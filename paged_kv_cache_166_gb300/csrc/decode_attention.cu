@@ -135,6 +135,7 @@ struct DecodeArgs {
   const float* k_scale;  // fp8 cache: per-KV-head scales (else NULL)
   const float* v_scale;
   int32_t S, Hq, Hkv, G, MAXB, NB;
+  int32_t block_size;  // 8, 16 or 32 tokens per cache block (steps are 16 tokens)
   int32_t total_warps;
   int32_t stages;    // per-warp pipeline depth
   int32_t q_bytes;   // G * D * elt
@@ -187,7 +188,7 @@ __host__ __device__ inline SmemLayout smem_layout(int stage_bytes, int stages, i
   L.bars = off;
   off += nw * stages * 8;
   L.ids = off;
-  off += nw * 64 * 4;
+  off += nw * 128 * 4;  // two windows of 32 steps, up to 2 block ids per step
   L.ctx = off;
   off += S * 4;
   L.pre = off;
@@ -209,10 +210,11 @@ __host__ __device__ inline SmemLayout smem_layout(int stage_bytes, int stages, i
 // Warp w owns the steps whose cost position lies in [w R, (w+1) R): equal cost,
 // not equal step count, so warps holding many short contexts get fewer steps.
 // ---------------------------------------------------------------------------------
-__device__ void build_schedule(const int32_t* __restrict__ context_lens, int S, int MAXB, int Hkv,
+__device__ void build_schedule(const int32_t* __restrict__ context_lens, int S, int MAXB,
+                               int block_size, int Hkv,
                                int unit_cost, int32_t* ctx_s, int32_t* pre, int32_t* prew,
                                int32_t* scratch, int32_t* status) {
-  const int limit = MAXB * kTok;
+  const int limit = MAXB * block_size;
   for (int s = threadIdx.x; s < S; s += blockDim.x) {
     int c = context_lens[s];
     if (c < 0 || c > limit) {
@@ -950,11 +952,14 @@ struct CutUnit {
 // ---------------------------------------------------------------------------------
 // The decode kernel: one persistent pass of every worker warp over its run.
 // ---------------------------------------------------------------------------------
-template <typename T, typename C, int D>
+// kBlk: 16 for caches of 16-token blocks; 0 for 8- or 32-token blocks (the size
+// then comes from the arguments).
+template <typename T, typename C, int D, int kBlk>
 __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     decode_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using Sh = Shape<C, D>;
+  constexpr int kIdStride = kBlk == kTok ? 1 : 2;  // block ids per step in the id windows
   const int NS = a.stages;
   extern __shared__ uint8_t smem_raw[];
   if (threadIdx.x == 0) {
@@ -995,7 +1000,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   int32_t* const ctx_s = reinterpret_cast<int32_t*>(base + L.ctx);
   int32_t* const pre = reinterpret_cast<int32_t*>(base + L.pre);
   int32_t* const prew = reinterpret_cast<int32_t*>(base + L.prew);
-  build_schedule(a.context_lens, a.S, a.MAXB, a.Hkv, a.unit_cost, ctx_s, pre, prew,
+  build_schedule(a.context_lens, a.S, a.MAXB, a.block_size, a.Hkv, a.unit_cost, ctx_s, pre, prew,
                  reinterpret_cast<int32_t*>(base + L.scratch), a.status);
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -1027,8 +1032,9 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   const uint32_t qslot_s = base_s + L.q + warp * NS * a.q_stride;
   const uint8_t* const qslot = base + L.q + warp * NS * a.q_stride;
   const uint32_t bars = base_s + L.bars + warp * NS * 8;
-  const int32_t* const ids = reinterpret_cast<const int32_t*>(base + L.ids) + warp * 64;
-  const uint32_t ids_s = base_s + L.ids + warp * 64 * 4;
+  const int32_t* const ids = reinterpret_cast<const int32_t*>(base + L.ids) + warp * 64 * kIdStride;
+  const uint32_t ids_s = base_s + L.ids + warp * 64 * kIdStride * 4;
+  const int Bsz = kBlk ? kBlk : a.block_size;
 
   if (lane == 0) {
     for (int st = 0; st < NS; ++st) ptx::mbar_init(bars + 8 * st, 1);
@@ -1036,13 +1042,24 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   }
   __syncwarp();
 
-  // Block-table prefetch: window k holds the ids of local steps [32k, 32k + 32).
+  // Block-table prefetch: window k holds, for local steps [32k, 32k + 32), the
+  // block ids each 16-token step reads: table[s][j] (block size 16), table[s][j/2]
+  // (32), or table[s][2j] and table[s][2j+1] (8; the second only if the context
+  // reaches it).
   auto load_window = [&](int k) {
     const int m = 32 * k + lane;
     if (m < nsteps) {
       const Cursor c = cursor_at(pre, S, Hkv, f0 + m);
-      ptx::cp_async_4(ids_s + ((k & 1) * 32 + lane) * 4,
-                      a.block_tables + static_cast<int64_t>(c.s) * MAXB + c.j);
+      const int32_t* row = a.block_tables + static_cast<int64_t>(c.s) * MAXB;
+      const uint32_t slot = ids_s + (((k & 1) * 32 + lane) * kIdStride) * 4;
+      if (kBlk == kTok || Bsz == 16) {
+        ptx::cp_async_4(slot, row + c.j);
+      } else if (Bsz == 32) {
+        ptx::cp_async_4(slot, row + (c.j >> 1));
+      } else {
+        ptx::cp_async_4(slot, row + 2 * c.j);
+        if (2 * c.j + 1 < (ctx_s[c.s] + 7) / 8) ptx::cp_async_4(slot + 4, row + 2 * c.j + 1);
+      }
     }
     ptx::cp_async_commit();
   };
@@ -1056,31 +1073,46 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
   const uint64_t policy = ptx::policy_evict_first();
-  const int32_t rows_total = a.NB * Hkv * kTok;
+  const int32_t rows_total = a.NB * Hkv * Bsz;
   const char* const qbase = reinterpret_cast<const char*>(a.q);
 
-  Cursor pc = cursor_at(pre, S, Hkv, f0);
-  int p_stage = 0;
-  auto issue = [&](int m) {  // warp-uniform; lane 0 issues the copies of local step m
-    if ((m & 31) == 0 && m > 0) {
-      load_window((m >> 5) + 1);
-      ptx::cp_async_wait<1>();
-      __syncwarp();
-    }
-    if (lane == 0) {
-      const int id = ids[((m >> 5) & 1) * 32 + (m & 31)];
-      const bool need_q = !Sh::kFp8 && ((m == 0) || (pc.j == 0));
-      const uint32_t bar = bars + 8 * p_stage;
-      ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
-      int32_t y;
-      if (static_cast<uint32_t>(id) < static_cast<uint32_t>(a.NB)) {
-        y = (id * Hkv + pc.g) * kTok;
-      } else {
-        atomicOr(a.status, PKV_DEV_BAD_BLOCK_ID);
-        y = rows_total;  // a box wholly past the end: the TMA unit fills it with zeros
+  // Copies of step (s, g, j) into stage `stage` (executed by one lane): the K and V
+  // rows of the step's 16 tokens, and the group's query rows when need_q.
+  auto issue_copies = [&](int stage, int s, int g, int j, int id0, int id1, bool need_q) {
+    // block size 8: the step's second block exists unless the context ends in the first
+    const bool second = kBlk != kTok && Bsz == 8 && j * kTok + 8 < ctx_s[s];
+    const uint32_t bar = bars + 8 * stage;
+    const uint32_t kt = tiles + stage * Sh::kStageBytes;
+    const uint32_t vt = kt + Sh::kTileBytes;
+    auto row_of = [&](int id, int within) -> int32_t {
+      if (static_cast<uint32_t>(id) < static_cast<uint32_t>(a.NB))
+        return (id * Hkv + g) * Bsz + within;
+      atomicOr(a.status, PKV_DEV_BAD_BLOCK_ID);
+      return rows_total;  // a box wholly past the end: the TMA unit fills it with zeros
+    };
+    if (kBlk != kTok && Bsz == 8) {
+      // two 8-row blocks per step, into rows 0-7 and 8-15 of every sub-tile
+      ptx::mbar_arrive_expect_tx(bar, (second ? Sh::kStageBytes : Sh::kStageBytes / 2) +
+                                          (need_q ? a.q_bytes : 0));
+      const int32_t y0 = row_of(id0, 0);
+#pragma unroll
+      for (int c = 0; c < Sh::kSub; ++c) {
+        ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y0, bar, policy);
+        ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y0, bar, policy);
       }
-      const uint32_t kt = tiles + p_stage * Sh::kStageBytes;
-      const uint32_t vt = kt + Sh::kTileBytes;
+      if (second) {
+        const int32_t y1 = row_of(id1, 0);
+#pragma unroll
+        for (int c = 0; c < Sh::kSub; ++c) {
+          ptx::tma_load_2d(kt + c * kSubTile + kSubTile / 2, &kmap, c * Sh::kBoxCols, y1, bar,
+                           policy);
+          ptx::tma_load_2d(vt + c * kSubTile + kSubTile / 2, &vmap, c * Sh::kBoxCols, y1, bar,
+                           policy);
+        }
+      }
+    } else {
+      ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
+      const int32_t y = row_of(id0, (kBlk != kTok && Bsz == 32) ? (j & 1) * kTok : 0);
       if constexpr (Sh::kSingleBox) {
         ptx::tma_load_2d(kt, &kmap, 0, y * Sh::kSub, bar, policy);
         ptx::tma_load_2d(vt, &vmap, 0, y * Sh::kSub, bar, policy);
@@ -1096,11 +1128,25 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
             ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
         }
       }
-      if (need_q) {
-        const char* src =
-            qbase + (static_cast<int64_t>(pc.s) * a.Hq + pc.g * a.G) * D * sizeof(T);
-        ptx::bulk_load(qslot_s + p_stage * a.q_stride, src, a.q_bytes, bar);
-      }
+    }
+    if (need_q) {
+      const char* src = qbase + (static_cast<int64_t>(s) * a.Hq + g * a.G) * D * sizeof(T);
+      ptx::bulk_load(qslot_s + stage * a.q_stride, src, a.q_bytes, bar);
+    }
+  };
+
+  Cursor pc = cursor_at(pre, S, Hkv, f0);
+  int p_stage = 0;
+  auto issue = [&](int m) {  // warp-uniform; lane 0 issues the copies of local step m
+    if ((m & 31) == 0 && m > 0) {
+      load_window((m >> 5) + 1);
+      ptx::cp_async_wait<1>();
+      __syncwarp();
+    }
+    if (lane == 0) {
+      const int w = (((m >> 5) & 1) * 32 + (m & 31)) * kIdStride;
+      issue_copies(p_stage, pc.s, pc.g, pc.j, ids[w], kIdStride == 2 ? ids[w + 1] : -1,
+                   !Sh::kFp8 && ((m == 0) || (pc.j == 0)));
     }
     if (++p_stage == NS) p_stage = 0;
     advance(pc, pre, S, Hkv);
@@ -1112,38 +1158,9 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     for (int m = 0; m < prologue; ++m) issue(m);
   } else if (lane < prologue) {
     const Cursor lc = cursor_at(pre, S, Hkv, f0 + lane);
-    const int id = ids[lane];
-    const bool need_q = !Sh::kFp8 && ((lane == 0) || (lc.j == 0));
-    const uint32_t bar = bars + 8 * lane;
-    ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
-    int32_t y;
-    if (static_cast<uint32_t>(id) < static_cast<uint32_t>(a.NB)) {
-      y = (id * Hkv + lc.g) * kTok;
-    } else {
-      atomicOr(a.status, PKV_DEV_BAD_BLOCK_ID);
-      y = rows_total;
-    }
-    const uint32_t kt = tiles + lane * Sh::kStageBytes;
-    const uint32_t vt = kt + Sh::kTileBytes;
-    if constexpr (Sh::kSingleBox) {
-      ptx::tma_load_2d(kt, &kmap, 0, y * Sh::kSub, bar, policy);
-      ptx::tma_load_2d(vt, &vmap, 0, y * Sh::kSub, bar, policy);
-    } else {
-#pragma unroll
-      for (int c = 0; c < Sh::kSub; ++c)
-        ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
-      if constexpr (Sh::kFp8) {
-        ptx::tma_load_2d(vt, &vmap, 0, (y / kTok) * (D / 8), bar, policy);
-      } else {
-#pragma unroll
-        for (int c = 0; c < Sh::kSub; ++c)
-          ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
-      }
-    }
-    if (need_q) {
-      const char* src = qbase + (static_cast<int64_t>(lc.s) * a.Hq + lc.g * a.G) * D * sizeof(T);
-      ptx::bulk_load(qslot_s + lane * a.q_stride, src, a.q_bytes, bar);
-    }
+    issue_copies(lane, lc.s, lc.g, lc.j, ids[kIdStride * lane],
+                 kIdStride == 2 ? ids[kIdStride * lane + 1] : -1,
+                 !Sh::kFp8 && ((lane == 0) || (lc.j == 0)));
   }
   if (PKV_PARALLEL_PROLOGUE) {
     __syncwarp();
@@ -1301,7 +1318,7 @@ int device_smem_optin(int* bytes) {
   return PKV_OK;
 }
 
-template <typename T, typename C, int D>
+template <typename T, typename C, int D, int kBlk>
 int ensure_smem_attr() {
   // Raise the dynamic shared-memory limit once per device for this instantiation.
   static std::once_flag flags[64];
@@ -1313,7 +1330,7 @@ int ensure_smem_attr() {
   int rc = device_smem_optin(&optin);
   if (rc != PKV_OK) return rc;
   std::call_once(flags[dev], [&] {
-    results[dev] = cudaFuncSetAttribute(decode_attention_kernel<T, C, D>,
+    results[dev] = cudaFuncSetAttribute(decode_attention_kernel<T, C, D, kBlk>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, optin);
   });
   if (results[dev] != cudaSuccess)
@@ -1376,8 +1393,10 @@ int validate(const HostArgs& h, int* warps_out) {
               "query heads per KV head %d not in {1,2,4,8}", G);
   PKV_REQUIRE(supported_head_dim(h.dtype, h.D), PKV_ERR_UNSUPPORTED,
               "head_dim %d unsupported for dtype %d", h.D, h.dtype);
-  PKV_REQUIRE(h.block_size == kTok, PKV_ERR_UNSUPPORTED, "block_size %d (kernels use 16)",
-              h.block_size);
+  PKV_REQUIRE(h.block_size == 8 || h.block_size == 16 || h.block_size == 32,
+              PKV_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32}", h.block_size);
+  PKV_REQUIRE(h.block_size == kTok || (!h.fp8 && !PKV_SINGLE_BOX && h.dtype != PKV_F32),
+              PKV_ERR_UNSUPPORTED, "block_size %d needs an f16 or bf16 cache", h.block_size);
   PKV_REQUIRE(h.MAXB > 0, PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
   PKV_REQUIRE(static_cast<int64_t>(h.S) * h.MAXB * h.Hkv < (int64_t(1) << 31),
               PKV_ERR_UNSUPPORTED, "num_seqs * max_blocks_per_seq * num_kv_heads >= 2^31");
@@ -1394,8 +1413,8 @@ int validate(const HostArgs& h, int* warps_out) {
               "workspace of %zu bytes < %zu needed", h.workspace_bytes,
               workspace_bytes_for(G, h.D, W));
   PKV_REQUIRE(h.NB > 0, PKV_ERR_INVALID_ARG, "num_blocks must be positive");
-  PKV_REQUIRE(static_cast<int64_t>(h.NB) * h.Hkv * kTok * 4 < (int64_t(1) << 31),
-              PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 64 >= 2^31");
+  PKV_REQUIRE(static_cast<int64_t>(h.NB) * h.Hkv * h.block_size * 4 < (int64_t(1) << 31),
+              PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * block_size * 4 >= 2^31");
   PKV_REQUIRE(static_cast<int64_t>(h.S) * h.MAXB * h.Hkv * 4 +
                       static_cast<int64_t>(h.S) * h.Hkv * 8 < (int64_t(1) << 31),
               PKV_ERR_UNSUPPORTED, "schedule cost exceeds 2^31 quarter steps");
@@ -1429,6 +1448,7 @@ DecodeArgs device_args(const HostArgs& h, int W) {
   a.G = G;
   a.MAXB = h.MAXB;
   a.NB = h.NB;
+  a.block_size = h.block_size;
   a.total_warps = W;
   a.q_bytes = G * h.D * elt;
   a.q_stride = (a.q_bytes + 127) & ~127;
@@ -1439,10 +1459,10 @@ DecodeArgs device_args(const HostArgs& h, int W) {
   return a;
 }
 
-template <typename T, typename C, int D>
+template <typename T, typename C, int D, int kBlk>
 int launch_decode(const HostArgs& h, int W) {
   using Sh = Shape<C, D>;
-  int rc = ensure_smem_attr<T, C, D>();
+  int rc = ensure_smem_attr<T, C, D, kBlk>();
   if (rc != PKV_OK) return rc;
   int optin = 0;
   rc = device_smem_optin(&optin);
@@ -1459,7 +1479,7 @@ int launch_decode(const HostArgs& h, int W) {
   a.stages = stages;
   const SmemLayout L = smem_layout(Sh::kStageBytes, stages, a.q_stride, h.S, Sh::kWarpsPerCta);
   CUtensorMap kmap, vmap;
-  const int64_t rows = static_cast<int64_t>(h.NB) * h.Hkv * kTok;
+  const int64_t rows = static_cast<int64_t>(h.NB) * h.Hkv * h.block_size;
   if constexpr (Sh::kFp8) {
     // K: [rows, D] bytes, boxes of 16 rows x 128 B, swizzled.  V: each transposed
     // [D x 16 B] tile is 16 D contiguous bytes, viewed as D/8 rows of 128 B so that
@@ -1476,7 +1496,8 @@ int launch_decode(const HostArgs& h, int W) {
   // half-rows (one whole tile).  Otherwise [rows, D], boxes of 16 rows x 128 B.
   const int64_t map_rows = Sh::kSingleBox ? rows * Sh::kSub : rows;
   const int map_cols = Sh::kSingleBox ? Sh::kBoxCols : D;
-  const int box_rows = Sh::kSingleBox ? kTok * Sh::kSub : kTok;
+  // boxes of one 16-token step, or of one 8-token block (two per step)
+  const int box_rows = Sh::kSingleBox ? kTok * Sh::kSub : (h.block_size == 8 ? 8 : kTok);
   rc = encode_cache_map(&kmap, h.k_cache, h.dtype, map_rows, map_cols, Sh::kBoxCols, box_rows);
   if (rc != PKV_OK) return rc;
   rc = encode_cache_map(&vmap, h.v_cache, h.dtype, map_rows, map_cols, Sh::kBoxCols, box_rows);
@@ -1492,14 +1513,14 @@ int launch_decode(const HostArgs& h, int W) {
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  PKV_CUDA(cudaLaunchKernelEx(&cfg, decode_attention_kernel<T, C, D>, kmap, vmap, a));
+  PKV_CUDA(cudaLaunchKernelEx(&cfg, decode_attention_kernel<T, C, D, kBlk>, kmap, vmap, a));
   return PKV_OK;
 }
 
 int dispatch(const HostArgs& h, int W) {
   if (h.fp8) {
 #define PKV_CASE8(DT, TT, DD) \
-  if (h.dtype == DT && h.D == DD) return launch_decode<TT, E4M3, DD>(h, W);
+  if (h.dtype == DT && h.D == DD) return launch_decode<TT, E4M3, DD, kTok>(h, W);
     PKV_CASE8(PKV_BF16, __nv_bfloat16, 128)
     PKV_CASE8(PKV_BF16, __nv_bfloat16, 256)
     PKV_CASE8(PKV_F16, __half, 128)
@@ -1507,8 +1528,20 @@ int dispatch(const HostArgs& h, int W) {
 #undef PKV_CASE8
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for the fp8 cache", h.D);
   }
+  if (h.block_size != kTok) {
+#define PKV_CASEB(DT, TT, DD) \
+  if (h.dtype == DT && h.D == DD) return launch_decode<TT, TT, DD, 0>(h, W);
+    PKV_CASEB(PKV_BF16, __nv_bfloat16, 64)
+    PKV_CASEB(PKV_BF16, __nv_bfloat16, 128)
+    PKV_CASEB(PKV_BF16, __nv_bfloat16, 256)
+    PKV_CASEB(PKV_F16, __half, 64)
+    PKV_CASEB(PKV_F16, __half, 128)
+    PKV_CASEB(PKV_F16, __half, 256)
+#undef PKV_CASEB
+    return fail(PKV_ERR_UNSUPPORTED, "block_size %d needs an f16 or bf16 cache", h.block_size);
+  }
 #define PKV_CASE(DT, TT, DD) \
-  if (h.dtype == DT && h.D == DD) return launch_decode<TT, TT, DD>(h, W);
+  if (h.dtype == DT && h.D == DD) return launch_decode<TT, TT, DD, kTok>(h, W);
   PKV_CASE(PKV_BF16, __nv_bfloat16, 64)
   PKV_CASE(PKV_BF16, __nv_bfloat16, 128)
   PKV_CASE(PKV_BF16, __nv_bfloat16, 256)

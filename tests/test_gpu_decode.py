@@ -233,10 +233,10 @@ def test_host_side_rejections():
     q2 = torch.zeros(2, 12, 128, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(m.PkvError):          # group of 3 is not supported
         m.paged_decode_attention(q2, kc, kc, t, c, 0.1, torch.empty_like(q2))
-    kc8 = torch.zeros(4, 4, 8, 128, dtype=torch.bfloat16, device="cuda")
+    kc12 = torch.zeros(4, 4, 12, 128, dtype=torch.bfloat16, device="cuda")
     q4 = torch.zeros(2, 4, 128, dtype=torch.bfloat16, device="cuda")
-    with pytest.raises(m.PkvError):          # block size 8 is not supported by the kernels
-        m.paged_decode_attention(q4, kc8, kc8, t, c, 0.1, torch.empty_like(q4))
+    with pytest.raises(m.PkvError):          # block size 12 is not one of 8, 16, 32
+        m.paged_decode_attention(q4, kc12, kc12, t, c, 0.1, torch.empty_like(q4))
 
 
 # ---- the decode step with the cache write folded into the attention launch ----

@@ -90,6 +90,11 @@ namespace pkv {
 #ifndef PKV_FP8_WIDEN_ALU
 #define PKV_FP8_WIDEN_ALU 1
 #endif
+// Read the query rows of a unit straight from global memory into registers
+// instead of copying them into each pipeline stage (always so for the fp8 cache).
+#ifndef PKV_Q_FROM_GLOBAL
+#define PKV_Q_FROM_GLOBAL 0
+#endif
 // Skip the accumulator rescale of a step whose running maxima did not change.
 #ifndef PKV_RESCALE_SKIP
 #define PKV_RESCALE_SKIP 0
@@ -160,6 +165,7 @@ struct Shape {
   static constexpr bool kFp8 = std::is_same<C, E4M3>::value;
   static constexpr int kElt = CacheBytes<C>::value;
   static constexpr int kWarpsPerCta = kFp8 ? fp8_warps_per_cta(D) : kWarps;
+  static constexpr bool kQRegs = kFp8 || PKV_Q_FROM_GLOBAL;  // no query slot per stage
   static constexpr int kTileBytes = kTok * D * kElt;
   static constexpr int kSub = D * kElt / kSwizzleRow;     // sub-tiles per tile
   static constexpr int kBoxCols = kSwizzleRow / kElt;      // elements per sub-tile row
@@ -1146,7 +1152,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     if (lane == 0) {
       const int w = (((m >> 5) & 1) * 32 + (m & 31)) * kIdStride;
       issue_copies(p_stage, pc.s, pc.g, pc.j, ids[w], kIdStride == 2 ? ids[w + 1] : -1,
-                   !Sh::kFp8 && ((m == 0) || (pc.j == 0)));
+                   !Sh::kQRegs && ((m == 0) || (pc.j == 0)));
     }
     if (++p_stage == NS) p_stage = 0;
     advance(pc, pre, S, Hkv);
@@ -1160,7 +1166,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     const Cursor lc = cursor_at(pre, S, Hkv, f0 + lane);
     issue_copies(lane, lc.s, lc.g, lc.j, ids[kIdStride * lane],
                  kIdStride == 2 ? ids[kIdStride * lane + 1] : -1,
-                 !Sh::kFp8 && ((lane == 0) || (lc.j == 0)));
+                 !Sh::kQRegs && ((lane == 0) || (lc.j == 0)));
   }
   if (PKV_PARALLEL_PROLOGUE) {
     __syncwarp();
@@ -1199,6 +1205,11 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
         st_.load_q_rows(reinterpret_cast<const T*>(a.q) +
                             (static_cast<int64_t>(cc.s) * a.Hq + cc.g * a.G) * D,
                         a.G, lane);
+      } else if constexpr (Sh::kQRegs) {
+        st_.load_q(reinterpret_cast<const uint8_t*>(
+                       reinterpret_cast<const T*>(a.q) +
+                       (static_cast<int64_t>(cc.s) * a.Hq + cc.g * a.G) * D),
+                   a.G, lane);
       } else {
         st_.load_q(qslot + c_stage * a.q_stride, a.G, lane);
       }
@@ -1468,7 +1479,7 @@ int launch_decode(const HostArgs& h, int W) {
   rc = device_smem_optin(&optin);
   if (rc != PKV_OK) return rc;
   DecodeArgs a = device_args(h, W);
-  if constexpr (Sh::kFp8) a.q_stride = 0;  // the fp8 path reads q rows straight into registers
+  if constexpr (Sh::kQRegs) a.q_stride = 0;  // q rows are read straight into registers
   // Deepest pipeline that fits the SM's shared memory.
   const uint32_t fixed = smem_layout(Sh::kStageBytes, 0, a.q_stride, h.S, Sh::kWarpsPerCta).total;
   const uint32_t per_stage = Sh::kWarpsPerCta * (Sh::kStageBytes + a.q_stride + 8);

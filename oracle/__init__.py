@@ -28,6 +28,8 @@ written from the pages that describe PagedAttention:
   quantising cache write and attention over the dequantised values
   ("PagedAttention — how vLLM stopped wasting 80%...", FAQ "How does this
   relate to quantization?").
+* ``int8``             — the int8 quantised KV cache (symmetric codes in
+  [-127, 127], per-KV-head scales, the fp8 cache's layouts; same FAQ).
 
 Every function here is pinned by ``tests/test_oracle_*.py`` against values the
 pages print, library routines on special cases, closed forms and invariants.

@@ -211,6 +211,13 @@ def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size
         k_scale, v_scale = W.fp8_scales(Hkv, seed), W.fp8_scales(Hkv, seed + 1)
         W.fill_fp8_codes_(kc, k_scale, seed, W.STREAM_K_POOL)
         W.fill_fp8_codes_(vc, v_scale, seed, W.STREAM_V_POOL)
+    elif kv == "int8":
+        # int8 codes of N(0,1) draws with per-KV-head scales; V tiles transposed
+        kc = torch.empty((NB, Hkv, B, D), dtype=torch.int8, device=device)
+        vc = torch.empty((NB, Hkv, D, B), dtype=torch.int8, device=device)
+        k_scale, v_scale = W.int8_scales(Hkv, seed), W.int8_scales(Hkv, seed + 1)
+        W.fill_int8_codes_(kc, k_scale, seed, W.STREAM_K_POOL)
+        W.fill_int8_codes_(vc, v_scale, seed, W.STREAM_V_POOL)
     else:
         kc = torch.empty((NB, Hkv, B, D), dtype=dt, device=device)
         vc = torch.empty_like(kc)
@@ -226,7 +233,7 @@ def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size
     }
     host = {k: v.pin_memory() for k, v in host.items()}
     dev = {k: v.to(device) for k, v in host.items()}
-    if kv == "fp8":
+    if kv in ("fp8", "int8"):
         dev["k_scale"] = torch.from_numpy(k_scale).to(device)
         dev["v_scale"] = torch.from_numpy(v_scale).to(device)
     return w, lens, NB, kc, vc, host, dev
@@ -330,7 +337,7 @@ def native(args):
     __graft_entry__.build()
     import paged_kv_cache_166_gb300 as pkv
 
-    fp8 = args.kv == "fp8"
+    q8 = args.kv if args.kv in ("fp8", "int8") else None   # the 8-bit cache kind
     w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, rank, args.kv,
                                                  args.block_size)
     S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
@@ -338,7 +345,7 @@ def native(args):
     q_elt = dev["q"].element_size()
     MAXB = dev["tables"].shape[1]
     out = torch.empty_like(dev["q"])
-    ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, "fp8" if fp8 else dev["q"].dtype,
+    ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, q8 or dev["q"].dtype,
                                          args.num_warps),
                      dtype=torch.uint8, device=device)
     flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
@@ -346,18 +353,19 @@ def native(args):
     attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B, q_elt)
 
     def decode_step(q, k_new, v_new, tables, ctx):
-        if fp8:
-            pkv.paged_decode_step_fp8(q, k_new, v_new, kc, vc, dev["k_scale"], dev["v_scale"],
-                                      tables, ctx, w.scale, out, ws, args.num_warps)
+        if q8:
+            fn = pkv.paged_decode_step_fp8 if q8 == "fp8" else pkv.paged_decode_step_int8
+            fn(q, k_new, v_new, kc, vc, dev["k_scale"], dev["v_scale"], tables, ctx, w.scale,
+               out, ws, args.num_warps)
         else:
             pkv.paged_decode_step(q, k_new, v_new, kc, vc, tables, ctx, w.scale, out, ws,
                                   args.num_warps)
 
     def attention():
-        if fp8:
-            pkv.paged_decode_attention_fp8(dev["q"], kc, vc, dev["k_scale"], dev["v_scale"],
-                                           dev["tables"], dev["ctx"], w.scale, out, ws,
-                                           args.num_warps)
+        if q8:
+            fn = pkv.paged_decode_attention_fp8 if q8 == "fp8" else pkv.paged_decode_attention_int8
+            fn(dev["q"], kc, vc, dev["k_scale"], dev["v_scale"], dev["tables"], dev["ctx"],
+               w.scale, out, ws, args.num_warps)
         else:
             pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out,
                                        ws, args.num_warps)
@@ -466,7 +474,8 @@ def native(args):
     peak, peak_kind = measured_peak()
     gbs = whole_job_gbs(attn_bytes, world, ms)
     part_gbs = attn_bytes / (pms * 1e-3) / 1e9
-    tag = f"decode_attention_fp8_{args.workload}" if fp8 else f"decode_attention_{args.workload}"
+    tag = f"decode_attention_{q8}_{args.workload}" if q8 else f"decode_attention_{args.workload}"
+    kv_name = {"fp8": "fp8 (E4M3)", "int8": "int8"}.get(q8)
     traffic = profile_traffic(tag)
     line = {
         "metric": METRIC,
@@ -479,20 +488,20 @@ def native(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": f"e4m3 KV, {w.dtype} q" if fp8 else w.dtype,
+        "dtype": f"{'e4m3' if q8 == 'fp8' else 'int8'} KV, {w.dtype} q" if q8 else w.dtype,
         "data": "synthetic",
         "config": {
             "workload": f"{w.name}: {S} seqs, {Hq} q / {Hkv} kv heads, head_dim {D}, {w.dtype}, "
                         f"block {B}, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks"
-                        + (", fp8 (E4M3) KV cache with per-KV-head scales" if fp8 else ""),
+                        + (f", {kv_name} KV cache with per-KV-head scales" if q8 else ""),
             "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
             "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
-            "step": ("paged_decode_step_fp8: quantising cache write of 1 new token/seq + decode attention "
-                     "(2 launches, PDL-chained)") if fp8 else
+            "step": (f"paged_decode_step_{q8}: quantising cache write of 1 new token/seq + decode "
+                     "attention (2 launches, PDL-chained)") if q8 else
                     "paged_decode_step: cache write of 1 new token/seq + decode attention (2 launches, PDL-chained)",
-            "kv_cache": "fp8 e4m3" if fp8 else w.dtype,
+            "kv_cache": {"fp8": "fp8 e4m3", "int8": "int8"}.get(q8, w.dtype),
             "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
-            "num_warps": args.num_warps or pkv.default_num_warps(D, "fp8" if fp8 else dev["q"].dtype),
+            "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
         "pct_of_peak": {"measured_copy": round(100 * gbs / peak, 1),
@@ -503,7 +512,7 @@ def native(args):
         "roofline": {
             "bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
             "frac": round(part_gbs / peak, 4), "traffic": traffic,
-            "kernel": "decode_attention_kernel" + (" (fp8 cache)" if fp8 else ""),
+            "kernel": "decode_attention_kernel" + (f" ({q8} cache)" if q8 else ""),
             "bytes_per_launch": attn_bytes,
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         },
@@ -588,7 +597,7 @@ def swap_bench(args):
         "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
         "warmup": args.warmup, "ms_per_step": round(t_out + t_in, 4), "higher_is_better": True,
         "scaling": "weak", "vs_baseline": None,
-        "dtype": "e4m3" if args.kv == "fp8" else w.dtype, "data": "synthetic",
+        "dtype": {"fp8": "e4m3", "int8": "int8"}.get(args.kv, w.dtype), "data": "synthetic",
         "config": {"workload": f"{w.name}: {len(picked)} longest sequences, {n} blocks of "
                                f"{block_bytes} B per cache ({2 * n * block_bytes / 1e6:.1f} MB "
                                "each way)", "op": "paged_swap_out then paged_swap_in"},
@@ -725,8 +734,9 @@ def main():
     ap.add_argument("--chunk", type=int, default=0, help="prefill chunk (0: the whole prompt)")
     ap.add_argument("--block-size", type=int, default=0, choices=[0, 8, 16, 32],
                     help="cache block size (0: the workload's, 16)")
-    ap.add_argument("--kv", choices=["native", "fp8"], default="native",
-                    help="cache element type: the workload's dtype, or fp8 E4M3 with per-head scales")
+    ap.add_argument("--kv", choices=["native", "fp8", "int8"], default="native",
+                    help="cache element type: the workload's dtype, or fp8 E4M3 / int8 codes "
+                         "with per-KV-head scales")
     ap.add_argument("--soak-s", type=float, default=0.6,
                     help="seconds of untimed steps run just before the timed ones, so that the "
                          "clock samples cover this load")

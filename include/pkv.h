@@ -30,8 +30,8 @@
  *     ("What is paged attention?", section "How it works").  Token slot s lives at
  *     cache[s / block_size, :, s % block_size, :].
  *   - dtype codes: PKV_F32, PKV_F16, PKV_BF16; q, out, k, v and the caches share
- *     one dtype, except on the fp8 entry points (section "fp8 KV cache").  Index
- *     tensors are int32.
+ *     one dtype, except on the 8-bit cache entry points (sections "fp8 KV cache"
+ *     and "int8 KV cache").  Index tensors are int32.
  */
 #ifndef PKV_H_
 #define PKV_H_
@@ -57,7 +57,8 @@ enum pkv_dtype {
   PKV_F32 = 0,
   PKV_F16 = 1,
   PKV_BF16 = 2,
-  PKV_FP8_E4M3 = 3 /* 8-bit quantised cache elements; only where an entry point says so */
+  PKV_FP8_E4M3 = 3, /* 8-bit quantised cache elements; only where an entry point says so */
+  PKV_INT8 = 4      /* the same, as int8 codes */
 };
 
 /* Device-side status bits recorded by the decode kernels in the workspace. */
@@ -123,8 +124,8 @@ int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int3
  * workspace again before reuse.
  * One workspace must not be used by two launches that may run concurrently.
  */
-/* dtype PKV_FP8_E4M3 sizes the workspace of pkv_decode_attention_fp8 and
- * pkv_decode_step_fp8 (whose default warp count differs). */
+/* dtype PKV_FP8_E4M3 (PKV_INT8) sizes the workspace of pkv_decode_attention_fp8
+ * and pkv_decode_step_fp8 (_int8), whose default warp count differs. */
 int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
                               int32_t dtype, int32_t num_warps, size_t* bytes);
 
@@ -213,7 +214,7 @@ int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k
 int pkv_decode_status(void* workspace, int32_t* status, void* stream);
 
 /* Number of worker warps the default launch uses on the current device. */
-/* (dtype PKV_FP8_E4M3: the default of attention over the fp8 cache.) */
+/* (dtype PKV_FP8_E4M3 or PKV_INT8: the default of attention over that cache.) */
 int pkv_decode_default_warps(int32_t head_dim, int32_t dtype, int32_t* num_warps);
 
 /*
@@ -318,7 +319,9 @@ int pkv_prefill_attention(const void* q, const void* k_cache, const void* v_cach
  *       the block at byte V_POS[t], the byte order being the tokens
  *       0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15 (byte j holds the j-th of these).
  *   pkv_copy_blocks copies fp8 blocks with dtype PKV_FP8_E4M3 and
- *   block_elems = num_kv_heads * 16 * head_dim.
+ *   block_elems = num_kv_heads * 16 * head_dim.  pkv_swap_out_blocks and
+ *   pkv_swap_in_blocks move 8-bit blocks like any others (block_bytes =
+ *   num_kv_heads * 16 * head_dim).
  */
 
 /*
@@ -381,6 +384,62 @@ int pkv_decode_step_fp8(const void* q, const void* k_new, const void* v_new, voi
                         size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream);
 
 /* ------------------------------------------------------------------------- */
+/* int8 KV cache                                                              */
+/* ------------------------------------------------------------------------- */
+
+/*
+ * The pages name int8 beside fp8 as the narrower element of a quantised KV cache
+ * ("PagedAttention — how vLLM stopped wasting 80% of your GPU memory", FAQ "How
+ * does this relate to quantization?") and fix no format; this library uses
+ * symmetric codes:
+ *   - elements: int8 codes c in [-127, 127] (-128 is never written); an element
+ *     reads back as c * scale;
+ *   - scales: one fp32 scale per KV head for K and one for V (device arrays
+ *     k_scale[num_kv_heads], v_scale[...]), as for the fp8 cache;
+ *   - quantisation on write: c = clamp(round(x / scale), -127, 127), x widened
+ *     to fp32, the quotient a correctly rounded fp32 division rounded to the
+ *     nearest integer with ties to even; +-infinity saturates, NaN gives 0;
+ *   - layouts: those of the fp8 cache (block_size 16, K [num_blocks,
+ *     num_kv_heads, 16, head_dim], V tiles transposed with the same byte order).
+ *   pkv_copy_blocks copies int8 blocks with dtype PKV_INT8.
+ * The three entry points take the arguments of their fp8 counterparts, with the
+ * same requirements, errors and guarantees; only the element format differs.
+ */
+
+/* pkv_kv_write_int8 — pkv_kv_write_fp8 with int8 codes:
+ *   k_cache[s / 16, h, s % 16, :]        = clamp(round(k[i, h, :] / k_scale[h]))
+ *   v_cache[s / 16, h, :, V_POS[s % 16]] = clamp(round(v[i, h, :] / v_scale[h])) */
+int pkv_kv_write_int8(const void* k, const void* v, const int32_t* slot_mapping,
+                      int32_t num_tokens, void* k_cache, void* v_cache, const float* k_scale,
+                      const float* v_scale, int32_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim, int32_t dtype, void* stream);
+
+/* pkv_decode_attention_int8 — decode attention over int8 caches:
+ *   scores = (scale * k_scale[g]) * q . c_k,  out = v_scale[g] * softmax . c_v,
+ * the codes widened exactly to f16 for the tensor-core contractions, q converted
+ * to f16, fp32 scores, softmax and accumulation.  Workspace sized for dtype
+ * PKV_INT8.  Supported: block_size 16, head_dim 128 or 256, G in {1, 2, 4, 8}. */
+int pkv_decode_attention_int8(const void* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int32_t num_blocks, float scale, void* out, void* workspace,
+                              size_t workspace_bytes, int32_t num_warps, int32_t dtype,
+                              void* stream);
+
+/* pkv_decode_step_int8 — the new tokens quantised into the int8 caches as
+ * pkv_kv_write_int8 would, then pkv_decode_attention_int8, chained with
+ * programmatic dependent launch; bit-identical to the two calls in sequence. */
+int pkv_decode_step_int8(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                         void* v_cache, const float* k_scale, const float* v_scale,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, float scale, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream);
+
+/* ------------------------------------------------------------------------- */
 /* Copy-on-write block copy                                                   */
 /* ------------------------------------------------------------------------- */
 
@@ -396,7 +455,7 @@ int pkv_decode_step_fp8(const void* q, const void* k_new, const void* v_new, voi
  * A dst that is also some pair's src, or two pairs with one dst: unspecified.
  * src_dst_pairs is device int32 [num_pairs, 2].  block_elems * element size
  * must be a multiple of 16 bytes and both caches 16-byte aligned.  dtype may
- * be PKV_FP8_E4M3 for fp8 caches (one byte per element).
+ * be PKV_FP8_E4M3 or PKV_INT8 for 8-bit caches (one byte per element).
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_CUDA.
  */
 int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int32_t num_pairs,

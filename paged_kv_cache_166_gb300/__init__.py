@@ -10,7 +10,8 @@ Public API (all device work runs in libpkv.so's sm_103a kernels):
 * ``paged_prefill_attention(q, k_cache, v_cache, block_tables, context_lens, query_start, scale, out)``
   — causal attention of each sequence's chunk of new prompt tokens
 * fp8 (E4M3) cache with per-KV-head scales: ``paged_kv_write_fp8``,
-  ``paged_decode_attention_fp8``, ``paged_decode_step_fp8``
+  ``paged_decode_attention_fp8``, ``paged_decode_step_fp8``; the int8 cache:
+  ``paged_kv_write_int8``, ``paged_decode_attention_int8``, ``paged_decode_step_int8``
 * ``paged_swap_out`` / ``paged_swap_in`` — blocks to and from pinned host memory
   (preemption by swapping, with ``BlockAllocator.swap_out`` / ``swap_in``)
 * ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free)
@@ -26,7 +27,8 @@ def __getattr__(name):
     # manager, the workload generators) do not need torch's CUDA runtime.
     if name in ("paged_kv_write", "paged_decode_attention", "paged_decode_step",
                 "paged_copy_blocks", "paged_kv_write_fp8", "paged_decode_attention_fp8",
-                "paged_decode_step_fp8", "paged_swap_out", "paged_swap_in",
+                "paged_decode_step_fp8", "paged_kv_write_int8", "paged_decode_attention_int8",
+                "paged_decode_step_int8", "paged_swap_out", "paged_swap_in",
                 "paged_prefill_attention",
                 "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
         from . import ops

@@ -19,7 +19,7 @@ PKV_ERR_CUDA = -4
 PKV_ERR_UNSUPPORTED = -5
 PKV_ERR_DEVICE = -6
 
-PKV_F32, PKV_F16, PKV_BF16, PKV_FP8_E4M3 = 0, 1, 2, 3
+PKV_F32, PKV_F16, PKV_BF16, PKV_FP8_E4M3, PKV_INT8 = 0, 1, 2, 3, 4
 
 PKV_DEV_BAD_CONTEXT_LEN = 1
 PKV_DEV_BAD_BLOCK_ID = 2
@@ -64,6 +64,14 @@ SIGNATURES = {
     "pkv_decode_step_fp8": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32,
                                            _i32, _i32, _i32, _i32, _f, _p, _p, _sz, _i32, _i32,
                                            _p]),
+    "pkv_kv_write_int8": (ctypes.c_int, [_p, _p, _p, _i32, _p, _p, _p, _p, _i32, _i32, _i32, _i32,
+                                         _i32, _p]),
+    "pkv_decode_attention_int8": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32,
+                                                 _i32, _i32, _i32, _i32, _f, _p, _p, _sz, _i32,
+                                                 _i32, _p]),
+    "pkv_decode_step_int8": (ctypes.c_int, [_p, _p, _p, _p, _p, _p, _p, _p, _i32, _p, _i32, _i32,
+                                            _i32, _i32, _i32, _i32, _f, _p, _p, _sz, _i32, _i32,
+                                            _p]),
     "pkv_allocator_create": (ctypes.c_int, [_i32, _i32, _pi32, ctypes.POINTER(_p)]),
     "pkv_allocator_destroy": (ctypes.c_int, [_p]),
     "pkv_block_alloc": (ctypes.c_int, [_p, _pi32]),

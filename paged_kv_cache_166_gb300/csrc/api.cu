@@ -90,7 +90,8 @@ int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t 
     case PKV_F32: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT32; break;
     case PKV_F16: dt = CU_TENSOR_MAP_DATA_TYPE_FLOAT16; break;
     case PKV_BF16: dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16; break;
-    case PKV_FP8_E4M3: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
+    case PKV_FP8_E4M3:
+    case PKV_INT8: dt = CU_TENSOR_MAP_DATA_TYPE_UINT8; break;
     default: return fail(PKV_ERR_DTYPE, "unknown dtype %d", dtype);
   }
   return encode_map_2d(map, base, dt, element_bytes(dtype), rows, cols, box_cols, box_rows,

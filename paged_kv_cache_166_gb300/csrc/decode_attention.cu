@@ -61,8 +61,8 @@ namespace pkv {
 #ifndef PKV_WARPS_PER_CTA
 #define PKV_WARPS_PER_CTA 4
 #endif
-// fp8 stages are half the size (and hold no query rows): more warps fit, and hide
-// each other's latency; at head_dim 256 the register budget allows fewer.
+// 8-bit (fp8 or int8) stages are half the size (and hold no query rows): more warps
+// fit, and hide each other's latency; at head_dim 256 the register budget allows fewer.
 #ifndef PKV_WARPS_PER_CTA_FP8
 #define PKV_WARPS_PER_CTA_FP8 16
 #endif
@@ -149,8 +149,10 @@ struct DecodeArgs {
   float scale_log2;  // scale * log2(e)
 };
 
-// Cache element tag of the fp8 (E4M3) cache; q and out stay 16-bit there.
+// Cache element tags of the 8-bit caches, fp8 (E4M3) and int8 codes with
+// per-KV-head scales; q and out stay 16-bit there.
 struct E4M3 {};
+struct I8 {};
 template <typename C>
 struct CacheBytes {
   static constexpr int value = sizeof(C);
@@ -159,22 +161,26 @@ template <>
 struct CacheBytes<E4M3> {
   static constexpr int value = 1;
 };
+template <>
+struct CacheBytes<I8> {
+  static constexpr int value = 1;
+};
 
 template <typename C, int D>
 struct Shape {
-  static constexpr bool kFp8 = std::is_same<C, E4M3>::value;
+  static constexpr bool kQ8 = std::is_same<C, E4M3>::value || std::is_same<C, I8>::value;
   static constexpr int kElt = CacheBytes<C>::value;
-  static constexpr int kWarpsPerCta = kFp8 ? fp8_warps_per_cta(D) : kWarps;
-  static constexpr bool kQRegs = kFp8 || PKV_Q_FROM_GLOBAL;  // no query slot per stage
+  static constexpr int kWarpsPerCta = kQ8 ? fp8_warps_per_cta(D) : kWarps;
+  static constexpr bool kQRegs = kQ8 || PKV_Q_FROM_GLOBAL;  // no query slot per stage
   static constexpr int kTileBytes = kTok * D * kElt;
   static constexpr int kSub = D * kElt / kSwizzleRow;     // sub-tiles per tile
   static constexpr int kBoxCols = kSwizzleRow / kElt;      // elements per sub-tile row
   static constexpr int kStageBytes = 2 * kTileBytes;       // K and V tile
   // fp16/bf16 tiles up to head_dim 128 fit in registers: release the stage early
   static constexpr bool kEarlyRelease = PKV_EARLY_RELEASE && (kElt == 2) && (D <= 128);
-  // fp8: K in kSub boxes of [16 rows x 128 B]; V (stored [D x 16 B]) in one box
+  // 8-bit: K in kSub boxes of [16 rows x 128 B]; V (stored [D x 16 B]) in one box
   // one box per tile: rows of the tile are viewed as kSub half-rows of 128 B
-  static constexpr bool kSingleBox = PKV_SINGLE_BOX && !kFp8 && (kSub <= 2);
+  static constexpr bool kSingleBox = PKV_SINGLE_BOX && !kQ8 && (kSub <= 2);
   static_assert(kSub * kSwizzleRow == D * kElt, "head_dim * elt must be a multiple of 128 B");
 };
 
@@ -572,12 +578,14 @@ struct MmaState {
   }
 };
 
-// fp8 (E4M3) tiles.  K: [16 tokens x D bytes] in 128-byte swizzled sub-tiles.
+// 8-bit tiles (fp8 E4M3 or int8 codes).  K: [16 tokens x D bytes] in 128-byte
+// swizzled sub-tiles.
 // V: stored transposed, [D x 16 bytes] unswizzled, each 16-byte row holding the
 // 16 tokens in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15.  Operand
 // fragments come from ldmatrix on bytes: a lane's 32-bit word holds 4 consecutive
 // bytes of one row, widened exactly to two f16 pairs (hardware conversion), and
-// the contractions run on the f16 tensor cores with fp32 accumulation:
+// the contractions run on the f16 tensor cores with fp32 accumulation (an int8
+// code, |c| <= 127, and an E4M3 value times 2^-8 are both exact in f16):
 //   scores: the MMA's k index maps to head_dim as k = 2i, 2i+1 -> d = 4i, 4i+1
 //     and k = 2i+8, 2i+9 -> d = 4i+2, 4i+3 (within each 16-wide step); q is loaded
 //     in the same order, so the dot products are unchanged;
@@ -585,8 +593,9 @@ struct MmaState {
 //     token order in which P^T comes out of movmatrix, so P needs no reshuffle.
 // q (f16 or bf16) is converted to f16; k_scale folds into the score scale and
 // v_scale multiplies the accumulator when it is written.
-template <typename T, int D>
-struct Fp8State {
+template <typename T, typename C, int D>
+struct Q8State {
+  static constexpr bool kInt8 = std::is_same<C, I8>::value;
   static constexpr int KS = D / 16;
   static constexpr int kSub = D / kSwizzleRow;
   float o[KS][4];   // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
@@ -594,6 +603,16 @@ struct Fp8State {
   float m0, m1, l0, l1;
   float sl2, vs;    // score scale (log2 units, k_scale folded in), v_scale
 
+  // int8: bytes 0-1 (widen) or 2-3 (widen_hi) of w as an exact f16 pair.  With the
+  // sign bit flipped a code c reads as c + 128 in [0, 255]; under the exponent
+  // byte 0x64 that is the f16 1024 + c + 128 (the f16 step is 1 on [1024, 2048)),
+  // and subtracting 1152 leaves c exactly.
+  static __device__ __forceinline__ uint32_t widen_i8(uint32_t w, uint32_t sel) {
+    const uint32_t b = __byte_perm(w ^ 0x80808080u, 0x64646464u, sel);
+    uint32_t r;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(b), "r"(0x64806480u));
+    return r;
+  }
 #if PKV_FP8_WIDEN_ALU
   // Bytes 0-1 (widen) or 2-3 (widen_hi) of w as an f16 pair holding value * 2^-8:
   // the E4M3 exponent and mantissa bits shifted left by 7 are exactly the f16 bits
@@ -603,19 +622,25 @@ struct Fp8State {
     return y + (y & 0x40004000u);
   }
   static __device__ __forceinline__ uint32_t widen(uint32_t w) {
+    if constexpr (kInt8) return widen_i8(w, 0x4140);
     return spread(__byte_perm(w, 0u, 0x4140));
   }
   static __device__ __forceinline__ uint32_t widen_hi(uint32_t w) {
+    if constexpr (kInt8) return widen_i8(w, 0x4342);
     return spread(__byte_perm(w, 0u, 0x4342));
   }
-  static constexpr float kWidenScale = 256.f;
+  static constexpr float kWidenScale = kInt8 ? 1.f : 256.f;
 #else
   static __device__ __forceinline__ uint32_t widen(uint32_t two_codes) {
+    if constexpr (kInt8) return widen_i8(two_codes, 0x4140);
     const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
         static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
     return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
   }
-  static __device__ __forceinline__ uint32_t widen_hi(uint32_t w) { return widen(w >> 16); }
+  static __device__ __forceinline__ uint32_t widen_hi(uint32_t w) {
+    if constexpr (kInt8) return widen_i8(w, 0x4342);
+    return widen(w >> 16);
+  }
   static constexpr float kWidenScale = 1.f;
 #endif
 
@@ -1126,7 +1151,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
 #pragma unroll
         for (int c = 0; c < Sh::kSub; ++c)
           ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
-        if constexpr (Sh::kFp8) {
+        if constexpr (Sh::kQ8) {
           ptx::tma_load_2d(vt, &vmap, 0, (y / kTok) * (D / 8), bar, policy);
         } else {
 #pragma unroll
@@ -1175,7 +1200,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   }
 
   using State = typename std::conditional<
-      Sh::kFp8, Fp8State<T, D>,
+      Sh::kQ8, Q8State<T, C, D>,
       typename std::conditional<sizeof(T) == 2, MmaState<T, D>, FmaState<D>>::type>::type;
   State st_;
   Cursor cc = cursor_at(pre, S, Hkv, f0);
@@ -1201,7 +1226,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
       return;
     }
     if (n == 0 || cc.j == 0) {
-      if constexpr (Sh::kFp8) {
+      if constexpr (Sh::kQ8) {
         st_.load_q_rows(reinterpret_cast<const T*>(a.q) +
                             (static_cast<int64_t>(cc.s) * a.Hq + cc.g * a.G) * D,
                         a.G, lane);
@@ -1214,7 +1239,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
         st_.load_q(qslot + c_stage * a.q_stride, a.G, lane);
       }
       st_.reset();
-      if constexpr (Sh::kFp8) st_.set_scales(a.k_scale[cc.g], a.v_scale[cc.g], a.scale_log2);
+      if constexpr (Sh::kQ8) st_.set_scales(a.k_scale[cc.g], a.v_scale[cc.g], a.scale_log2);
       first_j = cc.j;
     }
     const int valid = (cc.j == cc.nb - 1) ? ctx_s[cc.s] - cc.j * kTok : kTok;
@@ -1298,16 +1323,16 @@ struct HostArgs {
   void* workspace;
   size_t workspace_bytes;
   int32_t num_warps;
-  int32_t dtype;  // of q and out (and of the caches unless fp8)
+  int32_t dtype;  // of q and out (and of the caches unless 8-bit)
   cudaStream_t stream;
-  bool fp8 = false;  // E4M3 caches with per-KV-head scales
+  int32_t codes = 0;  // 8-bit caches with per-KV-head scales: PKV_FP8_E4M3 or PKV_INT8
   const float* k_scale = nullptr;
   const float* v_scale = nullptr;
 };
 
 bool supported_head_dim(int32_t dtype, int32_t D) {
   if (dtype == PKV_F32) return D == 32 || D == 64 || D == 128;
-  if (dtype == PKV_FP8_E4M3) return D == 128 || D == 256;
+  if (dtype == PKV_FP8_E4M3 || dtype == PKV_INT8) return D == 128 || D == 256;
   return D == 64 || D == 128 || D == 256;
 }
 
@@ -1350,15 +1375,16 @@ int ensure_smem_attr() {
 }
 
 // One CTA per SM (the kernel sizes its pipeline to fill the SM's shared memory),
-// so the default warp count is SMs x warps per CTA.  dtype PKV_FP8_E4M3 stands for
-// attention over the fp8 cache.
+// so the default warp count is SMs x warps per CTA.  dtype PKV_FP8_E4M3 or PKV_INT8
+// stands for attention over that 8-bit cache.
 int default_warps(int32_t dtype, int32_t D) {
   if (!supported_head_dim(dtype, D))
     return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for dtype %d", D, dtype);
   int sms = 0, dev = 0;
   int rc = device_sm_count(&sms, &dev);
   if (rc != PKV_OK) return rc;
-  return sms * (dtype == PKV_FP8_E4M3 ? fp8_warps_per_cta(D) : kWarps);
+  const bool q8 = dtype == PKV_FP8_E4M3 || dtype == PKV_INT8;
+  return sms * (q8 ? fp8_warps_per_cta(D) : kWarps);
 }
 
 size_t round256(size_t x) { return (x + 255) & ~static_cast<size_t>(255); }
@@ -1382,18 +1408,18 @@ size_t workspace_bytes_for(int32_t G, int32_t D, int32_t W) {
 
 int validate(const HostArgs& h, int* warps_out) {
   PKV_REQUIRE(element_bytes(h.dtype) != 0, PKV_ERR_DTYPE, "unknown dtype %d", h.dtype);
-  if (h.fp8) {
+  if (h.codes != 0) {
     PKV_REQUIRE(h.dtype == PKV_F16 || h.dtype == PKV_BF16, PKV_ERR_DTYPE,
-                "q dtype %d: attention over the fp8 cache takes f16 or bf16 q", h.dtype);
+                "q dtype %d: attention over an 8-bit cache takes f16 or bf16 q", h.dtype);
     PKV_REQUIRE(h.D == 128 || h.D == 256, PKV_ERR_UNSUPPORTED,
-                "head_dim %d unsupported for the fp8 cache (128 or 256)", h.D);
+                "head_dim %d unsupported for an 8-bit cache (128 or 256)", h.D);
     PKV_REQUIRE(h.S == 0 || (h.k_scale && h.v_scale), PKV_ERR_INVALID_ARG,
                 "NULL k_scale / v_scale");
     PKV_REQUIRE(static_cast<int64_t>(h.NB) * h.Hkv * h.D < (int64_t(1) << 31),
                 PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * head_dim >= 2^31");
   } else {
-    PKV_REQUIRE(h.dtype != PKV_FP8_E4M3, PKV_ERR_DTYPE,
-                "fp8 caches are read by pkv_decode_attention_fp8");
+    PKV_REQUIRE(h.dtype != PKV_FP8_E4M3 && h.dtype != PKV_INT8, PKV_ERR_DTYPE,
+                "8-bit caches are read by pkv_decode_attention_fp8 / _int8");
   }
   PKV_REQUIRE(h.S >= 0 && h.S <= kMaxSeqs, PKV_ERR_UNSUPPORTED,
               "num_seqs %d outside [0, %d]", h.S, kMaxSeqs);
@@ -1406,7 +1432,7 @@ int validate(const HostArgs& h, int* warps_out) {
               "head_dim %d unsupported for dtype %d", h.D, h.dtype);
   PKV_REQUIRE(h.block_size == 8 || h.block_size == 16 || h.block_size == 32,
               PKV_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32}", h.block_size);
-  PKV_REQUIRE(h.block_size == kTok || (!h.fp8 && !PKV_SINGLE_BOX && h.dtype != PKV_F32),
+  PKV_REQUIRE(h.block_size == kTok || (h.codes == 0 && !PKV_SINGLE_BOX && h.dtype != PKV_F32),
               PKV_ERR_UNSUPPORTED, "block_size %d needs an f16 or bf16 cache", h.block_size);
   PKV_REQUIRE(h.MAXB > 0, PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
   PKV_REQUIRE(static_cast<int64_t>(h.S) * h.MAXB * h.Hkv < (int64_t(1) << 31),
@@ -1414,7 +1440,7 @@ int validate(const HostArgs& h, int* warps_out) {
   PKV_REQUIRE(h.num_warps >= 0, PKV_ERR_INVALID_ARG, "negative num_warps");
   int W = h.num_warps;
   if (W == 0) {
-    W = default_warps(h.fp8 ? PKV_FP8_E4M3 : h.dtype, h.D);
+    W = default_warps(h.codes != 0 ? h.codes : h.dtype, h.D);
     if (W < 0) return W;
   }
   *warps_out = W;
@@ -1484,14 +1510,14 @@ int launch_decode(const HostArgs& h, int W) {
   const uint32_t fixed = smem_layout(Sh::kStageBytes, 0, a.q_stride, h.S, Sh::kWarpsPerCta).total;
   const uint32_t per_stage = Sh::kWarpsPerCta * (Sh::kStageBytes + a.q_stride + 8);
   int stages = optin > static_cast<int>(fixed) ? static_cast<int>((optin - fixed) / per_stage) : 0;
-  const int max_stages = Sh::kFp8 ? kMaxStagesFp8 : kMaxStages;
+  const int max_stages = Sh::kQ8 ? kMaxStagesFp8 : kMaxStages;
   stages = stages > max_stages ? max_stages : stages;
   PKV_REQUIRE(stages >= 2, PKV_ERR_UNSUPPORTED, "pipeline does not fit in shared memory");
   a.stages = stages;
   const SmemLayout L = smem_layout(Sh::kStageBytes, stages, a.q_stride, h.S, Sh::kWarpsPerCta);
   CUtensorMap kmap, vmap;
   const int64_t rows = static_cast<int64_t>(h.NB) * h.Hkv * h.block_size;
-  if constexpr (Sh::kFp8) {
+  if constexpr (Sh::kQ8) {
     // K: [rows, D] bytes, boxes of 16 rows x 128 B, swizzled.  V: each transposed
     // [D x 16 B] tile is 16 D contiguous bytes, viewed as D/8 rows of 128 B so that
     // one unswizzled box of D/8 rows moves it (the bytes land in the same order).
@@ -1529,15 +1555,22 @@ int launch_decode(const HostArgs& h, int W) {
 }
 
 int dispatch(const HostArgs& h, int W) {
-  if (h.fp8) {
-#define PKV_CASE8(DT, TT, DD) \
-  if (h.dtype == DT && h.D == DD) return launch_decode<TT, E4M3, DD, kTok>(h, W);
-    PKV_CASE8(PKV_BF16, __nv_bfloat16, 128)
-    PKV_CASE8(PKV_BF16, __nv_bfloat16, 256)
-    PKV_CASE8(PKV_F16, __half, 128)
-    PKV_CASE8(PKV_F16, __half, 256)
+  if (h.codes != 0) {
+#define PKV_CASE8(CT, DT, TT, DD) \
+  if (h.dtype == DT && h.D == DD) return launch_decode<TT, CT, DD, kTok>(h, W);
+    if (h.codes == PKV_FP8_E4M3) {
+      PKV_CASE8(E4M3, PKV_BF16, __nv_bfloat16, 128)
+      PKV_CASE8(E4M3, PKV_BF16, __nv_bfloat16, 256)
+      PKV_CASE8(E4M3, PKV_F16, __half, 128)
+      PKV_CASE8(E4M3, PKV_F16, __half, 256)
+    } else {
+      PKV_CASE8(I8, PKV_BF16, __nv_bfloat16, 128)
+      PKV_CASE8(I8, PKV_BF16, __nv_bfloat16, 256)
+      PKV_CASE8(I8, PKV_F16, __half, 128)
+      PKV_CASE8(I8, PKV_F16, __half, 256)
+    }
 #undef PKV_CASE8
-    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for the fp8 cache", h.D);
+    return fail(PKV_ERR_UNSUPPORTED, "head_dim %d unsupported for an 8-bit cache", h.D);
   }
   if (h.block_size != kTok) {
 #define PKV_CASEB(DT, TT, DD) \
@@ -1675,6 +1708,50 @@ int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k
   return rc == PKV_OK ? ok() : rc;
 }
 
+namespace {
+int decode_q8_entry(int32_t codes, const void* q, const void* k_cache, const void* v_cache,
+                    const float* k_scale, const float* v_scale, const int32_t* block_tables,
+                    int32_t max_blocks_per_seq, const int32_t* context_lens, int32_t num_seqs,
+                    int32_t num_q_heads, int32_t num_kv_heads, int32_t head_dim,
+                    int32_t block_size, int32_t num_blocks, float scale, void* out,
+                    void* workspace, size_t workspace_bytes, int32_t num_warps, int32_t dtype,
+                    void* stream) {
+  HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                         scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
+  h.codes = codes;
+  h.k_scale = k_scale;
+  h.v_scale = v_scale;
+  return decode_entry(h);
+}
+
+int decode_step_q8_entry(int32_t codes, const void* q, const void* k_new, const void* v_new,
+                         void* k_cache, void* v_cache, const float* k_scale,
+                         const float* v_scale, const int32_t* block_tables,
+                         int32_t max_blocks_per_seq, const int32_t* context_lens,
+                         int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                         int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
+                         void* out, void* workspace, size_t workspace_bytes, int32_t num_warps,
+                         int32_t dtype, void* stream) {
+  HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
+                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
+                         scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
+  h.codes = codes;
+  h.k_scale = k_scale;
+  h.v_scale = v_scale;
+  int W = 0;
+  int rc = validate(h, &W);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs == 0) return ok();
+  rc = launch_kv_write_q8(k_new, v_new, nullptr, block_tables, max_blocks_per_seq, context_lens,
+                          num_seqs, k_cache, v_cache, k_scale, v_scale, num_blocks, num_kv_heads,
+                          head_dim, dtype, codes, stream);
+  if (rc != PKV_OK) return rc;
+  rc = dispatch(h, W);
+  return rc == PKV_OK ? ok() : rc;
+}
+}  // namespace
+
 int pkv_decode_attention_fp8(const void* q, const void* k_cache, const void* v_cache,
                              const float* k_scale, const float* v_scale,
                              const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -1683,13 +1760,24 @@ int pkv_decode_attention_fp8(const void* q, const void* k_cache, const void* v_c
                              int32_t num_blocks, float scale, void* out, void* workspace,
                              size_t workspace_bytes, int32_t num_warps, int32_t dtype,
                              void* stream) {
-  HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                         scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
-  h.fp8 = true;
-  h.k_scale = k_scale;
-  h.v_scale = v_scale;
-  return decode_entry(h);
+  return decode_q8_entry(PKV_FP8_E4M3, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                         max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, scale, out, workspace,
+                         workspace_bytes, num_warps, dtype, stream);
+}
+
+int pkv_decode_attention_int8(const void* q, const void* k_cache, const void* v_cache,
+                              const float* k_scale, const float* v_scale,
+                              const int32_t* block_tables, int32_t max_blocks_per_seq,
+                              const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                              int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                              int32_t num_blocks, float scale, void* out, void* workspace,
+                              size_t workspace_bytes, int32_t num_warps, int32_t dtype,
+                              void* stream) {
+  return decode_q8_entry(PKV_INT8, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                         max_blocks_per_seq, context_lens, num_seqs, num_q_heads, num_kv_heads,
+                         head_dim, block_size, num_blocks, scale, out, workspace,
+                         workspace_bytes, num_warps, dtype, stream);
 }
 
 int pkv_decode_step_fp8(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -1699,22 +1787,23 @@ int pkv_decode_step_fp8(const void* q, const void* k_new, const void* v_new, voi
                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
                         int32_t num_blocks, float scale, void* out, void* workspace,
                         size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
-  HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                         num_seqs, num_q_heads, num_kv_heads, head_dim, block_size, num_blocks,
-                         scale, out, workspace, workspace_bytes, num_warps, dtype, stream);
-  h.fp8 = true;
-  h.k_scale = k_scale;
-  h.v_scale = v_scale;
-  int W = 0;
-  int rc = validate(h, &W);
-  if (rc != PKV_OK) return rc;
-  if (num_seqs == 0) return ok();
-  rc = launch_kv_write_fp8(k_new, v_new, nullptr, block_tables, max_blocks_per_seq, context_lens,
-                           num_seqs, k_cache, v_cache, k_scale, v_scale, num_blocks,
-                           num_kv_heads, head_dim, dtype, stream);
-  if (rc != PKV_OK) return rc;
-  rc = dispatch(h, W);
-  return rc == PKV_OK ? ok() : rc;
+  return decode_step_q8_entry(PKV_FP8_E4M3, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                              block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                              num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                              out, workspace, workspace_bytes, num_warps, dtype, stream);
+}
+
+int pkv_decode_step_int8(const void* q, const void* k_new, const void* v_new, void* k_cache,
+                         void* v_cache, const float* k_scale, const float* v_scale,
+                         const int32_t* block_tables, int32_t max_blocks_per_seq,
+                         const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                         int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                         int32_t num_blocks, float scale, void* out, void* workspace,
+                         size_t workspace_bytes, int32_t num_warps, int32_t dtype, void* stream) {
+  return decode_step_q8_entry(PKV_INT8, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                              block_tables, max_blocks_per_seq, context_lens, num_seqs,
+                              num_q_heads, num_kv_heads, head_dim, block_size, num_blocks, scale,
+                              out, workspace, workspace_bytes, num_warps, dtype, stream);
 }
 
 int pkv_decode_status(void* workspace, int32_t* status, void* stream) {

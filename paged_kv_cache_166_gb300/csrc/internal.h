@@ -17,6 +17,7 @@ inline int element_bytes(int32_t dtype) {
     case PKV_F16: return 2;
     case PKV_BF16: return 2;
     case PKV_FP8_E4M3: return 1;
+    case PKV_INT8: return 1;
     default: return 0;
   }
 }
@@ -43,15 +44,16 @@ int encode_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType type, 
                   int64_t rows, int32_t cols, int32_t box_cols, int32_t box_rows,
                   CUtensorMapSwizzle swizzle);
 
-// Launches the fp8 quantising cache write (kv_ops.cu).  With slot_mapping set,
-// token i goes to slot_mapping[i]; with it NULL, sequence i's token goes to
-// slot(t - 1) of its block table, t = context_lens[i] (the decode-step append).
-int launch_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
-                        const int32_t* block_tables, int32_t max_blocks_per_seq,
-                        const int32_t* context_lens, int32_t num_tokens, void* k_cache,
-                        void* v_cache, const float* k_scale, const float* v_scale,
-                        int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
-                        int32_t dtype, void* stream);
+// Launches the 8-bit quantising cache write (kv_ops.cu); codes is PKV_FP8_E4M3
+// or PKV_INT8.  With slot_mapping set, token i goes to slot_mapping[i]; with it
+// NULL, sequence i's token goes to slot(t - 1) of its block table,
+// t = context_lens[i] (the decode-step append).
+int launch_kv_write_q8(const void* k, const void* v, const int32_t* slot_mapping,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t num_tokens, void* k_cache,
+                       void* v_cache, const float* k_scale, const float* v_scale,
+                       int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t dtype, int32_t codes, void* stream);
 
 // Launches the decode-step cache write: for every sequence s with t = ctx[s] > 0,
 // the rows k_new[s], v_new[s] go to slot(t - 1) of its block table (kv_ops.cu).

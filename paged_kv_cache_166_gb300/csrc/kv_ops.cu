@@ -89,8 +89,8 @@ __global__ void decode_append_kernel(const uint4* __restrict__ k, const uint4* _
   }
 }
 
-// ---- fp8 (E4M3) quantising cache write --------------------------------------------
-// Byte of token t (0..15) inside a 16-byte head_dim row of an fp8 V tile: the
+// ---- 8-bit (fp8 E4M3 or int8) quantising cache write --------------------------------
+// Byte of token t (0..15) inside a 16-byte head_dim row of an 8-bit V tile: the
 // tokens are stored in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15.
 __device__ __forceinline__ int fp8_v_pos(int t) {
   return t < 8 ? 4 * (t >> 1) + (t & 1) : 4 * ((t - 8) >> 1) + 2 + (t & 1);
@@ -148,12 +148,34 @@ __device__ __forceinline__ uint4 quantize16(const float (&x)[16], float scale) {
   return make_uint4(w[0], w[1], w[2], w[3]);
 }
 
+// int8 codes of x[i] / scale, i < 16: the quotient a correctly rounded fp32
+// division, rounded to the nearest integer with ties to even, clamped to
+// [-127, 127]; NaN gives 0.  Byte i of the result is element i.
+__device__ __forceinline__ uint4 quantize16_int8(const float (&x)[16], float scale) {
+  uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+  for (int j = 0; j < 16; ++j) {
+    const float q = __fdiv_rn(x[j], scale);
+    int c = __float2int_rn(q);           // saturates at the int range for +-inf
+    c = q != q ? 0 : (c < -127 ? -127 : (c > 127 ? 127 : c));
+    w[j >> 2] |= (static_cast<uint32_t>(c) & 0xffu) << (8 * (j & 3));
+  }
+  return make_uint4(w[0], w[1], w[2], w[3]);
+}
+
+template <bool kInt8>
+__device__ __forceinline__ uint4 quantize16_as(const float (&x)[16], float scale) {
+  if constexpr (kInt8) return quantize16_int8(x, scale);
+  return quantize16(x, scale);
+}
+
 // Token i (or sequence i's new token, when slots is NULL: position ctx[i] - 1 of
-// its block table) for KV head h, elements [16 c, 16 c + 16) of the row:
-//   K8[slot / 16, h, slot % 16, 16c + e]       = E4M3(k[i, h, 16c + e] / k_scale[h])
-//   V8[slot / 16, h, 16c + e, V_POS[slot % 16]] = E4M3(v[i, h, 16c + e] / v_scale[h])
-template <typename Tin>
-__global__ void kv_write_fp8_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
+// its block table) for KV head h, elements [16 c, 16 c + 16) of the row, with Q
+// the E4M3 or the int8 quantisation:
+//   K8[slot / 16, h, slot % 16, 16c + e]       = Q(k[i, h, 16c + e] / k_scale[h])
+//   V8[slot / 16, h, 16c + e, V_POS[slot % 16]] = Q(v[i, h, 16c + e] / v_scale[h])
+template <typename Tin, bool kInt8>
+__global__ void kv_write_q8_kernel(const Tin* __restrict__ k, const Tin* __restrict__ v,
                                     const int32_t* __restrict__ slots,
                                     const int32_t* __restrict__ tables, int32_t MAXB,
                                     const int32_t* __restrict__ ctx, int64_t total, int32_t Hkv,
@@ -185,9 +207,10 @@ __global__ void kv_write_fp8_kernel(const Tin* __restrict__ k, const Tin* __rest
     const int64_t src = th * D + 16 * c;
     float x[16];
     load16(k + src, x);
-    *reinterpret_cast<uint4*>(kc + (tile * 16 + off) * D + 16 * c) = quantize16(x, __ldg(ks + h));
+    *reinterpret_cast<uint4*>(kc + (tile * 16 + off) * D + 16 * c) =
+        quantize16_as<kInt8>(x, __ldg(ks + h));
     load16(v + src, x);
-    const uint4 q = quantize16(x, __ldg(vs + h));
+    const uint4 q = quantize16_as<kInt8>(x, __ldg(vs + h));
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     uint8_t* const col = vc + (tile * D + 16 * c) * 16 + fp8_v_pos(off);
 #pragma unroll
@@ -235,14 +258,16 @@ int grid_for(int64_t work, int threads) {
 
 }  // namespace
 
-int launch_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
-                        const int32_t* block_tables, int32_t max_blocks_per_seq,
-                        const int32_t* context_lens, int32_t num_tokens, void* k_cache,
-                        void* v_cache, const float* k_scale, const float* v_scale,
-                        int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
-                        int32_t dtype, void* stream) {
+int launch_kv_write_q8(const void* k, const void* v, const int32_t* slot_mapping,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* context_lens, int32_t num_tokens, void* k_cache,
+                       void* v_cache, const float* k_scale, const float* v_scale,
+                       int32_t num_blocks, int32_t num_kv_heads, int32_t head_dim,
+                       int32_t dtype, int32_t codes, void* stream) {
   PKV_REQUIRE(dtype == PKV_F32 || dtype == PKV_F16 || dtype == PKV_BF16, PKV_ERR_DTYPE,
               "input dtype %d is not f32, f16 or bf16", dtype);
+  PKV_REQUIRE(codes == PKV_FP8_E4M3 || codes == PKV_INT8, PKV_ERR_DTYPE,
+              "cache code %d is not PKV_FP8_E4M3 or PKV_INT8", codes);
   PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && num_kv_heads > 0 && head_dim > 0 &&
                   head_dim % 16 == 0,
               PKV_ERR_INVALID_ARG, "bad sizes (head_dim must be a positive multiple of 16)");
@@ -261,15 +286,20 @@ int launch_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mappin
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   auto* kc = static_cast<uint8_t*>(k_cache);
   auto* vc = static_cast<uint8_t*>(v_cache);
-#define PKV_FP8_WRITE(TT)                                                                   \
-  kv_write_fp8_kernel<TT><<<grid, threads, 0, st>>>(                                        \
+#define PKV_Q8_WRITE(TT, I8)                                                                \
+  kv_write_q8_kernel<TT, I8><<<grid, threads, 0, st>>>(                                     \
       static_cast<const TT*>(k), static_cast<const TT*>(v), slot_mapping, block_tables,     \
       max_blocks_per_seq, context_lens, total, num_kv_heads, head_dim, num_blocks, k_scale, \
       v_scale, kc, vc)
-  if (dtype == PKV_F32) PKV_FP8_WRITE(float);
-  else if (dtype == PKV_F16) PKV_FP8_WRITE(__half);
-  else PKV_FP8_WRITE(__nv_bfloat16);
-#undef PKV_FP8_WRITE
+  const bool i8 = codes == PKV_INT8;
+  if (dtype == PKV_F32) {
+    if (i8) PKV_Q8_WRITE(float, true); else PKV_Q8_WRITE(float, false);
+  } else if (dtype == PKV_F16) {
+    if (i8) PKV_Q8_WRITE(__half, true); else PKV_Q8_WRITE(__half, false);
+  } else {
+    if (i8) PKV_Q8_WRITE(__nv_bfloat16, true); else PKV_Q8_WRITE(__nv_bfloat16, false);
+  }
+#undef PKV_Q8_WRITE
   PKV_CUDA(cudaGetLastError());
   return PKV_OK;
 }
@@ -354,8 +384,9 @@ int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int3
                  int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
   const int elt = element_bytes(dtype);
   PKV_REQUIRE(elt != 0, PKV_ERR_DTYPE, "unknown dtype %d", dtype);
-  PKV_REQUIRE(dtype != PKV_FP8_E4M3, PKV_ERR_DTYPE,
-              "fp8 caches are written by pkv_kv_write_fp8 (quantising, V tiles transposed)");
+  PKV_REQUIRE(dtype != PKV_FP8_E4M3 && dtype != PKV_INT8, PKV_ERR_DTYPE,
+              "8-bit caches are written by pkv_kv_write_fp8 / _int8 (quantising, V tiles "
+              "transposed)");
   PKV_REQUIRE(num_tokens >= 0 && num_blocks > 0 && num_kv_heads > 0 && block_size > 0 &&
                   head_dim > 0,
               PKV_ERR_INVALID_ARG, "sizes must be positive (num_tokens >= 0)");
@@ -378,17 +409,37 @@ int pkv_kv_write(const void* k, const void* v, const int32_t* slot_mapping, int3
   return ok();
 }
 
+namespace {
+int kv_write_q8_entry(int32_t codes, const void* k, const void* v, const int32_t* slot_mapping,
+                      int32_t num_tokens, void* k_cache, void* v_cache, const float* k_scale,
+                      const float* v_scale, int32_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
+  PKV_REQUIRE(block_size == 16, PKV_ERR_UNSUPPORTED, "8-bit caches use block_size 16, not %d",
+              block_size);
+  PKV_REQUIRE(num_tokens == 0 || slot_mapping, PKV_ERR_INVALID_ARG, "NULL slot_mapping");
+  const int rc = launch_kv_write_q8(k, v, slot_mapping, nullptr, 0, nullptr, num_tokens, k_cache,
+                                    v_cache, k_scale, v_scale, num_blocks, num_kv_heads,
+                                    head_dim, dtype, codes, stream);
+  return rc == PKV_OK ? ok() : rc;
+}
+}  // namespace
+
 int pkv_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
                      int32_t num_tokens, void* k_cache, void* v_cache, const float* k_scale,
                      const float* v_scale, int32_t num_blocks, int32_t num_kv_heads,
                      int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
-  PKV_REQUIRE(block_size == 16, PKV_ERR_UNSUPPORTED, "fp8 caches use block_size 16, not %d",
-              block_size);
-  PKV_REQUIRE(num_tokens == 0 || slot_mapping, PKV_ERR_INVALID_ARG, "NULL slot_mapping");
-  const int rc = launch_kv_write_fp8(k, v, slot_mapping, nullptr, 0, nullptr, num_tokens, k_cache,
-                                     v_cache, k_scale, v_scale, num_blocks, num_kv_heads,
-                                     head_dim, dtype, stream);
-  return rc == PKV_OK ? ok() : rc;
+  return kv_write_q8_entry(PKV_FP8_E4M3, k, v, slot_mapping, num_tokens, k_cache, v_cache,
+                           k_scale, v_scale, num_blocks, num_kv_heads, block_size, head_dim,
+                           dtype, stream);
+}
+
+int pkv_kv_write_int8(const void* k, const void* v, const int32_t* slot_mapping,
+                      int32_t num_tokens, void* k_cache, void* v_cache, const float* k_scale,
+                      const float* v_scale, int32_t num_blocks, int32_t num_kv_heads,
+                      int32_t block_size, int32_t head_dim, int32_t dtype, void* stream) {
+  return kv_write_q8_entry(PKV_INT8, k, v, slot_mapping, num_tokens, k_cache, v_cache, k_scale,
+                           v_scale, num_blocks, num_kv_heads, block_size, head_dim, dtype,
+                           stream);
 }
 
 int pkv_swap_out_blocks(const void* k_cache, const void* v_cache, const int32_t* block_ids,

@@ -14,6 +14,7 @@ import torch
 from . import _native as N
 
 _DTYPES = {torch.float32: N.PKV_F32, torch.float16: N.PKV_F16, torch.bfloat16: N.PKV_BF16}
+_CODES = {"fp8": N.PKV_FP8_E4M3, "int8": N.PKV_INT8}   # the 8-bit cache kinds
 _WORKSPACES: dict = {}
 
 
@@ -65,7 +66,7 @@ def paged_kv_write(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
 
 def default_num_warps(head_dim: int, dtype) -> int:
     """Default worker warps; ``dtype`` as in ``workspace_bytes``."""
-    code = N.PKV_FP8_E4M3 if dtype == "fp8" else _DTYPES[dtype]
+    code = _CODES[dtype] if isinstance(dtype, str) else _DTYPES[dtype]
     n = ctypes.c_int32(0)
     N.check(N.lib().pkv_decode_default_warps(head_dim, code, ctypes.byref(n)))
     return n.value
@@ -73,9 +74,9 @@ def default_num_warps(head_dim: int, dtype) -> int:
 
 def workspace_bytes(num_q_heads: int, num_kv_heads: int, head_dim: int, dtype,
                     num_warps: int = 0) -> int:
-    """Decode workspace bytes; ``dtype`` is q's torch dtype, or "fp8" for
-    attention over the fp8 cache."""
-    code = N.PKV_FP8_E4M3 if dtype == "fp8" else _DTYPES[dtype]
+    """Decode workspace bytes; ``dtype`` is q's torch dtype, or "fp8" / "int8"
+    for attention over that 8-bit cache."""
+    code = _CODES[dtype] if isinstance(dtype, str) else _DTYPES[dtype]
     n = ctypes.c_size_t(0)
     N.check(N.lib().pkv_decode_workspace_size(num_q_heads, num_kv_heads, head_dim, code,
                                               num_warps, ctypes.byref(n)))
@@ -157,14 +158,18 @@ def paged_decode_step(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
     return out
 
 
-def _fp8_caches(k_cache, v_cache):
-    """(k_cache, v_cache) as uint8 views: fp8 caches may be uint8 or float8_e4m3fn."""
+def _q8_caches(k_cache, v_cache, kind):
+    """(k_cache, v_cache) as byte views: fp8 caches are uint8 or float8_e4m3fn
+    tensors, int8 caches int8 tensors."""
     out = []
     for c in (k_cache, v_cache):
-        if c.dtype == getattr(torch, "float8_e4m3fn", None):
-            c = c.view(torch.uint8)
-        if c.dtype != torch.uint8:
-            raise TypeError("fp8 caches must be uint8 or float8_e4m3fn tensors")
+        if kind == "fp8":
+            if c.dtype == getattr(torch, "float8_e4m3fn", None):
+                c = c.view(torch.uint8)
+            if c.dtype != torch.uint8:
+                raise TypeError("fp8 caches must be uint8 or float8_e4m3fn tensors")
+        elif c.dtype != torch.int8:
+            raise TypeError("int8 caches must be int8 tensors")
         out.append(c)
     return out
 
@@ -175,12 +180,8 @@ def _check_scales(k_scale, v_scale, Hkv):
             raise ValueError(f"scales must be float32 [{Hkv}]")
 
 
-def paged_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
-                       k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
-                       v_scale: torch.Tensor) -> None:
-    """Quantise k, v [T, Hkv, D] to fp8 (E4M3, per-KV-head scales) and scatter them:
-    k_cache [NB, Hkv, 16, D], v_cache [NB, Hkv, D, 16] (uint8)."""
-    kc, vc = _fp8_caches(k_cache, v_cache)
+def _kv_write_q8(kind, k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale):
+    kc, vc = _q8_caches(k_cache, v_cache, kind)
     dev = _check_cuda(k, v, slot_mapping, kc, vc, k_scale, v_scale)
     _check_index(slot_mapping, "slot_mapping")
     if k.shape != v.shape or k.dim() != 3 or kc.dim() != 4 or vc.dim() != 4:
@@ -188,17 +189,33 @@ def paged_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Ten
     T, Hkv, D = k.shape
     NB, B = kc.shape[0], kc.shape[2]
     if kc.shape != (NB, Hkv, B, D) or vc.shape != (NB, Hkv, D, B) or slot_mapping.shape != (T,):
-        raise ValueError("shape mismatch between tokens, slots and fp8 caches")
+        raise ValueError(f"shape mismatch between tokens, slots and {kind} caches")
     _check_scales(k_scale, v_scale, Hkv)
     if k.dtype != v.dtype:
         raise TypeError("k and v must share a dtype")
-    N.check(N.lib().pkv_kv_write_fp8(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T,
-                                     kc.data_ptr(), vc.data_ptr(), k_scale.data_ptr(),
-                                     v_scale.data_ptr(), NB, Hkv, B, D, dtype_code(k),
-                                     _stream(dev)))
+    fn = N.lib().pkv_kv_write_fp8 if kind == "fp8" else N.lib().pkv_kv_write_int8
+    N.check(fn(k.data_ptr(), v.data_ptr(), slot_mapping.data_ptr(), T, kc.data_ptr(),
+               vc.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(), NB, Hkv, B, D,
+               dtype_code(k), _stream(dev)))
 
 
-def _fp8_shapes(q, kc, vc, block_tables, context_lens, out):
+def paged_kv_write_fp8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                       k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                       v_scale: torch.Tensor) -> None:
+    """Quantise k, v [T, Hkv, D] to fp8 (E4M3, per-KV-head scales) and scatter them:
+    k_cache [NB, Hkv, 16, D], v_cache [NB, Hkv, D, 16] (uint8)."""
+    _kv_write_q8("fp8", k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale)
+
+
+def paged_kv_write_int8(k: torch.Tensor, v: torch.Tensor, slot_mapping: torch.Tensor,
+                        k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                        v_scale: torch.Tensor) -> None:
+    """Quantise k, v [T, Hkv, D] to int8 codes in [-127, 127] (per-KV-head scales)
+    and scatter them: k_cache [NB, Hkv, 16, D], v_cache [NB, Hkv, D, 16] (int8)."""
+    _kv_write_q8("int8", k, v, slot_mapping, k_cache, v_cache, k_scale, v_scale)
+
+
+def _q8_shapes(q, kc, vc, block_tables, context_lens, out):
     if q.dim() != 3 or kc.dim() != 4 or vc.dim() != 4:
         raise ValueError("expected q [S, Hq, D], k_cache [NB, Hkv, 16, D], v_cache [NB, Hkv, D, 16]")
     S, Hq, D = q.shape
@@ -214,6 +231,49 @@ def _fp8_shapes(q, kc, vc, block_tables, context_lens, out):
     return S, Hq, D, NB, Hkv, B, block_tables.shape[1]
 
 
+def _q8_workspace(kind, dev, Hq, Hkv, D, num_warps, workspace):
+    need = workspace_bytes(Hq, Hkv, D, kind, num_warps)
+    ws = get_workspace(dev, Hq // Hkv, D, num_warps, need, kind) if workspace is None else workspace
+    if ws.numel() * ws.element_size() < need:
+        raise ValueError(f"workspace smaller than the {need} bytes needed")
+    return ws
+
+
+def _decode_attention_q8(kind, q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                         context_lens, scale, out, workspace, num_warps):
+    kc, vc = _q8_caches(k_cache, v_cache, kind)
+    dev = _check_cuda(q, kc, vc, k_scale, v_scale, block_tables, context_lens, out)
+    S, Hq, D, NB, Hkv, B, MAXB = _q8_shapes(q, kc, vc, block_tables, context_lens, out)
+    _check_scales(k_scale, v_scale, Hkv)
+    ws = _q8_workspace(kind, dev, Hq, Hkv, D, num_warps, workspace)
+    fn = N.lib().pkv_decode_attention_fp8 if kind == "fp8" else N.lib().pkv_decode_attention_int8
+    N.check(fn(q.data_ptr(), kc.data_ptr(), vc.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
+               block_tables.data_ptr(), MAXB, context_lens.data_ptr(), S, Hq, Hkv, D, B, NB,
+               float(scale), out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(),
+               num_warps, dtype_code(q), _stream(dev)))
+    return out
+
+
+def _decode_step_q8(kind, q, k_new, v_new, k_cache, v_cache, k_scale, v_scale, block_tables,
+                    context_lens, scale, out, workspace, num_warps):
+    kc, vc = _q8_caches(k_cache, v_cache, kind)
+    dev = _check_cuda(q, k_new, v_new, kc, vc, k_scale, v_scale, block_tables, context_lens, out)
+    S, Hq, D, NB, Hkv, B, MAXB = _q8_shapes(q, kc, vc, block_tables, context_lens, out)
+    _check_scales(k_scale, v_scale, Hkv)
+    if k_new.shape != (S, Hkv, D) or v_new.shape != (S, Hkv, D):
+        raise ValueError("k_new and v_new must be [S, Hkv, D]")
+    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
+        raise TypeError("k_new and v_new must share the dtype of q")
+    ws = _q8_workspace(kind, dev, Hq, Hkv, D, num_warps, workspace)
+    fn = N.lib().pkv_decode_step_fp8 if kind == "fp8" else N.lib().pkv_decode_step_int8
+    N.check(fn(q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), kc.data_ptr(), vc.data_ptr(),
+               k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(), MAXB,
+               context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), out.data_ptr(),
+               ws.data_ptr(), ws.numel() * ws.element_size(), num_warps, dtype_code(q),
+               _stream(dev)))
+    return out
+
+
 def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
                                k_scale: torch.Tensor, v_scale: torch.Tensor,
                                block_tables: torch.Tensor, context_lens: torch.Tensor,
@@ -221,20 +281,19 @@ def paged_decode_attention_fp8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: 
                                workspace: Optional[torch.Tensor] = None,
                                num_warps: int = 0) -> torch.Tensor:
     """Decode attention of q [S, Hq, D] (f16/bf16) over fp8 caches; writes and returns out."""
-    kc, vc = _fp8_caches(k_cache, v_cache)
-    dev = _check_cuda(q, kc, vc, k_scale, v_scale, block_tables, context_lens, out)
-    S, Hq, D, NB, Hkv, B, MAXB = _fp8_shapes(q, kc, vc, block_tables, context_lens, out)
-    _check_scales(k_scale, v_scale, Hkv)
-    need = workspace_bytes(Hq, Hkv, D, "fp8", num_warps)
-    ws = get_workspace(dev, Hq // Hkv, D, num_warps, need, "fp8") if workspace is None else workspace
-    if ws.numel() * ws.element_size() < need:
-        raise ValueError(f"workspace smaller than the {need} bytes needed")
-    N.check(N.lib().pkv_decode_attention_fp8(
-        q.data_ptr(), kc.data_ptr(), vc.data_ptr(), k_scale.data_ptr(), v_scale.data_ptr(),
-        block_tables.data_ptr(), MAXB, context_lens.data_ptr(), S, Hq, Hkv, D, B, NB,
-        float(scale), out.data_ptr(), ws.data_ptr(), ws.numel() * ws.element_size(), num_warps,
-        dtype_code(q), _stream(dev)))
-    return out
+    return _decode_attention_q8("fp8", q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                context_lens, scale, out, workspace, num_warps)
+
+
+def paged_decode_attention_int8(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
+                                k_scale: torch.Tensor, v_scale: torch.Tensor,
+                                block_tables: torch.Tensor, context_lens: torch.Tensor,
+                                scale: float, out: torch.Tensor,
+                                workspace: Optional[torch.Tensor] = None,
+                                num_warps: int = 0) -> torch.Tensor:
+    """Decode attention of q [S, Hq, D] (f16/bf16) over int8 caches; writes and returns out."""
+    return _decode_attention_q8("int8", q, k_cache, v_cache, k_scale, v_scale, block_tables,
+                                context_lens, scale, out, workspace, num_warps)
 
 
 def paged_decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
@@ -246,24 +305,21 @@ def paged_decode_step_fp8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Ten
     """One decode step over fp8 caches: quantise and write each sequence's new token
     (position context_lens[s] - 1), then attend (two launches, programmatic
     dependent launch)."""
-    kc, vc = _fp8_caches(k_cache, v_cache)
-    dev = _check_cuda(q, k_new, v_new, kc, vc, k_scale, v_scale, block_tables, context_lens, out)
-    S, Hq, D, NB, Hkv, B, MAXB = _fp8_shapes(q, kc, vc, block_tables, context_lens, out)
-    _check_scales(k_scale, v_scale, Hkv)
-    if k_new.shape != (S, Hkv, D) or v_new.shape != (S, Hkv, D):
-        raise ValueError("k_new and v_new must be [S, Hkv, D]")
-    if k_new.dtype != q.dtype or v_new.dtype != q.dtype:
-        raise TypeError("k_new and v_new must share the dtype of q")
-    need = workspace_bytes(Hq, Hkv, D, "fp8", num_warps)
-    ws = get_workspace(dev, Hq // Hkv, D, num_warps, need, "fp8") if workspace is None else workspace
-    if ws.numel() * ws.element_size() < need:
-        raise ValueError(f"workspace smaller than the {need} bytes needed")
-    N.check(N.lib().pkv_decode_step_fp8(
-        q.data_ptr(), k_new.data_ptr(), v_new.data_ptr(), kc.data_ptr(), vc.data_ptr(),
-        k_scale.data_ptr(), v_scale.data_ptr(), block_tables.data_ptr(), MAXB,
-        context_lens.data_ptr(), S, Hq, Hkv, D, B, NB, float(scale), out.data_ptr(),
-        ws.data_ptr(), ws.numel() * ws.element_size(), num_warps, dtype_code(q), _stream(dev)))
-    return out
+    return _decode_step_q8("fp8", q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                           block_tables, context_lens, scale, out, workspace, num_warps)
+
+
+def paged_decode_step_int8(q: torch.Tensor, k_new: torch.Tensor, v_new: torch.Tensor,
+                           k_cache: torch.Tensor, v_cache: torch.Tensor, k_scale: torch.Tensor,
+                           v_scale: torch.Tensor, block_tables: torch.Tensor,
+                           context_lens: torch.Tensor, scale: float, out: torch.Tensor,
+                           workspace: Optional[torch.Tensor] = None,
+                           num_warps: int = 0) -> torch.Tensor:
+    """One decode step over int8 caches: quantise and write each sequence's new
+    token (position context_lens[s] - 1), then attend (two launches, programmatic
+    dependent launch)."""
+    return _decode_step_q8("int8", q, k_new, v_new, k_cache, v_cache, k_scale, v_scale,
+                           block_tables, context_lens, scale, out, workspace, num_warps)
 
 
 def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: torch.Tensor,
@@ -353,8 +409,12 @@ def paged_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
         raise ValueError("src_dst_pairs must hold pairs")
     NB = k_cache.shape[0]
     block_elems = k_cache[0].numel()
-    fp8 = k_cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None))
-    code = N.PKV_FP8_E4M3 if fp8 else dtype_code(k_cache)
+    if k_cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        code = N.PKV_FP8_E4M3
+    elif k_cache.dtype == torch.int8:
+        code = N.PKV_INT8
+    else:
+        code = dtype_code(k_cache)
     N.check(N.lib().pkv_copy_blocks(k_cache.data_ptr(), v_cache.data_ptr(),
                                     src_dst_pairs.data_ptr(), n, NB, block_elems, code,
                                     _stream(dev)))

@@ -201,6 +201,30 @@ def fill_fp8_codes_(t, scales, seed: int, stream: int, chunk_rows: int = 4096):
     return t
 
 
+def int8_scales(num_kv_heads: int, seed: int) -> np.ndarray:
+    """Per-KV-head fp32 scales for an int8 cache of N(0,1) data: a seeded value in
+    [3, 6] / 127 per head, so that 3 to 6 standard deviations reach code 127."""
+    return (rng(seed, STREAM_SCALES).uniform(3.0, 6.0, num_kv_heads) / 127.0).astype(np.float32)
+
+
+def fill_int8_codes_(t, scales, seed: int, stream: int, chunk_rows: int = 4096):
+    """Fill an int8 cache ([NB, Hkv, ...], head axis 1) with N(0,1) draws divided
+    by the head's scale, rounded by torch and clipped to +-127, chunked along
+    dim 0: synthetic input only."""
+    import torch
+    gen = torch.Generator(device=t.device)
+    gen.manual_seed(int(seed) * 1000003 + int(stream))
+    inv = (1.0 / torch.as_tensor(np.asarray(scales, dtype=np.float32), device=t.device))
+    inv = inv.view((1, -1) + (1,) * (t.dim() - 2))
+    n = t.shape[0]
+    for r0 in range(0, n, chunk_rows):
+        r1 = min(n, r0 + chunk_rows)
+        x = torch.randn((r1 - r0,) + tuple(t.shape[1:]), generator=gen, device=t.device,
+                        dtype=torch.float32)
+        t[r0:r1].copy_((x * inv).round_().clamp_(-127.0, 127.0).to(torch.int8))
+    return t
+
+
 def describe(w: Workload, lengths: Optional[np.ndarray] = None) -> dict:
     lengths = context_lengths(w) if lengths is None else lengths
     return {

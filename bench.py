@@ -679,7 +679,7 @@ def prefill_bench(args):
         "tokens_per_s": round(S * C / (ms * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
-                     "kernel": "prefill_attention_kernel (mma.sync m16n8k16)",
+                     "kernel": "prefill_tc_kernel (tcgen05 MMAs, tensor-memory accumulators)",
                      "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({kind}; dense cuBLAS)"},
         "gpu_launches": args.steps,
     }

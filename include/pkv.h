@@ -275,24 +275,29 @@ int pkv_decode_attention_static_scratch(const void* q, const void* k_cache, cons
  *   out[row, h] = softmax_j(scale * q[row, h] . K[slot(j), g]) . V[slot(j), g].
  * A whole-prompt prefill is c = t.
  *
- * q, out        device [T, num_q_heads, head_dim] (T = query_start[num_seqs]),
- *               f16 or bf16, contiguous; only the T rows are written.
+ * q, out        device [num_tokens, num_q_heads, head_dim], f16 or bf16,
+ *               contiguous; num_tokens >= query_start[num_seqs] (a chunk reaching
+ *               past num_tokens is clamped and reported); only rows of the chunks
+ *               are written.
  * block_tables, context_lens, caches: as pkv_decode_attention.
  * query_start   device int32 [num_seqs + 1], non-decreasing, query_start[0] = 0.
  * status        device int32 word or NULL: PKV_DEV_* bits are ORed into it
  *               (lengths out of range are clamped, bad block ids read as zeros,
  *               a wait that timed out abandons the launch).
  * Supported: block_size 16, head_dim 64 or 128, G in {1, 2, 4, 8},
- * num_seqs <= 2048.  Computed on the tensor cores (bf16/f16 inputs, fp32
- * accumulation and softmax); results depend only on the values and lengths.
+ * num_seqs <= 2048.  Computed on the 5th-generation tensor cores (tcgen05 MMAs
+ * with tensor-memory accumulators; bf16/f16 inputs, probabilities rounded to the
+ * input type for P.V, fp32 accumulation and softmax); results depend only on the
+ * values and lengths.
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
 int pkv_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, int32_t max_blocks_per_seq,
                           const int32_t* context_lens, const int32_t* query_start,
-                          int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
-                          int32_t head_dim, int32_t block_size, int32_t num_blocks, float scale,
-                          void* out, int32_t* status, int32_t dtype, void* stream);
+                          int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                          int32_t num_kv_heads, int32_t head_dim, int32_t block_size,
+                          int32_t num_blocks, float scale, void* out, int32_t* status,
+                          int32_t dtype, void* stream);
 
 /* ------------------------------------------------------------------------- */
 /* fp8 KV cache                                                               */

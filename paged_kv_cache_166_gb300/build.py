@@ -18,7 +18,8 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libpkv.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-SOURCES = ["api.cu", "decode_attention.cu", "prefill_attention.cu", "kv_ops.cu", "allocator.cpp"]
+SOURCES = ["api.cu", "decode_attention.cu", "prefill_attention.cu", "prefill_tcgen05.cu",
+           "kv_ops.cu", "allocator.cpp"]
 
 
 def nvcc() -> str:

@@ -98,6 +98,27 @@ int encode_cache_map(CUtensorMap* map, const void* base, int32_t dtype, int64_t 
                        CU_TENSOR_MAP_SWIZZLE_128B);
 }
 
+int encode_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType type, int elt_bytes,
+                  const int64_t dims[3], const int64_t strides[2], const int32_t box[3],
+                  CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  (void)elt_bytes;
+  const cuuint64_t d[3] = {static_cast<cuuint64_t>(dims[0]), static_cast<cuuint64_t>(dims[1]),
+                           static_cast<cuuint64_t>(dims[2])};
+  const cuuint64_t st[2] = {static_cast<cuuint64_t>(strides[0]),
+                            static_cast<cuuint64_t>(strides[1])};
+  const cuuint32_t bx[3] = {static_cast<cuuint32_t>(box[0]), static_cast<cuuint32_t>(box[1]),
+                            static_cast<cuuint32_t>(box[2])};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUresult r = fn(map, type, 3, const_cast<void*>(base), d, st, bx, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (3-D) failed (%d)", (int)r);
+  return PKV_OK;
+}
+
 }  // namespace pkv
 
 extern "C" {

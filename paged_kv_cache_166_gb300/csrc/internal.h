@@ -44,6 +44,11 @@ int encode_map_2d(CUtensorMap* map, const void* base, CUtensorMapDataType type, 
                   int64_t rows, int32_t cols, int32_t box_cols, int32_t box_rows,
                   CUtensorMapSwizzle swizzle);
 
+// A 3-D map: dims innermost first, byte strides of dims 1 and 2, box innermost first.
+int encode_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType type, int elt_bytes,
+                  const int64_t dims[3], const int64_t strides[2], const int32_t box[3],
+                  CUtensorMapSwizzle swizzle);
+
 // Launches the 8-bit quantising cache write (kv_ops.cu); codes is PKV_FP8_E4M3
 // or PKV_INT8.  With slot_mapping set, token i goes to slot_mapping[i]; with it
 // NULL, sequence i's token goes to slot(t - 1) of its block table,

@@ -9,7 +9,10 @@
 // position j <= p read through the block table:
 //   out[row, h] = softmax_j(scale * q[row, h] . K[slot(j), g]) . V[slot(j), g].
 //
-// How.  A tile is 64 rows of one (sequence, KV head): row R is query R / G and
+// Two kernels compute it.  The default runs on the 5th-generation tensor cores
+// (tcgen05, tensor memory; prefill_tcgen05.cu).  The one below, kept as the
+// measured warp-level alternative (build with PKV_PREFILL_TCGEN05=0), uses
+// mma.sync:  a tile is 64 rows of one (sequence, KV head): row R is query R / G and
 // head g*G + R % G, so the G heads of a query share every K/V tile.  A CTA has
 // four consumer warps (16 rows each: scores and P.V on the tensor cores, m16n8k16
 // with fp32 accumulation, online softmax in fp32, base 2) and one producer warp
@@ -27,30 +30,21 @@
 #include <mutex>
 
 #include "internal.h"
+#include "prefill_common.cuh"
 #include "ptx.cuh"
+
+#ifndef PKV_PREFILL_TCGEN05
+#define PKV_PREFILL_TCGEN05 1
+#endif
 
 namespace pkv {
 namespace {
 
-constexpr int kPfTok = 16;                 // tokens per cache block (kernel requirement)
 constexpr int kPfRows = 64;                // rows of a tile
 constexpr int kPfConsumers = 4;            // consumer warps (16 rows each)
 constexpr int kPfThreads = (kPfConsumers + 1) * 32;
 constexpr int kPfStages = 4;
-constexpr int kPfMaxSeqs = 2048;
 constexpr int kPfCtasPerSm = 2;
-constexpr uint64_t kPfWaitNs = 1000000000ull;  // 1 s per wait before giving up
-
-struct PrefillArgs {
-  const void* q;
-  void* out;
-  const int32_t* block_tables;
-  const int32_t* context_lens;
-  const int32_t* query_start;
-  int32_t* status;  // device status word, may be NULL
-  int32_t S, Hq, Hkv, G, MAXB, NB;
-  float scale_log2;
-};
 
 template <typename T, int D>
 struct PfShape {
@@ -82,24 +76,6 @@ __host__ __device__ inline PfSmem pf_smem(int stage_bytes, int S) {
   off += 8 * 4;
   L.total = off + 1024;  // slack to align the tiles to 1024 B
   return L;
-}
-
-__device__ __forceinline__ void pf_flag(const PrefillArgs& a, int bits) {
-  if (a.status) atomicOr(a.status, bits);
-}
-
-// Chunk length and context of sequence s, clamped to 0 <= c <= t <= MAXB * 16.
-__device__ __forceinline__ void pf_seq(const PrefillArgs& a, int s, int& t, int& c, int& q0,
-                                       bool report) {
-  t = __ldg(a.context_lens + s);
-  q0 = __ldg(a.query_start + s);
-  c = __ldg(a.query_start + s + 1) - q0;
-  const int limit = a.MAXB * kPfTok;
-  if (t < 0 || t > limit || c < 0 || c > t) {
-    if (report) pf_flag(a, PKV_DEV_BAD_CONTEXT_LEN);
-    t = t < 0 ? 0 : (t > limit ? limit : t);
-    c = c < 0 ? 0 : (c > t ? t : c);
-  }
 }
 
 __device__ __forceinline__ int pf_tiles(const PrefillArgs& a, int c) {
@@ -451,7 +427,8 @@ using namespace pkv;
 extern "C" int pkv_prefill_attention(const void* q, const void* k_cache, const void* v_cache,
                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
                                      const int32_t* context_lens, const int32_t* query_start,
-                                     int32_t num_seqs, int32_t num_q_heads, int32_t num_kv_heads,
+                                     int32_t num_seqs, int32_t num_tokens, int32_t num_q_heads,
+                                     int32_t num_kv_heads,
                                      int32_t head_dim, int32_t block_size, int32_t num_blocks,
                                      float scale, void* out, int32_t* status, int32_t dtype,
                                      void* stream) {
@@ -474,7 +451,10 @@ extern "C" int pkv_prefill_attention(const void* q, const void* k_cache, const v
               PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 64 >= 2^31");
   PKV_REQUIRE(static_cast<int64_t>(num_seqs) * max_blocks_per_seq < (int64_t(1) << 31),
               PKV_ERR_UNSUPPORTED, "num_seqs * max_blocks_per_seq >= 2^31");
-  if (num_seqs == 0) return ok();
+  PKV_REQUIRE(num_tokens >= 0, PKV_ERR_INVALID_ARG, "negative num_tokens");
+  PKV_REQUIRE(static_cast<int64_t>(num_tokens) * num_q_heads * head_dim < (int64_t(1) << 40),
+              PKV_ERR_UNSUPPORTED, "q too large");
+  if (num_seqs == 0 || num_tokens == 0) return ok();
   PKV_REQUIRE(q && k_cache && v_cache && block_tables && context_lens && query_start && out,
               PKV_ERR_INVALID_ARG, "NULL pointer");
   PKV_REQUIRE(aligned(q, 16) && aligned(k_cache, 16) && aligned(v_cache, 16) && aligned(out, 16),
@@ -487,6 +467,7 @@ extern "C" int pkv_prefill_attention(const void* q, const void* k_cache, const v
   a.query_start = query_start;
   a.status = status;
   a.S = num_seqs;
+  a.T = num_tokens;
   a.Hq = num_q_heads;
   a.Hkv = num_kv_heads;
   a.G = G;
@@ -495,7 +476,9 @@ extern "C" int pkv_prefill_attention(const void* q, const void* k_cache, const v
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc;
-  if (dtype == PKV_BF16) {
+  if (PKV_PREFILL_TCGEN05) {
+    rc = launch_prefill_tc(a, k_cache, v_cache, dtype, head_dim, st);
+  } else if (dtype == PKV_BF16) {
     rc = head_dim == 64 ? launch_prefill<__nv_bfloat16, 64>(a, k_cache, v_cache, dtype, st)
                         : launch_prefill<__nv_bfloat16, 128>(a, k_cache, v_cache, dtype, st);
   } else {

@@ -1,0 +1,634 @@
+// Paged (chunked) prefill attention on the 5th-generation tensor cores (sm_103a).
+//
+// What is computed is pkv_prefill_attention's definition ("PagedAttention: How
+// vLLM Borrowed Virtual Memory to Unlock GPU Serving at Scale", section "Walking
+// Through the Lifecycle", Prefill): query row q0 + i of sequence s sits at
+// position p = t - c + i and, for query head h of KV group g = h / G, attends to
+// every position j <= p read through the block table.
+//
+// How.  A unit is a tile of 128 rows of one (sequence, KV head) — row R is query
+// R / G, head g*G + R % G — against the keys 0 .. p_max of its last row, taken
+// in KV tiles of 128 keys (eight 16-token cache blocks).  Per KV tile j:
+//   S_j = Q K_j^T    tcgen05 MMA, M = 128 rows, N = 128 keys, K = head_dim:
+//                    Q and K_j K-major in 128-byte-swizzled shared memory,
+//                    S_j in tensor memory (two buffers);
+//   softmax          two threads per row (its tensor-memory lane), one per half
+//                    of the keys: causal mask, the row max agreed through shared
+//                    memory, running max and sum in fp32 (base 2), P_j = exp2(S_j
+//                    - m) rounded to the input type and stored K-major into
+//                    shared memory (two buffers);
+//   O_j = P_j V_j    tcgen05 MMA, N = head_dim, K = 128 keys: V_j MN-major
+//                    (rows of keys, head_dim contiguous), O_j in tensor memory
+//                    (two buffers); the row's two threads fold their halves of
+//                    it into fp32 accumulators, O = O * exp2(m_{j-1} - m_j) + O_j.
+// Warp roles (11 warps): 0 = TMA producer of the unit's query tile (a 3-D map of
+// q) and of the K blocks of each KV tile (through the block table); 10 = TMA
+// producer of the V blocks; 1 = MMA issuer (one lane) and owner of the tensor
+// memory; 2..9 = softmax and epilogue (row 32 * (warp % 4) + lane, key and
+// head_dim half (warp - 2) / 4).  K and V have rings
+// of their own: a K stage is free again once S_j is computed, a V stage once O_j
+// is, so the loads of later tiles never wait behind P.V.  Hand-offs are
+// mbarriers: TMA transaction bytes, tcgen05 commits and thread arrivals.  The MMA
+// issue order S_j, O_{j-1}, S_{j+1}, O_j, ... lets S_{j+1} run while row threads
+// process S_j.
+// One CTA per SM, persistent: the units of all sequences, in order, are cut into
+// contiguous runs of equal cost (KV tiles + 1 per unit), one per CTA.  Every
+// wait is bounded; a wait that runs out sets PKV_DEV_WAIT_TIMEOUT and the CTA
+// drains its copies and MMAs, frees its tensor memory and returns.
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+
+#include <cstdint>
+#include <mutex>
+#include <type_traits>
+
+#include "internal.h"
+#include "prefill_common.cuh"
+#include "ptx.cuh"
+
+namespace pkv {
+namespace {
+
+constexpr int kTcRows = 128;          // rows of a unit = tensor-memory lanes = MMA M
+constexpr int kTcKeys = 128;          // keys of a KV tile = N of S = K of P.V
+constexpr int kTcBlocks = kTcKeys / kPfTok;
+constexpr int kTcRowWarps = 8;        // softmax warps 2 .. 9
+constexpr int kTcWarps = 3 + kTcRowWarps;
+constexpr int kTcVWarp = 2 + kTcRowWarps;  // V producer
+constexpr int kTcHalfKeys = kTcKeys / 2;
+constexpr int kTcThreads = kTcWarps * 32;
+constexpr int kTcChunk = 128 * 128;   // one [128 rows x 128 B] swizzled column chunk
+constexpr int kTcBox = 2048;          // one 16-row box of a chunk
+
+// mbarriers (8 bytes each), then the tensor-memory base and the CTA's schedule
+enum {
+  kBarKFull = 0,     // [3] K stage landed (TMA bytes)
+  kBarKEmpty = 3,    // [3] K stage consumed (commit after S_j)
+  kBarVFull = 6,     // [3] V stage landed
+  kBarVEmpty = 9,    // [3] V stage consumed (commit after O_j)
+  kBarQFull = 12,    // query tile landed
+  kBarQEmpty = 13,   // query tile consumed (commit after the unit's last S_j)
+  kBarSFull = 14,    // [2] S_j in tensor memory (commit)
+  kBarSEmpty = 16,   // [2] S_j read by the 4 row warps
+  kBarPFull = 18,    // [2] P_j in shared memory (4 row warps)
+  kBarPvDone = 20,   // [2] O_j computed: P_j buffer free, O_j readable (commit)
+  kBarOEmpty = 22,   // [2] O_j read by the 4 row warps
+  kBarDrain = 24,    // every MMA of the CTA done (final commit)
+  kNumBars = 25
+};
+constexpr uint32_t kSlotOff = 8 * kNumBars;          // tensor-memory base address
+constexpr uint32_t kSchedOff = kSlotOff + 8;         // TcSched (8-byte aligned)
+constexpr uint32_t kDeadOff = kSchedOff + 32;        // [4] give-up bits of the row-warp pairs
+
+template <typename T, int D>
+struct TcShape {
+  static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
+  static constexpr int kChunks = D * 2 / 128;         // 128-byte column chunks of a row
+  static constexpr int kTile = kTcRows * D * 2;       // Q, K or V tile
+  static constexpr int kStages = D == 128 ? 2 : 3;    // K ring and V ring
+  static constexpr int kP = kTcRows * kTcKeys * 2;    // P tile
+  static constexpr uint32_t kQOff = 0;
+  static constexpr uint32_t kKVOff = kTile;
+  static constexpr uint32_t kPOff = kKVOff + kStages * 2 * kTile;
+  static constexpr uint32_t kBarOff = kPOff + 2 * kP;
+  static constexpr uint32_t kXchOff = kBarOff + 256;   // [2 halves][128 rows] floats
+  static constexpr uint32_t kBytes = kXchOff + 2 * kTcRows * 4 + 1024;  // + alignment slack
+  static_assert(kDeadOff + 16 <= 256, "barrier area");
+  static constexpr uint32_t kTmemCols = 512;
+  static constexpr uint32_t kSCol = 0;                // S[b]: columns 128 b ..
+  static constexpr uint32_t kOCol = 2 * kTcKeys;      // O[b]: columns 256 + D b ..
+  static constexpr uint32_t kIdQK = ptx::idesc_f16(kTcRows, kTcKeys, kBf16, false);
+  static constexpr uint32_t kIdPV = ptx::idesc_f16(kTcRows, D, kBf16, true);
+  static constexpr int kHalfD = D / 2;                // O columns of a row thread
+  static_assert(kOCol + 2 * D <= kTmemCols, "tensor memory");
+  static_assert(kChunks * 64 == D, "head_dim 64 or 128");
+};
+
+struct TcSched {
+  int32_t s, g, tile, pad;
+  long long P;   // cost before the unit (s, g, tile)
+  long long hi;  // the CTA's units are those with P < hi
+};
+
+__device__ __forceinline__ int tc_tiles(const PrefillArgs& a, int c) {
+  return (c * a.G + kTcRows - 1) / kTcRows;
+}
+
+// KV tiles a unit reads: keys 0 .. p of its last row.
+__device__ __forceinline__ int tc_kv_tiles(const PrefillArgs& a, int t, int c, int tile) {
+  const int last_row = min((tile + 1) * kTcRows, c * a.G) - 1;
+  return (t - c + last_row / a.G) / kTcKeys + 1;
+}
+
+// Cost of a sequence: every unit's KV tiles + 1, for every KV head.
+__device__ __forceinline__ long long tc_seq_cost(const PrefillArgs& a, int s, bool report) {
+  int t, c, q0;
+  pf_seq(a, s, t, c, q0, report);
+  long long cost = 0;
+  const int nt = tc_tiles(a, c);
+  for (int tile = 0; tile < nt; ++tile) cost += tc_kv_tiles(a, t, c, tile) + 1;
+  return cost * a.Hkv;
+}
+
+// Next unit after u (which has nkt KV tiles); u.s == S past the last.
+__device__ __forceinline__ void tc_advance(const PrefillArgs& a, TcSched& u, int nkt) {
+  int t, c, q0;
+  u.P += nkt + 1;
+  pf_seq(a, u.s, t, c, q0, false);
+  if (++u.tile < tc_tiles(a, c)) return;
+  u.tile = 0;
+  if (++u.g < a.Hkv) return;
+  u.g = 0;
+  for (++u.s; u.s < a.S; ++u.s) {
+    pf_seq(a, u.s, t, c, q0, false);
+    if (c > 0) break;
+  }
+}
+
+template <typename T, int D>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
+                      const __grid_constant__ CUtensorMap kmap,
+                      const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
+  using Sh = TcShape<T, D>;
+  constexpr int NS = Sh::kStages;
+  extern __shared__ uint8_t smem_raw[];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t raw = ptx::smem_addr(smem_raw);
+  const uint32_t base_s = (raw + 1023u) & ~1023u;
+  uint8_t* const base = smem_raw + (base_s - raw);
+  const uint32_t bars = base_s + Sh::kBarOff;
+  auto bar = [&](int i) { return bars + 8u * static_cast<uint32_t>(i); };
+  uint32_t* const slot = reinterpret_cast<uint32_t*>(base + Sh::kBarOff + kSlotOff);
+  TcSched* const sched = reinterpret_cast<TcSched*>(base + Sh::kBarOff + kSchedOff);
+
+  if (threadIdx.x == 0) {
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
+    for (int st = 0; st < NS; ++st) {
+      ptx::mbar_init(bar(kBarKFull + st), 1);
+      ptx::mbar_init(bar(kBarKEmpty + st), 1);
+      ptx::mbar_init(bar(kBarVFull + st), 1);
+      ptx::mbar_init(bar(kBarVEmpty + st), 1);
+    }
+    ptx::mbar_init(bar(kBarQFull), 1);
+    ptx::mbar_init(bar(kBarQEmpty), 1);
+    for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(kBarSFull + b), 1);
+      ptx::mbar_init(bar(kBarSEmpty + b), kTcRowWarps);
+      ptx::mbar_init(bar(kBarPFull + b), kTcRowWarps);
+      ptx::mbar_init(bar(kBarPvDone + b), 1);
+      ptx::mbar_init(bar(kBarOEmpty + b), kTcRowWarps);
+    }
+    ptx::mbar_init(bar(kBarDrain), 1);
+    ptx::fence_barrier_init();
+    for (int i = 0; i < 4; ++i) reinterpret_cast<int*>(base + Sh::kBarOff + kDeadOff)[i] = 0;
+  }
+  if (warp == 1) {
+    ptx::tmem_alloc(ptx::smem_addr(slot), Sh::kTmemCols);
+    ptx::tmem_relinquish();
+  }
+
+  // ---- schedule: per-sequence cost prefix (in the P area, free until the first
+  // softmax), then this CTA's first unit and cost bound --------------------------
+  {
+    long long* const cpre = reinterpret_cast<long long*>(base + Sh::kPOff);
+    long long* const wsum = cpre + a.S + 1;
+    const int nth = blockDim.x, tid = threadIdx.x;
+    const int per = (a.S + nth - 1) / nth;
+    const int b0 = min(a.S, tid * per), b1 = min(a.S, b0 + per);
+    long long local = 0;
+    for (int s = b0; s < b1; ++s) local += tc_seq_cost(a, s, blockIdx.x == 0);
+    long long x = local;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const long long y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    long long run = x - local;
+    for (int w = 0; w < warp; ++w) run += wsum[w];
+    for (int s = b0; s < b1; ++s) {
+      cpre[s] = run;
+      run += tc_seq_cost(a, s, false);
+    }
+    if (tid == nth - 1) cpre[a.S] = run;
+    __syncthreads();
+    if (tid == 0) {
+      const long long C = cpre[a.S];
+      const long long lo = C * blockIdx.x / gridDim.x;
+      TcSched u{a.S, 0, 0, 0, lo, C * (blockIdx.x + 1) / gridDim.x};
+      if (lo < C) {
+        int l = 0, h = a.S;  // largest s with cpre[s] <= lo
+        while (h - l > 1) {
+          const int mid = (l + h) >> 1;
+          if (cpre[mid] <= lo) l = mid; else h = mid;
+        }
+        int t, c, q0;
+        pf_seq(a, l, t, c, q0, false);
+        const long long cost_g = (cpre[l + 1] - cpre[l]) / a.Hkv;
+        const int g = static_cast<int>((lo - cpre[l]) / cost_g);
+        long long P = cpre[l] + g * cost_g;
+        int tile = 0;
+        const int nt = tc_tiles(a, c);
+        while (tile < nt && P < lo) P += tc_kv_tiles(a, t, c, tile++) + 1;
+        u.s = l;
+        u.g = g;
+        u.tile = tile;
+        u.P = P;
+        if (tile == nt) {  // lo fell inside the last unit of (l, g): start at the next one
+          u.tile = nt - 1;
+          u.P = P - (tc_kv_tiles(a, t, c, nt - 1) + 1);
+          tc_advance(a, u, tc_kv_tiles(a, t, c, nt - 1));
+        }
+      }
+      *sched = u;
+    }
+  }
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  const uint32_t tmem = *slot;
+  const TcSched start = *sched;
+
+  if (warp == 0 || warp == kTcVWarp) {
+    // ---- TMA producers: warp 0 the query tiles and K, warp 6 V ---------------------
+    const bool is_k = warp == 0;
+    const uint64_t policy = ptx::policy_evict_normal();  // later units of (s, g) re-read K/V
+    const int32_t rows_total = a.NB * a.Hkv * kPfTok;
+    const CUtensorMap* const map = is_k ? &kmap : &vmap;
+    const int full0 = is_k ? kBarKFull : kBarVFull, empty0 = is_k ? kBarKEmpty : kBarVEmpty;
+    const uint32_t ring = base_s + Sh::kKVOff + (is_k ? 0 : Sh::kTile);
+    uint32_t it = 0, un = 0;
+    bool alive = true;
+    TcSched u = start;
+    while (alive && u.s < a.S && u.P < start.hi) {
+      int t, c, q0;
+      pf_seq(a, u.s, t, c, q0, false);
+      const int nkt = tc_kv_tiles(a, t, c, u.tile);
+      bool ok = true;
+      if (is_k) {
+        if (lane == 0) {
+          ok = ptx::mbar_wait(bar(kBarQEmpty), (un & 1u) ^ 1u, kPfWaitNs);
+          if (ok) {
+            ptx::mbar_arrive_expect_tx(bar(kBarQFull), Sh::kTile);
+#pragma unroll
+            for (int cc = 0; cc < Sh::kChunks; ++cc)
+              ptx::tma_load_3d(base_s + Sh::kQOff + cc * kTcChunk, &qmap, cc * 64, u.g * a.G,
+                               q0 + u.tile * (kTcRows / a.G), bar(kBarQFull));
+          }
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+        ++un;
+      }
+      for (int j = 0; j < nkt; ++j, ++it) {
+        const int st = static_cast<int>(it % NS);
+        const int bi = kTcBlocks * j + (lane & 7);
+        int32_t y = rows_total;  // a box wholly past the end: zero-filled
+        if (lane < kTcBlocks && bi * kPfTok < t) {
+          const int id = __ldg(a.block_tables + static_cast<int64_t>(u.s) * a.MAXB + bi);
+          if (static_cast<uint32_t>(id) < static_cast<uint32_t>(a.NB))
+            y = (id * a.Hkv + u.g) * kPfTok;
+          else if (is_k)
+            pf_flag(a, PKV_DEV_BAD_BLOCK_ID);
+        }
+        if (lane == 0) {
+          ok = ptx::mbar_wait(bar(empty0 + st), ((it / NS) & 1u) ^ 1u, kPfWaitNs);
+          if (ok) ptx::mbar_arrive_expect_tx(bar(full0 + st), Sh::kTile);
+        }
+        if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+        __syncwarp();
+        if (lane < kTcBlocks) {
+          const uint32_t dst = ring + st * 2 * Sh::kTile + lane * kTcBox;
+#pragma unroll
+          for (int cc = 0; cc < Sh::kChunks; ++cc)
+            ptx::tma_load_2d(dst + cc * kTcChunk, map, cc * 64, y, bar(full0 + st), policy);
+        }
+      }
+      if (!alive) break;
+      tc_advance(a, u, nkt);
+    }
+    if (lane == 0) {
+      if (!alive) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
+      // let the copies in flight land before the CTA can leave
+      for (uint32_t k = it > static_cast<uint32_t>(NS) ? it - NS : 0; k < it; ++k)
+        ptx::mbar_wait(bar(full0 + k % NS), (k / NS) & 1u, kPfWaitNs / 8);
+      if (is_k && un > 0) ptx::mbar_wait(bar(kBarQFull), (un - 1) & 1u, kPfWaitNs / 8);
+    }
+  } else if (warp == 1) {
+    // ---- MMA issuer (lane 0) -----------------------------------------------------
+    uint32_t it = 0, un = 0;
+    bool alive = true;
+    auto wait1 = [&](uint32_t b, uint32_t parity) {
+      bool ok = true;
+      if (lane == 0) ok = ptx::mbar_wait(b, parity, kPfWaitNs);
+      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+    };
+    // O_x = P_x V_x for the unit's KV tile j (context t)
+    auto pv = [&](uint32_t x, int j, int t) {
+      const int b = static_cast<int>(x & 1u), st = static_cast<int>(x % NS);
+      if (!wait1(bar(kBarPFull + b), (x >> 1) & 1u)) return false;
+      if (!wait1(bar(kBarOEmpty + b), ((x >> 1) & 1u) ^ 1u)) return false;
+      if (!wait1(bar(kBarVFull + st), (x / NS) & 1u)) return false;
+      ptx::tc_fence_after();
+      const uint32_t vt = base_s + Sh::kKVOff + st * 2 * Sh::kTile + Sh::kTile;
+      // keys past the context inside its last cache block may hold anything (NaN
+      // included) and P is 0 there: zero those V rows so that 0 * V stays 0
+      const int last = (t - 1) / kPfTok;
+      if ((t % kPfTok) != 0 && last / kTcBlocks == j) {
+        const int r0 = (last % kTcBlocks) * kPfTok + t % kPfTok;
+        const int n16 = (kPfTok - t % kPfTok) * 8 * Sh::kChunks;  // 16-byte units
+        for (int i = lane; i < n16; i += 32) {
+          const int row = r0 + i / (8 * Sh::kChunks), rem = i % (8 * Sh::kChunks);
+          ptx::st_shared_v4(vt + (rem / 8) * kTcChunk + row * 128 + (rem % 8) * 16, 0u, 0u, 0u,
+                            0u);
+        }
+        ptx::fence_proxy_async_smem();
+        __syncwarp();
+      }
+      if (lane == 0) {
+        const uint32_t pb = base_s + Sh::kPOff + b * Sh::kP;
+#pragma unroll
+        for (int ks = 0; ks < kTcKeys / 16; ++ks)
+          ptx::umma_f16(tmem + Sh::kOCol + b * D,
+                        ptx::smem_desc_sw128(pb + (ks >> 2) * kTcChunk + (ks & 3) * 32, 16, 1024),
+                        ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV, ks > 0);
+        ptx::umma_commit(bar(kBarPvDone + b));
+        ptx::umma_commit(bar(kBarVEmpty + st));
+      }
+      __syncwarp();
+      return true;
+    };
+    TcSched u = start;
+    while (alive && u.s < a.S && u.P < start.hi) {
+      int t, c, q0;
+      pf_seq(a, u.s, t, c, q0, false);
+      const int nkt = tc_kv_tiles(a, t, c, u.tile);
+      if (!wait1(bar(kBarQFull), un & 1u)) { alive = false; break; }
+      ++un;
+      ptx::tc_fence_after();
+      for (int j = 0; j < nkt; ++j, ++it) {
+        const int st = static_cast<int>(it % NS), b = static_cast<int>(it & 1u);
+        if (!wait1(bar(kBarKFull + st), (it / NS) & 1u) ||
+            !wait1(bar(kBarSEmpty + b), ((it >> 1) & 1u) ^ 1u)) {
+          alive = false;
+          break;
+        }
+        ptx::tc_fence_after();
+        if (lane == 0) {
+          const uint32_t qb = base_s + Sh::kQOff;
+          const uint32_t kb = base_s + Sh::kKVOff + st * 2 * Sh::kTile;
+#pragma unroll
+          for (int ks = 0; ks < D / 16; ++ks) {
+            const uint32_t off = (ks >> 2) * kTcChunk + (ks & 3) * 32;
+            ptx::umma_f16(tmem + Sh::kSCol + b * kTcKeys, ptx::smem_desc_sw128(qb + off, 16, 1024),
+                          ptx::smem_desc_sw128(kb + off, 16, 1024), Sh::kIdQK, ks > 0);
+          }
+          ptx::umma_commit(bar(kBarSFull + b));
+          ptx::umma_commit(bar(kBarKEmpty + st));
+          if (j == nkt - 1) ptx::umma_commit(bar(kBarQEmpty));
+        }
+        __syncwarp();
+        if (j > 0 && !pv(it - 1, j - 1, t)) { alive = false; break; }
+      }
+      if (!alive || !pv(it - 1, nkt - 1, t)) { alive = false; break; }
+      tc_advance(a, u, nkt);
+    }
+    if (lane == 0) {
+      if (!alive) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
+      ptx::umma_commit(bar(kBarDrain));  // lands once every MMA issued above is done
+      ptx::mbar_wait(bar(kBarDrain), 0, kPfWaitNs);
+    }
+    __syncwarp();
+  } else if (warp >= 2 && warp < 2 + kTcRowWarps) {
+    // ---- row threads: softmax, accumulation, output --------------------------------
+    // The two warps of a lane quarter meet at every exchange (named barrier); a
+    // warp whose wait ran out skips ahead to the next exchange and flags itself
+    // there, and both leave together, so neither is left waiting at the barrier.
+    constexpr int HD = Sh::kHalfD;
+    const int q4 = warp & 3, h = (warp - 2) >> 2;
+    const int r = 32 * q4 + lane;  // tile row = tensor-memory lane
+    const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
+    // this thread's keys 64 h .. 64 h + 63 of row r: one chunk of the P tile
+    const uint32_t prow = base_s + Sh::kPOff + h * kTcChunk + r * 128;
+    const int swz = r & 7;
+    float* const xch = reinterpret_cast<float*>(base + Sh::kXchOff);
+    volatile int* const dead_bits = reinterpret_cast<volatile int*>(base + Sh::kBarOff + kDeadOff);
+    const uint32_t pair_bar = 1 + q4;
+    bool dead = false;       // this warp gave up a wait
+    bool pair_dead = false;  // either warp of the pair did
+    // the other half's value of x for this row
+    auto exchange = [&](float x) {
+      ptx::named_bar_sync(pair_bar, 64);  // the previous exchange has been read
+      if (dead && lane == 0) dead_bits[q4] = dead_bits[q4] | (1 << h);
+      xch[h * kTcRows + r] = x;
+      ptx::named_bar_sync(pair_bar, 64);
+      pair_dead = dead_bits[q4] != 0;
+      return xch[(1 - h) * kTcRows + r];
+    };
+    T* const og = reinterpret_cast<T*>(a.out);
+    uint32_t it = 0;
+    auto wait_all = [&](uint32_t b, uint32_t parity) {
+      if (dead) return;
+      dead = !__all_sync(0xffffffffu, ptx::mbar_wait(b, parity, kPfWaitNs));
+    };
+    float o[HD];
+    // O = O * al + O_x (this thread's head_dim half), then free O_x's buffer
+    auto consume = [&](uint32_t x, float al) {
+      const int b = static_cast<int>(x & 1u);
+      wait_all(bar(kBarPvDone + b), (x >> 1) & 1u);
+      if (dead) return;
+      ptx::tc_fence_after();
+#pragma unroll
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t v[32];
+        ptx::tmem_ld32(tmem + lane_off + Sh::kOCol + b * D + h * HD + c0, v);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], al, __uint_as_float(v[i]));
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty + b));
+    };
+    TcSched u = start;
+    while (!pair_dead && u.s < a.S && u.P < start.hi) {
+      int t, c, q0;
+      pf_seq(a, u.s, t, c, q0, false);
+      const int nkt = tc_kv_tiles(a, t, c, u.tile);
+      const int R = u.tile * kTcRows + r;
+      const bool valid = R < c * a.G;
+      const int p = valid ? t - c + R / a.G : t - 1;
+#pragma unroll
+      for (int i = 0; i < HD; ++i) o[i] = 0.f;
+      float m = -INFINITY, l = 0.f, al_pend = 0.f;
+      for (int j = 0; j < nkt; ++j, ++it) {
+        const int b = static_cast<int>(it & 1u);
+        wait_all(bar(kBarSFull + b), (it >> 1) & 1u);
+        uint32_t v[kTcHalfKeys];
+        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
+        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
+        const uint32_t sa = tmem + lane_off + Sh::kSCol + b * kTcKeys + h * kTcHalfKeys;
+        const int lim = p - kTcKeys * j - kTcHalfKeys * h;  // keys 0 .. lim of the half visible
+        const bool full = lim >= kTcHalfKeys - 1;
+        float mx = -INFINITY;
+        if (!dead) {
+          ptx::tc_fence_after();
+          ptx::tmem_ld32_nowait(sa, v0);
+          ptx::tmem_ld32_nowait(sa + 32, v1);
+          ptx::tmem_wait_ld();
+          if (full) {
+#pragma unroll
+            for (int i = 0; i < kTcHalfKeys; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
+          } else {
+#pragma unroll
+            for (int i = 0; i < kTcHalfKeys; ++i)
+              if (i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]));
+          }
+        }
+        mx = fmaxf(mx, exchange(mx));
+        if (pair_dead) break;
+        const float m_new = fmaxf(m, mx * a.scale_log2);
+        const float al = ptx::ex2(m - m_new);
+        // P_j's buffer is free once O_{j-2} is computed
+        wait_all(bar(kBarPvDone + b), ((it >> 1) & 1u) ^ 1u);
+        if (dead) continue;  // on to the next exchange
+        // S again (cheaper than holding it in registers across the exchange)
+        ptx::tmem_ld32_nowait(sa, v0);
+        ptx::tmem_ld32_nowait(sa + 32, v1);
+        ptx::tmem_wait_ld();
+        const uint32_t pb = prow + b * Sh::kP;
+        float s0 = 0.f, s1 = 0.f;
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {  // 16-byte units: keys 8 q .. 8 q + 7 of the half
+          float pe[8];
+#pragma unroll
+          for (int e = 0; e < 8; ++e) {
+            const int i = 8 * q + e;
+            const float x = ptx::ex2(fmaf(__uint_as_float(v[i]), a.scale_log2, -m_new));
+            pe[e] = (full || i <= lim) ? x : 0.f;
+          }
+          s0 += (pe[0] + pe[1]) + (pe[2] + pe[3]);
+          s1 += (pe[4] + pe[5]) + (pe[6] + pe[7]);
+          ptx::st_shared_v4(pb + (((q ^ swz) & 7) << 4), ptx::pack2<T>(pe[0], pe[1]),
+                            ptx::pack2<T>(pe[2], pe[3]), ptx::pack2<T>(pe[4], pe[5]),
+                            ptx::pack2<T>(pe[6], pe[7]));
+        }
+        ptx::fence_proxy_async_smem();
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) {
+          ptx::mbar_arrive(bar(kBarSEmpty + b));
+          ptx::mbar_arrive(bar(kBarPFull + b));
+        }
+        l = l * al + (s0 + s1);
+        m = m_new;
+        if (j > 0) consume(it - 1, al_pend);
+        al_pend = al;
+      }
+      if (pair_dead) break;
+      consume(it - 1, al_pend);
+      const float lt = l + exchange(l);
+      if (pair_dead) break;
+      if (valid) {
+        const float inv = 1.f / lt;
+        T* const row =
+            og + (static_cast<int64_t>(q0 + R / a.G) * a.Hq + u.g * a.G + R % a.G) * D + h * HD;
+#pragma unroll
+        for (int d = 0; d < HD; d += 8) {
+          uint4 w;
+          w.x = ptx::pack2<T>(o[d] * inv, o[d + 1] * inv);
+          w.y = ptx::pack2<T>(o[d + 2] * inv, o[d + 3] * inv);
+          w.z = ptx::pack2<T>(o[d + 4] * inv, o[d + 5] * inv);
+          w.w = ptx::pack2<T>(o[d + 6] * inv, o[d + 7] * inv);
+          *reinterpret_cast<uint4*>(row + d) = w;
+        }
+      }
+      tc_advance(a, u, nkt);
+    }
+    if (pair_dead && lane == 0) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
+  }
+
+  ptx::tc_fence_before();
+  __syncthreads();
+  ptx::tc_fence_after();
+  if (warp == 1) ptx::tmem_dealloc(tmem, Sh::kTmemCols);
+}
+
+int tc_smem_optin(int* bytes) {
+  static std::once_flag flags[64];
+  static int values[64];
+  int dev = 0;
+  PKV_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  std::call_once(flags[dev], [&] {
+    int v = 0;
+    if (cudaDeviceGetAttribute(&v, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+      v = 0;
+    values[dev] = v;
+  });
+  if (values[dev] <= 0) return fail(PKV_ERR_CUDA, "could not query shared memory of device %d", dev);
+  *bytes = values[dev];
+  return PKV_OK;
+}
+
+template <typename T, int D>
+int launch_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache, int32_t dtype,
+              cudaStream_t stream) {
+  using Sh = TcShape<T, D>;
+  static std::once_flag flags[64];
+  static int results[64];
+  int dev = 0, optin = 0;
+  PKV_CUDA(cudaGetDevice(&dev));
+  if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
+  int rc = tc_smem_optin(&optin);
+  if (rc != PKV_OK) return rc;
+  PKV_REQUIRE(static_cast<int>(Sh::kBytes) <= optin, PKV_ERR_UNSUPPORTED,
+              "prefill needs %u bytes of shared memory, the device offers %d", Sh::kBytes, optin);
+  // the schedule's cost prefix lives in the P area
+  PKV_REQUIRE(static_cast<int64_t>(a.S + 1 + kTcWarps) * 8 <= 2 * Sh::kP, PKV_ERR_UNSUPPORTED,
+              "too many sequences");
+  std::call_once(flags[dev], [&] {
+    results[dev] = cudaFuncSetAttribute(prefill_tc_kernel<T, D>,
+                                        cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kBytes);
+  });
+  if (results[dev] != cudaSuccess)
+    return cuda_fail(static_cast<cudaError_t>(results[dev]), "cudaFuncSetAttribute");
+  CUtensorMap qmap, kmap, vmap;
+  // q [T, Hq, D]: boxes of 64 head_dim elements (128 B) x G heads x 128 / G queries,
+  // landing as the 128 swizzled rows (query, head) of one column chunk
+  const CUtensorMapDataType ty =
+      dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+  const int64_t qdims[3] = {D, a.Hq, a.T};
+  const int64_t qstrides[2] = {static_cast<int64_t>(D) * 2, static_cast<int64_t>(a.Hq) * D * 2};
+  const int32_t qbox[3] = {64, a.G, kTcRows / a.G};
+  rc = encode_map_3d(&qmap, a.q, ty, 2, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
+  if (rc != PKV_OK) return rc;
+  const int64_t rows = static_cast<int64_t>(a.NB) * a.Hkv * kPfTok;
+  rc = encode_cache_map(&kmap, k_cache, dtype, rows, D, 64, kPfTok);
+  if (rc != PKV_OK) return rc;
+  rc = encode_cache_map(&vmap, v_cache, dtype, rows, D, 64, kPfTok);
+  if (rc != PKV_OK) return rc;
+  int sms = 0;
+  rc = device_sm_count(&sms, &dev);
+  if (rc != PKV_OK) return rc;
+  prefill_tc_kernel<T, D><<<sms, kTcThreads, Sh::kBytes, stream>>>(qmap, kmap, vmap, a);
+  PKV_CUDA(cudaGetLastError());
+  return PKV_OK;
+}
+
+}  // namespace
+
+int launch_prefill_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache,
+                      int32_t dtype, int32_t head_dim, cudaStream_t stream) {
+  if (dtype == PKV_BF16)
+    return head_dim == 64 ? launch_tc<__nv_bfloat16, 64>(a, k_cache, v_cache, dtype, stream)
+                          : launch_tc<__nv_bfloat16, 128>(a, k_cache, v_cache, dtype, stream);
+  return head_dim == 64 ? launch_tc<__half, 64>(a, k_cache, v_cache, dtype, stream)
+                        : launch_tc<__half, 128>(a, k_cache, v_cache, dtype, stream);
+}
+
+}  // namespace pkv

@@ -350,7 +350,7 @@ def paged_prefill_attention(q: torch.Tensor, k_cache: torch.Tensor, v_cache: tor
         st = status.data_ptr()
     N.check(N.lib().pkv_prefill_attention(
         q.data_ptr(), k_cache.data_ptr(), v_cache.data_ptr(), block_tables.data_ptr(),
-        block_tables.shape[1], context_lens.data_ptr(), query_start.data_ptr(), S, Hq, Hkv, D, B,
+        block_tables.shape[1], context_lens.data_ptr(), query_start.data_ptr(), S, T, Hq, Hkv, D, B,
         NB, float(scale), out.data_ptr(), st or None, dtype_code(q), _stream(dev)))
     return out
 

@@ -14,13 +14,18 @@
 //                    S_j in tensor memory (two buffers);
 //   softmax          two threads per row (its tensor-memory lane), one per half
 //                    of the keys: causal mask, the row max agreed through shared
-//                    memory, running max and sum in fp32 (base 2), P_j = exp2(S_j
-//                    - m) rounded to the input type and stored K-major into
-//                    shared memory (two buffers);
-//   O_j = P_j V_j    tcgen05 MMA, N = head_dim, K = 128 keys: V_j MN-major
-//                    (rows of keys, head_dim contiguous), O_j in tensor memory
-//                    (two buffers); the row's two threads fold their halves of
-//                    it into fp32 accumulators, O = O * exp2(m_{j-1} - m_j) + O_j.
+//                    memory, P_j = exp2(S_j - m) in fp32 (base 2) rounded to the
+//                    input type and stored K-major into shared memory (two
+//                    buffers), the row sum in fp32;
+//   O += P_j V_j     tcgen05 MMA, N = head_dim, K = 128 keys: V_j MN-major
+//                    (rows of keys, head_dim contiguous), O accumulating in
+//                    tensor memory over the unit's KV tiles (two buffers, one per
+//                    unit in flight).
+// The reference m of a row is its running max, moved only when the max grows by
+// more than 2^8: then the row's threads scale their halves of O (tensor memory)
+// and the sum by exp2(m_old - m_new) between two P.V products.  In between P may
+// exceed 1 (by at most 2^8), which the output's final division absorbs: the
+// result is softmax(S) V whatever the reference.
 // Warp roles (11 warps): 0 = TMA producer of the unit's query tile (a 3-D map of
 // q) and of the K blocks of each KV tile (through the block table); 10 = TMA
 // producer of the V blocks; 1 = MMA issuer (one lane) and owner of the tensor
@@ -58,6 +63,7 @@ constexpr int kTcRowWarps = 8;        // softmax warps 2 .. 9
 constexpr int kTcWarps = 3 + kTcRowWarps;
 constexpr int kTcVWarp = 2 + kTcRowWarps;  // V producer
 constexpr int kTcHalfKeys = kTcKeys / 2;
+constexpr float kTcRescale = 8.f;     // log2 of the growth of the row max that moves m
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcChunk = 128 * 128;   // one [128 rows x 128 B] swizzled column chunk
 constexpr int kTcBox = 2048;          // one 16-row box of a chunk
@@ -74,7 +80,7 @@ enum {
   kBarSEmpty = 16,   // [2] S_j read by the 4 row warps
   kBarPFull = 18,    // [2] P_j in shared memory (4 row warps)
   kBarPvDone = 20,   // [2] O_j computed: P_j buffer free, O_j readable (commit)
-  kBarOEmpty = 22,   // [2] O_j read by the 4 row warps
+  kBarOEmpty = 22,   // [2] a unit's O read by the row warps (per unit)
   kBarDrain = 24,    // every MMA of the CTA done (final commit)
   kNumBars = 25
 };
@@ -98,7 +104,7 @@ struct TcShape {
   static_assert(kDeadOff + 16 <= 256, "barrier area");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = 0;                // S[b]: columns 128 b ..
-  static constexpr uint32_t kOCol = 2 * kTcKeys;      // O[b]: columns 256 + D b ..
+  static constexpr uint32_t kOCol = 2 * kTcKeys;      // O of unit n: columns 256 + D (n % 2) ..
   static constexpr uint32_t kIdQK = ptx::idesc_f16(kTcRows, kTcKeys, kBf16, false);
   static constexpr uint32_t kIdPV = ptx::idesc_f16(kTcRows, D, kBf16, true);
   static constexpr int kHalfD = D / 2;                // O columns of a row thread
@@ -328,11 +334,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) ok = ptx::mbar_wait(b, parity, kPfWaitNs);
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    // O_x = P_x V_x for the unit's KV tile j (context t)
-    auto pv = [&](uint32_t x, int j, int t) {
+    // O (+)= P_x V_x for the unit's KV tile j (context t), O buffer ob
+    auto pv = [&](uint32_t x, int j, int t, int ob) {
       const int b = static_cast<int>(x & 1u), st = static_cast<int>(x % NS);
       if (!wait1(bar(kBarPFull + b), (x >> 1) & 1u)) return false;
-      if (!wait1(bar(kBarOEmpty + b), ((x >> 1) & 1u) ^ 1u)) return false;
       if (!wait1(bar(kBarVFull + st), (x / NS) & 1u)) return false;
       ptx::tc_fence_after();
       const uint32_t vt = base_s + Sh::kKVOff + st * 2 * Sh::kTile + Sh::kTile;
@@ -354,9 +359,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t pb = base_s + Sh::kPOff + b * Sh::kP;
 #pragma unroll
         for (int ks = 0; ks < kTcKeys / 16; ++ks)
-          ptx::umma_f16(tmem + Sh::kOCol + b * D,
+          ptx::umma_f16(tmem + Sh::kOCol + ob * D,
                         ptx::smem_desc_sw128(pb + (ks >> 2) * kTcChunk + (ks & 3) * 32, 16, 1024),
-                        ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV, ks > 0);
+                        ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV,
+                        j > 0 || ks > 0);
         ptx::umma_commit(bar(kBarPvDone + b));
         ptx::umma_commit(bar(kBarVEmpty + st));
       }
@@ -368,7 +374,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int t, c, q0;
       pf_seq(a, u.s, t, c, q0, false);
       const int nkt = tc_kv_tiles(a, t, c, u.tile);
-      if (!wait1(bar(kBarQFull), un & 1u)) { alive = false; break; }
+      const int ob = static_cast<int>(un & 1u);
+      // the unit's O buffer: free once the unit two before has been written out
+      if (!wait1(bar(kBarQFull), un & 1u) ||
+          !wait1(bar(kBarOEmpty + ob), ((un >> 1) & 1u) ^ 1u)) {
+        alive = false;
+        break;
+      }
       ++un;
       ptx::tc_fence_after();
       for (int j = 0; j < nkt; ++j, ++it) {
@@ -393,9 +405,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (j == nkt - 1) ptx::umma_commit(bar(kBarQEmpty));
         }
         __syncwarp();
-        if (j > 0 && !pv(it - 1, j - 1, t)) { alive = false; break; }
+        if (j > 0 && !pv(it - 1, j - 1, t, ob)) { alive = false; break; }
       }
-      if (!alive || !pv(it - 1, nkt - 1, t)) { alive = false; break; }
+      if (!alive || !pv(it - 1, nkt - 1, t, ob)) { alive = false; break; }
       tc_advance(a, u, nkt);
     }
     if (lane == 0) {
@@ -405,7 +417,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     }
     __syncwarp();
   } else if (warp >= 2 && warp < 2 + kTcRowWarps) {
-    // ---- row threads: softmax, accumulation, output --------------------------------
+    // ---- row threads: softmax, rescaling, output -----------------------------------
     // The two warps of a lane quarter meet at every exchange (named barrier); a
     // warp whose wait ran out skips ahead to the next exchange and flags itself
     // there, and both leave together, so neither is left waiting at the barrier.
@@ -431,28 +443,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return xch[(1 - h) * kTcRows + r];
     };
     T* const og = reinterpret_cast<T*>(a.out);
-    uint32_t it = 0;
+    uint32_t it = 0, un = 0;
     auto wait_all = [&](uint32_t b, uint32_t parity) {
       if (dead) return;
       dead = !__all_sync(0xffffffffu, ptx::mbar_wait(b, parity, kPfWaitNs));
-    };
-    float o[HD];
-    // O = O * al + O_x (this thread's head_dim half), then free O_x's buffer
-    auto consume = [&](uint32_t x, float al) {
-      const int b = static_cast<int>(x & 1u);
-      wait_all(bar(kBarPvDone + b), (x >> 1) & 1u);
-      if (dead) return;
-      ptx::tc_fence_after();
-#pragma unroll
-      for (int c0 = 0; c0 < HD; c0 += 32) {
-        uint32_t v[32];
-        ptx::tmem_ld32(tmem + lane_off + Sh::kOCol + b * D + h * HD + c0, v);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) o[c0 + i] = fmaf(o[c0 + i], al, __uint_as_float(v[i]));
-      }
-      ptx::tc_fence_before();
-      __syncwarp();
-      if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty + b));
     };
     TcSched u = start;
     while (!pair_dead && u.s < a.S && u.P < start.hi) {
@@ -462,23 +456,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int R = u.tile * kTcRows + r;
       const bool valid = R < c * a.G;
       const int p = valid ? t - c + R / a.G : t - 1;
-#pragma unroll
-      for (int i = 0; i < HD; ++i) o[i] = 0.f;
-      float m = -INFINITY, l = 0.f, al_pend = 0.f;
+      const uint32_t oa = tmem + lane_off + Sh::kOCol + (un & 1u) * D + h * HD;  // O half
+      float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nkt; ++j, ++it) {
         const int b = static_cast<int>(it & 1u);
         wait_all(bar(kBarSFull + b), (it >> 1) & 1u);
         uint32_t v[kTcHalfKeys];
-        uint32_t (&v0)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[0]);
-        uint32_t (&v1)[32] = *reinterpret_cast<uint32_t(*)[32]>(&v[32]);
-        const uint32_t sa = tmem + lane_off + Sh::kSCol + b * kTcKeys + h * kTcHalfKeys;
         const int lim = p - kTcKeys * j - kTcHalfKeys * h;  // keys 0 .. lim of the half visible
         const bool full = lim >= kTcHalfKeys - 1;
         float mx = -INFINITY;
         if (!dead) {
           ptx::tc_fence_after();
-          ptx::tmem_ld32_nowait(sa, v0);
-          ptx::tmem_ld32_nowait(sa + 32, v1);
+          const uint32_t sa = tmem + lane_off + Sh::kSCol + b * kTcKeys + h * kTcHalfKeys;
+          ptx::tmem_ld32_nowait(sa, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
+          ptx::tmem_ld32_nowait(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           ptx::tmem_wait_ld();
           if (full) {
 #pragma unroll
@@ -491,25 +482,53 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         mx = fmaxf(mx, exchange(mx));
         if (pair_dead) break;
-        const float m_new = fmaxf(m, mx * a.scale_log2);
-        const float al = ptx::ex2(m - m_new);
-        // P_j's buffer is free once O_{j-2} is computed
+        const float mt = mx * a.scale_log2;  // the row's max over this tile, log2 units
+        // P_j's buffer is free once O_{j-2}'s product is done
         wait_all(bar(kBarPvDone + b), ((it >> 1) & 1u) ^ 1u);
+        if (j == 0) {
+          m = mt;
+        } else {
+          // move the reference of the rows whose max grew by more than 2^8: O and l
+          // scaled by exp2(m - mt), once P_{j-1} V_{j-1} has landed in O.  The
+          // tensor-memory accesses are warp-wide, so the whole warp takes the branch
+          // and the other rows scale by exactly 1.
+          const bool move = mt > m + kTcRescale;
+          if (__any_sync(0xffffffffu, move)) {
+            const float al = move ? ptx::ex2(m - mt) : 1.f;
+            wait_all(bar(kBarPvDone + (b ^ 1)), ((it - 1) >> 1) & 1u);
+            if (!dead) {
+              ptx::tc_fence_after();
+#pragma unroll
+              for (int c0 = 0; c0 < HD; c0 += 32) {
+                uint32_t w[32];
+                ptx::tmem_ld32(oa + c0, w);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) w[i] = __float_as_uint(__uint_as_float(w[i]) * al);
+                ptx::tmem_st32(oa + c0, w);
+              }
+            }
+            if (move) {
+              l *= al;
+              m = mt;
+            }
+          }
+        }
         if (dead) continue;  // on to the next exchange
-        // S again (cheaper than holding it in registers across the exchange)
-        ptx::tmem_ld32_nowait(sa, v0);
-        ptx::tmem_ld32_nowait(sa + 32, v1);
-        ptx::tmem_wait_ld();
         const uint32_t pb = prow + b * Sh::kP;
         float s0 = 0.f, s1 = 0.f;
 #pragma unroll
         for (int q = 0; q < 8; ++q) {  // 16-byte units: keys 8 q .. 8 q + 7 of the half
           float pe[8];
+          if (full) {
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const int i = 8 * q + e;
-            const float x = ptx::ex2(fmaf(__uint_as_float(v[i]), a.scale_log2, -m_new));
-            pe[e] = (full || i <= lim) ? x : 0.f;
+            for (int e = 0; e < 8; ++e)
+              pe[e] = ptx::ex2(fmaf(__uint_as_float(v[8 * q + e]), a.scale_log2, -m));
+          } else {
+#pragma unroll
+            for (int e = 0; e < 8; ++e) {
+              const float x = ptx::ex2(fmaf(__uint_as_float(v[8 * q + e]), a.scale_log2, -m));
+              pe[e] = 8 * q + e <= lim ? x : 0.f;
+            }
           }
           s0 += (pe[0] + pe[1]) + (pe[2] + pe[3]);
           s1 += (pe[4] + pe[5]) + (pe[6] + pe[7]);
@@ -524,29 +543,39 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ptx::mbar_arrive(bar(kBarSEmpty + b));
           ptx::mbar_arrive(bar(kBarPFull + b));
         }
-        l = l * al + (s0 + s1);
-        m = m_new;
-        if (j > 0) consume(it - 1, al_pend);
-        al_pend = al;
+        l += s0 + s1;
       }
       if (pair_dead) break;
-      consume(it - 1, al_pend);
       const float lt = l + exchange(l);
       if (pair_dead) break;
-      if (valid) {
+      // the unit's last product done: write this half of the row, free the O buffer
+      wait_all(bar(kBarPvDone + ((it - 1) & 1u)), ((it - 1) >> 1) & 1u);
+      if (!dead) {
+        ptx::tc_fence_after();
         const float inv = 1.f / lt;
         T* const row =
             og + (static_cast<int64_t>(q0 + R / a.G) * a.Hq + u.g * a.G + R % a.G) * D + h * HD;
 #pragma unroll
-        for (int d = 0; d < HD; d += 8) {
-          uint4 w;
-          w.x = ptx::pack2<T>(o[d] * inv, o[d + 1] * inv);
-          w.y = ptx::pack2<T>(o[d + 2] * inv, o[d + 3] * inv);
-          w.z = ptx::pack2<T>(o[d + 4] * inv, o[d + 5] * inv);
-          w.w = ptx::pack2<T>(o[d + 6] * inv, o[d + 7] * inv);
-          *reinterpret_cast<uint4*>(row + d) = w;
+        for (int c0 = 0; c0 < HD; c0 += 32) {
+          uint32_t w[32];
+          ptx::tmem_ld32(oa + c0, w);
+          if (valid) {
+#pragma unroll
+            for (int d = 0; d < 32; d += 8) {
+              uint4 o4;
+              o4.x = ptx::pack2<T>(__uint_as_float(w[d]) * inv, __uint_as_float(w[d + 1]) * inv);
+              o4.y = ptx::pack2<T>(__uint_as_float(w[d + 2]) * inv, __uint_as_float(w[d + 3]) * inv);
+              o4.z = ptx::pack2<T>(__uint_as_float(w[d + 4]) * inv, __uint_as_float(w[d + 5]) * inv);
+              o4.w = ptx::pack2<T>(__uint_as_float(w[d + 6]) * inv, __uint_as_float(w[d + 7]) * inv);
+              *reinterpret_cast<uint4*>(row + c0 + d) = o4;
+            }
+          }
         }
+        ptx::tc_fence_before();
+        __syncwarp();
+        if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty + (un & 1u)));
       }
+      ++un;
       tc_advance(a, u, nkt);
     }
     if (pair_dead && lane == 0) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);

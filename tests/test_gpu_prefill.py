@@ -5,7 +5,9 @@ Covered: whole-prompt prefills of lengths 1 to several hundred, chunks of 1 to
 65 queries at the end of longer contexts, an empty chunk, every group size
 {1, 2, 4, 8}, head_dim 64 and 128, f16 and bf16; NaN in every cache slot no
 query may read (block tails past the context, unused blocks); a clean status
-word; rows outside the chunks left untouched.
+word; rows outside the chunks left untouched; keys whose magnitude grows with
+their position (scores rising along the sequence by many factors of 2^8, so
+the kernel's running reference max moves again and again).
 """
 import numpy as np
 import pytest
@@ -32,7 +34,7 @@ def pkv():
     return m
 
 
-def case(dtype, Hq, Hkv, D, lens, chunks, seed=11):
+def case(dtype, Hq, Hkv, D, lens, chunks, seed=11, ramp=False):
     B = 16
     NB = int(sum(-(-t // B) for t in lens)) + 7
     mgr = BlockManager(NB, B, W.pool_order(NB, seed))
@@ -46,6 +48,12 @@ def case(dtype, Hq, Hkv, D, lens, chunks, seed=11):
     vc = torch.empty_like(kc)
     W.fill_normal_(kc, seed, W.STREAM_K_POOL)
     W.fill_normal_(vc, seed, W.STREAM_V_POOL)
+    if ramp:  # K at position p scaled by 1 + p / 32
+        f = np.ones((NB, B), dtype=np.float32)
+        for s, t in enumerate(lens):
+            for p in range(t):
+                f[tables[s, p // B], p % B] = 1 + p / 32
+        kc.mul_(torch.from_numpy(f).cuda().view(NB, 1, B, 1).to(tdt))
     # NaN in every slot no query may read
     used = np.zeros((NB, B), dtype=bool)
     for s, t in enumerate(lens):
@@ -86,6 +94,29 @@ def test_prefill_matches_oracle(dtype, Hq, Hkv, D, lens, chunks):
     assert np.all(got[T:] == 7.0)                        # rows past the chunks untouched
     err = BT.row_errors(got[:T], ref)
     assert np.isfinite(got[:T]).all()
+    assert err.max() <= BT.tolerance(dtype), f"row error {err.max():.3e}"
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,lens,chunks", [
+    ("bf16", 16, 2, 128, (1000, 300), (1000, 77)),
+    ("f16", 8, 8, 64, (700, 129), None),
+])
+def test_prefill_rising_scores(dtype, Hq, Hkv, D, lens, chunks):
+    chunks = lens if chunks is None else chunks
+    kc, vc, q, tables, ctx, qstart = case(dtype, Hq, Hkv, D, lens, chunks, seed=13, ramp=True)
+    T = int(qstart[-1])
+    ref = opf.paged_prefill_attention(BT.np64(q[:T]), BT.np64(kc), BT.np64(vc), tables, ctx,
+                                      qstart, 1 / np.sqrt(D))
+    out = torch.full_like(q, 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(ctx).cuda(), torch.from_numpy(qstart).cuda(),
+                                  1 / np.sqrt(D), out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = BT.np64(out)
+    assert np.isfinite(got[:T]).all()
+    err = BT.row_errors(got[:T], ref)
     assert err.max() <= BT.tolerance(dtype), f"row error {err.max():.3e}"
 
 

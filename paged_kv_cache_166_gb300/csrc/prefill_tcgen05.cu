@@ -15,12 +15,15 @@
 //   softmax          two threads per row (its tensor-memory lane), one per half
 //                    of the keys: causal mask, the row max agreed through shared
 //                    memory, P_j = exp2(S_j - m) in fp32 (base 2) rounded to the
-//                    input type and stored K-major into shared memory (two
-//                    buffers), the row sum in fp32;
-//   O += P_j V_j     tcgen05 MMA, N = head_dim, K = 128 keys: V_j MN-major
-//                    (rows of keys, head_dim contiguous), O accumulating in
-//                    tensor memory over the unit's KV tiles (two buffers, one per
-//                    unit in flight).
+//                    input type and stored into tensor memory (two buffers; row
+//                    r in lane r, keys 2c and 2c + 1 packed in column c), the
+//                    row sum in fp32;
+//   O += P_j V_j     tcgen05 MMA with A = P_j read from tensor memory, N =
+//                    head_dim, K = 128 keys: V_j MN-major in shared memory (rows
+//                    of keys, head_dim contiguous), O accumulating in tensor
+//                    memory over the unit's KV tiles.
+// Keeping P out of shared memory leaves the shared-memory bandwidth to the
+// operand reads of the MMAs and the TMA writes of K and V, which bound the kernel.
 // The reference m of a row is its running max, moved only when the max grows by
 // more than 2^8: then the row's threads scale their halves of O (tensor memory)
 // and the sum by exp2(m_old - m_new) between two P.V products.  In between P may
@@ -70,45 +73,45 @@ constexpr int kTcBox = 2048;          // one 16-row box of a chunk
 
 // mbarriers (8 bytes each), then the tensor-memory base and the CTA's schedule
 enum {
-  kBarKFull = 0,     // [3] K stage landed (TMA bytes)
-  kBarKEmpty = 3,    // [3] K stage consumed (commit after S_j)
-  kBarVFull = 6,     // [3] V stage landed
-  kBarVEmpty = 9,    // [3] V stage consumed (commit after O_j)
-  kBarQFull = 12,    // query tile landed
-  kBarQEmpty = 13,   // query tile consumed (commit after the unit's last S_j)
-  kBarSFull = 14,    // [2] S_j in tensor memory (commit)
-  kBarSEmpty = 16,   // [2] S_j read by the 4 row warps
-  kBarPFull = 18,    // [2] P_j in shared memory (4 row warps)
-  kBarPvDone = 20,   // [2] O_j computed: P_j buffer free, O_j readable (commit)
-  kBarOEmpty = 22,   // [2] a unit's O read by the row warps (per unit)
-  kBarDrain = 24,    // every MMA of the CTA done (final commit)
-  kNumBars = 25
+  kBarKFull = 0,     // [4] K stage landed (TMA bytes)
+  kBarKEmpty = 4,    // [4] K stage consumed (commit after S_j)
+  kBarVFull = 8,     // [4] V stage landed
+  kBarVEmpty = 12,   // [4] V stage consumed (commit after P_j V_j)
+  kBarQFull = 16,    // query tile landed
+  kBarQEmpty = 17,   // query tile consumed (commit after the unit's last S_j)
+  kBarSFull = 18,    // [2] S_j in tensor memory (commit)
+  kBarSEmpty = 20,   // [2] S_j read by the row warps
+  kBarPFull = 22,    // [2] P_j in tensor memory (row warps)
+  kBarPvDone = 24,   // [2] P_j V_j done: P_j's buffer free (commit)
+  kBarOEmpty = 26,   // the unit's O read out by the row warps
+  kBarDrain = 27,    // every MMA of the CTA done (final commit)
+  kNumBars = 28
 };
 constexpr uint32_t kSlotOff = 8 * kNumBars;          // tensor-memory base address
 constexpr uint32_t kSchedOff = kSlotOff + 8;         // TcSched (8-byte aligned)
 constexpr uint32_t kDeadOff = kSchedOff + 32;        // [4] give-up bits of the row-warp pairs
+constexpr uint32_t kBarArea = 512;
 
 template <typename T, int D>
 struct TcShape {
   static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   static constexpr int kChunks = D * 2 / 128;         // 128-byte column chunks of a row
   static constexpr int kTile = kTcRows * D * 2;       // Q, K or V tile
-  static constexpr int kStages = D == 128 ? 2 : 3;    // K ring and V ring
-  static constexpr int kP = kTcRows * kTcKeys * 2;    // P tile
+  static constexpr int kStages = D == 128 ? 3 : 4;    // K ring and V ring
   static constexpr uint32_t kQOff = 0;
   static constexpr uint32_t kKVOff = kTile;
-  static constexpr uint32_t kPOff = kKVOff + kStages * 2 * kTile;
-  static constexpr uint32_t kBarOff = kPOff + 2 * kP;
-  static constexpr uint32_t kXchOff = kBarOff + 256;   // [2 halves][128 rows] floats
+  static constexpr uint32_t kBarOff = kKVOff + kStages * 2 * kTile;
+  static constexpr uint32_t kXchOff = kBarOff + kBarArea;  // [2 halves][128 rows] floats
   static constexpr uint32_t kBytes = kXchOff + 2 * kTcRows * 4 + 1024;  // + alignment slack
-  static_assert(kDeadOff + 16 <= 256, "barrier area");
+  static_assert(kDeadOff + 16 <= kBarArea, "barrier area");
   static constexpr uint32_t kTmemCols = 512;
   static constexpr uint32_t kSCol = 0;                // S[b]: columns 128 b ..
-  static constexpr uint32_t kOCol = 2 * kTcKeys;      // O of unit n: columns 256 + D (n % 2) ..
+  static constexpr uint32_t kOCol = 2 * kTcKeys;      // O: columns 256 .. 256 + D - 1
+  static constexpr uint32_t kPCol = 384;              // P[b]: columns 384 + 64 b .. (packed pairs)
   static constexpr uint32_t kIdQK = ptx::idesc_f16(kTcRows, kTcKeys, kBf16, false);
   static constexpr uint32_t kIdPV = ptx::idesc_f16(kTcRows, D, kBf16, true);
   static constexpr int kHalfD = D / 2;                // O columns of a row thread
-  static_assert(kOCol + 2 * D <= kTmemCols, "tensor memory");
+  static_assert(kOCol + D <= kPCol && kPCol + 2 * kTcKeys / 2 <= kTmemCols, "tensor memory");
   static_assert(kChunks * 64 == D, "head_dim 64 or 128");
 };
 
@@ -187,8 +190,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       ptx::mbar_init(bar(kBarSEmpty + b), kTcRowWarps);
       ptx::mbar_init(bar(kBarPFull + b), kTcRowWarps);
       ptx::mbar_init(bar(kBarPvDone + b), 1);
-      ptx::mbar_init(bar(kBarOEmpty + b), kTcRowWarps);
     }
+    ptx::mbar_init(bar(kBarOEmpty), kTcRowWarps);
     ptx::mbar_init(bar(kBarDrain), 1);
     ptx::fence_barrier_init();
     for (int i = 0; i < 4; ++i) reinterpret_cast<int*>(base + Sh::kBarOff + kDeadOff)[i] = 0;
@@ -201,7 +204,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- schedule: per-sequence cost prefix (in the P area, free until the first
   // softmax), then this CTA's first unit and cost bound --------------------------
   {
-    long long* const cpre = reinterpret_cast<long long*>(base + Sh::kPOff);
+    long long* const cpre = reinterpret_cast<long long*>(base + Sh::kKVOff);  // free until the first load
     long long* const wsum = cpre + a.S + 1;
     const int nth = blockDim.x, tid = threadIdx.x;
     const int per = (a.S + nth - 1) / nth;
@@ -334,9 +337,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) ok = ptx::mbar_wait(b, parity, kPfWaitNs);
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    // O (+)= P_x V_x for the unit's KV tile j (context t), O buffer ob
-    auto pv = [&](uint32_t x, int j, int t, int ob) {
+    // O (+)= P_x V_x for the unit's KV tile j (context t); before a unit's first
+    // product, O must have been read out for the unit before (n = its index)
+    auto pv = [&](uint32_t x, int j, int t, uint32_t n) {
       const int b = static_cast<int>(x & 1u), st = static_cast<int>(x % NS);
+      if (j == 0 && !wait1(bar(kBarOEmpty), (n & 1u) ^ 1u)) return false;
       if (!wait1(bar(kBarPFull + b), (x >> 1) & 1u)) return false;
       if (!wait1(bar(kBarVFull + st), (x / NS) & 1u)) return false;
       ptx::tc_fence_after();
@@ -356,13 +361,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         __syncwarp();
       }
       if (lane == 0) {
-        const uint32_t pb = base_s + Sh::kPOff + b * Sh::kP;
+        const uint32_t pt = tmem + Sh::kPCol + b * (kTcKeys / 2);
 #pragma unroll
-        for (int ks = 0; ks < kTcKeys / 16; ++ks)
-          ptx::umma_f16(tmem + Sh::kOCol + ob * D,
-                        ptx::smem_desc_sw128(pb + (ks >> 2) * kTcChunk + (ks & 3) * 32, 16, 1024),
-                        ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV,
-                        j > 0 || ks > 0);
+        for (int ks = 0; ks < kTcKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
+          ptx::umma_f16_ta(tmem + Sh::kOCol, pt + ks * 8,
+                           ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV,
+                           j > 0 || ks > 0);
         ptx::umma_commit(bar(kBarPvDone + b));
         ptx::umma_commit(bar(kBarVEmpty + st));
       }
@@ -374,14 +378,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       int t, c, q0;
       pf_seq(a, u.s, t, c, q0, false);
       const int nkt = tc_kv_tiles(a, t, c, u.tile);
-      const int ob = static_cast<int>(un & 1u);
-      // the unit's O buffer: free once the unit two before has been written out
-      if (!wait1(bar(kBarQFull), un & 1u) ||
-          !wait1(bar(kBarOEmpty + ob), ((un >> 1) & 1u) ^ 1u)) {
-        alive = false;
-        break;
-      }
-      ++un;
+      if (!wait1(bar(kBarQFull), un & 1u)) { alive = false; break; }
+      const uint32_t n = un++;
       ptx::tc_fence_after();
       for (int j = 0; j < nkt; ++j, ++it) {
         const int st = static_cast<int>(it % NS), b = static_cast<int>(it & 1u);
@@ -405,9 +403,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           if (j == nkt - 1) ptx::umma_commit(bar(kBarQEmpty));
         }
         __syncwarp();
-        if (j > 0 && !pv(it - 1, j - 1, t, ob)) { alive = false; break; }
+        if (j > 0 && !pv(it - 1, j - 1, t, n)) { alive = false; break; }
       }
-      if (!alive || !pv(it - 1, nkt - 1, t, ob)) { alive = false; break; }
+      if (!alive || !pv(it - 1, nkt - 1, t, n)) { alive = false; break; }
       tc_advance(a, u, nkt);
     }
     if (lane == 0) {
@@ -425,9 +423,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const int q4 = warp & 3, h = (warp - 2) >> 2;
     const int r = 32 * q4 + lane;  // tile row = tensor-memory lane
     const uint32_t lane_off = static_cast<uint32_t>(32 * q4) << 16;
-    // this thread's keys 64 h .. 64 h + 63 of row r: one chunk of the P tile
-    const uint32_t prow = base_s + Sh::kPOff + h * kTcChunk + r * 128;
-    const int swz = r & 7;
+    // this thread's keys 64 h .. 64 h + 63 of row r: 32 packed columns of P
+    const uint32_t pcol = tmem + lane_off + Sh::kPCol + h * (kTcHalfKeys / 2);
     float* const xch = reinterpret_cast<float*>(base + Sh::kXchOff);
     volatile int* const dead_bits = reinterpret_cast<volatile int*>(base + Sh::kBarOff + kDeadOff);
     const uint32_t pair_bar = 1 + q4;
@@ -456,7 +453,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int R = u.tile * kTcRows + r;
       const bool valid = R < c * a.G;
       const int p = valid ? t - c + R / a.G : t - 1;
-      const uint32_t oa = tmem + lane_off + Sh::kOCol + (un & 1u) * D + h * HD;  // O half
+      const uint32_t oa = tmem + lane_off + Sh::kOCol + h * HD;  // this thread's half of O
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nkt; ++j, ++it) {
         const int b = static_cast<int>(it & 1u);
@@ -514,10 +511,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
         }
         if (dead) continue;  // on to the next exchange
-        const uint32_t pb = prow + b * Sh::kP;
         float s0 = 0.f, s1 = 0.f;
+        uint32_t pk[kTcHalfKeys / 2];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // 16-byte units: keys 8 q .. 8 q + 7 of the half
+        for (int q = 0; q < 8; ++q) {  // keys 8 q .. 8 q + 7 of the half
           float pe[8];
           if (full) {
 #pragma unroll
@@ -532,11 +529,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           }
           s0 += (pe[0] + pe[1]) + (pe[2] + pe[3]);
           s1 += (pe[4] + pe[5]) + (pe[6] + pe[7]);
-          ptx::st_shared_v4(pb + (((q ^ swz) & 7) << 4), ptx::pack2<T>(pe[0], pe[1]),
-                            ptx::pack2<T>(pe[2], pe[3]), ptx::pack2<T>(pe[4], pe[5]),
-                            ptx::pack2<T>(pe[6], pe[7]));
+          pk[4 * q] = ptx::pack2<T>(pe[0], pe[1]);
+          pk[4 * q + 1] = ptx::pack2<T>(pe[2], pe[3]);
+          pk[4 * q + 2] = ptx::pack2<T>(pe[4], pe[5]);
+          pk[4 * q + 3] = ptx::pack2<T>(pe[6], pe[7]);
         }
-        ptx::fence_proxy_async_smem();
+        ptx::tmem_st32(pcol + b * (kTcKeys / 2), pk);
         ptx::tc_fence_before();
         __syncwarp();
         if (lane == 0) {
@@ -573,7 +571,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         ptx::tc_fence_before();
         __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty + (un & 1u)));
+        if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty));
       }
       ++un;
       tc_advance(a, u, nkt);
@@ -618,7 +616,8 @@ int launch_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache, in
   PKV_REQUIRE(static_cast<int>(Sh::kBytes) <= optin, PKV_ERR_UNSUPPORTED,
               "prefill needs %u bytes of shared memory, the device offers %d", Sh::kBytes, optin);
   // the schedule's cost prefix lives in the P area
-  PKV_REQUIRE(static_cast<int64_t>(a.S + 1 + kTcWarps) * 8 <= 2 * Sh::kP, PKV_ERR_UNSUPPORTED,
+  PKV_REQUIRE(static_cast<int64_t>(a.S + 1 + kTcWarps) * 8 <= Sh::kStages * 2 * Sh::kTile,
+              PKV_ERR_UNSUPPORTED,
               "too many sequences");
   std::call_once(flags[dev], [&] {
     results[dev] = cudaFuncSetAttribute(prefill_tc_kernel<T, D>,

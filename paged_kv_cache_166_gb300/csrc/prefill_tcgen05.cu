@@ -29,16 +29,17 @@
 // and the sum by exp2(m_old - m_new) between two P.V products.  In between P may
 // exceed 1 (by at most 2^8), which the output's final division absorbs: the
 // result is softmax(S) V whatever the reference.
-// Warp roles (11 warps): 0 = TMA producer of the unit's query tile (a 3-D map of
-// q) and of the K blocks of each KV tile (through the block table); 10 = TMA
-// producer of the V blocks; 1 = MMA issuer (one lane) and owner of the tensor
+// Warp roles (12 warps): 11 = TMA producer of the query tiles (a 3-D map of q; two
+// buffers, so the next unit's tile is in place before the current one ends);
+// 0 = TMA producer of the K blocks of each KV tile and 10 of the V blocks
+// (through the block table); 1 = MMA issuer (one lane) and owner of the tensor
 // memory; 2..9 = softmax and epilogue (row 32 * (warp % 4) + lane, key and
-// head_dim half (warp - 2) / 4).  K and V have rings
-// of their own: a K stage is free again once S_j is computed, a V stage once O_j
-// is, so the loads of later tiles never wait behind P.V.  Hand-offs are
+// head_dim half (warp - 2) / 4).  K and V have rings of their own: a K stage is
+// free again once S_j is computed, a V stage once P_j V_j is.  Hand-offs are
 // mbarriers: TMA transaction bytes, tcgen05 commits and thread arrivals.  The MMA
-// issue order S_j, O_{j-1}, S_{j+1}, O_j, ... lets S_{j+1} run while row threads
-// process S_j.
+// issuer runs one stream over all KV tiles of the CTA, S_{j+1} ahead of P_j V_j,
+// across unit boundaries too, so the tensor cores work on S while row threads
+// process the tile before.
 // One CTA per SM, persistent: the units of all sequences, in order, are cut into
 // contiguous runs of equal cost (KV tiles + 1 per unit), one per CTA.  Every
 // wait is bounded; a wait that runs out sets PKV_DEV_WAIT_TIMEOUT and the CTA
@@ -63,8 +64,9 @@ constexpr int kTcRows = 128;          // rows of a unit = tensor-memory lanes = 
 constexpr int kTcKeys = 128;          // keys of a KV tile = N of S = K of P.V
 constexpr int kTcBlocks = kTcKeys / kPfTok;
 constexpr int kTcRowWarps = 8;        // softmax warps 2 .. 9
-constexpr int kTcWarps = 3 + kTcRowWarps;
 constexpr int kTcVWarp = 2 + kTcRowWarps;  // V producer
+constexpr int kTcQWarp = 3 + kTcRowWarps;  // query-tile producer
+constexpr int kTcWarps = 4 + kTcRowWarps;
 constexpr int kTcHalfKeys = kTcKeys / 2;
 constexpr float kTcRescale = 8.f;     // log2 of the growth of the row max that moves m
 constexpr int kTcThreads = kTcWarps * 32;
@@ -77,15 +79,15 @@ enum {
   kBarKEmpty = 4,    // [4] K stage consumed (commit after S_j)
   kBarVFull = 8,     // [4] V stage landed
   kBarVEmpty = 12,   // [4] V stage consumed (commit after P_j V_j)
-  kBarQFull = 16,    // query tile landed
-  kBarQEmpty = 17,   // query tile consumed (commit after the unit's last S_j)
-  kBarSFull = 18,    // [2] S_j in tensor memory (commit)
-  kBarSEmpty = 20,   // [2] S_j read by the row warps
-  kBarPFull = 22,    // [2] P_j in tensor memory (row warps)
-  kBarPvDone = 24,   // [2] P_j V_j done: P_j's buffer free (commit)
-  kBarOEmpty = 26,   // the unit's O read out by the row warps
-  kBarDrain = 27,    // every MMA of the CTA done (final commit)
-  kNumBars = 28
+  kBarQFull = 16,    // [2] query tile landed
+  kBarQEmpty = 18,   // [2] query tile consumed (commit after the unit's last S_j)
+  kBarSFull = 20,    // [2] S_j in tensor memory (commit)
+  kBarSEmpty = 22,   // [2] S_j read by the row warps
+  kBarPFull = 24,    // [2] P_j in tensor memory (row warps)
+  kBarPvDone = 26,   // [2] P_j V_j done: P_j's buffer free (commit)
+  kBarOEmpty = 28,   // the unit's O read out by the row warps
+  kBarDrain = 29,    // every MMA of the CTA done (final commit)
+  kNumBars = 30
 };
 constexpr uint32_t kSlotOff = 8 * kNumBars;          // tensor-memory base address
 constexpr uint32_t kSchedOff = kSlotOff + 8;         // TcSched (8-byte aligned)
@@ -97,10 +99,12 @@ struct TcShape {
   static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   static constexpr int kChunks = D * 2 / 128;         // 128-byte column chunks of a row
   static constexpr int kTile = kTcRows * D * 2;       // Q, K or V tile
-  static constexpr int kStages = D == 128 ? 3 : 4;    // K ring and V ring
-  static constexpr uint32_t kQOff = 0;
-  static constexpr uint32_t kKVOff = kTile;
-  static constexpr uint32_t kBarOff = kKVOff + kStages * 2 * kTile;
+  static constexpr int kKStages = D == 128 ? 2 : 3;   // K ring (freed as soon as S_j is done)
+  static constexpr int kVStages = D == 128 ? 3 : 4;   // V ring
+  static constexpr uint32_t kQOff = 0;                // two query tiles
+  static constexpr uint32_t kKOff = 2 * kTile;
+  static constexpr uint32_t kVOff = kKOff + kKStages * kTile;
+  static constexpr uint32_t kBarOff = kVOff + kVStages * kTile;
   static constexpr uint32_t kXchOff = kBarOff + kBarArea;  // [2 halves][128 rows] floats
   static constexpr uint32_t kBytes = kXchOff + 2 * kTcRows * 4 + 1024;  // + alignment slack
   static_assert(kDeadOff + 16 <= kBarArea, "barrier area");
@@ -162,7 +166,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                       const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap, const PrefillArgs a) {
   using Sh = TcShape<T, D>;
-  constexpr int NS = Sh::kStages;
+  constexpr int NK = Sh::kKStages, NV = Sh::kVStages;
   extern __shared__ uint8_t smem_raw[];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -177,15 +181,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&qmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&kmap)) : "memory");
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
-    for (int st = 0; st < NS; ++st) {
+    for (int st = 0; st < 4; ++st) {
       ptx::mbar_init(bar(kBarKFull + st), 1);
       ptx::mbar_init(bar(kBarKEmpty + st), 1);
       ptx::mbar_init(bar(kBarVFull + st), 1);
       ptx::mbar_init(bar(kBarVEmpty + st), 1);
     }
-    ptx::mbar_init(bar(kBarQFull), 1);
-    ptx::mbar_init(bar(kBarQEmpty), 1);
     for (int b = 0; b < 2; ++b) {
+      ptx::mbar_init(bar(kBarQFull + b), 1);
+      ptx::mbar_init(bar(kBarQEmpty + b), 1);
       ptx::mbar_init(bar(kBarSFull + b), 1);
       ptx::mbar_init(bar(kBarSEmpty + b), kTcRowWarps);
       ptx::mbar_init(bar(kBarPFull + b), kTcRowWarps);
@@ -204,7 +208,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   // ---- schedule: per-sequence cost prefix (in the P area, free until the first
   // softmax), then this CTA's first unit and cost bound --------------------------
   {
-    long long* const cpre = reinterpret_cast<long long*>(base + Sh::kKVOff);  // free until the first load
+    long long* const cpre = reinterpret_cast<long long*>(base + Sh::kKOff);  // free until the first load
     long long* const wsum = cpre + a.S + 1;
     const int nth = blockDim.x, tid = threadIdx.x;
     const int per = (a.S + nth - 1) / nth;
@@ -264,15 +268,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *slot;
   const TcSched start = *sched;
 
-  if (warp == 0 || warp == kTcVWarp) {
-    // ---- TMA producers: warp 0 the query tiles and K, warp 6 V ---------------------
+  if (warp == kTcQWarp) {
+    // ---- TMA producer of the query tiles (two buffers, one per unit in flight) -----
+    uint32_t un = 0;
+    bool alive = true;
+    TcSched u = start;
+    while (alive && u.s < a.S && u.P < start.hi) {
+      int t, c, q0;
+      pf_seq(a, u.s, t, c, q0, false);
+      const int qb = static_cast<int>(un & 1u);
+      bool ok = true;
+      if (lane == 0) {
+        ok = ptx::mbar_wait(bar(kBarQEmpty + qb), ((un >> 1) & 1u) ^ 1u, kPfWaitNs);
+        if (ok) {
+          ptx::mbar_arrive_expect_tx(bar(kBarQFull + qb), Sh::kTile);
+#pragma unroll
+          for (int cc = 0; cc < Sh::kChunks; ++cc)
+            ptx::tma_load_3d(base_s + Sh::kQOff + qb * Sh::kTile + cc * kTcChunk, &qmap, cc * 64,
+                             u.g * a.G, q0 + u.tile * (kTcRows / a.G), bar(kBarQFull + qb));
+        }
+      }
+      if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
+      ++un;
+      tc_advance(a, u, tc_kv_tiles(a, t, c, u.tile));
+    }
+    if (lane == 0) {
+      if (!alive) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
+      for (uint32_t k = un > 2u ? un - 2u : 0u; k < un; ++k)  // copies in flight land first
+        ptx::mbar_wait(bar(kBarQFull + (k & 1u)), (k >> 1) & 1u, kPfWaitNs / 8);
+    }
+  } else if (warp == 0 || warp == kTcVWarp) {
+    // ---- TMA producers: warp 0 K, warp 10 V --------------------------------------
     const bool is_k = warp == 0;
     const uint64_t policy = ptx::policy_evict_normal();  // later units of (s, g) re-read K/V
     const int32_t rows_total = a.NB * a.Hkv * kPfTok;
     const CUtensorMap* const map = is_k ? &kmap : &vmap;
     const int full0 = is_k ? kBarKFull : kBarVFull, empty0 = is_k ? kBarKEmpty : kBarVEmpty;
-    const uint32_t ring = base_s + Sh::kKVOff + (is_k ? 0 : Sh::kTile);
-    uint32_t it = 0, un = 0;
+    const uint32_t ring = base_s + (is_k ? Sh::kKOff : Sh::kVOff);
+    const uint32_t NS = is_k ? NK : NV;
+    uint32_t it = 0;
     bool alive = true;
     TcSched u = start;
     while (alive && u.s < a.S && u.P < start.hi) {
@@ -280,22 +314,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       pf_seq(a, u.s, t, c, q0, false);
       const int nkt = tc_kv_tiles(a, t, c, u.tile);
       bool ok = true;
-      if (is_k) {
-        if (lane == 0) {
-          ok = ptx::mbar_wait(bar(kBarQEmpty), (un & 1u) ^ 1u, kPfWaitNs);
-          if (ok) {
-            ptx::mbar_arrive_expect_tx(bar(kBarQFull), Sh::kTile);
-#pragma unroll
-            for (int cc = 0; cc < Sh::kChunks; ++cc)
-              ptx::tma_load_3d(base_s + Sh::kQOff + cc * kTcChunk, &qmap, cc * 64, u.g * a.G,
-                               q0 + u.tile * (kTcRows / a.G), bar(kBarQFull));
-          }
-        }
-        if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
-        ++un;
-      }
       for (int j = 0; j < nkt; ++j, ++it) {
-        const int st = static_cast<int>(it % NS);
+        const uint32_t st = it % NS;
         const int bi = kTcBlocks * j + (lane & 7);
         int32_t y = rows_total;  // a box wholly past the end: zero-filled
         if (lane < kTcBlocks && bi * kPfTok < t) {
@@ -312,7 +332,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
         __syncwarp();
         if (lane < kTcBlocks) {
-          const uint32_t dst = ring + st * 2 * Sh::kTile + lane * kTcBox;
+          const uint32_t dst = ring + st * Sh::kTile + lane * kTcBox;
 #pragma unroll
           for (int cc = 0; cc < Sh::kChunks; ++cc)
             ptx::tma_load_2d(dst + cc * kTcChunk, map, cc * 64, y, bar(full0 + st), policy);
@@ -324,12 +344,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     if (lane == 0) {
       if (!alive) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
       // let the copies in flight land before the CTA can leave
-      for (uint32_t k = it > static_cast<uint32_t>(NS) ? it - NS : 0; k < it; ++k)
+      for (uint32_t k = it > NS ? it - NS : 0; k < it; ++k)
         ptx::mbar_wait(bar(full0 + k % NS), (k / NS) & 1u, kPfWaitNs / 8);
-      if (is_k && un > 0) ptx::mbar_wait(bar(kBarQFull), (un - 1) & 1u, kPfWaitNs / 8);
     }
   } else if (warp == 1) {
-    // ---- MMA issuer (lane 0) -----------------------------------------------------
+    // ---- MMA issuer (lane 0): one stream over the CTA's KV tiles, S of a tile
+    // issued before P.V of the one before, across unit boundaries too ------------------
     uint32_t it = 0, un = 0;
     bool alive = true;
     auto wait1 = [&](uint32_t b, uint32_t parity) {
@@ -337,15 +357,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (lane == 0) ok = ptx::mbar_wait(b, parity, kPfWaitNs);
       return __shfl_sync(0xffffffffu, ok, 0) != 0;
     };
-    // O (+)= P_x V_x for the unit's KV tile j (context t); before a unit's first
-    // product, O must have been read out for the unit before (n = its index)
+    // O (+)= P_x V_x for KV tile j (context t) of unit n; before a unit's first
+    // product, O must have been read out for the unit before
     auto pv = [&](uint32_t x, int j, int t, uint32_t n) {
-      const int b = static_cast<int>(x & 1u), st = static_cast<int>(x % NS);
+      const int b = static_cast<int>(x & 1u);
+      const uint32_t st = x % NV;
       if (j == 0 && !wait1(bar(kBarOEmpty), (n & 1u) ^ 1u)) return false;
       if (!wait1(bar(kBarPFull + b), (x >> 1) & 1u)) return false;
-      if (!wait1(bar(kBarVFull + st), (x / NS) & 1u)) return false;
+      if (!wait1(bar(kBarVFull + st), (x / NV) & 1u)) return false;
       ptx::tc_fence_after();
-      const uint32_t vt = base_s + Sh::kKVOff + st * 2 * Sh::kTile + Sh::kTile;
+      const uint32_t vt = base_s + Sh::kVOff + st * Sh::kTile;
       // keys past the context inside its last cache block may hold anything (NaN
       // included) and P is 0 there: zero those V rows so that 0 * V stays 0
       const int last = (t - 1) / kPfTok;
@@ -373,41 +394,52 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       __syncwarp();
       return true;
     };
+    bool pending = false;  // a P.V product not issued yet: tile px, index pj of unit pn
+    uint32_t px = 0, pn = 0;
+    int pj = 0, pt = 0;
     TcSched u = start;
     while (alive && u.s < a.S && u.P < start.hi) {
       int t, c, q0;
       pf_seq(a, u.s, t, c, q0, false);
       const int nkt = tc_kv_tiles(a, t, c, u.tile);
-      if (!wait1(bar(kBarQFull), un & 1u)) { alive = false; break; }
+      const int qb = static_cast<int>(un & 1u);
+      if (!wait1(bar(kBarQFull + qb), (un >> 1) & 1u)) { alive = false; break; }
       const uint32_t n = un++;
       ptx::tc_fence_after();
       for (int j = 0; j < nkt; ++j, ++it) {
-        const int st = static_cast<int>(it % NS), b = static_cast<int>(it & 1u);
-        if (!wait1(bar(kBarKFull + st), (it / NS) & 1u) ||
+        const uint32_t st = it % NK;
+        const int b = static_cast<int>(it & 1u);
+        if (!wait1(bar(kBarKFull + st), (it / NK) & 1u) ||
             !wait1(bar(kBarSEmpty + b), ((it >> 1) & 1u) ^ 1u)) {
           alive = false;
           break;
         }
         ptx::tc_fence_after();
         if (lane == 0) {
-          const uint32_t qb = base_s + Sh::kQOff;
-          const uint32_t kb = base_s + Sh::kKVOff + st * 2 * Sh::kTile;
+          const uint32_t qa = base_s + Sh::kQOff + qb * Sh::kTile;
+          const uint32_t kb = base_s + Sh::kKOff + st * Sh::kTile;
 #pragma unroll
           for (int ks = 0; ks < D / 16; ++ks) {
             const uint32_t off = (ks >> 2) * kTcChunk + (ks & 3) * 32;
-            ptx::umma_f16(tmem + Sh::kSCol + b * kTcKeys, ptx::smem_desc_sw128(qb + off, 16, 1024),
+            ptx::umma_f16(tmem + Sh::kSCol + b * kTcKeys, ptx::smem_desc_sw128(qa + off, 16, 1024),
                           ptx::smem_desc_sw128(kb + off, 16, 1024), Sh::kIdQK, ks > 0);
           }
           ptx::umma_commit(bar(kBarSFull + b));
           ptx::umma_commit(bar(kBarKEmpty + st));
-          if (j == nkt - 1) ptx::umma_commit(bar(kBarQEmpty));
+          if (j == nkt - 1) ptx::umma_commit(bar(kBarQEmpty + qb));
         }
         __syncwarp();
-        if (j > 0 && !pv(it - 1, j - 1, t, n)) { alive = false; break; }
+        if (pending && !pv(px, pj, pt, pn)) { alive = false; break; }
+        pending = true;
+        px = it;
+        pj = j;
+        pt = t;
+        pn = n;
       }
-      if (!alive || !pv(it - 1, nkt - 1, t, n)) { alive = false; break; }
+      if (!alive) break;
       tc_advance(a, u, nkt);
     }
+    if (alive && pending && !pv(px, pj, pt, pn)) alive = false;
     if (lane == 0) {
       if (!alive) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
       ptx::umma_commit(bar(kBarDrain));  // lands once every MMA issued above is done
@@ -440,10 +472,45 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return xch[(1 - h) * kTcRows + r];
     };
     T* const og = reinterpret_cast<T*>(a.out);
-    uint32_t it = 0, un = 0;
+    uint32_t it = 0;
     auto wait_all = [&](uint32_t b, uint32_t parity) {
       if (dead) return;
       dead = !__all_sync(0xffffffffu, ptx::mbar_wait(b, parity, kPfWaitNs));
+    };
+    const uint32_t oa = tmem + lane_off + Sh::kOCol + h * HD;  // this thread's half of O
+    // A unit's output is written after the first tile of the next unit (its last
+    // P.V is done by then), so that the tensor cores are not left waiting on it.
+    bool pend = false, pend_valid = false;
+    T* pend_row = nullptr;
+    float pend_l = 0.f;
+    uint32_t pend_x = 0;  // the unit's last KV tile
+    auto epilogue = [&]() {
+      pend = false;
+      const float lt = pend_l + exchange(pend_l);
+      if (pair_dead) return;
+      wait_all(bar(kBarPvDone + (pend_x & 1u)), (pend_x >> 1) & 1u);
+      if (dead) return;
+      ptx::tc_fence_after();
+      const float inv = 1.f / lt;
+#pragma unroll
+      for (int c0 = 0; c0 < HD; c0 += 32) {
+        uint32_t w[32];
+        ptx::tmem_ld32(oa + c0, w);
+        if (pend_valid) {
+#pragma unroll
+          for (int d = 0; d < 32; d += 8) {
+            uint4 o4;
+            o4.x = ptx::pack2<T>(__uint_as_float(w[d]) * inv, __uint_as_float(w[d + 1]) * inv);
+            o4.y = ptx::pack2<T>(__uint_as_float(w[d + 2]) * inv, __uint_as_float(w[d + 3]) * inv);
+            o4.z = ptx::pack2<T>(__uint_as_float(w[d + 4]) * inv, __uint_as_float(w[d + 5]) * inv);
+            o4.w = ptx::pack2<T>(__uint_as_float(w[d + 6]) * inv, __uint_as_float(w[d + 7]) * inv);
+            *reinterpret_cast<uint4*>(pend_row + c0 + d) = o4;
+          }
+        }
+      }
+      ptx::tc_fence_before();
+      __syncwarp();
+      if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty));
     };
     TcSched u = start;
     while (!pair_dead && u.s < a.S && u.P < start.hi) {
@@ -453,7 +520,6 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int R = u.tile * kTcRows + r;
       const bool valid = R < c * a.G;
       const int p = valid ? t - c + R / a.G : t - 1;
-      const uint32_t oa = tmem + lane_off + Sh::kOCol + h * HD;  // this thread's half of O
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nkt; ++j, ++it) {
         const int b = static_cast<int>(it & 1u);
@@ -542,40 +608,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ptx::mbar_arrive(bar(kBarPFull + b));
         }
         l += s0 + s1;
-      }
-      if (pair_dead) break;
-      const float lt = l + exchange(l);
-      if (pair_dead) break;
-      // the unit's last product done: write this half of the row, free the O buffer
-      wait_all(bar(kBarPvDone + ((it - 1) & 1u)), ((it - 1) >> 1) & 1u);
-      if (!dead) {
-        ptx::tc_fence_after();
-        const float inv = 1.f / lt;
-        T* const row =
-            og + (static_cast<int64_t>(q0 + R / a.G) * a.Hq + u.g * a.G + R % a.G) * D + h * HD;
-#pragma unroll
-        for (int c0 = 0; c0 < HD; c0 += 32) {
-          uint32_t w[32];
-          ptx::tmem_ld32(oa + c0, w);
-          if (valid) {
-#pragma unroll
-            for (int d = 0; d < 32; d += 8) {
-              uint4 o4;
-              o4.x = ptx::pack2<T>(__uint_as_float(w[d]) * inv, __uint_as_float(w[d + 1]) * inv);
-              o4.y = ptx::pack2<T>(__uint_as_float(w[d + 2]) * inv, __uint_as_float(w[d + 3]) * inv);
-              o4.z = ptx::pack2<T>(__uint_as_float(w[d + 4]) * inv, __uint_as_float(w[d + 5]) * inv);
-              o4.w = ptx::pack2<T>(__uint_as_float(w[d + 6]) * inv, __uint_as_float(w[d + 7]) * inv);
-              *reinterpret_cast<uint4*>(row + c0 + d) = o4;
-            }
-          }
+        if (j == 0 && pend) {  // the previous unit's output
+          epilogue();
+          if (pair_dead) break;
         }
-        ptx::tc_fence_before();
-        __syncwarp();
-        if (lane == 0) ptx::mbar_arrive(bar(kBarOEmpty));
       }
-      ++un;
+      if (pair_dead) break;
+      pend = true;
+      pend_valid = valid;
+      pend_row = og + (static_cast<int64_t>(q0 + R / a.G) * a.Hq + u.g * a.G + R % a.G) * D + h * HD;
+      pend_l = l;
+      pend_x = it - 1;
       tc_advance(a, u, nkt);
     }
+    if (pend && !pair_dead) epilogue();
     if (pair_dead && lane == 0) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
   }
 
@@ -616,7 +662,7 @@ int launch_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache, in
   PKV_REQUIRE(static_cast<int>(Sh::kBytes) <= optin, PKV_ERR_UNSUPPORTED,
               "prefill needs %u bytes of shared memory, the device offers %d", Sh::kBytes, optin);
   // the schedule's cost prefix lives in the P area
-  PKV_REQUIRE(static_cast<int64_t>(a.S + 1 + kTcWarps) * 8 <= Sh::kStages * 2 * Sh::kTile,
+  PKV_REQUIRE(static_cast<int64_t>(a.S + 1 + kTcWarps) * 8 <= Sh::kKStages * Sh::kTile,
               PKV_ERR_UNSUPPORTED,
               "too many sequences");
   std::call_once(flags[dev], [&] {

@@ -32,9 +32,9 @@
 // Warp roles (12 warps): 11 = TMA producer of the query tiles (a 3-D map of q; two
 // buffers, so the next unit's tile is in place before the current one ends);
 // 0 = TMA producer of the K blocks of each KV tile and 10 of the V blocks
-// (through the block table); 1 = MMA issuer (one lane) and owner of the tensor
-// memory; 2..9 = softmax and epilogue (row 32 * (warp % 4) + lane, key and
-// head_dim half (warp - 2) / 4).  K and V have rings of their own: a K stage is
+// (through the block table); 1 = MMA issuer (the whole warp, one elected lane
+// issuing) and owner of the tensor memory; 2..9 = softmax and epilogue (row
+// 32 * (warp % 4) + lane, key and head_dim half (warp - 2) / 4).  K and V have rings of their own: a K stage is
 // free again once S_j is computed, a V stage once P_j V_j is.  Hand-offs are
 // mbarriers: TMA transaction bytes, tcgen05 commits and thread arrivals.  The MMA
 // issuer runs one stream over all KV tiles of the CTA, S_{j+1} ahead of P_j V_j,
@@ -381,16 +381,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         ptx::fence_proxy_async_smem();
         __syncwarp();
       }
-      if (lane == 0) {
-        const uint32_t pt = tmem + Sh::kPCol + b * (kTcKeys / 2);
+      // the whole warp issues (one elected lane), so the operands stay uniform
+      const uint32_t pt = tmem + Sh::kPCol + b * (kTcKeys / 2);
 #pragma unroll
-        for (int ks = 0; ks < kTcKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
-          ptx::umma_f16_ta(tmem + Sh::kOCol, pt + ks * 8,
-                           ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV,
-                           j > 0 || ks > 0);
-        ptx::umma_commit(bar(kBarPvDone + b));
-        ptx::umma_commit(bar(kBarVEmpty + st));
-      }
+      for (int ks = 0; ks < kTcKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
+        ptx::umma_f16_ta_elect(tmem + Sh::kOCol, pt + ks * 8,
+                               ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV,
+                               j > 0 || ks > 0);
+      ptx::umma_commit_elect(bar(kBarPvDone + b));
+      ptx::umma_commit_elect(bar(kBarVEmpty + st));
       __syncwarp();
       return true;
     };
@@ -415,19 +414,17 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           break;
         }
         ptx::tc_fence_after();
-        if (lane == 0) {
-          const uint32_t qa = base_s + Sh::kQOff + qb * Sh::kTile;
-          const uint32_t kb = base_s + Sh::kKOff + st * Sh::kTile;
+        const uint32_t qa = base_s + Sh::kQOff + qb * Sh::kTile;
+        const uint32_t kb = base_s + Sh::kKOff + st * Sh::kTile;
 #pragma unroll
-          for (int ks = 0; ks < D / 16; ++ks) {
-            const uint32_t off = (ks >> 2) * kTcChunk + (ks & 3) * 32;
-            ptx::umma_f16(tmem + Sh::kSCol + b * kTcKeys, ptx::smem_desc_sw128(qa + off, 16, 1024),
-                          ptx::smem_desc_sw128(kb + off, 16, 1024), Sh::kIdQK, ks > 0);
-          }
-          ptx::umma_commit(bar(kBarSFull + b));
-          ptx::umma_commit(bar(kBarKEmpty + st));
-          if (j == nkt - 1) ptx::umma_commit(bar(kBarQEmpty + qb));
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off = (ks >> 2) * kTcChunk + (ks & 3) * 32;
+          ptx::umma_f16_elect(tmem + Sh::kSCol + b * kTcKeys, ptx::smem_desc_sw128(qa + off, 16, 1024),
+                              ptx::smem_desc_sw128(kb + off, 16, 1024), Sh::kIdQK, ks > 0);
         }
+        ptx::umma_commit_elect(bar(kBarSFull + b));
+        ptx::umma_commit_elect(bar(kBarKEmpty + st));
+        if (j == nkt - 1) ptx::umma_commit_elect(bar(kBarQEmpty + qb));
         __syncwarp();
         if (pending && !pv(px, pj, pt, pn)) { alive = false; break; }
         pending = true;

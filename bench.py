@@ -92,17 +92,20 @@ def whole_job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
     return bytes_per_rank * world / (ms * 1e-3) / 1e9
 
 
-def profile_traffic(kernel_tag: str):
+def profile_traffic(kernel_tag: str, source: str = "decode_attention.cu", workload_key=None):
     """Per-launch DRAM bytes from the committed ncu summary of this kernel, if the
-    kernel source is unchanged since it was captured."""
+    kernel source is unchanged since it was captured (and, when given, the summary
+    was taken on the same workload)."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
-    src = os.path.join(ROOT, "paged_kv_cache_166_gb300", "csrc", "decode_attention.cu")
+    src = os.path.join(ROOT, "paged_kv_cache_166_gb300", "csrc", source)
     try:
         text = open(path).read()
         sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
         fields = dict(l.strip("- ").split(": ", 1) for l in text.splitlines()
                       if l.startswith("- ") and ": " in l)
         if fields.get("source_sha") != sha:
+            return None
+        if workload_key is not None and fields.get("workload_key") != workload_key:
             return None
         return int(fields["traffic_bytes_per_launch"])
     except Exception:
@@ -678,7 +681,9 @@ def prefill_bench(args):
                    "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)"},
         "tokens_per_s": round(S * C / (ms * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
-                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4), "traffic": None,
+                     "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
+                     "traffic": profile_traffic(f"prefill_attention_{w.name}", "prefill_tcgen05.cu",
+                                                f"{w.name} {S}x{P} chunk {C}"),
                      "kernel": "prefill_tc_kernel (tcgen05 MMAs, tensor-memory accumulators)",
                      "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({kind}; dense cuBLAS)"},
         "gpu_launches": args.steps,

@@ -272,6 +272,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // ---- TMA producer of the query tiles (two buffers, one per unit in flight) -----
     uint32_t un = 0;
     bool alive = true;
+    const uint64_t qpolicy = ptx::policy_evict_first();  // each query tile is read once
     TcSched u = start;
     while (alive && u.s < a.S && u.P < start.hi) {
       int t, c, q0;
@@ -285,7 +286,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < Sh::kChunks; ++cc)
             ptx::tma_load_3d(base_s + Sh::kQOff + qb * Sh::kTile + cc * kTcChunk, &qmap, cc * 64,
-                             u.g * a.G, q0 + u.tile * (kTcRows / a.G), bar(kBarQFull + qb));
+                             u.g * a.G, q0 + u.tile * (kTcRows / a.G), bar(kBarQFull + qb), qpolicy);
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
@@ -300,7 +301,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   } else if (warp == 0 || warp == kTcVWarp) {
     // ---- TMA producers: warp 0 K, warp 10 V --------------------------------------
     const bool is_k = warp == 0;
-    const uint64_t policy = ptx::policy_evict_normal();  // later units of (s, g) re-read K/V
+    // later units of (s, g) read K/V again: keep them in L2 ahead of the q and out streams
+    const uint64_t policy = ptx::policy_evict_last();
     const int32_t rows_total = a.NB * a.Hkv * kPfTok;
     const CUtensorMap* const map = is_k ? &kmap : &vmap;
     const int full0 = is_k ? kBarKFull : kBarVFull, empty0 = is_k ? kBarKEmpty : kBarVEmpty;
@@ -469,6 +471,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       return xch[(1 - h) * kTcRows + r];
     };
     T* const og = reinterpret_cast<T*>(a.out);
+    const uint64_t opolicy = ptx::policy_evict_first();  // the output is not read here
     uint32_t it = 0;
     auto wait_all = [&](uint32_t b, uint32_t parity) {
       if (dead) return;
@@ -501,7 +504,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             o4.y = ptx::pack2<T>(__uint_as_float(w[d + 2]) * inv, __uint_as_float(w[d + 3]) * inv);
             o4.z = ptx::pack2<T>(__uint_as_float(w[d + 4]) * inv, __uint_as_float(w[d + 5]) * inv);
             o4.w = ptx::pack2<T>(__uint_as_float(w[d + 6]) * inv, __uint_as_float(w[d + 7]) * inv);
-            *reinterpret_cast<uint4*>(pend_row + c0 + d) = o4;
+            ptx::st_global_v4_hint(pend_row + c0 + d, o4, opolicy);
           }
         }
       }

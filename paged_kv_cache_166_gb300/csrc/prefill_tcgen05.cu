@@ -354,10 +354,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // issued before P.V of the one before, across unit boundaries too ------------------
     uint32_t it = 0, un = 0;
     bool alive = true;
+    // every lane polls (the warp stays converged for the elected MMA issue); the
+    // vote keeps a time-out seen by one lane a time-out for all
     auto wait1 = [&](uint32_t b, uint32_t parity) {
-      bool ok = true;
-      if (lane == 0) ok = ptx::mbar_wait(b, parity, kPfWaitNs);
-      return __shfl_sync(0xffffffffu, ok, 0) != 0;
+      return __all_sync(0xffffffffu, ptx::mbar_wait(b, parity, kPfWaitNs)) != 0;
     };
     // O (+)= P_x V_x for KV tile j (context t) of unit n; before a unit's first
     // product, O must have been read out for the unit before

@@ -7,7 +7,8 @@ Covered: whole-prompt prefills of lengths 1 to several hundred, chunks of 1 to
 query may read (block tails past the context, unused blocks); a clean status
 word; rows outside the chunks left untouched; keys whose magnitude grows with
 their position (scores rising along the sequence by many factors of 2^8, so
-the kernel's running reference max moves again and again).
+the kernel's running reference max moves again and again); and the bench's own
+workload at full size (16 prompts of 2048 tokens, 70B shape) on sampled rows.
 """
 import numpy as np
 import pytest
@@ -138,3 +139,44 @@ def test_prefill_last_query_agrees_with_decode_kernel():
     ref = BT.np64(dec)
     err = BT.row_errors(BT.np64(out[last]), ref)
     assert err.max() <= 2 * BT.tolerance(dtype)
+
+
+def test_prefill_bench_size_sampled_rows():
+    """The bench's own prefill (70B shape: 16 prompts of 2048 tokens, 64 q / 8 KV heads,
+    bf16, whole prompts, one launch over all of them) checked on sampled query rows:
+    prefill row p of a prompt equals decode attention at context p + 1, which the
+    fp64 oracle computes row by row."""
+    from oracle import paged_attention as opa
+    from paged_kv_cache_166_gb300 import BlockAllocator
+    w = W.WORKLOADS["gqa70b"]
+    S, P, B, Hq, Hkv, D = 16, 2048, w.block_size, w.num_q_heads, w.num_kv_heads, w.head_dim
+    NB = S * (P // B) + 1
+    alloc = BlockAllocator(NB, B, W.pool_order(NB, w.seed))
+    sids = [alloc.create() for _ in range(S)]
+    for s_ in sids:
+        alloc.append(s_, P)
+    tables, ctx = alloc.export_tables(sids, P // B)
+    kc = torch.empty((NB, Hkv, B, D), dtype=torch.bfloat16, device="cuda")
+    vc = torch.empty_like(kc)
+    W.fill_normal_(kc, w.seed, W.STREAM_K_POOL)
+    W.fill_normal_(vc, w.seed, W.STREAM_V_POOL)
+    q = W.normal_tensor((S * P, Hq, D), "bf16", w.seed, W.STREAM_Q, "cuda")
+    out = torch.empty_like(q)
+    qstart = torch.arange(0, S * P + 1, P, dtype=torch.int32, device="cuda")
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(ctx).cuda(), qstart, w.scale, out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    rng = np.random.default_rng(5)
+    picks = [(0, 0), (0, 1), (1, 15), (2, 16), (3, 127), (4, 128), (5, 255), (6, 256),
+             (15, 2047), (14, 2046)] + [(int(s), int(i)) for s, i in
+                                        zip(rng.integers(0, S, 22), rng.integers(0, P, 22))]
+    for s, i in picks:
+        nb = -(-(i + 1) // B)
+        idx = torch.from_numpy(tables[s, :nb].astype(np.int64)).cuda()
+        kc_s, vc_s = BT.np64(kc.index_select(0, idx)), BT.np64(vc.index_select(0, idx))
+        ref = opa.paged_attention(BT.np64(q[s * P + i])[None], kc_s, vc_s,
+                                  np.arange(nb, dtype=np.int32)[None], np.array([i + 1]), w.scale)
+        err = BT.row_errors(BT.np64(out[s * P + i])[None], ref)
+        assert err.max() <= BT.tolerance("bf16"), f"sequence {s} query {i}: row error {err.max():.3e}"

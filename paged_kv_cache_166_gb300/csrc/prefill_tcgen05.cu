@@ -145,21 +145,6 @@ __device__ __forceinline__ long long tc_seq_cost(const PrefillArgs& a, int s, bo
   return cost * a.Hkv;
 }
 
-// 2^x on the FMA pipe, for x <= 9 (the exponents of P): x rounded to an integer
-// n by the 1.5 * 2^23 addition trick, 2^(x - n) for x - n in [-1/2, 1/2] from a
-// degree-3 polynomial (coefficients fitted to 2^f by weighted least squares;
-// relative error below 7.6e-5, under the rounding of P to 16 bits), and 2^n added
-// to the exponent field.  x is clamped at -125 so the result stays a normal
-// number (2^-125 is far below anything P's rounding keeps).  Part of each row's
-// exponentials are taken here so that the ex2 unit is not the row threads' limit.
-__device__ __forceinline__ float exp2_fma(float x) {
-  x = fmaxf(x, -125.f);
-  const float t = x + 12582912.f;
-  const float f = x - (t - 12582912.f);
-  const float p = fmaf(fmaf(fmaf(0.0551708f, f, 0.24260983f), f, 0.69326103f), f, 0.99992818f);
-  return __int_as_float(__float_as_int(p) + ((__float_as_int(t) - 0x4B400000) << 23));
-}
-
 // Next unit after u (which has nkt KV tiles); u.s == S past the last.
 __device__ __forceinline__ void tc_advance(const PrefillArgs& a, TcSched& u, int nkt) {
   int t, c, q0;
@@ -597,12 +582,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
         for (int q = 0; q < 8; ++q) {  // keys 8 q .. 8 q + 7 of the half
           float pe[8];
-          // keys 8 q + 3 and 8 q + 7 on the FMA pipe, the others on the ex2 unit
+          // exponents rounded to f16 pairs, two 2^x per ex2 instruction
 #pragma unroll
-          for (int e = 0; e < 8; ++e) {
-            const float y = fmaf(__uint_as_float(v[8 * q + e]), a.scale_log2, -m);
-            const float x = (e & 3) == 3 ? exp2_fma(y) : ptx::ex2(y);
-            pe[e] = (full || 8 * q + e <= lim) ? x : 0.f;
+          for (int e = 0; e < 8; e += 2) {
+            const float y0 = fmaf(__uint_as_float(v[8 * q + e]), a.scale_log2, -m);
+            const float y1 = fmaf(__uint_as_float(v[8 * q + e + 1]), a.scale_log2, -m);
+            float x0, x1;
+            ptx::f32_of_f16x2(ptx::ex2_f16x2(ptx::f16x2_of(y0, y1)), x0, x1);
+            pe[e] = (full || 8 * q + e <= lim) ? x0 : 0.f;
+            pe[e + 1] = (full || 8 * q + e + 1 <= lim) ? x1 : 0.f;
           }
           s0 += (pe[0] + pe[1]) + (pe[2] + pe[3]);
           s1 += (pe[4] + pe[5]) + (pe[6] + pe[7]);

@@ -14,10 +14,11 @@
 //                    S_j in tensor memory (two buffers);
 //   softmax          two threads per row (its tensor-memory lane), one per half
 //                    of the keys: causal mask, the row max agreed through shared
-//                    memory, P_j = exp2(S_j - m) in fp32 (base 2) rounded to the
-//                    input type and stored into tensor memory (two buffers; row
-//                    r in lane r, keys 2c and 2c + 1 packed in column c), the
-//                    row sum in fp32;
+//                    memory, P_j = exp2(S_j - m) (base 2; the exponents of a
+//                    key pair rounded to f16 and raised by one f16x2 ex2)
+//                    rounded to the input type and stored into tensor memory
+//                    (two buffers; row r in lane r, keys 2c and 2c + 1 packed in
+//                    column c), the row sum in fp32;
 //   O += P_j V_j     tcgen05 MMA with A = P_j read from tensor memory, N =
 //                    head_dim, K = 128 keys: V_j MN-major in shared memory (rows
 //                    of keys, head_dim contiguous), O accumulating in tensor

@@ -180,3 +180,36 @@ def test_prefill_bench_size_sampled_rows():
                                   np.arange(nb, dtype=np.int32)[None], np.array([i + 1]), w.scale)
         err = BT.row_errors(BT.np64(out[s * P + i])[None], ref)
         assert err.max() <= BT.tolerance("bf16"), f"sequence {s} query {i}: row error {err.max():.3e}"
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_prefill_random_shapes(seed):
+    """Seeded random configurations: group size, head_dim, dtype, number of
+    sequences, prompt lengths and chunk lengths (whole prompts, empty chunks and
+    chunks of any length) all drawn; every output row against the fp64 oracle."""
+    rng = np.random.default_rng(1000 + seed)
+    dtype = ["f16", "bf16"][int(rng.integers(0, 2))]
+    D = [64, 128][int(rng.integers(0, 2))]
+    G = [1, 2, 4, 8][int(rng.integers(0, 4))]
+    Hkv = int(rng.integers(1, 3))
+    S = int(rng.integers(1, 6))
+    lens = tuple(int(x) for x in rng.integers(1, 400, S))
+    chunks = tuple(t if rng.random() < 0.4 else int(rng.integers(0, t + 1)) for t in lens)
+    kc, vc, q, tables, ctx, qstart = case(dtype, G * Hkv, Hkv, D, lens, chunks, seed=20 + seed)
+    T = int(qstart[-1])
+    out = torch.full_like(q, 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(ctx).cuda(), torch.from_numpy(qstart).cuda(),
+                                  1 / np.sqrt(D), out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = BT.np64(out)
+    assert np.all(got[T:] == 7.0)
+    if T == 0:
+        return
+    ref = opf.paged_prefill_attention(BT.np64(q[:T]), BT.np64(kc), BT.np64(vc), tables, ctx,
+                                      qstart, 1 / np.sqrt(D))
+    err = BT.row_errors(got[:T], ref)
+    assert np.isfinite(got[:T]).all()
+    assert err.max() <= BT.tolerance(dtype), f"row error {err.max():.3e} ({dtype}, D {D}, G {G})"

@@ -49,6 +49,23 @@ FALLBACK_HBM_GBS = 6800.0
 FLUSH_BYTES = 512 << 20  # > 129 MB L2
 
 
+class L2Flush:
+    """Between timed steps: writes a buffer larger than L2, then reads another as
+    large, so that the next launch finds neither its inputs in L2 nor dirty lines of
+    the flush buffer that it would have to write back to DRAM on its own clock."""
+
+    LABEL = f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, then {FLUSH_BYTES >> 20} MiB read, untimed)"
+
+    def __init__(self, device):
+        import torch
+        self.w = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+        self.r = torch.ones(FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    def __call__(self):
+        self.w.zero_()
+        self.r.max()
+
+
 def attention_bytes(lens, Hq, Hkv, D, elt, B=16, q_elt=None) -> int:
     """Algorithmic bytes decode attention must move: K and V rows of the cached
     tokens (no padded block tails, `elt` bytes per element), the int32 table
@@ -351,7 +368,7 @@ def native(args):
     ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, q8 or dev["q"].dtype,
                                          args.num_warps),
                      dtype=torch.uint8, device=device)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     stream = torch.cuda.current_stream(device)
     attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B, q_elt)
 
@@ -378,7 +395,7 @@ def native(args):
 
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         step()
     torch.cuda.synchronize()
     if pkv.decode_status(ws) != 0:
@@ -395,13 +412,13 @@ def native(args):
         t_end = time.perf_counter() + args.soak_s
         while time.perf_counter() < t_end:
             for _ in range(20):
-                flush.zero_()
+                flush()
                 step()
             torch.cuda.synchronize()
         torch.cuda.synchronize()
         t_wall = time.perf_counter()
         for i in range(args.steps):
-            flush.zero_()              # L2 flush, outside the timed events
+            flush()              # L2 flush, outside the timed events
             starts[i].record(stream)
             step()
             ends[i].record(stream)
@@ -418,7 +435,7 @@ def native(args):
     def kernel_ms(fn):
         ts = []
         for i in range(args.warmup + args.steps):
-            flush.zero_()
+            flush()
             e0.record(stream)
             fn()
             e1.record(stream)
@@ -452,12 +469,12 @@ def native(args):
         out_h.copy_(out, non_blocking=True)
 
     for _ in range(args.warmup):
-        flush.zero_()
+        flush()
         e2e_step()
     torch.cuda.synchronize()
     e2e_ms = []
     for _ in range(args.steps):
-        flush.zero_()
+        flush()
         e0.record(stream)
         e2e_step()
         e1.record(stream)
@@ -503,7 +520,7 @@ def native(args):
                      "attention (2 launches, PDL-chained)") if q8 else
                     "paged_decode_step: cache write of 1 new token/seq + decode attention (2 launches, PDL-chained)",
             "kv_cache": {"fp8": "fp8 e4m3", "int8": "int8"}.get(q8, w.dtype),
-            "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)",
+            "l2": L2Flush.LABEL,
             "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
@@ -654,10 +671,10 @@ def prefill_bench(args):
     flops = 4.0 * D * Hq * pairs
     stream = torch.cuda.current_stream(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-    flush = torch.empty(FLUSH_BYTES, dtype=torch.uint8, device=device)
+    flush = L2Flush(device)
     ts = []
     for i in range(args.warmup + args.steps):
-        flush.zero_()
+        flush()
         e0.record(stream)
         pkv.paged_prefill_attention(q, kc, vc, tab_d, ctx_d, qstart, w.scale, out)
         e1.record(stream)
@@ -678,7 +695,7 @@ def prefill_bench(args):
         "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
         "config": {"workload": f"{w.name} shape: {S} sequences x {P}-token context, chunk of {C} "
                                f"queries each, {Hq} q / {Hkv} kv heads, head_dim {D}, {dt}",
-                   "l2": f"flushed between steps ({FLUSH_BYTES >> 20} MiB write, untimed)"},
+                   "l2": L2Flush.LABEL},
         "tokens_per_s": round(S * C / (ms * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4),

@@ -198,6 +198,26 @@ class ClockSampler:
 # --------------------------------------------------------------------------------------
 # workload construction through the library (block manager -> tables, slots)
 # --------------------------------------------------------------------------------------
+def workload_config(w, lens, NB: int, q8=None) -> dict:
+    """The workload keys of a decode line's config (the same for both arms)."""
+    kv_name = {"fp8": "fp8 (E4M3)", "int8": "int8"}.get(q8)
+    S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
+    return {
+        "workload": f"{w.name}: {S} seqs, {Hq} q / {Hkv} kv heads, head_dim {D}, {w.dtype}, "
+                    f"block {B}, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks"
+                    + (f", {kv_name} KV cache with per-KV-head scales" if q8 else ""),
+        "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
+        "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
+        "kv_cache": {"fp8": "fp8 e4m3", "int8": "int8"}.get(q8, w.dtype),
+    }
+
+
+def pool_blocks(w, lens) -> int:
+    B = w.block_size
+    blocks = int(((lens + B - 1) // B).sum())
+    return w.fixed_pool_blocks or int(math.ceil(blocks * (1 + w.pool_spare))) + 1
+
+
 def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size: int = 0):
     import torch
     from paged_kv_cache_166_gb300 import BlockAllocator
@@ -213,8 +233,7 @@ def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size
         import dataclasses
         lens = W.context_lengths(dataclasses.replace(w, seed=seed)) if w.length_kind != "fixed" else lens
     B = w.block_size
-    blocks = int(((lens + B - 1) // B).sum())
-    NB = w.fixed_pool_blocks or int(math.ceil(blocks * (1 + w.pool_spare))) + 1
+    NB = pool_blocks(w, lens)
     alloc = BlockAllocator(NB, B, W.pool_order(NB, seed))
     sids = [alloc.create() for _ in range(len(lens))]
     for s, t in zip(sids, lens):
@@ -495,7 +514,6 @@ def native(args):
     gbs = whole_job_gbs(attn_bytes, world, ms)
     part_gbs = attn_bytes / (pms * 1e-3) / 1e9
     tag = f"decode_attention_{q8}_{args.workload}" if q8 else f"decode_attention_{args.workload}"
-    kv_name = {"fp8": "fp8 (E4M3)", "int8": "int8"}.get(q8)
     traffic = profile_traffic(tag)
     line = {
         "metric": METRIC,
@@ -511,15 +529,10 @@ def native(args):
         "dtype": f"{'e4m3' if q8 == 'fp8' else 'int8'} KV, {w.dtype} q" if q8 else w.dtype,
         "data": "synthetic",
         "config": {
-            "workload": f"{w.name}: {S} seqs, {Hq} q / {Hkv} kv heads, head_dim {D}, {w.dtype}, "
-                        f"block {B}, lengths sum {int(lens.sum())} max {int(lens.max())}, pool {NB} blocks"
-                        + (f", {kv_name} KV cache with per-KV-head scales" if q8 else ""),
-            "num_seqs": S, "num_q_heads": Hq, "num_kv_heads": Hkv, "head_dim": D,
-            "block_size": B, "sum_context": int(lens.sum()), "num_blocks": NB,
+            **workload_config(w, lens, NB, q8),
             "step": (f"paged_decode_step_{q8}: quantising cache write of 1 new token/seq + decode "
                      "attention (2 launches, PDL-chained)") if q8 else
                     "paged_decode_step: cache write of 1 new token/seq + decode attention (2 launches, PDL-chained)",
-            "kv_cache": {"fp8": "fp8 e4m3", "int8": "int8"}.get(q8, w.dtype),
             "l2": L2Flush.LABEL,
             "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
@@ -731,7 +744,8 @@ def reference(args):
         "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
         "ms_per_step": round(sec * 1e3, 2), "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "f64", "data": "synthetic",
-        "config": {"workload": f"{w.name} (host oracle on a bounded sample)"},
+        "config": {**workload_config(w, W.context_lengths(w), pool_blocks(w, W.context_lengths(w))),
+                   "step": "fp64 numpy oracle of the decode attention on the host cores"},
         "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": res["cores"],
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,

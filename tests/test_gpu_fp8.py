@@ -8,7 +8,8 @@
   row's L2 norm), on reduced versions of the workload shapes under several
   warp counts, on edge lengths with NaN codes in every unused slot and block,
   for head_dim 128 and 256 and all group sizes, and on sampled rows of the
-  full-size 13B-shaped batch in the launch configuration bench.py times.
+  full-size 13B, 70B and long-context batches in the launch configuration
+  bench.py times.
 * The fp8 decode step equals the quantising write followed by the attention,
   bit for bit (output and caches), and results are bit-identical between runs.
 """
@@ -203,13 +204,21 @@ def test_fp8_step_equals_write_then_attend_and_is_deterministic():
     check(b, list(range(len(lens))), out_b, ref)
 
 
-def test_fp8_full_13b_shaped_batch_sampled_rows():
-    fb = Fp8Batch(fp8_workload("mha13b"), None)
+@pytest.mark.parametrize("name", ["mha13b", "gqa70b", "longctx"])
+def test_fp8_full_batches_sampled_rows(name):
+    """The bench's full-size batches (13B, 70B and long-context shapes) in the launch
+    configuration the bench times, on sampled rows: the shortest and longest
+    sequences and random ones (fewer on the long-context batch, whose sequences run
+    to 131k tokens)."""
+    fb = Fp8Batch(fp8_workload(name), None)
     lens = fb.b.lens
     order = np.argsort(lens)
     r = np.random.default_rng(0)
-    seqs = sorted(set([int(order[0]), int(order[-1]), int(order[-2])] +
-                      r.choice(len(lens), 5, replace=False).tolist()))
+    if name == "longctx":
+        seqs = sorted({int(order[0]), int(order[len(lens) // 2])})
+    else:
+        seqs = sorted(set([int(order[0]), int(order[-1]), int(order[-2])] +
+                          r.choice(len(lens), 5, replace=False).tolist()))
     ref = fb.oracle_rows(seqs)
     fb.write()
     check(fb, seqs, fb.attend(), ref)

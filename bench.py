@@ -721,6 +721,79 @@ def prefill_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def allocator_bench(args):
+    """The host block manager through the C ABI, on the shared-prefix
+    parallel-sampling workload: per prompt, create and append the 1000-token prompt,
+    fork the other 7 samples, then decode — one append per sample per step in round
+    robin, each first write into the shared partial block a copy-on-write — until every
+    sample has its suffix, and free all.  Host only, one thread; the figure includes the
+    ctypes call overhead of each operation (the C++ work itself is O(1) per call)."""
+    from paged_kv_cache_166_gb300 import BlockAllocator
+    from paged_kv_cache_166_gb300 import workloads as W
+    w = W.WORKLOADS["prefix"]
+    suf = W.suffix_lengths(w)
+    P, K = w.num_prompts, w.samples_per_prompt
+    B = w.block_size
+    blocks = P * (-(-w.prompt_len // B)) + int(sum(-(-int(x) // B) + 1 for x in suf))
+    NB = int(math.ceil(blocks * (1 + w.pool_spare))) + 1
+
+    def run():
+        alloc = BlockAllocator(NB, B, W.pool_order(NB, w.seed))
+        ops = cows = 0
+        t0 = time.perf_counter()
+        seqs = []
+        for p in range(P):
+            root = alloc.create()
+            alloc.append(root, w.prompt_len)
+            seqs.append(root)
+            for _ in range(K - 1):
+                seqs.append(alloc.fork(root))
+            ops += 1 + 1 + (K - 1)
+        left = suf.copy()
+        steps = 0
+        while left.max() > 0:
+            active = np.nonzero(left)[0]
+            if args.batched:  # one call per decode step
+                _, cow = alloc.append_one_each([seqs[int(i)] for i in active])
+                cows += len(cow)
+            else:
+                for i in active:
+                    _, cow = alloc.append(seqs[int(i)], 1)
+                    cows += len(cow)
+            left[active] -= 1
+            ops += len(active)
+            steps += 1
+        for sq in seqs:
+            alloc.free(sq)
+            ops += 1
+        dt = time.perf_counter() - t0
+        assert alloc.num_free() == NB
+        alloc.close()
+        return ops, cows, dt, steps
+
+    for _ in range(args.warmup):
+        run()
+    res = [run() for _ in range(args.steps)]
+    ops, cows = res[0][0], res[0][1]
+    dt = float(np.median([r[2] for r in res]))
+    print(json.dumps({
+        "metric": "block-manager operations per second (host, through the C ABI)",
+        "value": round(ops / dt, 1), "unit": "ops/s", "n_gpus": 0, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(dt * 1e3, 2), "higher_is_better": True,
+        "scaling": "none", "vs_baseline": None, "dtype": "int32", "data": "synthetic",
+        "config": {"workload": f"prefix: {P} prompts x {K} samples, prompt {w.prompt_len} tokens, "
+                               f"suffixes {int(suf.sum())} tokens in all, pool {NB} blocks",
+                   "step": "one whole lifecycle: create + prompt append + forks, one new token "
+                           "per live sample per decode step ("
+                           + ("pkv_seq_append_one_each, one call per step" if args.batched
+                              else "pkv_seq_append per sequence") + "), frees"},
+        "ops_per_lifecycle": ops, "copy_on_write_pairs": cows,
+        "us_per_op": round(dt / ops * 1e6, 3),
+        "decode_steps": res[0][3],
+        "gpu_launches": 0,
+    }), flush=True)
+
+
 def reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -762,7 +835,9 @@ def main():
     ap.add_argument("--workload", default="mha13b",
                     choices=["tiny", "mha13b", "gqa70b", "prefix", "longctx"])
     ap.add_argument("--num-warps", type=int, default=0)
-    ap.add_argument("--op", choices=["decode", "swap", "prefill"], default="decode",
+    ap.add_argument("--batched", type=int, default=1,
+                    help="allocator bench: one batched append call per decode step (1) or one per sequence (0)")
+    ap.add_argument("--op", choices=["decode", "swap", "prefill", "allocator"], default="decode",
                     help="decode: the decode step (default); swap: blocks to host and back; "
                          "prefill: causal prefill attention")
     ap.add_argument("--prefill-seqs", type=int, default=16)
@@ -788,6 +863,9 @@ def main():
         return
     if args.op == "prefill":
         prefill_bench(args)
+        return
+    if args.op == "allocator":
+        allocator_bench(args)
         return
     (reference if args.impl == "reference" else native)(args)
 

@@ -569,6 +569,26 @@ int pkv_seq_blocks_needed(pkv_allocator_t* a, int32_t seq, int32_t n_tokens, int
 int pkv_seq_append(pkv_allocator_t* a, int32_t seq, int32_t n_tokens, int32_t* slots_out,
                    int32_t* cow_pair_out, int32_t* n_cow);
 
+/*
+ * pkv_seq_append_one_each — one decode step's bookkeeping in one call: appends one
+ * position to each of the k distinct sequences seqs[0..k-1], in that order, with the
+ * result pkv_seq_append(a, seqs[i], 1, ...) would give called for each in turn
+ * ("PagedAttention: How vLLM Borrowed Virtual Memory...", section "Walking Through
+ * the Lifecycle", Decode: each sequence's new token goes into its last block, a new
+ * block when the last one is full; section "Copy-on-Write for Beam Search and
+ * Parallel Sampling": a write into a shared block moves the writer onto a copy, and
+ * a later writer that finds itself the last holder writes in place).
+ * seqs          host int32 [k], resident sequence ids, no id twice.
+ * slots_out     host int32 [k]: the slot of each new position.
+ * cow_pairs_out host int32 [2 k]: the (src, dst) pairs of the copies needed, in
+ *               list order, *n_cow of them.
+ * All or nothing: PKV_ERR_OUT_OF_BLOCKS (state unchanged) if the pool cannot serve
+ * every block the k appends take; PKV_ERR_INVALID_ARG for a bad, swapped-out or
+ * repeated id.  k = 0 is a no-op.
+ */
+int pkv_seq_append_one_each(pkv_allocator_t* a, const int32_t* seqs, int32_t k,
+                            int32_t* slots_out, int32_t* cow_pairs_out, int32_t* n_cow);
+
 int pkv_seq_len(pkv_allocator_t* a, int32_t seq, int32_t* len);
 /* Copies up to `capacity` ids of seq's table to ids_out; *n = table length. */
 int pkv_seq_table(pkv_allocator_t* a, int32_t seq, int32_t* ids_out, int32_t capacity, int32_t* n);

@@ -84,6 +84,7 @@ SIGNATURES = {
     "pkv_seq_free": (ctypes.c_int, [_p, _i32]),
     "pkv_seq_blocks_needed": (ctypes.c_int, [_p, _i32, _i32, _pi32]),
     "pkv_seq_append": (ctypes.c_int, [_p, _i32, _i32, _pi32, _pi32, _pi32]),
+    "pkv_seq_append_one_each": (ctypes.c_int, [_p, _pi32, _i32, _pi32, _pi32, _pi32]),
     "pkv_seq_len": (ctypes.c_int, [_p, _i32, _pi32]),
     "pkv_seq_table": (ctypes.c_int, [_p, _i32, _pi32, _i32, _pi32]),
     "pkv_export_tables": (ctypes.c_int, [_p, _pi32, _i32, _i32, _pi32, _pi32]),

@@ -93,6 +93,21 @@ class BlockAllocator:
         cows = [(int(pair[0]), int(pair[1]))] if ncow.value else []
         return slots[:n], cows
 
+    def append_one_each(self, seqs: Sequence[int]) -> Tuple[np.ndarray, List[Tuple[int, int]]]:
+        """One decode step: one new position for each listed sequence (distinct ids),
+        in list order, as append(seq, 1) for each would do, in one library call.
+        Returns (slots int32 [k], [(src, dst)] copy-on-write pairs in list order);
+        all or nothing."""
+        ids = np.ascontiguousarray(seqs, dtype=np.int32)
+        k = len(ids)
+        slots = np.empty(max(k, 1), dtype=np.int32)
+        pairs = np.empty(max(2 * k, 2), dtype=np.int32)
+        ncow = ctypes.c_int32(0)
+        N.check(self._lib.pkv_seq_append_one_each(self._h, _ptr(ids), k, _ptr(slots),
+                                                  _ptr(pairs), ctypes.byref(ncow)))
+        cows = [(int(pairs[2 * i]), int(pairs[2 * i + 1])) for i in range(ncow.value)]
+        return slots[:k], cows
+
     def swap_out(self, seq: int) -> List[int]:
         """Preempt by swapping: the sequence's block ids (logical order), all given
         back to the pool; copy their contents out (paged_swap_out) before reuse."""

@@ -17,9 +17,11 @@
 //     blocks, all or nothing.
 // Every public call validates first and mutates only once it cannot fail, so a
 // failing call leaves the state unchanged.
+#include <climits>
 #include <cstdint>
 #include <cstring>
 #include <new>
+#include <utility>
 #include <vector>
 
 #include "pkv.h"
@@ -255,6 +257,64 @@ int pkv_seq_append(pkv_allocator_t* a, int32_t seq, int32_t n, int32_t* slots_ou
     slots_out[i] = static_cast<int32_t>(s.table[p / B] * B + p % B);
     s.len = static_cast<int32_t>(p + 1);
   }
+  return pkv::ok();
+}
+
+int pkv_seq_append_one_each(pkv_allocator_t* a, const int32_t* seqs, int32_t k,
+                            int32_t* slots_out, int32_t* cow_pairs_out, int32_t* n_cow) {
+  PKV_REQUIRE(a && n_cow, PKV_ERR_INVALID_ARG, "NULL argument");
+  PKV_REQUIRE(k >= 0, PKV_ERR_INVALID_ARG, "negative sequence count");
+  PKV_REQUIRE(k == 0 || (seqs && slots_out && cow_pairs_out), PKV_ERR_INVALID_ARG,
+              "NULL array");
+  const int64_t B = a->block_size;
+  // validate every sequence, and count the blocks the appends take in order: a
+  // copy-on-write earlier in the list may leave a later sequence the last holder
+  // of its block, which it then writes in place
+  std::vector<std::pair<int32_t, int32_t>> drops;  // (block, refcount dropped so far)
+  int64_t need = 0;
+  for (int32_t i = 0; i < k; ++i) {
+    const int32_t q = seqs[i];
+    PKV_REQUIRE(a->resident_seq(q), PKV_ERR_INVALID_ARG, "unknown or swapped-out sequence %d", q);
+    for (int32_t j = 0; j < i; ++j)
+      PKV_REQUIRE(seqs[j] != q, PKV_ERR_INVALID_ARG, "sequence %d listed twice", q);
+    const auto& s = a->seqs[q];
+    PKV_REQUIRE(s.len < INT32_MAX, PKV_ERR_INVALID_ARG, "sequence length overflow");
+    if (s.len % B == 0) {
+      ++need;
+      continue;
+    }
+    const int32_t last = s.table.back();
+    int32_t rc = a->refcount[last];
+    size_t d = 0;
+    while (d < drops.size() && drops[d].first != last) ++d;
+    if (d < drops.size()) rc -= drops[d].second;
+    if (rc > 1) {
+      ++need;
+      if (d < drops.size()) ++drops[d].second; else drops.emplace_back(last, 1);
+    }
+  }
+  PKV_REQUIRE(need <= static_cast<int64_t>(a->free_stack.size()), PKV_ERR_OUT_OF_BLOCKS,
+              "appending one token to each of %d sequences needs %lld blocks, %zu free", k,
+              static_cast<long long>(need), a->free_stack.size());
+  int32_t nc = 0;
+  for (int32_t i = 0; i < k; ++i) {
+    auto& s = a->seqs[seqs[i]];
+    const int64_t p = s.len;
+    if (p % B == 0) {
+      s.table.push_back(a->pop());
+    } else if (a->refcount[s.table.back()] > 1) {
+      const int32_t old_id = s.table.back();
+      const int32_t new_id = a->pop();
+      cow_pairs_out[2 * nc] = old_id;
+      cow_pairs_out[2 * nc + 1] = new_id;
+      ++nc;
+      a->decref(old_id);
+      s.table.back() = new_id;
+    }
+    slots_out[i] = static_cast<int32_t>(s.table[p / B] * B + p % B);
+    s.len = static_cast<int32_t>(p + 1);
+  }
+  *n_cow = nc;
   return pkv::ok();
 }
 

@@ -241,3 +241,52 @@ def test_library_rejects_bad_operations_without_state_change():
         a.free(s)
     with pytest.raises(N.PkvError):
         a.incref(0)
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_append_one_each_equals_appends_in_list_order(seed):
+    """pkv_seq_append_one_each against the oracle's block manager appending one
+    token to each listed sequence in turn: the same slots, the same copy-on-write
+    pairs in list order, the same state afterwards; when the pool cannot serve all
+    of them, PKV_ERR_OUT_OF_BLOCKS and no change at all.  Forked siblings put
+    shared partial blocks in the lists (the last holder writes in place)."""
+    import copy
+    r = np.random.default_rng(100 + seed)
+    B = int(r.choice([2, 4, 16]))
+    NB = int(r.integers(16, 80))
+    p = Pair(NB, B, r.permutation(NB).astype(np.int32))
+    live = []
+    for _ in range(300):
+        op = r.integers(0, 10)
+        if op < 2 or not live:
+            live.append(p.create())
+        elif op < 4:
+            p.append(live[r.integers(len(live))], int(r.integers(0, 2 * B + 2)))
+        elif op < 5:
+            live.append(p.fork(live[r.integers(len(live))]))
+        elif op < 6 and len(live) > 1:
+            p.free(live.pop(r.integers(len(live))))
+        else:
+            k = int(r.integers(0, len(live) + 1))
+            seqs = [live[i] for i in r.permutation(len(live))[:k]]
+            trial = copy.deepcopy(p.o)
+            try:
+                expect = [trial.append(s, 1) for s in seqs]
+            except OracleOOB:
+                before = p.c.num_free()
+                with pytest.raises(N.OutOfBlocks):
+                    p.c.append_one_each(seqs)
+                assert p.c.num_free() == before
+            else:
+                slots, cows = p.c.append_one_each(seqs)
+                assert list(slots) == [e[0][0] for e in expect]
+                assert cows == [c for e in expect for c in e[1]]
+                p.o = trial
+        p.compare()
+    if live:
+        with pytest.raises(N.PkvError):  # an id listed twice
+            p.c.append_one_each([live[0], live[0]])
+    with pytest.raises(N.PkvError):  # an unknown id
+        p.c.append_one_each([10 ** 6])
+    slots, cows = p.c.append_one_each([])
+    assert len(slots) == 0 and cows == []

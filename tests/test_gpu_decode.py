@@ -291,3 +291,26 @@ def test_decode_step_full_mha13b_every_row():
     seqs = list(range(len(b.lens)))
     ref = BT.oracle_rows(b, seqs)
     check_rows(b, seqs, run_step(b), ref)
+
+
+@pytest.mark.parametrize("num_warps", [0, 61])
+def test_maximum_sequence_count(num_warps):
+    """2048 sequences, the most one launch takes, with ragged lengths (1..300, zero
+    included): sampled rows against the oracle; one more sequence is refused."""
+    import dataclasses
+    r = np.random.default_rng(7)
+    lens = r.integers(0, 301, 2048)
+    lens[:3] = (0, 1, 300)
+    w = dataclasses.replace(W.WORKLOADS["gqa70b"], num_q_heads=16, num_kv_heads=2)
+    b = BT.decode_batch(w, lens)
+    seqs = sorted({0, 1, 2, 2047} | set(r.choice(2048, 12, replace=False).tolist()))
+    ref = BT.oracle_rows(b, seqs)
+    out = run(b, num_warps)
+    check_rows(b, seqs, out, ref)
+    assert torch.count_nonzero(out[0]) == 0  # empty context: zero row
+    m = pkv()
+    q = torch.zeros(2049, 16, 128, dtype=torch.bfloat16, device="cuda")
+    t = torch.zeros(2049, 1, dtype=torch.int32, device="cuda")
+    c = torch.ones(2049, dtype=torch.int32, device="cuda")
+    with pytest.raises(m.PkvError):
+        m.paged_decode_attention(q, b.kc, b.vc, t, c, 0.1, torch.empty_like(q))

@@ -213,3 +213,31 @@ def test_prefill_random_shapes(seed):
     err = BT.row_errors(got[:T], ref)
     assert np.isfinite(got[:T]).all()
     assert err.max() <= BT.tolerance(dtype), f"row error {err.max():.3e} ({dtype}, D {D}, G {G})"
+
+
+def test_prefill_maximum_sequence_count():
+    """2048 sequences, the most one launch takes (whole prompts and chunks of 0..40
+    queries, contexts up to 90 tokens): every row against the oracle; one more
+    sequence is refused."""
+    r = np.random.default_rng(9)
+    lens = tuple(int(x) for x in r.integers(1, 91, 2048))
+    chunks = tuple(t if r.random() < 0.3 else int(r.integers(0, min(t, 40) + 1)) for t in lens)
+    kc, vc, q, tables, ctx, qstart = case("bf16", 4, 2, 128, lens, chunks, seed=31)
+    T = int(qstart[-1])
+    ref = opf.paged_prefill_attention(BT.np64(q[:T]), BT.np64(kc), BT.np64(vc), tables, ctx,
+                                      qstart, 1 / np.sqrt(128))
+    out = torch.full_like(q, 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(ctx).cuda(), torch.from_numpy(qstart).cuda(),
+                                  1 / np.sqrt(128), out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = BT.np64(out)
+    assert np.all(got[T:] == 7.0)
+    err = BT.row_errors(got[:T], ref)
+    assert err.max() <= BT.tolerance("bf16"), f"row error {err.max():.3e}"
+    qs2 = torch.zeros(2050, dtype=torch.int32, device="cuda")
+    t2 = torch.zeros(2049, 1, dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv().PkvError):
+        pkv().paged_prefill_attention(q, kc, vc, t2, t2[:, 0].contiguous(), qs2, 0.1, out)

@@ -664,7 +664,7 @@ def prefill_bench(args):
     dt = "bf16" if w.dtype == "f32" else w.dtype
     S, P = args.prefill_seqs, args.prefill_len
     C = args.chunk or P
-    B, Hq, Hkv, D = w.block_size, w.num_q_heads, w.num_kv_heads, w.head_dim
+    B, Hq, Hkv, D = args.block_size or w.block_size, w.num_q_heads, w.num_kv_heads, w.head_dim
     NB = S * (-(-P // B)) + 1
     alloc = BlockAllocator(NB, B, W.pool_order(NB, w.seed))
     sids = [alloc.create() for _ in range(S)]
@@ -708,12 +708,13 @@ def prefill_bench(args):
         "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
         "config": {"workload": f"{w.name} shape: {S} sequences x {P}-token context, chunk of {C} "
                                f"queries each, {Hq} q / {Hkv} kv heads, head_dim {D}, {dt}",
-                   "l2": L2Flush.LABEL},
+                   "block_size": B, "l2": L2Flush.LABEL},
         "tokens_per_s": round(S * C / (ms * 1e-3), 1),
         "roofline": {"bound": "tensor", "achieved": round(tflops, 1), "peak": peak,
                      "unit": "TFLOP/s", "frac": round(tflops / peak, 4),
                      "traffic": profile_traffic(f"prefill_attention_{w.name}", "prefill_tcgen05.cu",
-                                                f"{w.name} {S}x{P} chunk {C}"),
+                                                f"{w.name} {S}x{P} chunk {C}")
+                     if B == w.block_size else None,
                      "kernel": "prefill_tc_kernel (tcgen05 MMAs, tensor-memory accumulators)",
                      "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({kind}; dense cuBLAS)"},
         "gpu_launches": args.steps,

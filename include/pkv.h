@@ -284,8 +284,9 @@ int pkv_decode_attention_static_scratch(const void* q, const void* k_cache, cons
  * status        device int32 word or NULL: PKV_DEV_* bits are ORed into it
  *               (lengths out of range are clamped, bad block ids read as zeros,
  *               a wait that timed out abandons the launch).
- * Supported: block_size 16, head_dim 64 or 128, G in {1, 2, 4, 8},
- * num_seqs <= 2048.  Computed on the 5th-generation tensor cores (tcgen05 MMAs
+ * Supported: block_size 8, 16 or 32 (a 128-key tile is read as 16, 8 or 4
+ * blocks), head_dim 64 or 128, G in {1, 2, 4, 8}, num_seqs <= 2048,
+ * max_blocks_per_seq * block_size < 2^31.  Computed on the 5th-generation tensor cores (tcgen05 MMAs
  * with tensor-memory accumulators; bf16/f16 inputs, probabilities rounded to the
  * input type for P.V, fp32 accumulation and softmax); results depend only on the
  * values and lengths.

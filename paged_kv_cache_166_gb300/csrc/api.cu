@@ -119,6 +119,27 @@ int encode_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType type, 
   return PKV_OK;
 }
 
+int encode_map_4d(CUtensorMap* map, const void* base, CUtensorMapDataType type,
+                  const int64_t dims[4], const int64_t strides[3], const int32_t box[4],
+                  CUtensorMapSwizzle swizzle) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  cuuint64_t d[4], st[3];
+  cuuint32_t bx[4];
+  const cuuint32_t estr[4] = {1u, 1u, 1u, 1u};
+  for (int i = 0; i < 4; ++i) {
+    d[i] = static_cast<cuuint64_t>(dims[i]);
+    bx[i] = static_cast<cuuint32_t>(box[i]);
+    if (i < 3) st[i] = static_cast<cuuint64_t>(strides[i]);
+  }
+  CUresult r = fn(map, type, 4, const_cast<void*>(base), d, st, bx, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, swizzle, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS)
+    return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled (4-D) failed (%d)", (int)r);
+  return PKV_OK;
+}
+
 }  // namespace pkv
 
 extern "C" {

@@ -49,6 +49,13 @@ int encode_map_3d(CUtensorMap* map, const void* base, CUtensorMapDataType type, 
                   const int64_t dims[3], const int64_t strides[2], const int32_t box[3],
                   CUtensorMapSwizzle swizzle);
 
+// A 4-D map, laid out as the 3-D one.  The byte strides need not increase with the
+// dimension: a box then lands in shared memory in the order of the map's dims,
+// which is how a caller reorders the axes of a tile on the way in.
+int encode_map_4d(CUtensorMap* map, const void* base, CUtensorMapDataType type,
+                  const int64_t dims[4], const int64_t strides[3], const int32_t box[4],
+                  CUtensorMapSwizzle swizzle);
+
 // Launches the 8-bit quantising cache write (kv_ops.cu); codes is PKV_FP8_E4M3
 // or PKV_INT8.  With slot_mapping set, token i goes to slot_mapping[i]; with it
 // NULL, sequence i's token goes to slot(t - 1) of its block table,

@@ -444,11 +444,17 @@ extern "C" int pkv_prefill_attention(const void* q, const void* k_cache, const v
               "query heads per KV head %d not in {1,2,4,8}", G);
   PKV_REQUIRE(head_dim == 64 || head_dim == 128, PKV_ERR_UNSUPPORTED,
               "prefill head_dim %d not in {64, 128}", head_dim);
-  PKV_REQUIRE(block_size == kPfTok, PKV_ERR_UNSUPPORTED, "block_size %d (kernels use 16)",
-              block_size);
+  if (PKV_PREFILL_TCGEN05)
+    PKV_REQUIRE(block_size == 8 || block_size == 16 || block_size == 32, PKV_ERR_UNSUPPORTED,
+                "block_size %d not in {8, 16, 32}", block_size);
+  else
+    PKV_REQUIRE(block_size == kPfTok, PKV_ERR_UNSUPPORTED, "block_size %d (kernel uses 16)",
+                block_size);
   PKV_REQUIRE(max_blocks_per_seq > 0 && num_blocks > 0, PKV_ERR_INVALID_ARG, "bad sizes");
-  PKV_REQUIRE(static_cast<int64_t>(num_blocks) * num_kv_heads * kPfTok * 4 < (int64_t(1) << 31),
-              PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * 64 >= 2^31");
+  PKV_REQUIRE(static_cast<int64_t>(max_blocks_per_seq) * block_size < (int64_t(1) << 31),
+              PKV_ERR_UNSUPPORTED, "max_blocks_per_seq * block_size >= 2^31");
+  PKV_REQUIRE(static_cast<int64_t>(num_blocks) * num_kv_heads * block_size * 4 < (int64_t(1) << 31),
+              PKV_ERR_UNSUPPORTED, "num_blocks * num_kv_heads * block_size * 4 >= 2^31");
   PKV_REQUIRE(static_cast<int64_t>(num_seqs) * max_blocks_per_seq < (int64_t(1) << 31),
               PKV_ERR_UNSUPPORTED, "num_seqs * max_blocks_per_seq >= 2^31");
   PKV_REQUIRE(num_tokens >= 0, PKV_ERR_INVALID_ARG, "negative num_tokens");
@@ -473,6 +479,7 @@ extern "C" int pkv_prefill_attention(const void* q, const void* k_cache, const v
   a.G = G;
   a.MAXB = max_blocks_per_seq;
   a.NB = num_blocks;
+  a.bs = block_size;
   a.scale_log2 = scale * 1.4426950408889634f;
   cudaStream_t st = static_cast<cudaStream_t>(stream);
   int rc;

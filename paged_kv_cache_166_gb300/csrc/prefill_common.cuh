@@ -11,7 +11,7 @@
 
 namespace pkv {
 
-constexpr int kPfTok = 16;                     // tokens per cache block (kernel requirement)
+constexpr int kPfTok = 16;                     // tokens per cache block of the warp-level kernel
 constexpr int kPfMaxSeqs = 2048;
 constexpr uint64_t kPfWaitNs = 1000000000ull;  // 1 s per wait before giving up
 
@@ -23,6 +23,7 @@ struct PrefillArgs {
   const int32_t* query_start;
   int32_t* status;  // device status word, may be NULL
   int32_t S, T, Hq, Hkv, G, MAXB, NB;  // T: rows of q and out
+  int32_t bs;                          // tokens per cache block
   float scale_log2;
 };
 
@@ -31,14 +32,14 @@ __device__ __forceinline__ void pf_flag(const PrefillArgs& a, int bits) {
 }
 
 // Context t, chunk length c and first query row q0 of sequence s, clamped to
-// 0 <= c <= t <= MAXB * 16 and 0 <= q0, q0 + c <= T (a clamp is reported once,
+// 0 <= c <= t <= MAXB * bs and 0 <= q0, q0 + c <= T (a clamp is reported once,
 // by the caller that passes report).
 __device__ __forceinline__ void pf_seq(const PrefillArgs& a, int s, int& t, int& c, int& q0,
                                        bool report) {
   t = __ldg(a.context_lens + s);
   q0 = __ldg(a.query_start + s);
   c = __ldg(a.query_start + s + 1) - q0;
-  const int limit = a.MAXB * kPfTok;
+  const int limit = a.MAXB * a.bs;
   if (t < 0 || t > limit || c < 0 || c > t || q0 < 0 || q0 > a.T || c > a.T - q0) {
     if (report) pf_flag(a, PKV_DEV_BAD_CONTEXT_LEN);
     t = t < 0 ? 0 : (t > limit ? limit : t);

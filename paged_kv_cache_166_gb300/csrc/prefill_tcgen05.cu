@@ -8,10 +8,16 @@
 //
 // How.  A unit is a tile of 128 rows of one (sequence, KV head) — row R is query
 // R / G, head g*G + R % G — against the keys 0 .. p_max of its last row, taken
-// in KV tiles of 128 keys (eight 16-token cache blocks).  Per KV tile j:
+// in KV tiles of 128 keys (16, 8 or 4 cache blocks of 8, 16 or 32 tokens).  Per
+// KV tile j:
 //   S_j = Q K_j^T    tcgen05 MMA, M = 128 rows, N = 128 keys, K = head_dim:
 //                    Q and K_j K-major in 128-byte-swizzled shared memory,
-//                    S_j in tensor memory (two buffers);
+//                    S_j in tensor memory (two buffers).  A K or V tile is 16
+//                    groups of 8 keys; each group holds one 1024-byte swizzle
+//                    atom (8 rows x 128 B) per 64-column chunk of head_dim, side
+//                    by side, so that a cache block (BS / 8 groups, every chunk)
+//                    arrives as one 4-D TMA box whose axes are reordered on the
+//                    way in (column, row, chunk, group);
 //   softmax          two threads per row (its tensor-memory lane), one per half
 //                    of the keys: causal mask, the row max agreed through shared
 //                    memory, P_j = exp2(S_j - m) (base 2; the exponents of a
@@ -63,7 +69,6 @@ namespace {
 
 constexpr int kTcRows = 128;          // rows of a unit = tensor-memory lanes = MMA M
 constexpr int kTcKeys = 128;          // keys of a KV tile = N of S = K of P.V
-constexpr int kTcBlocks = kTcKeys / kPfTok;
 constexpr int kTcRowWarps = 8;        // softmax warps 2 .. 9
 constexpr int kTcVWarp = 2 + kTcRowWarps;  // V producer
 constexpr int kTcQWarp = 3 + kTcRowWarps;  // query-tile producer
@@ -72,7 +77,6 @@ constexpr int kTcHalfKeys = kTcKeys / 2;
 constexpr float kTcRescale = 8.f;     // log2 of the growth of the row max that moves m
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcChunk = 128 * 128;   // one [128 rows x 128 B] swizzled column chunk
-constexpr int kTcBox = 2048;          // one 16-row box of a chunk
 
 // mbarriers (8 bytes each), then the tensor-memory base and the CTA's schedule
 enum {
@@ -100,6 +104,7 @@ struct TcShape {
   static constexpr bool kBf16 = std::is_same<T, __nv_bfloat16>::value;
   static constexpr int kChunks = D * 2 / 128;         // 128-byte column chunks of a row
   static constexpr int kTile = kTcRows * D * 2;       // Q, K or V tile
+  static constexpr uint32_t kGroup = kChunks * 1024;  // 8 keys of a K or V tile, every chunk
   static constexpr int kKStages = D == 128 ? 2 : 3;   // K ring (freed as soon as S_j is done)
   static constexpr int kVStages = D == 128 ? 3 : 4;   // V ring
   static constexpr uint32_t kQOff = 0;                // two query tiles
@@ -161,7 +166,7 @@ __device__ __forceinline__ void tc_advance(const PrefillArgs& a, TcSched& u, int
   }
 }
 
-template <typename T, int D>
+template <typename T, int D, int BS>
 __global__ void __launch_bounds__(kTcThreads, 1)
     prefill_tc_kernel(const __grid_constant__ CUtensorMap qmap,
                       const __grid_constant__ CUtensorMap kmap,
@@ -304,7 +309,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     const bool is_k = warp == 0;
     // later units of (s, g) read K/V again: keep them in L2 ahead of the q and out streams
     const uint64_t policy = ptx::policy_evict_last();
-    const int32_t rows_total = a.NB * a.Hkv * kPfTok;
+    const int32_t groups_total = a.NB * a.Hkv * (BS / 8);  // 8-row groups of the cache
+    constexpr int nblk = kTcKeys / BS;  // cache blocks (TMA boxes) of a KV tile
     const CUtensorMap* const map = is_k ? &kmap : &vmap;
     const int full0 = is_k ? kBarKFull : kBarVFull, empty0 = is_k ? kBarKEmpty : kBarVEmpty;
     const uint32_t ring = base_s + (is_k ? Sh::kKOff : Sh::kVOff);
@@ -319,12 +325,12 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       bool ok = true;
       for (int j = 0; j < nkt; ++j, ++it) {
         const uint32_t st = it % NS;
-        const int bi = kTcBlocks * j + (lane & 7);
-        int32_t y = rows_total;  // a box wholly past the end: zero-filled
-        if (lane < kTcBlocks && bi * kPfTok < t) {
+        const int bi = nblk * j + (lane & (nblk - 1));
+        int32_t y = groups_total;  // a box wholly past the end: zero-filled
+        if (lane < nblk && bi * BS < t) {
           const int id = __ldg(a.block_tables + static_cast<int64_t>(u.s) * a.MAXB + bi);
           if (static_cast<uint32_t>(id) < static_cast<uint32_t>(a.NB))
-            y = (id * a.Hkv + u.g) * kPfTok;
+            y = (id * a.Hkv + u.g) * (BS / 8);
           else if (is_k)
             pf_flag(a, PKV_DEV_BAD_BLOCK_ID);
         }
@@ -334,12 +340,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         }
         if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
         __syncwarp();
-        if (lane < kTcBlocks) {
-          const uint32_t dst = ring + st * Sh::kTile + lane * kTcBox;
-#pragma unroll
-          for (int cc = 0; cc < Sh::kChunks; ++cc)
-            ptx::tma_load_2d(dst + cc * kTcChunk, map, cc * 64, y, bar(full0 + st), policy);
-        }
+        if (lane < nblk)  // block `lane`: key groups lane * BS / 8 ..
+          ptx::tma_load_4d(ring + st * Sh::kTile + lane * (BS / 8) * Sh::kGroup, map, 0, 0, 0, y,
+                           bar(full0 + st), policy);
       }
       if (!alive) break;
       tc_advance(a, u, nkt);
@@ -372,14 +375,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const uint32_t vt = base_s + Sh::kVOff + st * Sh::kTile;
       // keys past the context inside its last cache block may hold anything (NaN
       // included) and P is 0 there: zero those V rows so that 0 * V stays 0
-      const int last = (t - 1) / kPfTok;
-      if ((t % kPfTok) != 0 && last / kTcBlocks == j) {
-        const int r0 = (last % kTcBlocks) * kPfTok + t % kPfTok;
-        const int n16 = (kPfTok - t % kPfTok) * 8 * Sh::kChunks;  // 16-byte units
+      constexpr int nblk = kTcKeys / BS;
+      const int last = (t - 1) / BS;
+      if ((t % BS) != 0 && last / nblk == j) {
+        const int r0 = (last % nblk) * BS + t % BS;
+        const int n16 = (BS - t % BS) * 8 * Sh::kChunks;  // 16-byte units
         for (int i = lane; i < n16; i += 32) {
           const int row = r0 + i / (8 * Sh::kChunks), rem = i % (8 * Sh::kChunks);
-          ptx::st_shared_v4(vt + (rem / 8) * kTcChunk + row * 128 + (rem % 8) * 16, 0u, 0u, 0u,
-                            0u);
+          ptx::st_shared_v4(vt + (row >> 3) * Sh::kGroup + (rem / 8) * 1024 + (row & 7) * 128 +
+                                (rem % 8) * 16,
+                            0u, 0u, 0u, 0u);
         }
         ptx::fence_proxy_async_smem();
         __syncwarp();
@@ -389,7 +394,8 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
       for (int ks = 0; ks < kTcKeys / 16; ++ks)  // 16 keys = 8 packed columns of P
         ptx::umma_f16_ta_elect(tmem + Sh::kOCol, pt + ks * 8,
-                               ptx::smem_desc_sw128(vt + ks * kTcBox, kTcChunk, 1024), Sh::kIdPV,
+                               ptx::smem_desc_sw128(vt + ks * 2 * Sh::kGroup, 1024, Sh::kGroup),
+                               Sh::kIdPV,
                                j > 0 || ks > 0);
       ptx::umma_commit_elect(bar(kBarPvDone + b));
       ptx::umma_commit_elect(bar(kBarVEmpty + st));
@@ -421,9 +427,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         const uint32_t kb = base_s + Sh::kKOff + st * Sh::kTile;
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks) {
-          const uint32_t off = (ks >> 2) * kTcChunk + (ks & 3) * 32;
-          ptx::umma_f16_elect(tmem + Sh::kSCol + b * kTcKeys, ptx::smem_desc_sw128(qa + off, 16, 1024),
-                              ptx::smem_desc_sw128(kb + off, 16, 1024), Sh::kIdQK, ks > 0);
+          const uint32_t kin = (ks & 3) * 32;  // 16 columns inside a 128-byte chunk
+          ptx::umma_f16_elect(tmem + Sh::kSCol + b * kTcKeys,
+                              ptx::smem_desc_sw128(qa + (ks >> 2) * kTcChunk + kin, 16, 1024),
+                              ptx::smem_desc_sw128(kb + (ks >> 2) * 1024 + kin, 16, Sh::kGroup),
+                              Sh::kIdQK, ks > 0);
         }
         ptx::umma_commit_elect(bar(kBarSFull + b));
         ptx::umma_commit_elect(bar(kBarKEmpty + st));
@@ -648,7 +656,7 @@ int tc_smem_optin(int* bytes) {
   return PKV_OK;
 }
 
-template <typename T, int D>
+template <typename T, int D, int BS>
 int launch_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache, int32_t dtype,
               cudaStream_t stream) {
   using Sh = TcShape<T, D>;
@@ -666,7 +674,7 @@ int launch_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache, in
               PKV_ERR_UNSUPPORTED,
               "too many sequences");
   std::call_once(flags[dev], [&] {
-    results[dev] = cudaFuncSetAttribute(prefill_tc_kernel<T, D>,
+    results[dev] = cudaFuncSetAttribute(prefill_tc_kernel<T, D, BS>,
                                         cudaFuncAttributeMaxDynamicSharedMemorySize, Sh::kBytes);
   });
   if (results[dev] != cudaSuccess)
@@ -681,17 +689,33 @@ int launch_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache, in
   const int32_t qbox[3] = {64, a.G, kTcRows / a.G};
   rc = encode_map_3d(&qmap, a.q, ty, 2, qdims, qstrides, qbox, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != PKV_OK) return rc;
-  const int64_t rows = static_cast<int64_t>(a.NB) * a.Hkv * kPfTok;
-  rc = encode_cache_map(&kmap, k_cache, dtype, rows, D, 64, kPfTok);
+  // K and V [rows, D] viewed as (column in chunk, row in group, chunk, 8-row group):
+  // one box = one cache block of one KV head, landing chunk-major within each group
+  const int64_t kvdims[4] = {64, 8, Sh::kChunks, static_cast<int64_t>(a.NB) * a.Hkv * (BS / 8)};
+  const int64_t kvstrides[3] = {static_cast<int64_t>(D) * 2, 128, 8 * static_cast<int64_t>(D) * 2};
+  const int32_t kvbox[4] = {64, 8, Sh::kChunks, BS / 8};
+  rc = encode_map_4d(&kmap, k_cache, ty, kvdims, kvstrides, kvbox, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != PKV_OK) return rc;
-  rc = encode_cache_map(&vmap, v_cache, dtype, rows, D, 64, kPfTok);
+  rc = encode_map_4d(&vmap, v_cache, ty, kvdims, kvstrides, kvbox, CU_TENSOR_MAP_SWIZZLE_128B);
   if (rc != PKV_OK) return rc;
   int sms = 0;
   rc = device_sm_count(&sms, &dev);
   if (rc != PKV_OK) return rc;
-  prefill_tc_kernel<T, D><<<sms, kTcThreads, Sh::kBytes, stream>>>(qmap, kmap, vmap, a);
+  prefill_tc_kernel<T, D, BS><<<sms, kTcThreads, Sh::kBytes, stream>>>(qmap, kmap, vmap, a);
   PKV_CUDA(cudaGetLastError());
   return PKV_OK;
+}
+
+// One kernel per block size, so that the producers' box arithmetic is constant.
+template <typename T, int D>
+int launch_tc_bs(const PrefillArgs& a, const void* k_cache, const void* v_cache, int32_t dtype,
+                 cudaStream_t stream) {
+  switch (a.bs) {
+    case 8: return launch_tc<T, D, 8>(a, k_cache, v_cache, dtype, stream);
+    case 16: return launch_tc<T, D, 16>(a, k_cache, v_cache, dtype, stream);
+    case 32: return launch_tc<T, D, 32>(a, k_cache, v_cache, dtype, stream);
+    default: return fail(PKV_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32}", a.bs);
+  }
 }
 
 }  // namespace
@@ -699,10 +723,10 @@ int launch_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache, in
 int launch_prefill_tc(const PrefillArgs& a, const void* k_cache, const void* v_cache,
                       int32_t dtype, int32_t head_dim, cudaStream_t stream) {
   if (dtype == PKV_BF16)
-    return head_dim == 64 ? launch_tc<__nv_bfloat16, 64>(a, k_cache, v_cache, dtype, stream)
-                          : launch_tc<__nv_bfloat16, 128>(a, k_cache, v_cache, dtype, stream);
-  return head_dim == 64 ? launch_tc<__half, 64>(a, k_cache, v_cache, dtype, stream)
-                        : launch_tc<__half, 128>(a, k_cache, v_cache, dtype, stream);
+    return head_dim == 64 ? launch_tc_bs<__nv_bfloat16, 64>(a, k_cache, v_cache, dtype, stream)
+                          : launch_tc_bs<__nv_bfloat16, 128>(a, k_cache, v_cache, dtype, stream);
+  return head_dim == 64 ? launch_tc_bs<__half, 64>(a, k_cache, v_cache, dtype, stream)
+                        : launch_tc_bs<__half, 128>(a, k_cache, v_cache, dtype, stream);
 }
 
 }  // namespace pkv

@@ -7,7 +7,9 @@ Covered: whole-prompt prefills of lengths 1 to several hundred, chunks of 1 to
 query may read (block tails past the context, unused blocks); a clean status
 word; rows outside the chunks left untouched; keys whose magnitude grows with
 their position (scores rising along the sequence by many factors of 2^8, so
-the kernel's running reference max moves again and again); and the bench's own
+the kernel's running reference max moves again and again); cache blocks of 8
+and 32 tokens (a 128-key tile read as 16 or 4 blocks; lengths ending inside a
+block, on a block boundary and on a tile boundary); and the bench's own
 workload at full size (16 prompts of 2048 tokens, 70B shape) on sampled rows.
 """
 import numpy as np
@@ -35,8 +37,7 @@ def pkv():
     return m
 
 
-def case(dtype, Hq, Hkv, D, lens, chunks, seed=11, ramp=False):
-    B = 16
+def case(dtype, Hq, Hkv, D, lens, chunks, seed=11, ramp=False, B=16):
     NB = int(sum(-(-t // B) for t in lens)) + 7
     mgr = BlockManager(NB, B, W.pool_order(NB, seed))
     sids = [mgr.create() for _ in lens]
@@ -241,3 +242,45 @@ def test_prefill_maximum_sequence_count():
     t2 = torch.zeros(2049, 1, dtype=torch.int32, device="cuda")
     with pytest.raises(pkv().PkvError):
         pkv().paged_prefill_attention(q, kc, vc, t2, t2[:, 0].contiguous(), qs2, 0.1, out)
+
+
+BLOCK_CASES = [
+    ("f16", 8, 8, 128, (1, 7, 8, 9, 128, 129, 333), None),
+    ("bf16", 64, 8, 128, (40, 700, 256), (40, 65, 1)),
+    ("bf16", 16, 4, 64, (33, 64, 500, 31), (7, 64, 0, 31)),
+    ("f16", 8, 2, 128, (1000, 31, 32, 33), (200, 31, 1, 33)),
+]
+
+
+@pytest.mark.parametrize("B", [8, 32])
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,lens,chunks", BLOCK_CASES)
+def test_prefill_block_sizes(B, dtype, Hq, Hkv, D, lens, chunks):
+    chunks = lens if chunks is None else chunks
+    kc, vc, q, tables, ctx, qstart = case(dtype, Hq, Hkv, D, lens, chunks, seed=17 + B, B=B)
+    assert kc.shape[2] == B
+    T = int(qstart[-1])
+    ref = opf.paged_prefill_attention(BT.np64(q[:T]), BT.np64(kc), BT.np64(vc), tables, ctx,
+                                      qstart, 1 / np.sqrt(D))
+    out = torch.full_like(q, 7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                  torch.from_numpy(ctx).cuda(), torch.from_numpy(qstart).cuda(),
+                                  1 / np.sqrt(D), out, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    got = BT.np64(out)
+    assert np.all(got[T:] == 7.0)
+    assert np.isfinite(got[:T]).all()
+    err = BT.row_errors(got[:T], ref)
+    assert err.max() <= BT.tolerance(dtype), f"row error {err.max():.3e}"
+
+
+@pytest.mark.parametrize("B", [4, 64])
+def test_prefill_unsupported_block_size_refused(B):
+    kc, vc, q, tables, ctx, qstart = case("f16", 8, 8, 64, (40,), (40,), B=B)
+    out = torch.zeros_like(q)
+    with pytest.raises(pkv().PkvError):
+        pkv().paged_prefill_attention(q, kc, vc, torch.from_numpy(tables).cuda(),
+                                      torch.from_numpy(ctx).cuda(),
+                                      torch.from_numpy(qstart).cuda(), 0.125, out)
+    torch.cuda.synchronize()

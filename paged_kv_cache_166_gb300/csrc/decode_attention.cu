@@ -82,6 +82,12 @@ namespace pkv {
 #ifndef PKV_SINGLE_BOX
 #define PKV_SINGLE_BOX 0
 #endif
+// 16-bit caches: tiles stored as groups of 8 tokens (one swizzle atom per 128 B of
+// row, side by side), so that one 4-D TMA box moves a whole 16-token step, or a
+// whole 8-token block.
+#ifndef PKV_GROUPED_TILES
+#define PKV_GROUPED_TILES 1
+#endif
 #ifndef PKV_PREFETCH_TABLES
 #define PKV_PREFETCH_TABLES 1
 #endif
@@ -179,8 +185,10 @@ struct Shape {
   // fp16/bf16 tiles up to head_dim 128 fit in registers: release the stage early
   static constexpr bool kEarlyRelease = PKV_EARLY_RELEASE && (kElt == 2) && (D <= 128);
   // 8-bit: K in kSub boxes of [16 rows x 128 B]; V (stored [D x 16 B]) in one box
+  // 16-bit: one 4-D box per step (or per 8-token block) into grouped tiles
+  static constexpr bool kGrouped = PKV_GROUPED_TILES && !kQ8 && kElt == 2;
   // one box per tile: rows of the tile are viewed as kSub half-rows of 128 B
-  static constexpr bool kSingleBox = PKV_SINGLE_BOX && !kQ8 && (kSub <= 2);
+  static constexpr bool kSingleBox = PKV_SINGLE_BOX && !kGrouped && !kQ8 && (kSub <= 2);
   static_assert(kSub * kSwizzleRow == D * kElt, "head_dim * elt must be a multiple of 128 B");
 };
 
@@ -369,10 +377,15 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* pre, int S, in
 // chunk c of row r sits at chunk position c ^ (r & 7) (the TMA 128-byte swizzle).
 // ---------------------------------------------------------------------------------
 // Single-box tiles are instead [16 * kSub half-rows x 128 B], half-row r*kSub + c
-// holding chunks 8c..8c+7 of token row r.
-template <int kSub, bool kSingleBox>
+// holding chunks 8c..8c+7 of token row r.  Grouped tiles are two groups of 8 rows,
+// each group kSub swizzle atoms [8 rows x 128 B] side by side (atom c holding
+// chunks 8c..8c+7 of its rows).
+template <int kSub, bool kSingleBox, bool kGrouped = false>
 __device__ __forceinline__ uint32_t tile_offset(int row, int chunk16) {
-  if constexpr (kSingleBox) {
+  if constexpr (kGrouped) {
+    return (row >> 3) * (kSub * 8 * kSwizzleRow) + (chunk16 >> 3) * (8 * kSwizzleRow) +
+           (row & 7) * kSwizzleRow + (((chunk16 & 7) ^ (row & 7)) << 4);
+  } else if constexpr (kSingleBox) {
     const int hr = row * kSub + (chunk16 >> 3);
     return hr * kSwizzleRow + (((chunk16 & 7) ^ (hr & 7)) << 4);
   } else {
@@ -384,9 +397,10 @@ template <typename T, int D>
 struct MmaState {
   static constexpr int KS = D / 16;
   static constexpr int kSub = D * static_cast<int>(sizeof(T)) / kSwizzleRow;
-  static constexpr bool kSingle = PKV_SINGLE_BOX && (kSub <= 2);
+  static constexpr bool kGrouped = PKV_GROUPED_TILES;
+  static constexpr bool kSingle = PKV_SINGLE_BOX && !kGrouped && (kSub <= 2);
   static __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk16) {
-    return tile + tile_offset<kSub, kSingle>(row, chunk16);
+    return tile + tile_offset<kSub, kSingle, kGrouped>(row, chunk16);
   }
   float o[KS][4];   // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
   uint32_t qb[KS][2];
@@ -1121,7 +1135,27 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
       atomicOr(a.status, PKV_DEV_BAD_BLOCK_ID);
       return rows_total;  // a box wholly past the end: the TMA unit fills it with zeros
     };
-    if (kBlk != kTok && Bsz == 8) {
+    if constexpr (Sh::kGrouped) {
+      // 8-row groups of the cache: a 16-token step is one box of two groups, an
+      // 8-token block one box of one group (the step's second block in group 1)
+      if (kBlk != kTok && Bsz == 8) {
+        ptx::mbar_arrive_expect_tx(bar, (second ? Sh::kStageBytes : Sh::kStageBytes / 2) +
+                                            (need_q ? a.q_bytes : 0));
+        const int32_t g0 = row_of(id0, 0) >> 3;
+        ptx::tma_load_4d(kt, &kmap, 0, 0, 0, g0, bar, policy);
+        ptx::tma_load_4d(vt, &vmap, 0, 0, 0, g0, bar, policy);
+        if (second) {
+          const int32_t g1 = row_of(id1, 0) >> 3;
+          ptx::tma_load_4d(kt + Sh::kTileBytes / 2, &kmap, 0, 0, 0, g1, bar, policy);
+          ptx::tma_load_4d(vt + Sh::kTileBytes / 2, &vmap, 0, 0, 0, g1, bar, policy);
+        }
+      } else {
+        ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
+        const int32_t g = row_of(id0, (kBlk != kTok && Bsz == 32) ? (j & 1) * kTok : 0) >> 3;
+        ptx::tma_load_4d(kt, &kmap, 0, 0, 0, g, bar, policy);
+        ptx::tma_load_4d(vt, &vmap, 0, 0, 0, g, bar, policy);
+      }
+    } else if (kBlk != kTok && Bsz == 8) {
       // two 8-row blocks per step, into rows 0-7 and 8-15 of every sub-tile
       ptx::mbar_arrive_expect_tx(bar, (second ? Sh::kStageBytes : Sh::kStageBytes / 2) +
                                           (need_q ? a.q_bytes : 0));
@@ -1527,6 +1561,19 @@ int launch_decode(const HostArgs& h, int W) {
     rc = encode_map_2d(&vmap, h.v_cache, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1,
                        static_cast<int64_t>(h.NB) * h.Hkv * (D / 8), kSwizzleRow, kSwizzleRow,
                        D / 8, CU_TENSOR_MAP_SWIZZLE_NONE);
+    if (rc != PKV_OK) return rc;
+  } else if constexpr (Sh::kGrouped) {
+    // [rows, D] viewed as (column in a 128-byte chunk, row in an 8-row group, chunk,
+    // group); a box is two groups (a 16-token step) or one (an 8-token block)
+    const CUtensorMapDataType ty =
+        h.dtype == PKV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16 : CU_TENSOR_MAP_DATA_TYPE_FLOAT16;
+    const int64_t dims[4] = {Sh::kBoxCols, 8, Sh::kSub, rows / 8};
+    const int64_t strides[3] = {static_cast<int64_t>(D) * 2, kSwizzleRow,
+                                8 * static_cast<int64_t>(D) * 2};
+    const int32_t box[4] = {Sh::kBoxCols, 8, Sh::kSub, h.block_size == 8 ? 1 : 2};
+    rc = encode_map_4d(&kmap, h.k_cache, ty, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    if (rc != PKV_OK) return rc;
+    rc = encode_map_4d(&vmap, h.v_cache, ty, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != PKV_OK) return rc;
   } else {
   // Single box: the cache as [rows * kSub, 128 B] half-rows, boxes of 16 * kSub

@@ -646,6 +646,81 @@ def swap_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def cow_bench(args):
+    """Copy-on-write block copies in every layer's caches: one
+    pkv_copy_blocks_layers launch against one pkv_copy_blocks launch per layer.
+    Pairs have distinct sources and destinations (each block read once), so the
+    bytes are algorithmic: read and write of K and V for every pair and layer."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_166_gb300 as pkv
+    from paged_kv_cache_166_gb300 import workloads as W
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = W.WORKLOADS[args.workload]
+    L, n = args.layers, args.cow_pairs
+    B, Hkv, D = w.block_size, w.num_kv_heads, w.head_dim
+    dt = "bf16" if w.dtype == "f32" else w.dtype
+    NB = 2 * n + 16
+    rng = np.random.default_rng(w.seed)
+    perm = rng.permutation(NB)
+    pairs = torch.from_numpy(np.stack([perm[:n], perm[n:2 * n]], 1).astype(np.int32)).to(device)
+    kc = [torch.empty((NB, Hkv, B, D), dtype=W.torch_dtype(dt), device=device) for _ in range(L)]
+    vc = [torch.empty_like(kc[0]) for _ in range(L)]
+    for l in range(L):
+        W.fill_normal_(kc[l], w.seed + l, W.STREAM_K_POOL)
+        W.fill_normal_(vc[l], w.seed + l, W.STREAM_V_POOL)
+    block_bytes = kc[0][0].numel() * kc[0].element_size()
+    moved = 2 * 2 * L * n * block_bytes          # K and V, read and written
+    flush = L2Flush(device)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            flush()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    def per_layer():
+        for l in range(L):
+            pkv.paged_copy_blocks(kc[l], vc[l], pairs)
+
+    with ClockSampler(0) as clocks:
+        clocks.mark("t0")
+        t_one = timed(lambda: pkv.paged_copy_blocks_layers(kc, vc, pairs))
+        clocks.mark("t1")
+        t_per = timed(per_layer)
+    gbs = lambda ms: moved / (ms * 1e-3) / 1e9
+    peak, peak_kind = measured_peak()
+    line = {
+        "metric": "copy-on-write block copy GB/s (K and V of every layer, read + written)",
+        "value": round(gbs(t_one), 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_one, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": f"{w.name} shape: {L} layers, {n} pairs with distinct source and "
+                               f"destination blocks of {block_bytes} B per cache, pool {NB} blocks",
+                   "op": "pkv_copy_blocks_layers (one launch)", "l2": L2Flush.LABEL},
+        "per_layer_launches": {"ms": round(t_per, 4), "gbs": round(gbs(t_per), 1),
+                               "launches": L},
+        "roofline": {"bound": "hbm", "achieved": round(gbs(t_one), 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(gbs(t_one) / peak, 4), "traffic": None,
+                     "kernel": "copy_blocks_layers_kernel",
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind}; copy, read + write)"},
+        "clocks": clocks.summary(getattr(clocks, "t0", None), getattr(clocks, "t1", None)),
+        "gpu_launches": args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def prefill_bench(args):
     """Paged prefill: every sequence's prompt processed in one causal pass (or, with
     --chunk C, its last C positions as a chunk over the rest of its context) over
@@ -838,9 +913,13 @@ def main():
     ap.add_argument("--num-warps", type=int, default=0)
     ap.add_argument("--batched", type=int, default=1,
                     help="allocator bench: one batched append call per decode step (1) or one per sequence (0)")
-    ap.add_argument("--op", choices=["decode", "swap", "prefill", "allocator"], default="decode",
+    ap.add_argument("--op", choices=["decode", "swap", "prefill", "allocator", "cow"],
+                    default="decode",
                     help="decode: the decode step (default); swap: blocks to host and back; "
-                         "prefill: causal prefill attention")
+                         "prefill: causal prefill attention; allocator: the host block manager; "
+                         "cow: copy-on-write block copies in every layer's caches")
+    ap.add_argument("--layers", type=int, default=32, help="layers of the cow op")
+    ap.add_argument("--cow-pairs", type=int, default=256, help="copy pairs of the cow op")
     ap.add_argument("--prefill-seqs", type=int, default=16)
     ap.add_argument("--prefill-len", type=int, default=2048)
     ap.add_argument("--chunk", type=int, default=0, help="prefill chunk (0: the whole prompt)")
@@ -867,6 +946,9 @@ def main():
         return
     if args.op == "allocator":
         allocator_bench(args)
+        return
+    if args.op == "cow":
+        cow_bench(args)
         return
     (reference if args.impl == "reference" else native)(args)
 

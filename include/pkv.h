@@ -467,6 +467,25 @@ int pkv_decode_step_int8(const void* q, const void* k_new, const void* v_new, vo
 int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, int32_t num_pairs,
                     int32_t num_blocks, int64_t block_elems, int32_t dtype, void* stream);
 
+/*
+ * pkv_copy_blocks_layers — pkv_copy_blocks for the caches of num_layers layers
+ * in one launch.  A physical block id names the same block in every layer's
+ * tensors (section "Copy-on-Write for Beam Search and Parallel Sampling": the
+ * copy is of the block's content, which spans all layers), so each pair is
+ * copied in every layer.
+ *
+ * k_caches, v_caches  HOST arrays of num_layers device pointers, layer l's K and
+ *               V cache; every layer's caches have the same shape and dtype
+ *               (num_blocks blocks of block_elems elements), each 16-byte aligned.
+ * The other arguments, the skipping of out-of-range pairs and the unspecified
+ * cases are those of pkv_copy_blocks.  1 <= num_layers <= 128.  The arrays are
+ * read before the call returns.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+int pkv_copy_blocks_layers(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                           const int32_t* src_dst_pairs, int32_t num_pairs, int32_t num_blocks,
+                           int64_t block_elems, int32_t dtype, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Swapping blocks to host memory                                             */
 /* ------------------------------------------------------------------------- */

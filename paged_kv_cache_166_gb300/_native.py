@@ -50,6 +50,7 @@ SIGNATURES = {
                                                            _i32, _i32, _i32, _i32, _f, _p, _i32,
                                                            _i32, _p]),
     "pkv_copy_blocks": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i64, _i32, _p]),
+    "pkv_copy_blocks_layers": (ctypes.c_int, [_p, _p, _i32, _p, _i32, _i32, _i64, _i32, _p]),
     "pkv_prefill_attention": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32,
                                              _i32, _i32, _i32, _f, _p, _p, _i32, _p]),
     "pkv_swap_out_blocks": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i64, _p, _p, _p]),

@@ -31,6 +31,10 @@ int cuda_fail(cudaError_t e, const char* what);
     if (e_ != cudaSuccess) return ::pkv::cuda_fail(e_, #call); \
   } while (0)
 
+// Layers one pkv_copy_blocks_layers launch takes (their cache pointers travel as
+// kernel parameters: 2 x 128 x 8 bytes).
+constexpr int kMaxCopyLayers = 128;
+
 // Number of SMs of the current device (cached per device).
 int device_sm_count(int* sms, int* device);
 

@@ -61,6 +61,36 @@ __global__ void copy_blocks_kernel(uint4* __restrict__ kc, uint4* __restrict__ v
   }
 }
 
+// The same copies in every layer's caches at once: a block id indexes the same
+// block in each layer's tensors, so a copy-on-write pair applies to all of them.
+// Work item i is vector c of pair p in layer l, layer outermost, so consecutive
+// threads move consecutive bytes of one block.
+struct LayerCaches {
+  uint4* k[kMaxCopyLayers];
+  uint4* v[kMaxCopyLayers];
+};
+
+__global__ void copy_blocks_layers_kernel(const __grid_constant__ LayerCaches caches, int32_t L,
+                                          const int32_t* __restrict__ pairs, int32_t n,
+                                          int32_t NB, int64_t block_vecs) {
+  const int64_t per_layer = static_cast<int64_t>(n) * block_vecs;
+  const int64_t total = per_layer * L;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int32_t l = static_cast<int32_t>(i / per_layer);
+    const int64_t r = i - l * per_layer;
+    const int64_t p = r / block_vecs;
+    const int64_t c = r - p * block_vecs;
+    const int32_t src = __ldg(pairs + 2 * p), dst = __ldg(pairs + 2 * p + 1);
+    if (src < 0 || src >= NB || dst < 0 || dst >= NB) continue;
+    uint4* const kc = caches.k[l];
+    uint4* const vc = caches.v[l];
+    kc[dst * block_vecs + c] = kc[src * block_vecs + c];
+    vc[dst * block_vecs + c] = vc[src * block_vecs + c];
+  }
+}
+
 // Decode-step cache write: sequence s's new token is its position t - 1, t = ctx[s];
 // its slot comes from the block table, slot = table[s][(t-1) / B] * B + (t-1) % B
 // ("What is paged attention?", section "How it works"), and its rows of every KV
@@ -476,6 +506,37 @@ int pkv_copy_blocks(void* k_cache, void* v_cache, const int32_t* src_dst_pairs, 
                        static_cast<cudaStream_t>(stream)>>>(
       static_cast<uint4*>(k_cache), static_cast<uint4*>(v_cache), src_dst_pairs, num_pairs,
       num_blocks, block_vecs);
+  PKV_CUDA(cudaGetLastError());
+  return ok();
+}
+
+int pkv_copy_blocks_layers(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                           const int32_t* src_dst_pairs, int32_t num_pairs, int32_t num_blocks,
+                           int64_t block_elems, int32_t dtype, void* stream) {
+  const int elt = element_bytes(dtype);
+  PKV_REQUIRE(elt != 0, PKV_ERR_DTYPE, "unknown dtype %d", dtype);
+  PKV_REQUIRE(num_layers >= 1 && num_layers <= kMaxCopyLayers, PKV_ERR_UNSUPPORTED,
+              "num_layers %d outside [1, %d]", num_layers, kMaxCopyLayers);
+  PKV_REQUIRE(num_pairs >= 0 && num_blocks > 0 && block_elems > 0, PKV_ERR_INVALID_ARG,
+              "bad sizes");
+  PKV_REQUIRE((block_elems * elt) % 16 == 0, PKV_ERR_INVALID_ARG,
+              "block_elems * element size must be a multiple of 16 bytes");
+  PKV_REQUIRE(k_caches && v_caches, PKV_ERR_INVALID_ARG, "NULL cache list");
+  LayerCaches caches{};
+  for (int l = 0; l < num_layers; ++l) {
+    PKV_REQUIRE(k_caches[l] && v_caches[l], PKV_ERR_INVALID_ARG, "NULL cache of layer %d", l);
+    PKV_REQUIRE(aligned(k_caches[l], 16) && aligned(v_caches[l], 16), PKV_ERR_INVALID_ARG,
+                "caches of layer %d must be 16-byte aligned", l);
+    caches.k[l] = static_cast<uint4*>(k_caches[l]);
+    caches.v[l] = static_cast<uint4*>(v_caches[l]);
+  }
+  if (num_pairs == 0) return ok();
+  PKV_REQUIRE(src_dst_pairs, PKV_ERR_INVALID_ARG, "NULL pointer");
+  const int64_t block_vecs = block_elems * elt / 16;
+  const int threads = 256;
+  copy_blocks_layers_kernel<<<grid_for(num_layers * num_pairs * block_vecs, threads), threads,
+                              0, static_cast<cudaStream_t>(stream)>>>(
+      caches, num_layers, src_dst_pairs, num_pairs, num_blocks, block_vecs);
   PKV_CUDA(cudaGetLastError());
   return ok();
 }

@@ -399,6 +399,36 @@ def decode_status(workspace: torch.Tensor) -> int:
     return v.value
 
 
+def _copy_code(cache: torch.Tensor) -> int:
+    if cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
+        return N.PKV_FP8_E4M3
+    if cache.dtype == torch.int8:
+        return N.PKV_INT8
+    return dtype_code(cache)
+
+
+def paged_copy_blocks_layers(k_caches, v_caches, src_dst_pairs: torch.Tensor) -> None:
+    """Copy whole blocks src -> dst in every layer's K and V caches, one launch
+    (lists of per-layer caches of one shape; pairs [n, 2] int32 on their device)."""
+    k_caches, v_caches = list(k_caches), list(v_caches)
+    if not k_caches or len(k_caches) != len(v_caches):
+        raise ValueError("one K and one V cache per layer, at least one layer")
+    dev = _check_cuda(*k_caches, *v_caches, src_dst_pairs)
+    _check_index(src_dst_pairs, "src_dst_pairs")
+    n = src_dst_pairs.numel() // 2
+    if src_dst_pairs.numel() != 2 * n:
+        raise ValueError("src_dst_pairs must hold pairs")
+    ref = k_caches[0]
+    for c in k_caches + v_caches:
+        if c.shape != ref.shape or c.dtype != ref.dtype:
+            raise ValueError("every layer's caches must have one shape and dtype")
+    L = len(k_caches)
+    kp = (ctypes.c_void_p * L)(*[c.data_ptr() for c in k_caches])
+    vp = (ctypes.c_void_p * L)(*[c.data_ptr() for c in v_caches])
+    N.check(N.lib().pkv_copy_blocks_layers(kp, vp, L, src_dst_pairs.data_ptr(), n, ref.shape[0],
+                                           ref[0].numel(), _copy_code(ref), _stream(dev)))
+
+
 def paged_copy_blocks(k_cache: torch.Tensor, v_cache: torch.Tensor,
                       src_dst_pairs: torch.Tensor) -> None:
     """Copy whole blocks src -> dst (pairs [n, 2] int32 on the caches' device)."""

@@ -106,3 +106,55 @@ def test_copy_blocks_bit_exact(dtype):
     cache_ops.copy_blocks(kh, vh, valid)
     assert np.array_equal(kd.float().cpu().numpy(), kh)
     assert np.array_equal(vd.float().cpu().numpy(), vh)
+
+
+@pytest.mark.parametrize("dtype,L", [(torch.float16, 1), (torch.bfloat16, 5), (torch.uint8, 3),
+                                     (torch.int8, 2), (torch.bfloat16, 128)])
+def test_copy_blocks_layers_bit_exact(dtype, L):
+    """Every layer's caches equal the oracle's per-layer copies, bit for bit, and
+    equal L single-layer calls; pairs out of the pool are skipped in every layer."""
+    import paged_kv_cache_166_gb300 as pkv
+    g = torch.Generator().manual_seed(5 + L)
+    NB, Hkv, B, D = 24, 4, 16, 64
+    if dtype in (torch.uint8, torch.int8):
+        lo, hi = (0, 256) if dtype == torch.uint8 else (-128, 128)
+        make = lambda: torch.randint(lo, hi, (NB, Hkv, B, D), generator=g, dtype=dtype)
+    else:
+        make = lambda: torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    kh = [make() for _ in range(L)]
+    vh = [make() for _ in range(L)]
+    perm = torch.randperm(NB, generator=g).numpy()
+    pairs = np.stack([perm[:8], perm[8:16]], axis=1).astype(np.int32)
+    pairs = np.concatenate([pairs, [[NB, 3], [2, -1]]]).astype(np.int32)
+    kd = [t.cuda() for t in kh]
+    vd = [t.cuda() for t in vh]
+    ks = [t.clone() for t in kd]
+    vs = [t.clone() for t in vd]
+    pd = torch.from_numpy(pairs).cuda()
+    pkv.paged_copy_blocks_layers(kd, vd, pd)
+    for l in range(L):
+        pkv.paged_copy_blocks(ks[l], vs[l], pd)
+    torch.cuda.synchronize()
+    valid = pairs[(pairs >= 0).all(1) & (pairs < NB).all(1)]
+    raw = lambda t: (t.view(torch.int16) if t.element_size() == 2 else t).cpu().numpy()
+    for l in range(L):
+        ko, vo = raw(kh[l]).copy(), raw(vh[l]).copy()
+        cache_ops.copy_blocks(ko, vo, valid)
+        assert np.array_equal(raw(kd[l]), ko)
+        assert np.array_equal(raw(vd[l]), vo)
+        assert np.array_equal(raw(kd[l]), raw(ks[l])) and np.array_equal(raw(vd[l]), raw(vs[l]))
+
+
+def test_copy_blocks_layers_refusals():
+    import paged_kv_cache_166_gb300 as pkv
+    kc = [torch.zeros(4, 2, 16, 64, dtype=torch.float16, device="cuda") for _ in range(129)]
+    pairs = torch.tensor([[0, 1]], dtype=torch.int32, device="cuda")
+    with pytest.raises(pkv.PkvError):
+        pkv.paged_copy_blocks_layers(kc, kc, pairs)        # more than 128 layers
+    with pytest.raises(ValueError):
+        pkv.paged_copy_blocks_layers(kc[:2], kc[:1], pairs)  # K and V lists differ
+    odd = torch.zeros(5, 2, 16, 64, dtype=torch.float16, device="cuda")
+    with pytest.raises(ValueError):
+        pkv.paged_copy_blocks_layers([kc[0], odd], [kc[1], kc[2]], pairs)
+    pkv.paged_copy_blocks_layers(kc[:3], kc[3:6], pairs[:0])   # no pairs: nothing to do
+    torch.cuda.synchronize()

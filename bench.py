@@ -721,6 +721,92 @@ def cow_bench(args):
     print(json.dumps(line), flush=True)
 
 
+def swap_layers_bench(args):
+    """Preempting one sequence in every layer: its blocks of all L layers to pinned
+    host memory and back, one launch each way, against one launch per layer and
+    against a contiguous copy of the same bytes (the link's rate)."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_166_gb300 as pkv
+    from paged_kv_cache_166_gb300 import workloads as W
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w = W.WORKLOADS[args.workload]
+    L, P = args.layers, args.prefill_len
+    B, Hkv, D = w.block_size, w.num_kv_heads, w.head_dim
+    dt = "bf16" if w.dtype == "f32" else w.dtype
+    n = -(-P // B)
+    NB = 2 * n + 16
+    rng = np.random.default_rng(w.seed)
+    ids = torch.from_numpy(rng.permutation(NB)[:n].astype(np.int32)).to(device)
+    kc = [torch.empty((NB, Hkv, B, D), dtype=W.torch_dtype(dt), device=device) for _ in range(L)]
+    vc = [torch.empty_like(kc[0]) for _ in range(L)]
+    for l in range(L):
+        W.fill_normal_(kc[l], w.seed + l, W.STREAM_K_POOL)
+        W.fill_normal_(vc[l], w.seed + l, W.STREAM_V_POOL)
+    bb = kc[0][0].numel() * kc[0].element_size()
+    moved = 2 * L * n * bb                        # K and V, one direction
+    hk = torch.empty((L * n * bb,), dtype=torch.uint8).pin_memory()
+    hv = torch.empty_like(hk).pin_memory()
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def timed(fn):
+        ts = []
+        for i in range(args.warmup + args.steps):
+            torch.cuda.synchronize()
+            e0.record(stream)
+            fn()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+        return float(np.median(ts))
+
+    def per_layer(out):
+        for l in range(L):
+            hk_l, hv_l = hk[l * n * bb:(l + 1) * n * bb], hv[l * n * bb:(l + 1) * n * bb]
+            if out:
+                pkv.paged_swap_out(kc[l], vc[l], ids, hk_l, hv_l)
+            else:
+                pkv.paged_swap_in(hk_l, hv_l, ids, kc[l], vc[l])
+
+    t_out = timed(lambda: pkv.paged_swap_out_layers(kc, vc, ids, hk, hv))
+    t_in = timed(lambda: pkv.paged_swap_in_layers(hk, hv, ids, kc, vc))
+    p_out = timed(lambda: per_layer(True))
+    p_in = timed(lambda: per_layer(False))
+    dbuf = torch.empty(moved, dtype=torch.uint8, device=device)
+    hbuf = torch.empty(moved, dtype=torch.uint8).pin_memory()
+    c_out = timed(lambda: hbuf.copy_(dbuf, non_blocking=True))
+    c_in = timed(lambda: dbuf.copy_(hbuf, non_blocking=True))
+    gbs = lambda ms: moved / (ms * 1e-3) / 1e9
+    value = 2 * moved / ((t_out + t_in) * 1e-3) / 1e9
+    peak = 2 * moved / ((c_out + c_in) * 1e-3) / 1e9
+    line = {
+        "metric": "swap GB/s: one sequence's K/V blocks of every layer to pinned host memory "
+                  "and back",
+        "value": round(value, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(t_out + t_in, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": dt, "data": "synthetic",
+        "config": {"workload": f"{w.name} shape: {L} layers, one {P}-token sequence ({n} blocks "
+                               f"of {bb} B per cache and layer, {moved / 1e6:.1f} MB each way)",
+                   "op": "paged_swap_out_layers then paged_swap_in_layers (one launch each)"},
+        "swap_out": {"ms": round(t_out, 4), "gbs": round(gbs(t_out), 1)},
+        "swap_in": {"ms": round(t_in, 4), "gbs": round(gbs(t_in), 1)},
+        "per_layer_launches": {"ms": round(p_out + p_in, 4),
+                               "gbs": round(2 * moved / ((p_out + p_in) * 1e-3) / 1e9, 1),
+                               "launches": 2 * L},
+        "roofline": {"bound": "link", "achieved": round(value, 1), "peak": round(peak, 1),
+                     "unit": "GB/s", "frac": round(value / peak, 4), "traffic": None,
+                     "peak_source": "measured in this run: contiguous cudaMemcpyAsync of the "
+                                    "same bytes device->pinned host and back"},
+        "gpu_launches": 2 * args.steps,
+    }
+    print(json.dumps(line), flush=True)
+
+
 def prefill_bench(args):
     """Paged prefill: every sequence's prompt processed in one causal pass (or, with
     --chunk C, its last C positions as a chunk over the rest of its context) over
@@ -913,12 +999,15 @@ def main():
     ap.add_argument("--num-warps", type=int, default=0)
     ap.add_argument("--batched", type=int, default=1,
                     help="allocator bench: one batched append call per decode step (1) or one per sequence (0)")
-    ap.add_argument("--op", choices=["decode", "swap", "prefill", "allocator", "cow"],
+    ap.add_argument("--op", choices=["decode", "swap", "prefill", "allocator", "cow",
+                                     "swap_layers"],
                     default="decode",
                     help="decode: the decode step (default); swap: blocks to host and back; "
                          "prefill: causal prefill attention; allocator: the host block manager; "
-                         "cow: copy-on-write block copies in every layer's caches")
-    ap.add_argument("--layers", type=int, default=32, help="layers of the cow op")
+                         "cow: copy-on-write block copies in every layer's caches; "
+                         "swap_layers: one sequence (--prefill-len tokens) swapped in every "
+                         "layer")
+    ap.add_argument("--layers", type=int, default=32, help="layers of the cow and swap_layers ops")
     ap.add_argument("--cow-pairs", type=int, default=256, help="copy pairs of the cow op")
     ap.add_argument("--prefill-seqs", type=int, default=16)
     ap.add_argument("--prefill-len", type=int, default=2048)
@@ -949,6 +1038,9 @@ def main():
         return
     if args.op == "cow":
         cow_bench(args)
+        return
+    if args.op == "swap_layers":
+        swap_layers_bench(args)
         return
     (reference if args.impl == "reference" else native)(args)
 

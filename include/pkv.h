@@ -516,6 +516,28 @@ int pkv_swap_in_blocks(const void* host_k, const void* host_v, const int32_t* bl
                        int32_t num_ids, int32_t num_blocks, int64_t block_bytes, void* k_cache,
                        void* v_cache, void* stream);
 
+/*
+ * pkv_swap_out_blocks_layers / pkv_swap_in_blocks_layers — the same copies for
+ * the caches of num_layers layers in one launch (a block id names the same block
+ * in every layer's tensors, so preempting a sequence moves its blocks in all of
+ * them).  host_k and host_v hold the layers one after another: layer l's copy of
+ * block_ids[i] is host block l * num_ids + i (bytes [(l * num_ids + i) *
+ * block_bytes, ... + block_bytes)), so each buffer needs num_layers * num_ids *
+ * block_bytes bytes.  k_caches, v_caches: HOST arrays of num_layers device
+ * pointers, every layer's caches of one shape, each 16-byte aligned; read before
+ * the call returns.  1 <= num_layers <= 128.  Everything else as
+ * pkv_swap_out_blocks / pkv_swap_in_blocks.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
+ */
+int pkv_swap_out_blocks_layers(const void* const* k_caches, const void* const* v_caches,
+                               int32_t num_layers, const int32_t* block_ids, int32_t num_ids,
+                               int32_t num_blocks, int64_t block_bytes, void* host_k,
+                               void* host_v, void* stream);
+int pkv_swap_in_blocks_layers(const void* host_k, const void* host_v, const int32_t* block_ids,
+                              int32_t num_ids, int32_t num_blocks, int64_t block_bytes,
+                              void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                              void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Host block manager                                                         */
 /* ------------------------------------------------------------------------- */

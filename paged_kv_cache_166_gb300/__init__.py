@@ -14,7 +14,8 @@ Public API (all device work runs in libpkv.so's sm_103a kernels):
   ``paged_decode_attention_fp8``, ``paged_decode_step_fp8``; the int8 cache:
   ``paged_kv_write_int8``, ``paged_decode_attention_int8``, ``paged_decode_step_int8``
 * ``paged_swap_out`` / ``paged_swap_in`` — blocks to and from pinned host memory
-  (preemption by swapping, with ``BlockAllocator.swap_out`` / ``swap_in``)
+  (preemption by swapping, with ``BlockAllocator.swap_out`` / ``swap_in``);
+  ``paged_swap_out_layers`` / ``paged_swap_in_layers`` — every layer's caches, one launch
 * ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free)
 
 The library is loaded on first use; importing this package needs no GPU.
@@ -29,7 +30,7 @@ def __getattr__(name):
     if name in ("paged_kv_write", "paged_decode_attention", "paged_decode_step",
                 "paged_copy_blocks", "paged_copy_blocks_layers", "paged_kv_write_fp8", "paged_decode_attention_fp8",
                 "paged_decode_step_fp8", "paged_kv_write_int8", "paged_decode_attention_int8",
-                "paged_decode_step_int8", "paged_swap_out", "paged_swap_in",
+                "paged_decode_step_int8", "paged_swap_out", "paged_swap_in", "paged_swap_out_layers", "paged_swap_in_layers",
                 "paged_prefill_attention",
                 "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
         from . import ops

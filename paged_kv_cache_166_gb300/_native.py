@@ -55,6 +55,10 @@ SIGNATURES = {
                                              _i32, _i32, _i32, _f, _p, _p, _i32, _p]),
     "pkv_swap_out_blocks": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i64, _p, _p, _p]),
     "pkv_swap_in_blocks": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i64, _p, _p, _p]),
+    "pkv_swap_out_blocks_layers": (ctypes.c_int, [_p, _p, _i32, _p, _i32, _i32, _i64, _p, _p,
+                                                  _p]),
+    "pkv_swap_in_blocks_layers": (ctypes.c_int, [_p, _p, _p, _i32, _i32, _i64, _p, _p, _i32,
+                                                 _p]),
     "pkv_seq_swap_out": (ctypes.c_int, [_p, _i32, _pi32, _i32, _pi32]),
     "pkv_seq_swap_in": (ctypes.c_int, [_p, _i32, _pi32, _i32, _pi32]),
     "pkv_kv_write_fp8": (ctypes.c_int, [_p, _p, _p, _i32, _p, _p, _p, _p, _i32, _i32, _i32, _i32,

@@ -349,6 +349,72 @@ int host_buffer_device_ptr(const void* host, void** dev_ptr) {
   return PKV_OK;
 }
 
+// Swapping of every layer's caches in one launch: host buffer of layer l holds its
+// n blocks at [l * n, (l + 1) * n) (layer-major), so layer l's block i of the id
+// list is host block l * n + i.  Layer outermost, as in the multi-layer copy.
+__global__ void swap_blocks_layers_kernel(const __grid_constant__ LayerCaches caches, int32_t L,
+                                          uint4* __restrict__ host_k, uint4* __restrict__ host_v,
+                                          const int32_t* __restrict__ ids, int32_t n, int32_t NB,
+                                          int64_t block_vecs, bool to_host) {
+  const int64_t per_layer = static_cast<int64_t>(n) * block_vecs;
+  const int64_t total = per_layer * L;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+       i += stride) {
+    const int32_t l = static_cast<int32_t>(i / per_layer);
+    const int64_t r = i - l * per_layer;
+    const int64_t p = r / block_vecs;
+    const int64_t c = r - p * block_vecs;
+    const int32_t b = __ldg(ids + p);
+    if (b < 0 || b >= NB) continue;
+    const int64_t cache_at = static_cast<int64_t>(b) * block_vecs + c;
+    uint4* const kc = caches.k[l];
+    uint4* const vc = caches.v[l];
+    if (to_host) {
+      host_k[i] = __ldcs(kc + cache_at);
+      host_v[i] = __ldcs(vc + cache_at);
+    } else {
+      kc[cache_at] = __ldcs(host_k + i);
+      vc[cache_at] = __ldcs(host_v + i);
+    }
+  }
+}
+
+int launch_swap_layers(const void* const* k_caches, const void* const* v_caches, int32_t L,
+                       void* host_k, void* host_v, const int32_t* ids, int32_t n, int32_t NB,
+                       int64_t block_bytes, bool to_host, void* stream) {
+  PKV_REQUIRE(L >= 1 && L <= kMaxCopyLayers, PKV_ERR_UNSUPPORTED, "num_layers %d outside [1, %d]",
+              L, kMaxCopyLayers);
+  PKV_REQUIRE(n >= 0 && NB > 0 && block_bytes > 0 && block_bytes % 16 == 0, PKV_ERR_INVALID_ARG,
+              "bad sizes (block_bytes must be a positive multiple of 16)");
+  PKV_REQUIRE(k_caches && v_caches, PKV_ERR_INVALID_ARG, "NULL cache list");
+  LayerCaches caches{};
+  for (int l = 0; l < L; ++l) {
+    PKV_REQUIRE(k_caches[l] && v_caches[l], PKV_ERR_INVALID_ARG, "NULL cache of layer %d", l);
+    PKV_REQUIRE(aligned(k_caches[l], 16) && aligned(v_caches[l], 16), PKV_ERR_INVALID_ARG,
+                "caches of layer %d must be 16-byte aligned", l);
+    caches.k[l] = static_cast<uint4*>(const_cast<void*>(k_caches[l]));
+    caches.v[l] = static_cast<uint4*>(const_cast<void*>(v_caches[l]));
+  }
+  if (n == 0) return PKV_OK;
+  PKV_REQUIRE(host_k && host_v && ids, PKV_ERR_INVALID_ARG, "NULL pointer");
+  PKV_REQUIRE(aligned(host_k, 16) && aligned(host_v, 16), PKV_ERR_INVALID_ARG,
+              "host buffers must be 16-byte aligned");
+  void *dk = nullptr, *dv = nullptr;
+  int rc = host_buffer_device_ptr(host_k, &dk);
+  if (rc != PKV_OK) return rc;
+  rc = host_buffer_device_ptr(host_v, &dv);
+  if (rc != PKV_OK) return rc;
+  const int64_t block_vecs = block_bytes / 16;
+  const int threads = 256;
+  swap_blocks_layers_kernel<<<grid_for(static_cast<int64_t>(L) * n * block_vecs, threads), threads,
+                              0, static_cast<cudaStream_t>(stream)>>>(
+      caches, L, static_cast<uint4*>(dk), static_cast<uint4*>(dv), ids, n, NB, block_vecs,
+      to_host);
+  PKV_CUDA(cudaGetLastError());
+  return PKV_OK;
+}
+
 int launch_swap(const void* src_k, const void* src_v, void* dst_k, void* dst_v,
                 const int32_t* ids, int32_t n, int32_t NB, int64_t block_bytes, bool to_host,
                 void* stream) {
@@ -477,6 +543,26 @@ int pkv_swap_out_blocks(const void* k_cache, const void* v_cache, const int32_t*
                         void* host_v, void* stream) {
   const int rc = launch_swap(k_cache, v_cache, host_k, host_v, block_ids, num_ids, num_blocks,
                              block_bytes, true, stream);
+  return rc == PKV_OK ? ok() : rc;
+}
+
+int pkv_swap_out_blocks_layers(const void* const* k_caches, const void* const* v_caches,
+                               int32_t num_layers, const int32_t* block_ids, int32_t num_ids,
+                               int32_t num_blocks, int64_t block_bytes, void* host_k,
+                               void* host_v, void* stream) {
+  const int rc = launch_swap_layers(k_caches, v_caches, num_layers, host_k, host_v, block_ids,
+                                    num_ids, num_blocks, block_bytes, true, stream);
+  return rc == PKV_OK ? ok() : rc;
+}
+
+int pkv_swap_in_blocks_layers(const void* host_k, const void* host_v, const int32_t* block_ids,
+                              int32_t num_ids, int32_t num_blocks, int64_t block_bytes,
+                              void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                              void* stream) {
+  const int rc = launch_swap_layers(const_cast<const void* const*>(k_caches),
+                                    const_cast<const void* const*>(v_caches), num_layers,
+                                    const_cast<void*>(host_k), const_cast<void*>(host_v),
+                                    block_ids, num_ids, num_blocks, block_bytes, false, stream);
   return rc == PKV_OK ? ok() : rc;
 }
 

@@ -391,6 +391,51 @@ def paged_swap_in(host_k: torch.Tensor, host_v: torch.Tensor, block_ids: torch.T
                                        k_cache.data_ptr(), v_cache.data_ptr(), _stream(dev)))
 
 
+def _swap_layers_args(k_caches, v_caches, block_ids, host_k, host_v):
+    k_caches, v_caches = list(k_caches), list(v_caches)
+    if not k_caches or len(k_caches) != len(v_caches):
+        raise ValueError("one K and one V cache per layer, at least one layer")
+    ref = k_caches[0]
+    for c in k_caches + v_caches:
+        if c.shape != ref.shape or c.element_size() != ref.element_size():
+            raise ValueError("every layer's caches must hold blocks of one shape")
+    dev = _check_cuda(*k_caches, *v_caches, block_ids)
+    _check_index(block_ids, "block_ids")
+    if block_ids.dim() != 1:
+        raise ValueError("block_ids must be [n]")
+    L, n = len(k_caches), block_ids.shape[0]
+    block_bytes = ref[0].numel() * ref.element_size()
+    for h in (host_k, host_v):
+        if h.is_cuda or not h.is_pinned() or not h.is_contiguous():
+            raise ValueError("host buffers must be contiguous page-locked (pinned) CPU tensors")
+        if h.numel() * h.element_size() < L * n * block_bytes:
+            raise ValueError(f"host buffer smaller than {L} layers x {n} blocks of "
+                             f"{block_bytes} bytes")
+    kp = (ctypes.c_void_p * L)(*[c.data_ptr() for c in k_caches])
+    vp = (ctypes.c_void_p * L)(*[c.data_ptr() for c in v_caches])
+    return dev, L, n, ref.shape[0], block_bytes, kp, vp
+
+
+def paged_swap_out_layers(k_caches, v_caches, block_ids: torch.Tensor, host_k: torch.Tensor,
+                          host_v: torch.Tensor) -> None:
+    """paged_swap_out for every layer's caches in one launch: layer l's copy of
+    block block_ids[i] goes to host block l * n + i (host buffers of L * n blocks)."""
+    dev, L, n, NB, bb, kp, vp = _swap_layers_args(k_caches, v_caches, block_ids, host_k, host_v)
+    N.check(N.lib().pkv_swap_out_blocks_layers(kp, vp, L, block_ids.data_ptr(), n, NB, bb,
+                                               host_k.data_ptr(), host_v.data_ptr(),
+                                               _stream(dev)))
+
+
+def paged_swap_in_layers(host_k: torch.Tensor, host_v: torch.Tensor, block_ids: torch.Tensor,
+                         k_caches, v_caches) -> None:
+    """paged_swap_in for every layer's caches in one launch: layer l's block
+    block_ids[i] = host block l * n + i."""
+    dev, L, n, NB, bb, kp, vp = _swap_layers_args(k_caches, v_caches, block_ids, host_k, host_v)
+    N.check(N.lib().pkv_swap_in_blocks_layers(host_k.data_ptr(), host_v.data_ptr(),
+                                              block_ids.data_ptr(), n, NB, bb, kp, vp, L,
+                                              _stream(dev)))
+
+
 def decode_status(workspace: torch.Tensor) -> int:
     """Reads and clears the device status bits the decode kernels recorded."""
     v = ctypes.c_int32(0)

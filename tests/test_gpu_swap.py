@@ -11,7 +11,9 @@ memory", section "Preemption: what happens when memory runs out anyway"):
 * after the released blocks are overwritten with NaN and the sequence is
   swapped back in, decode attention over the batch is bit-identical to before
   the swap, and matches the oracle;
-* host memory the device cannot address is refused before any work is queued.
+* host memory the device cannot address is refused before any work is queued;
+* the all-layer calls move every layer's blocks to and from host block
+  l * n + i exactly as one single-layer call per layer does.
 """
 import ctypes
 
@@ -141,6 +143,86 @@ def test_swap_refuses_pageable_host_memory():
     ptr = buf.ctypes.data_as(ctypes.c_void_p)
     rc = N.lib().pkv_swap_out_blocks(kc.data_ptr(), vc.data_ptr(), ids.data_ptr(), 1, 4,
                                      16 * 64 * 2, ptr, ptr, torch.cuda.current_stream().cuda_stream)
+    assert rc == N.PKV_ERR_INVALID_ARG
+    torch.cuda.synchronize()
+    assert not buf.any()
+
+
+def _raw(t):
+    return (t.view(torch.int16) if t.element_size() == 2 else t).cpu().numpy()
+
+
+@pytest.mark.parametrize("dtype,L", [(torch.float16, 3), (torch.bfloat16, 5), (torch.uint8, 2)])
+def test_swap_layers_round_trip_matches_oracle(dtype, L):
+    """Every layer's blocks go to host block l * n + i in one launch (bytes equal the
+    oracle's per-layer copies and one single-layer call per layer); out-of-pool ids
+    leave their host blocks alone; swapping back in to fresh ids restores every
+    layer's blocks bit for bit and touches nothing else."""
+    g = torch.Generator().manual_seed(40 + L)
+    NB, Hkv, B, D = 16, 2, 16, 64
+    if dtype == torch.uint8:
+        make = lambda: torch.randint(0, 256, (NB, Hkv, B, D), generator=g, dtype=dtype)
+    else:
+        make = lambda: torch.randn(NB, Hkv, B, D, generator=g).to(dtype)
+    kh = [make() for _ in range(L)]
+    vh = [make() for _ in range(L)]
+    kd = [t.cuda() for t in kh]
+    vd = [t.cuda() for t in vh]
+    ids_np = np.array([7, 2, -1, 11, 0], dtype=np.int32)
+    n = len(ids_np)
+    ids = torch.from_numpy(ids_np).cuda()
+    bb = Hkv * B * D * kd[0].element_size()
+    hk = torch.full((L * n * bb,), 0x5A, dtype=torch.uint8).pin_memory()
+    hv = torch.full((L * n * bb,), 0x5A, dtype=torch.uint8).pin_memory()
+    pkv().paged_swap_out_layers(kd, vd, ids, hk, hv)
+    # the same through one single-layer call per layer
+    sk = [torch.full((n * bb,), 0x5A, dtype=torch.uint8).pin_memory() for _ in range(L)]
+    sv = [torch.full((n * bb,), 0x5A, dtype=torch.uint8).pin_memory() for _ in range(L)]
+    for l in range(L):
+        pkv().paged_swap_out(kd[l], vd[l], ids, sk[l], sv[l])
+    torch.cuda.synchronize()
+    valid = ids_np >= 0
+    for l in range(L):
+        ok_, ov_ = cache_ops.swap_out_blocks(_raw(kh[l]), _raw(vh[l]), ids_np[valid])
+        hk_l = hk[l * n * bb:(l + 1) * n * bb].numpy().reshape(n, bb)
+        hv_l = hv[l * n * bb:(l + 1) * n * bb].numpy().reshape(n, bb)
+        assert np.array_equal(hk_l[valid], ok_.reshape(valid.sum(), -1).view(np.uint8))
+        assert np.array_equal(hv_l[valid], ov_.reshape(valid.sum(), -1).view(np.uint8))
+        assert (hk_l[~valid] == 0x5A).all() and (hv_l[~valid] == 0x5A).all()
+        assert torch.equal(hk[l * n * bb:(l + 1) * n * bb], sk[l])
+        assert torch.equal(hv[l * n * bb:(l + 1) * n * bb], sv[l])
+    # back in, to fresh ids (the out-of-pool entry stays skipped)
+    new_np = np.array([1, 3, -1, 5, 9], dtype=np.int32)
+    for t in kd + vd:
+        t[torch.from_numpy(new_np[valid]).long().cuda()] = 0
+    pkv().paged_swap_in_layers(hk, hv, torch.from_numpy(new_np).cuda(), kd, vd)
+    torch.cuda.synchronize()
+    for l in range(L):
+        for src_h, got in ((kh[l], kd[l]), (vh[l], vd[l])):
+            want = _raw(src_h).copy()
+            want[new_np[valid]] = _raw(src_h)[ids_np[valid]]
+            assert np.array_equal(_raw(got), want)
+
+
+def test_swap_layers_refusals():
+    from paged_kv_cache_166_gb300 import _native as N
+    kc = [torch.zeros((4, 1, 16, 64), dtype=torch.float16, device="cuda") for _ in range(129)]
+    ids = torch.tensor([1], dtype=torch.int32, device="cuda")
+    bb = 16 * 64 * 2
+    pinned = torch.empty((129 * bb,), dtype=torch.uint8).pin_memory()
+    with pytest.raises(pkv().PkvError):
+        pkv().paged_swap_out_layers(kc, kc, ids, pinned, pinned)     # more than 128 layers
+    pageable = torch.empty((2 * bb,), dtype=torch.uint8)
+    with pytest.raises(ValueError):
+        pkv().paged_swap_out_layers(kc[:2], kc[2:4], ids, pageable, pageable)
+    with pytest.raises(ValueError):                                  # too small for 3 layers
+        pkv().paged_swap_in_layers(pinned[:2 * bb], pinned[:2 * bb], ids, kc[:3], kc[3:6])
+    buf = np.zeros(2 * bb, dtype=np.uint8)                           # plain host memory
+    ptr = buf.ctypes.data_as(ctypes.c_void_p)
+    kp = (ctypes.c_void_p * 2)(kc[0].data_ptr(), kc[1].data_ptr())
+    vp = (ctypes.c_void_p * 2)(kc[2].data_ptr(), kc[3].data_ptr())
+    rc = N.lib().pkv_swap_out_blocks_layers(kp, vp, 2, ids.data_ptr(), 1, 4, bb, ptr, ptr,
+                                            torch.cuda.current_stream().cuda_stream)
     assert rc == N.PKV_ERR_INVALID_ARG
     torch.cuda.synchronize()
     assert not buf.any()

@@ -846,15 +846,26 @@ def prefill_bench(args):
     stream = torch.cuda.current_stream(device)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     flush = L2Flush(device)
+    step = lambda: pkv.paged_prefill_attention(q, kc, vc, tab_d, ctx_d, qstart, w.scale, out)
     ts = []
-    for i in range(args.warmup + args.steps):
-        flush()
-        e0.record(stream)
-        pkv.paged_prefill_attention(q, kc, vc, tab_d, ctx_d, qstart, w.scale, out)
-        e1.record(stream)
-        e1.synchronize()
-        if i >= args.warmup:
-            ts.append(e0.elapsed_time(e1))
+    with ClockSampler(0) as clocks:
+        # untimed soak of the same launch so that the clock samples see this load
+        clocks.mark("t0")
+        t_end = time.perf_counter() + args.soak_s
+        while time.perf_counter() < t_end:
+            for _ in range(10):
+                flush()
+                step()
+            torch.cuda.synchronize()
+        for i in range(args.warmup + args.steps):
+            flush()
+            e0.record(stream)
+            step()
+            e1.record(stream)
+            e1.synchronize()
+            if i >= args.warmup:
+                ts.append(e0.elapsed_time(e1))
+        clocks.mark("t1")
     ms = float(np.median(ts))
     tflops = flops / (ms * 1e-3) / 1e12
     try:
@@ -878,6 +889,7 @@ def prefill_bench(args):
                      if B == w.block_size else None,
                      "kernel": "prefill_tc_kernel (tcgen05 MMAs, tensor-memory accumulators)",
                      "peak_source": f"MEASURED_PEAKS.json bf16_tflops ({kind}; dense cuBLAS)"},
+        "clocks": clocks.summary(getattr(clocks, "t0", None), getattr(clocks, "t1", None)),
         "gpu_launches": args.steps,
     }
     print(json.dumps(line), flush=True)

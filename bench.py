@@ -109,18 +109,31 @@ def whole_job_gbs(bytes_per_rank: int, world: int, ms: float) -> float:
     return bytes_per_rank * world / (ms * 1e-3) / 1e9
 
 
+def code_sha(text: str) -> str:
+    """First 16 hex digits of sha256 of a C++/CUDA source with its comments removed
+    and its whitespace collapsed: unchanged by edits to comments alone."""
+    import re
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return hashlib.sha256(" ".join(text.split()).encode()).hexdigest()[:16]
+
+
 def profile_traffic(kernel_tag: str, source: str = "decode_attention.cu", workload_key=None):
     """Per-launch DRAM bytes from the committed ncu summary of this kernel, if the
-    kernel source is unchanged since it was captured (and, when given, the summary
-    was taken on the same workload)."""
+    kernel's code is unchanged since it was captured (the summary's code_sha, else
+    its whole-file source_sha) and, when given, the summary was taken on the same
+    workload."""
     path = os.path.join(ROOT, "profiles", f"{kernel_tag}.md")
     src = os.path.join(ROOT, "paged_kv_cache_166_gb300", "csrc", source)
     try:
         text = open(path).read()
-        sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
+        raw = open(src, "rb").read()
         fields = dict(l.strip("- ").split(": ", 1) for l in text.splitlines()
                       if l.startswith("- ") and ": " in l)
-        if fields.get("source_sha") != sha:
+        if "code_sha" in fields:
+            if fields["code_sha"] != code_sha(raw.decode()):
+                return None
+        elif fields.get("source_sha") != hashlib.sha256(raw).hexdigest()[:16]:
             return None
         if workload_key is not None and fields.get("workload_key") != workload_key:
             return None

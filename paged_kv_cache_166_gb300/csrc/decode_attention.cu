@@ -15,9 +15,10 @@
 //   * lane 0 issues TMA tiled loads of the step's K and V tiles (the
 //     [16, head_dim] rows of one block and one KV head are contiguous in the
 //     [num_blocks, num_kv_heads, 16, head_dim] layout of "PagedAttention: How
-//     vLLM Borrowed Virtual Memory...", section "The Custom CUDA Kernel") into a
-//     ring of shared-memory stages, with the G query rows of the group
-//     bulk-copied alongside the first tile of each (s, g);
+//     vLLM Borrowed Virtual Memory...", section "The Custom CUDA Kernel"; for
+//     16-bit caches one 4-D box per tile lands it as two 8-row groups of
+//     swizzle atoms) into a ring of shared-memory stages, with the G query rows
+//     of the group bulk-copied alongside the first tile of each (s, g);
 //   * the block-table entries of the run are prefetched 32 at a time into shared
 //     memory with cp.async, a window ahead of the loads that need them;
 //   * the stage of a step is refilled as soon as its arithmetic is done (moving
@@ -373,8 +374,9 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* pre, int S, in
 
 // ---------------------------------------------------------------------------------
 // Per-warp compute on one staged K/V tile.
-// Tile layout in shared memory: kSub sub-tiles of [16 rows x 128 B]; the 16-byte
-// chunk c of row r sits at chunk position c ^ (r & 7) (the TMA 128-byte swizzle).
+// Tile layout in shared memory (8-bit and fp32 caches): kSub sub-tiles of
+// [16 rows x 128 B]; the 16-byte chunk c of row r sits at chunk position
+// c ^ (r & 7) (the TMA 128-byte swizzle).
 // ---------------------------------------------------------------------------------
 // Single-box tiles are instead [16 * kSub half-rows x 128 B], half-row r*kSub + c
 // holding chunks 8c..8c+7 of token row r.  Grouped tiles are two groups of 8 rows,

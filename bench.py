@@ -332,36 +332,78 @@ def oracle_inputs(name: str, seqs=None):
     return w, lens, seqs, tasks
 
 
-def time_oracle(name: str, budget_s: float = 15.0, steps: int = 1):
+def _oracle_worker(conn, name, seqs):
+    """One host core: builds the oracle inputs of its sequences once, then runs the
+    oracle over all of them each time the parent says go."""
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ[var] = "1"
+    _, _, _, tasks = oracle_inputs(name, seqs)
+    conn.send("ready")
+    while conn.recv():
+        for t in tasks:
+            _oracle_task(t)
+        conn.send("done")
+    conn.close()
+
+
+def time_oracle(name: str, budget_s: float = 15.0, steps: int = 1, fill_s: float = 0.0):
     """Wall time of the oracle over a bounded sample of the workload on all host
-    cores (one single-threaded process per core, spawned)."""
+    cores: one spawned single-threaded process per core holds its share of the
+    sample (shares balanced by tokens) and runs the oracle over it on each step;
+    `steps` timed passes over the same sample, each sized to about `budget_s`, and
+    more passes while their total is under `fill_s` seconds."""
     import multiprocessing as mp
     cores = os.cpu_count() or 1
     for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ[var] = "1"
     w, lens, _, _ = oracle_inputs(name, [])
-    order = list(np.argsort(-lens))  # longest first: a sample that covers the tail
+    order = [int(s) for s in np.argsort(-lens)]  # longest first: a sample that covers the tail
+    # calibrate one core on a sequence of middle length, then fill the cores: each
+    # sequence (longest first) goes to the least loaded core if that core's share
+    # stays within the budget; at least one sequence (the shortest)
+    probe = order[len(order) // 2]
+    _, _, _, tasks = oracle_inputs(name, [probe])
+    per_tok = _oracle_task(tasks[0]) / max(1, int(lens[probe]))
+    shares, load, sample = [[] for _ in range(cores)], [0] * cores, []
+    for s in order:
+        i = int(np.argmin(load))
+        if (load[i] + int(lens[s])) * per_tok <= budget_s:
+            shares[i].append(s)
+            load[i] += int(lens[s])
+            sample.append(s)
+    if not sample:
+        sample = [order[-1]]
+        shares[0] = [order[-1]]
     ctx = mp.get_context("spawn")
-    with ctx.Pool(cores) as pool:
-        # calibrate on a few sequences, then size the sample to the budget
-        probe = order[:min(len(order), cores)]
-        _, _, _, tasks = oracle_inputs(name, probe)
-        t0 = time.perf_counter()
-        pool.map(_oracle_task, tasks)
-        per_tok = (time.perf_counter() - t0) / max(1, sum(int(lens[s]) for s in probe))
-        want_tokens = budget_s / max(per_tok, 1e-9)
-        sample, tok = [], 0
-        for s in order:
-            if tok >= want_tokens and sample:
-                break
-            sample.append(int(s))
-            tok += int(lens[s])
-        _, _, _, tasks = oracle_inputs(name, sample)
+    workers = []
+    try:
+        for sh in shares:
+            if not sh:
+                continue
+            a, b = ctx.Pipe()
+            proc = ctx.Process(target=_oracle_worker, args=(b, name, sh), daemon=True)
+            proc.start()
+            workers.append((proc, a))
+        for _, c in workers:
+            c.recv()  # inputs built
         times = []
-        for _ in range(steps):
+        while len(times) < steps or sum(times) < fill_s:
             t0 = time.perf_counter()
-            pool.map(_oracle_task, tasks)
+            for _, c in workers:
+                c.send(True)
+            for _, c in workers:
+                c.recv()
             times.append(time.perf_counter() - t0)
+    finally:
+        for proc, c in workers:
+            try:
+                c.send(False)
+            except Exception:
+                pass
+        for proc, _ in workers:
+            proc.join(timeout=10)
+            if proc.is_alive():
+                proc.terminate()
     elt = {"f32": 4, "f16": 2, "bf16": 2}[w.dtype]
     nbytes = attention_bytes(lens[sample], w.num_q_heads, w.num_kv_heads, w.head_dim, elt)
     return {"seconds": times, "bytes": nbytes, "tokens": int(lens[sample].sum()),
@@ -382,7 +424,7 @@ def native(args):
     device = torch.device("cuda", local)
 
     # the oracle pool is spawned before the first GPU call of this process
-    cpu = time_oracle(args.workload, budget_s=args.cpu_budget) if (
+    cpu = time_oracle(args.workload, budget_s=args.cpu_budget, fill_s=args.cpu_budget) if (
         rank == 0 and world == 1 and not args.no_cpu_baseline and args.kv == "native") else None
 
     import __graft_entry__
@@ -575,8 +617,10 @@ def native(args):
         line["cpu_baseline"] = {
             "value": round(cpu["bytes"] / cs / 1e9, 4), "unit": "GB/s", "cores": cpu["cores"],
             "kind": "oracle",
-            "sample": f"{cpu['num_seqs']} of {cpu['total_seqs']} sequences (longest first, "
-                      f"{cpu['tokens']} tokens), fp64 numpy oracle, one spawned process per core",
+            "sample": f"{cpu['num_seqs']} of {cpu['total_seqs']} sequences (longest first that fit "
+                      f"the budget, {cpu['tokens']} tokens) per pass, median of "
+                      f"{len(cpu['seconds'])} passes, fp64 numpy oracle, one spawned process "
+                      "per core",
             "seconds": round(cs, 3)}
     print(json.dumps(line), flush=True)
     if world > 1:
@@ -981,23 +1025,25 @@ def allocator_bench(args):
     }), flush=True)
 
 
+REF_RUN_S = 90.0   # oracle seconds of a whole reference-arm run
+
+
 def reference(args):
     world = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
     if rank != 0:
         return
-    res = None
-    times = []
-    for i in range(args.warmup + args.steps):
-        r = time_oracle(args.workload, budget_s=args.ref_budget, steps=1)
-        if i >= args.warmup:
-            times.append(r["seconds"][0])
-            res = r
+    # every step times the same bounded sample; the sample is sized so that the
+    # whole run (warm-up included) takes about REF_RUN_S seconds of oracle work
+    n = args.warmup + args.steps
+    per_step = min(args.ref_budget, REF_RUN_S / n)
+    res = time_oracle(args.workload, budget_s=per_step, steps=n)
+    times = res["seconds"][args.warmup:]
     from paged_kv_cache_166_gb300 import workloads as W
     w = W.WORKLOADS[args.workload]
     sec = float(np.mean(times))
     gbs = res["bytes"] / sec / 1e9
-    sample = (f"{res['num_seqs']} of {res['total_seqs']} sequences (longest first, "
+    sample = (f"{res['num_seqs']} of {res['total_seqs']} sequences (longest first that fit the per-step budget, "
               f"{res['tokens']} tokens) per step, fp64 numpy oracle, one spawned process per core")
     print(json.dumps({
         "impl": "reference", "metric": METRIC, "value": round(gbs, 4), "unit": "GB/s",
@@ -1046,7 +1092,9 @@ def main():
                     help="seconds of untimed steps run just before the timed ones, so that the "
                          "clock samples cover this load")
     ap.add_argument("--cpu-budget", type=float, default=10.0)
-    ap.add_argument("--ref-budget", type=float, default=5.0)
+    ap.add_argument("--ref-budget", type=float, default=5.0,
+                    help="most oracle seconds of one reference-arm step (the whole run is "
+                         "held to about 90 s)")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
     args.warmup = max(3, args.warmup)   # at least three untimed warm-up steps

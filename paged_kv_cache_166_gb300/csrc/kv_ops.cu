@@ -620,8 +620,9 @@ int pkv_copy_blocks_layers(void* const* k_caches, void* const* v_caches, int32_t
   PKV_REQUIRE(src_dst_pairs, PKV_ERR_INVALID_ARG, "NULL pointer");
   const int64_t block_vecs = block_elems * elt / 16;
   const int threads = 256;
-  copy_blocks_layers_kernel<<<grid_for(num_layers * num_pairs * block_vecs, threads), threads,
-                              0, static_cast<cudaStream_t>(stream)>>>(
+  const int64_t work = static_cast<int64_t>(num_layers) * num_pairs * block_vecs;
+  copy_blocks_layers_kernel<<<grid_for(work, threads), threads, 0,
+                              static_cast<cudaStream_t>(stream)>>>(
       caches, num_layers, src_dst_pairs, num_pairs, num_blocks, block_vecs);
   PKV_CUDA(cudaGetLastError());
   return ok();

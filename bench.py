@@ -982,10 +982,11 @@ def allocator_bench(args):
             ops += 1 + 1 + (K - 1)
         left = suf.copy()
         steps = 0
+        seq_ids = np.asarray(seqs, dtype=np.int32)
         while left.max() > 0:
             active = np.nonzero(left)[0]
             if args.batched:  # one call per decode step
-                _, cow = alloc.append_one_each([seqs[int(i)] for i in active])
+                _, cow = alloc.append_one_each(seq_ids[active])
                 cows += len(cow)
             else:
                 for i in active:

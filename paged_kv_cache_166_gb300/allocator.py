@@ -12,6 +12,12 @@ _I32P = ctypes.POINTER(ctypes.c_int32)
 
 
 def _ptr(a: np.ndarray):
+    # an int32 element passed for a POINTER(c_int32) argument is taken by reference,
+    # which ctypes does faster than building a pointer object
+    if a.nbytes == 0:
+        return None
+    if a.flags.writeable and a.flags.c_contiguous:
+        return ctypes.c_int32.from_buffer(a)
     return a.ctypes.data_as(_I32P)
 
 

@@ -44,6 +44,7 @@ def _case(seed, Hq, Hkv, D, lens, chunks, B):
     (4, 4, 32, 16, (1, 17, 40)),
     (8, 2, 16, 4, (9, 33)),
     (8, 1, 16, 8, (23, 5, 64)),
+    (4, 2, 16, 32, (31, 32, 33, 70)),
 ])
 def test_whole_prompt_matches_causal_sdpa(Hq, Hkv, D, B, lens):
     q, Ks, Vs, kc, vc, tables, qstart = _case(3, Hq, Hkv, D, lens, lens, B)
@@ -62,6 +63,8 @@ def test_whole_prompt_matches_causal_sdpa(Hq, Hkv, D, B, lens):
 @pytest.mark.parametrize("Hq,Hkv,D,B,lens,chunks", [
     (4, 2, 32, 16, (40, 100), (7, 33)),
     (8, 8, 16, 4, (9, 31, 64), (1, 31, 16)),
+    (8, 4, 16, 8, (17, 48), (9, 1)),
+    (4, 4, 16, 32, (65, 96), (33, 64)),
 ])
 def test_chunk_matches_masked_sdpa(Hq, Hkv, D, B, lens, chunks):
     q, Ks, Vs, kc, vc, tables, qstart = _case(4, Hq, Hkv, D, lens, chunks, B)

@@ -33,3 +33,32 @@ def test_every_profile_summary_parses_and_names_its_capture():
         text = open(os.path.join(ROOT, "paged_kv_cache_166_gb300", "csrc", src)).read()
         same = bench.code_sha(text) == fields["code_sha"]
         assert (got == int(fields["traffic_bytes_per_launch"])) if same else got is None, p
+
+
+def _ref_args(**kw):
+    import types
+    a = dict(workload="tiny", steps=2, warmup=3, ref_budget=0.5)
+    a.update(kw)
+    return types.SimpleNamespace(**a)
+
+
+def test_reference_arm_other_ranks_do_no_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    monkeypatch.setenv("WORLD_SIZE", "2")
+    bench.reference(_ref_args())
+    assert capsys.readouterr().out == ""
+
+
+def test_reference_arm_line(monkeypatch, capsys):
+    """The oracle arm's JSON line on the small workload: its own cpu_baseline and an
+    e2e with no host-device bytes, every pass over one bounded sample."""
+    import json
+    monkeypatch.setenv("RANK", "0")
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    bench.reference(_ref_args())
+    line = json.loads(capsys.readouterr().out.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["steps"] == 2 and line["warmup"] == 3
+    assert line["value"] > 0 and line["higher_is_better"] is True
+    assert line["cpu_baseline"]["kind"] == "oracle" and line["cpu_baseline"]["value"] == line["value"]
+    assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["e2e"]["d2h_bytes_per_step"] == 0
+    assert "4 of 4 sequences" in line["cpu_baseline"]["sample"]

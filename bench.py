@@ -953,7 +953,7 @@ def prefill_bench(args):
 
 
 def allocator_bench(args):
-    """The host block manager through the C ABI, on the shared-prefix
+    """The host block manager (allocation, fork, copy-on-write, free) through the C ABI, on the shared-prefix
     parallel-sampling workload: per prompt, create and append the 1000-token prompt,
     fork the other 7 samples, then decode — one append per sample per step in round
     robin, each first write into the shared partial block a copy-on-write — until every

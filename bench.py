@@ -953,8 +953,8 @@ def prefill_bench(args):
 
 
 def allocator_bench(args):
-    """The host block manager (allocation, fork, copy-on-write, free) through the C ABI, on the shared-prefix
-    parallel-sampling workload: per prompt, create and append the 1000-token prompt,
+    """The host block manager (allocation, fork, copy-on-write, free) through the C
+    ABI, on the shared-prefix parallel-sampling workload: per prompt, create and append the 1000-token prompt,
     fork the other 7 samples, then decode — one append per sample per step in round
     robin, each first write into the shared partial block a copy-on-write — until every
     sample has its suffix, and free all.  Host only, one thread; the figure includes the

@@ -1,6 +1,7 @@
 """Host-side tests of the C ABI (no GPU needed).
 
 * libpkv.so loads without a GPU and exports every function include/pkv.h declares,
+  the header compiles as strict C99 and a C program links and runs against it,
   each with a ctypes signature in the binding.
 * The library's block manager matches the oracle model bit for bit — tables,
   lengths, slots, copy-on-write pairs, refcounts and free counts after every
@@ -290,3 +291,44 @@ def test_append_one_each_equals_appends_in_list_order(seed):
         p.c.append_one_each([10 ** 6])
     slots, cows = p.c.append_one_each([])
     assert len(slots) == 0 and cows == []
+
+
+def test_header_is_plain_c_and_links_against_the_library(tmp_path):
+    """include/pkv.h compiles as strict C99 and every function it declares resolves
+    against libpkv.so at link time; the program then drives the block manager through
+    the C ABI alone (no Python in between)."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    names = header_functions()
+    table = ",\n".join(f"  (void (*)(void))&{n}" for n in names)
+    src = tmp_path / "abi.c"
+    src.write_text(f"""#include <stdio.h>
+#include "pkv.h"
+static void (*const fns[])(void) = {{
+{table}
+}};
+int main(void) {{
+  pkv_allocator_t* a = 0;
+  int32_t s = -1, slots[20], cow[2], ncow = -1, nfree = -1;
+  if (pkv_allocator_create(4, 16, 0, &a) != PKV_OK) return 1;
+  if (pkv_seq_create(a, &s) != PKV_OK) return 2;
+  if (pkv_seq_append(a, s, 20, slots, cow, &ncow) != PKV_OK || ncow != 0) return 3;
+  if (slots[0] != 0 || slots[15] != 15 || slots[16] != 16 || slots[19] != 19) return 4;
+  if (pkv_num_free_blocks(a, &nfree) != PKV_OK || nfree != 2) return 5;
+  if (pkv_seq_append(a, 99, 1, slots, cow, &ncow) == PKV_OK) return 6;
+  pkv_allocator_destroy(a);
+  printf("%d\\n", (int)(sizeof(fns) / sizeof(fns[0])));
+  return 0;
+}}
+""")
+    lib = os.path.join(ROOT, "paged_kv_cache_166_gb300", "libpkv.so")
+    exe = tmp_path / "abi"
+    subprocess.run([cc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror",
+                    "-I", os.path.join(ROOT, "include"), str(src), lib,
+                    "-Wl,-rpath," + os.path.dirname(lib), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True)
+    assert out.returncode == 0, out
+    assert int(out.stdout) == len(names)

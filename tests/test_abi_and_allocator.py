@@ -1,8 +1,8 @@
 """Host-side tests of the C ABI (no GPU needed).
 
 * libpkv.so loads without a GPU and exports every function include/pkv.h declares,
-  the header compiles as strict C99 and a C program links and runs against it,
-  each with a ctypes signature in the binding.
+  each with a ctypes signature in the binding; the header compiles as strict C99
+  and a C program links and runs against the library.
 * The library's block manager matches the oracle model bit for bit — tables,
   lengths, slots, copy-on-write pairs, refcounts and free counts after every
   operation — on the pages' worked examples and on seeded random operation

@@ -15,7 +15,11 @@ TEST INFRASTRUCTURE (see ``oracle/__init__.py``): never imported by the library.
   count of the measured metric: the K and V rows of the ``t`` cached tokens of
   every KV head (padded block tails are not counted), the ``ceil(t / B)``
   int32 table entries, the context length, and one query and one output row
-  per query head.
+  per query head.  With an 8-bit cache the K/V rows take one byte per element
+  while the query and output rows keep their 16-bit type ("PagedAttention —
+  how vLLM stopped wasting 80%...", FAQ "How does this relate to
+  quantization?": the cache elements are what shrink), so the query/output
+  element size is a separate argument that defaults to the cache's.
 """
 from __future__ import annotations
 
@@ -34,11 +38,12 @@ def waste_slots(t: int, block_size: int) -> int:
 
 
 def decode_bytes(context_lens, num_q_heads: int, num_kv_heads: int, head_dim: int,
-                 elem_bytes: int, block_size: int) -> int:
+                 elem_bytes: int, block_size: int, q_elem_bytes: int | None = None) -> int:
+    q_elem_bytes = elem_bytes if q_elem_bytes is None else q_elem_bytes
     total = 0
     for t in context_lens:
         t = int(t)
         total += 2 * t * num_kv_heads * head_dim * elem_bytes
         total += 4 * blocks_for(t, block_size) + 4
-        total += 2 * num_q_heads * head_dim * elem_bytes
+        total += 2 * num_q_heads * head_dim * q_elem_bytes
     return total

@@ -192,11 +192,14 @@ int pkv_decode_attention(const void* q, const void* k_cache, const void* v_cache
  * write the new token's K,V into the last block", "PagedAttention and vLLM: Virtual
  * Memory for the KV Cache", section "L2 — Mechanism"): its K and V rows are written
  * to slot(t - 1) of the caches, the slot read from block_tables, exactly as
- * pkv_kv_write with that slot would; then the attention of the step runs over the
- * updated caches.  The two launches are chained with programmatic dependent launch,
- * so the attention's prologue overlaps the write.  Output and caches are
- * bit-identical to pkv_kv_write followed by pkv_decode_attention with the same
- * num_warps.  Arguments are validated before anything is written.
+ * pkv_kv_write with that slot would; the attention of the step covers the new
+ * token.  Two launches chained with programmatic dependent launch: the write, then
+ * the attention, whose prologue (schedule, table prefetch) overlaps the write.
+ * Output and caches are bit-identical to pkv_kv_write followed by
+ * pkv_decode_attention with the same num_warps.  Sequences with t <= 0 or
+ * t > max_blocks_per_seq * block_size, and slots outside the pool, write nothing.
+ * Arguments are validated before anything is written; k_new and v_new must be
+ * non-NULL and 16-byte aligned.
  * Errors: as pkv_decode_attention.
  */
 int pkv_decode_step(const void* q, const void* k_new, const void* v_new, void* k_cache,
@@ -245,8 +248,11 @@ int pkv_decode_default_warps(int32_t head_dim, int32_t dtype, int32_t* num_warps
  * different host threads without ordering) race on it and give wrong results:
  * order them on one stream.  A request whose partial states need more than
  * PKV_STATIC_SCRATCH_BYTES (pkv_decode_workspace_size with the same head shape,
- * dtype and num_warps) is rejected with PKV_ERR_UNSUPPORTED before any work is
- * enqueued; a smaller num_warps needs less scratch.
+ * dtype and num_warps) is rejected with PKV_ERR_UNSUPPORTED; a smaller num_warps
+ * needs less scratch.  Every argument is checked before any work is enqueued, so
+ * a refused call (oversized, or anything pkv_decode_attention would refuse) writes
+ * nothing, the shared array included.  If the array's address cannot be resolved
+ * the call fails with PKV_ERR_CUDA and the next call tries again.
  */
 #define PKV_STATIC_SCRATCH_BYTES (16u << 20)
 int pkv_decode_attention_static_scratch(const void* q, const void* k_cache, const void* v_cache,

@@ -41,8 +41,9 @@
 // O^T[D x 8] += V^T P^T on the tensor cores.  fp32: CUDA-core FMA.
 //
 // The kernel is launched with programmatic stream serialisation: its prologue
-// (schedule, block-table prefetch) overlaps the tail of the preceding cache
-// write, and griddepcontrol.wait orders every K/V read after that write.
+// (schedule, block-table prefetch) overlaps the tail of the preceding cache write
+// (pkv_kv_write, or the decode step's write of each new token), and
+// griddepcontrol.wait orders every K/V read after that write.
 #include <cuda.h>
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
@@ -53,6 +54,7 @@
 #include <mutex>
 #include <type_traits>
 
+#include "decode_layout.h"
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -75,39 +77,6 @@ namespace pkv {
 #endif
 #ifndef PKV_MAX_STAGES_FP8
 #define PKV_MAX_STAGES_FP8 12
-#endif
-#ifndef PKV_EARLY_RELEASE
-#define PKV_EARLY_RELEASE 0
-#endif
-// One TMA box per K or V tile (128-byte half-row view) when head_dim * elt <= 256 B.
-#ifndef PKV_SINGLE_BOX
-#define PKV_SINGLE_BOX 0
-#endif
-// 16-bit caches: tiles stored as groups of 8 tokens (one swizzle atom per 128 B of
-// row, side by side), so that one 4-D TMA box moves a whole 16-token step, or a
-// whole 8-token block.
-#ifndef PKV_GROUPED_TILES
-#define PKV_GROUPED_TILES 1
-#endif
-#ifndef PKV_PREFETCH_TABLES
-#define PKV_PREFETCH_TABLES 1
-#endif
-// fp8 cache: widen codes to f16 with integer ops (value * 2^-8) instead of the
-// conversion instruction.
-#ifndef PKV_FP8_WIDEN_ALU
-#define PKV_FP8_WIDEN_ALU 1
-#endif
-// Read the query rows of a unit straight from global memory into registers
-// instead of copying them into each pipeline stage (always so for the fp8 cache).
-#ifndef PKV_Q_FROM_GLOBAL
-#define PKV_Q_FROM_GLOBAL 0
-#endif
-// Skip the accumulator rescale of a step whose running maxima did not change.
-#ifndef PKV_RESCALE_SKIP
-#define PKV_RESCALE_SKIP 0
-#endif
-#ifndef PKV_PARALLEL_PROLOGUE
-#define PKV_PARALLEL_PROLOGUE 1
 #endif
 // Start-up cost of a (sequence, KV head) unit in quarter steps, for group sizes
 // below 4 and from 4 up (query copy, finalise, output write).
@@ -178,50 +147,19 @@ struct Shape {
   static constexpr bool kQ8 = std::is_same<C, E4M3>::value || std::is_same<C, I8>::value;
   static constexpr int kElt = CacheBytes<C>::value;
   static constexpr int kWarpsPerCta = kQ8 ? fp8_warps_per_cta(D) : kWarps;
-  static constexpr bool kQRegs = kQ8 || PKV_Q_FROM_GLOBAL;  // no query slot per stage
+  static constexpr bool kQRegs = kQ8;  // 8-bit: q rows straight to registers, no stage slot
   static constexpr int kTileBytes = kTok * D * kElt;
   static constexpr int kSub = D * kElt / kSwizzleRow;     // sub-tiles per tile
   static constexpr int kBoxCols = kSwizzleRow / kElt;      // elements per sub-tile row
   static constexpr int kStageBytes = 2 * kTileBytes;       // K and V tile
-  // fp16/bf16 tiles up to head_dim 128 fit in registers: release the stage early
-  static constexpr bool kEarlyRelease = PKV_EARLY_RELEASE && (kElt == 2) && (D <= 128);
-  // 8-bit: K in kSub boxes of [16 rows x 128 B]; V (stored [D x 16 B]) in one box
-  // 16-bit: one 4-D box per step (or per 8-token block) into grouped tiles
-  static constexpr bool kGrouped = PKV_GROUPED_TILES && !kQ8 && kElt == 2;
-  // one box per tile: rows of the tile are viewed as kSub half-rows of 128 B
-  static constexpr bool kSingleBox = PKV_SINGLE_BOX && !kGrouped && !kQ8 && (kSub <= 2);
+  // 8-bit: K in kSub boxes of [16 rows x 128 B]; V (stored [D x 16 B]) in one box.
+  // 16-bit: tiles stored as groups of 8 tokens (one swizzle atom per 128 B of row,
+  // side by side), so that one 4-D box moves a whole step, or a whole 8-token block.
+  // fp32: kSub boxes of [16 rows x 128 B].
+  static constexpr bool kGrouped = !kQ8 && kElt == 2;
   static_assert(kSub * kSwizzleRow == D * kElt, "head_dim * elt must be a multiple of 128 B");
 };
 
-struct SmemLayout {
-  uint32_t tiles, q, bars, ids, ctx, pre, prew, scratch, total;
-};
-
-__host__ __device__ inline SmemLayout smem_layout(int stage_bytes, int stages, int q_stride,
-                                                  int S, int nw) {
-  SmemLayout L;
-  uint32_t off = 0;
-  L.tiles = off;
-  off += nw * stages * stage_bytes;
-  L.q = off;
-  off += nw * stages * q_stride;
-  off = (off + 15u) & ~15u;
-  L.bars = off;
-  off += nw * stages * 8;
-  L.ids = off;
-  off += nw * 128 * 4;  // two windows of 32 steps, up to 2 block ids per step
-  L.ctx = off;
-  off += S * 4;
-  L.pre = off;
-  off += (S + 1) * 4;
-  L.prew = off;
-  off += (S + 1) * 4;
-  off = (off + 15u) & ~15u;
-  L.scratch = off;
-  off += 2 * 32 * 4;
-  L.total = off + 1024;  // slack for aligning the tiles to 1024 B
-  return L;
-}
 
 // ---------------------------------------------------------------------------------
 // Schedule, built by every CTA from the context lengths:
@@ -378,18 +316,14 @@ __device__ __forceinline__ void advance(Cursor& c, const int32_t* pre, int S, in
 // [16 rows x 128 B]; the 16-byte chunk c of row r sits at chunk position
 // c ^ (r & 7) (the TMA 128-byte swizzle).
 // ---------------------------------------------------------------------------------
-// Single-box tiles are instead [16 * kSub half-rows x 128 B], half-row r*kSub + c
-// holding chunks 8c..8c+7 of token row r.  Grouped tiles are two groups of 8 rows,
-// each group kSub swizzle atoms [8 rows x 128 B] side by side (atom c holding
-// chunks 8c..8c+7 of its rows).
-template <int kSub, bool kSingleBox, bool kGrouped = false>
+// Grouped tiles (16-bit caches) are instead two groups of 8 rows, each group kSub
+// swizzle atoms [8 rows x 128 B] side by side (atom c holding chunks 8c..8c+7 of
+// its rows).
+template <int kSub, bool kGrouped = false>
 __device__ __forceinline__ uint32_t tile_offset(int row, int chunk16) {
   if constexpr (kGrouped) {
     return (row >> 3) * (kSub * 8 * kSwizzleRow) + (chunk16 >> 3) * (8 * kSwizzleRow) +
            (row & 7) * kSwizzleRow + (((chunk16 & 7) ^ (row & 7)) << 4);
-  } else if constexpr (kSingleBox) {
-    const int hr = row * kSub + (chunk16 >> 3);
-    return hr * kSwizzleRow + (((chunk16 & 7) ^ (hr & 7)) << 4);
   } else {
     return (chunk16 >> 3) * kSubTile + row * kSwizzleRow + (((chunk16 & 7) ^ (row & 7)) << 4);
   }
@@ -399,10 +333,8 @@ template <typename T, int D>
 struct MmaState {
   static constexpr int KS = D / 16;
   static constexpr int kSub = D * static_cast<int>(sizeof(T)) / kSwizzleRow;
-  static constexpr bool kGrouped = PKV_GROUPED_TILES;
-  static constexpr bool kSingle = PKV_SINGLE_BOX && !kGrouped && (kSub <= 2);
   static __device__ __forceinline__ uint32_t swz(uint32_t tile, int row, int chunk16) {
-    return tile + tile_offset<kSub, kSingle, kGrouped>(row, chunk16);
+    return tile + tile_offset<kSub, true>(row, chunk16);
   }
   float o[KS][4];   // O^T[d = mt*16 + gid (+8)][h = 2*tig (+1)]
   uint32_t qb[KS][2];
@@ -478,7 +410,7 @@ struct MmaState {
     l1 = l1 * al1 + (p1 + p3);
     m0 = mn0;
     m1 = mn1;
-    if (!PKV_RESCALE_SKIP || __any_sync(0xffffffffu, al0 != 1.f || al1 != 1.f)) {
+    {
 #pragma unroll
       for (int mt = 0; mt < KS; ++mt) {
         o[mt][0] *= al0;
@@ -503,20 +435,6 @@ struct MmaState {
     a[1] &= mlo;
     a[2] &= mhi;
     a[3] &= mhi;
-  }
-
-  // Whole step from registers (tile already loaded).
-  __device__ __forceinline__ void step_regs(const uint32_t (&kf)[KS][4], uint32_t (&vf)[KS][4],
-                                            int valid, float scale_log2, int lane) {
-    float x[4];
-    scores(kf, valid, scale_log2, lane, x);
-    uint32_t pb0, pb1;
-    softmax(x, pb0, pb1);
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      if (valid < kTok) mask_v(vf[mt], valid, lane);
-      ptx::mma_16816<T>(o[mt], vf[mt], pb0, pb1);
-    }
   }
 
   // Whole step reading the tile from shared memory as it goes.
@@ -629,7 +547,6 @@ struct Q8State {
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(b), "r"(0x64806480u));
     return r;
   }
-#if PKV_FP8_WIDEN_ALU
   // Bytes 0-1 (widen) or 2-3 (widen_hi) of w as an f16 pair holding value * 2^-8:
   // the E4M3 exponent and mantissa bits shifted left by 7 are exactly the f16 bits
   // of value * 2^-8 (subnormals included), and the sign moves from bit 14 to 15.
@@ -646,19 +563,6 @@ struct Q8State {
     return spread(__byte_perm(w, 0u, 0x4342));
   }
   static constexpr float kWidenScale = kInt8 ? 1.f : 256.f;
-#else
-  static __device__ __forceinline__ uint32_t widen(uint32_t two_codes) {
-    if constexpr (kInt8) return widen_i8(two_codes, 0x4140);
-    const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(
-        static_cast<__nv_fp8x2_storage_t>(two_codes & 0xffffu), __NV_E4M3);
-    return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
-  }
-  static __device__ __forceinline__ uint32_t widen_hi(uint32_t w) {
-    if constexpr (kInt8) return widen_i8(w, 0x4342);
-    return widen(w >> 16);
-  }
-  static constexpr float kWidenScale = 1.f;
-#endif
 
   __device__ __forceinline__ void reset() {
 #pragma unroll
@@ -699,7 +603,7 @@ struct Q8State {
 #pragma unroll
     for (int p = 0; p < KS / 2; ++p) {
       uint32_t w[4], a[4];
-      ptx::ldsm_x4(ktile + tile_offset<kSub, false>(krow, 2 * p + (mi >> 1)), w);
+      ptx::ldsm_x4(ktile + tile_offset<kSub>(krow, 2 * p + (mi >> 1)), w);
       a[0] = widen(w[0]);
       a[1] = widen(w[1]);
       a[2] = widen_hi(w[0]);
@@ -830,7 +734,6 @@ template <int D>
 struct FmaState {
   static constexpr int E = D / 32;  // elements of a row per lane: d = lane + 32 * e
   static constexpr int kSub = D * 4 / kSwizzleRow;
-  static constexpr bool kSingle = PKV_SINGLE_BOX && (kSub <= 2);
   float qv[kMaxGroup][E];
   float acc[kMaxGroup][E];
   float m[kMaxGroup], l[kMaxGroup];
@@ -855,7 +758,7 @@ struct FmaState {
 
   static __device__ __forceinline__ float at(const uint8_t* tile, int t, int d) {
     const int chunk = d >> 2;  // 16-byte chunk of the 128-byte row
-    return *reinterpret_cast<const float*>(tile + tile_offset<kSub, kSingle>(t, chunk) +
+    return *reinterpret_cast<const float*>(tile + tile_offset<kSub>(t, chunk) +
                                            (d & 3) * 4);
   }
 
@@ -1006,6 +909,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     decode_attention_kernel(const __grid_constant__ CUtensorMap kmap,
                             const __grid_constant__ CUtensorMap vmap, const DecodeArgs a) {
   using Sh = Shape<C, D>;
+  static_assert(Sh::kGrouped || kBlk == kTok, "8- and 32-token blocks need a 16-bit cache");
   constexpr int kIdStride = kBlk == kTok ? 1 : 2;  // block ids per step in the id windows
   const int NS = a.stages;
   extern __shared__ uint8_t smem_raw[];
@@ -1014,7 +918,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(&vmap)) : "memory");
     // The block tables are read a window at a time once the schedule is known:
     // start pulling this CTA's slice of them into L2 now (16-byte aligned interior).
-    if (PKV_PREFETCH_TABLES) {
+    {
       const uintptr_t t0 = reinterpret_cast<uintptr_t>(a.block_tables);
       const uintptr_t t1 = t0 + static_cast<uintptr_t>(a.S) * a.MAXB * sizeof(int32_t);
       const uintptr_t lo = (t0 + 15) & ~uintptr_t(15), hi = t1 & ~uintptr_t(15);
@@ -1137,12 +1041,13 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
       atomicOr(a.status, PKV_DEV_BAD_BLOCK_ID);
       return rows_total;  // a box wholly past the end: the TMA unit fills it with zeros
     };
+    const int32_t extra = need_q ? a.q_bytes : 0;
     if constexpr (Sh::kGrouped) {
       // 8-row groups of the cache: a 16-token step is one box of two groups, an
       // 8-token block one box of one group (the step's second block in group 1)
       if (kBlk != kTok && Bsz == 8) {
         ptx::mbar_arrive_expect_tx(bar, (second ? Sh::kStageBytes : Sh::kStageBytes / 2) +
-                                            (need_q ? a.q_bytes : 0));
+                                            extra);
         const int32_t g0 = row_of(id0, 0) >> 3;
         ptx::tma_load_4d(kt, &kmap, 0, 0, 0, g0, bar, policy);
         ptx::tma_load_4d(vt, &vmap, 0, 0, 0, g0, bar, policy);
@@ -1152,48 +1057,25 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
           ptx::tma_load_4d(vt + Sh::kTileBytes / 2, &vmap, 0, 0, 0, g1, bar, policy);
         }
       } else {
-        ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
+        ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + extra);
         const int32_t g = row_of(id0, (kBlk != kTok && Bsz == 32) ? (j & 1) * kTok : 0) >> 3;
         ptx::tma_load_4d(kt, &kmap, 0, 0, 0, g, bar, policy);
         ptx::tma_load_4d(vt, &vmap, 0, 0, 0, g, bar, policy);
       }
-    } else if (kBlk != kTok && Bsz == 8) {
-      // two 8-row blocks per step, into rows 0-7 and 8-15 of every sub-tile
-      ptx::mbar_arrive_expect_tx(bar, (second ? Sh::kStageBytes : Sh::kStageBytes / 2) +
-                                          (need_q ? a.q_bytes : 0));
-      const int32_t y0 = row_of(id0, 0);
-#pragma unroll
-      for (int c = 0; c < Sh::kSub; ++c) {
-        ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y0, bar, policy);
-        ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y0, bar, policy);
-      }
-      if (second) {
-        const int32_t y1 = row_of(id1, 0);
-#pragma unroll
-        for (int c = 0; c < Sh::kSub; ++c) {
-          ptx::tma_load_2d(kt + c * kSubTile + kSubTile / 2, &kmap, c * Sh::kBoxCols, y1, bar,
-                           policy);
-          ptx::tma_load_2d(vt + c * kSubTile + kSubTile / 2, &vmap, c * Sh::kBoxCols, y1, bar,
-                           policy);
-        }
-      }
     } else {
-      ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + (need_q ? a.q_bytes : 0));
-      const int32_t y = row_of(id0, (kBlk != kTok && Bsz == 32) ? (j & 1) * kTok : 0);
-      if constexpr (Sh::kSingleBox) {
-        ptx::tma_load_2d(kt, &kmap, 0, y * Sh::kSub, bar, policy);
-        ptx::tma_load_2d(vt, &vmap, 0, y * Sh::kSub, bar, policy);
+      // 8-bit and fp32 caches (16-token blocks only): kSub boxes of [16 rows x 128 B]
+      // for K; V likewise, or one box of the transposed 8-bit tile
+      ptx::mbar_arrive_expect_tx(bar, Sh::kStageBytes + extra);
+      const int32_t y = row_of(id0, 0);
+#pragma unroll
+      for (int c = 0; c < Sh::kSub; ++c)
+        ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
+      if constexpr (Sh::kQ8) {
+        ptx::tma_load_2d(vt, &vmap, 0, (y / kTok) * (D / 8), bar, policy);
       } else {
 #pragma unroll
         for (int c = 0; c < Sh::kSub; ++c)
-          ptx::tma_load_2d(kt + c * kSubTile, &kmap, c * Sh::kBoxCols, y, bar, policy);
-        if constexpr (Sh::kQ8) {
-          ptx::tma_load_2d(vt, &vmap, 0, (y / kTok) * (D / 8), bar, policy);
-        } else {
-#pragma unroll
-          for (int c = 0; c < Sh::kSub; ++c)
-            ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
-        }
+          ptx::tma_load_2d(vt + c * kSubTile, &vmap, c * Sh::kBoxCols, y, bar, policy);
       }
     }
     if (need_q) {
@@ -1221,19 +1103,15 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
 
   // Fill the ring: lanes 0..NS-1 issue the first NS steps at once, one step each.
   const int prologue = nsteps < NS ? nsteps : NS;
-  if (!PKV_PARALLEL_PROLOGUE) {
-    for (int m = 0; m < prologue; ++m) issue(m);
-  } else if (lane < prologue) {
+  if (lane < prologue) {
     const Cursor lc = cursor_at(pre, S, Hkv, f0 + lane);
     issue_copies(lane, lc.s, lc.g, lc.j, ids[kIdStride * lane],
                  kIdStride == 2 ? ids[kIdStride * lane + 1] : -1,
                  !Sh::kQRegs && ((lane == 0) || (lc.j == 0)));
   }
-  if (PKV_PARALLEL_PROLOGUE) {
-    __syncwarp();
-    p_stage = prologue == NS ? 0 : prologue;
-    if (prologue > 0) pc = cursor_at(pre, S, Hkv, min(f0 + prologue, total - 1));
-  }
+  __syncwarp();
+  p_stage = prologue == NS ? 0 : prologue;
+  if (prologue > 0) pc = cursor_at(pre, S, Hkv, min(f0 + prologue, total - 1));
 
   using State = typename std::conditional<
       Sh::kQ8, Q8State<T, C, D>,
@@ -1266,11 +1144,6 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
         st_.load_q_rows(reinterpret_cast<const T*>(a.q) +
                             (static_cast<int64_t>(cc.s) * a.Hq + cc.g * a.G) * D,
                         a.G, lane);
-      } else if constexpr (Sh::kQRegs) {
-        st_.load_q(reinterpret_cast<const uint8_t*>(
-                       reinterpret_cast<const T*>(a.q) +
-                       (static_cast<int64_t>(cc.s) * a.Hq + cc.g * a.G) * D),
-                   a.G, lane);
       } else {
         st_.load_q(qslot + c_stage * a.q_stride, a.G, lane);
       }
@@ -1280,27 +1153,15 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     }
     const int valid = (cc.j == cc.nb - 1) ? ctx_s[cc.s] - cc.j * kTok : kTok;
     const uint32_t kt = tiles + c_stage * Sh::kStageBytes;
-    if constexpr (Sh::kEarlyRelease) {
-      constexpr int KS = D / 16;
-      uint32_t kf[KS][4], vf[KS][4];
-#pragma unroll
-      for (int i = 0; i < KS; ++i) {
-        MmaState<T, D>::load_k(kt, i, lane, kf[i]);
-        MmaState<T, D>::load_v(kt + Sh::kTileBytes, i, lane, vf[i]);
-      }
-      __syncwarp();
-      if (n + NS < nsteps) issue(n + NS);
-      st_.step_regs(kf, vf, valid, a.scale_log2, lane);
+    if constexpr (sizeof(T) == 2) {
+      st_.step_smem(kt, kt + Sh::kTileBytes, valid, a.scale_log2, lane);
     } else {
-      if constexpr (sizeof(T) == 2) {
-        st_.step_smem(kt, kt + Sh::kTileBytes, valid, a.scale_log2, lane);
-      } else {
-        const uint8_t* ktp = base + (kt - base_s);
-        st_.step(ktp, ktp + Sh::kTileBytes, valid, a.scale_log2, a.G, lane);
-      }
-      __syncwarp();
-      if (n + NS < nsteps) issue(n + NS);
+      const uint8_t* ktp = base + (kt - base_s);
+      st_.step(ktp, ktp + Sh::kTileBytes, valid, a.scale_log2, a.G, lane);
     }
+    // the stage is refilled once its arithmetic is done
+    __syncwarp();
+    if (n + NS < nsteps) issue(n + NS);
     if (++c_stage == NS) { c_stage = 0; parity ^= 1u; }
     const bool unit_end = (cc.j == cc.nb - 1);
     if (unit_end || n == nsteps - 1) {
@@ -1468,7 +1329,7 @@ int validate(const HostArgs& h, int* warps_out) {
               "head_dim %d unsupported for dtype %d", h.D, h.dtype);
   PKV_REQUIRE(h.block_size == 8 || h.block_size == 16 || h.block_size == 32,
               PKV_ERR_UNSUPPORTED, "block_size %d not in {8, 16, 32}", h.block_size);
-  PKV_REQUIRE(h.block_size == kTok || (h.codes == 0 && !PKV_SINGLE_BOX && h.dtype != PKV_F32),
+  PKV_REQUIRE(h.block_size == kTok || (h.codes == 0 && h.dtype != PKV_F32),
               PKV_ERR_UNSUPPORTED, "block_size %d needs an f16 or bf16 cache", h.block_size);
   PKV_REQUIRE(h.MAXB > 0, PKV_ERR_INVALID_ARG, "max_blocks_per_seq must be positive");
   PKV_REQUIRE(static_cast<int64_t>(h.S) * h.MAXB * h.Hkv < (int64_t(1) << 31),
@@ -1543,14 +1404,19 @@ int launch_decode(const HostArgs& h, int W) {
   DecodeArgs a = device_args(h, W);
   if constexpr (Sh::kQRegs) a.q_stride = 0;  // q rows are read straight into registers
   // Deepest pipeline that fits the SM's shared memory.
-  const uint32_t fixed = smem_layout(Sh::kStageBytes, 0, a.q_stride, h.S, Sh::kWarpsPerCta).total;
+  const uint32_t fixed =
+      smem_layout(Sh::kStageBytes, 0, a.q_stride, h.S, Sh::kWarpsPerCta).total;
   const uint32_t per_stage = Sh::kWarpsPerCta * (Sh::kStageBytes + a.q_stride + 8);
   int stages = optin > static_cast<int>(fixed) ? static_cast<int>((optin - fixed) / per_stage) : 0;
   const int max_stages = Sh::kQ8 ? kMaxStagesFp8 : kMaxStages;
   stages = stages > max_stages ? max_stages : stages;
   PKV_REQUIRE(stages >= 2, PKV_ERR_UNSUPPORTED, "pipeline does not fit in shared memory");
   a.stages = stages;
-  const SmemLayout L = smem_layout(Sh::kStageBytes, stages, a.q_stride, h.S, Sh::kWarpsPerCta);
+  const SmemLayout L =
+      smem_layout(Sh::kStageBytes, stages, a.q_stride, h.S, Sh::kWarpsPerCta);
+  // an access past its boundary faults the launch: refuse the launch instead
+  PKV_REQUIRE(smem_layout_aligned(L, Sh::kStageBytes, a.q_stride), PKV_ERR_UNSUPPORTED,
+              "shared-memory layout misaligned (%d sequences)", h.S);
   CUtensorMap kmap, vmap;
   const int64_t rows = static_cast<int64_t>(h.NB) * h.Hkv * h.block_size;
   if constexpr (Sh::kQ8) {
@@ -1578,16 +1444,11 @@ int launch_decode(const HostArgs& h, int W) {
     rc = encode_map_4d(&vmap, h.v_cache, ty, dims, strides, box, CU_TENSOR_MAP_SWIZZLE_128B);
     if (rc != PKV_OK) return rc;
   } else {
-  // Single box: the cache as [rows * kSub, 128 B] half-rows, boxes of 16 * kSub
-  // half-rows (one whole tile).  Otherwise [rows, D], boxes of 16 rows x 128 B.
-  const int64_t map_rows = Sh::kSingleBox ? rows * Sh::kSub : rows;
-  const int map_cols = Sh::kSingleBox ? Sh::kBoxCols : D;
-  // boxes of one 16-token step, or of one 8-token block (two per step)
-  const int box_rows = Sh::kSingleBox ? kTok * Sh::kSub : (h.block_size == 8 ? 8 : kTok);
-  rc = encode_cache_map(&kmap, h.k_cache, h.dtype, map_rows, map_cols, Sh::kBoxCols, box_rows);
-  if (rc != PKV_OK) return rc;
-  rc = encode_cache_map(&vmap, h.v_cache, h.dtype, map_rows, map_cols, Sh::kBoxCols, box_rows);
-  if (rc != PKV_OK) return rc;
+    // fp32: [rows, D], boxes of 16 rows x 128 B
+    rc = encode_cache_map(&kmap, h.k_cache, h.dtype, rows, D, Sh::kBoxCols, kTok);
+    if (rc != PKV_OK) return rc;
+    rc = encode_cache_map(&vmap, h.v_cache, h.dtype, rows, D, Sh::kBoxCols, kTok);
+    if (rc != PKV_OK) return rc;
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3((W + Sh::kWarpsPerCta - 1) / Sh::kWarpsPerCta);
@@ -1880,21 +1741,26 @@ namespace {
 
 static __device__ __align__(256) unsigned char g_static_scratch[PKV_STATIC_SCRATCH_BYTES];
 
-// Device address of g_static_scratch for the current device, resolved once per
-// device with that device current.
+// Device address of g_static_scratch for the current device, resolved with that
+// device current and remembered once it succeeds (a failed lookup is retried on
+// the next call rather than remembered).
 int static_scratch_address(void** ptr) {
-  static std::once_flag flags[64];
+  static std::mutex mu;
   static void* addrs[64];
-  static cudaError_t errs[64];
   int dev = 0;
   PKV_CUDA(cudaGetDevice(&dev));
   if (dev < 0 || dev >= 64) return fail(PKV_ERR_UNSUPPORTED, "device ordinal %d", dev);
-  std::call_once(flags[dev], [&] {
+  std::lock_guard<std::mutex> lock(mu);
+  if (addrs[dev] == nullptr) {
     void* p = nullptr;
-    errs[dev] = cudaGetSymbolAddress(&p, g_static_scratch);
+    const cudaError_t e = cudaGetSymbolAddress(&p, g_static_scratch);
+    if (e != cudaSuccess || p == nullptr) {
+      cudaGetLastError();  // leave no sticky error behind for the caller's next call
+      return cuda_fail(e != cudaSuccess ? e : cudaErrorInvalidSymbol,
+                       "cudaGetSymbolAddress(static scratch)");
+    }
     addrs[dev] = p;
-  });
-  if (errs[dev] != cudaSuccess) return cuda_fail(errs[dev], "cudaGetSymbolAddress(static scratch)");
+  }
   *ptr = addrs[dev];
   return PKV_OK;
 }
@@ -1926,13 +1792,20 @@ extern "C" int pkv_decode_attention_static_scratch(
   void* scratch = nullptr;
   int rc = static_scratch_address(&scratch);
   if (rc != PKV_OK) return rc;
+  // Every argument is checked before anything is queued, so a refused call leaves
+  // the shared array (and everything else) untouched.
+  const HostArgs h = host_args(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                               context_lens, num_seqs, num_q_heads, num_kv_heads, head_dim,
+                               block_size, num_blocks, scale, out, scratch,
+                               PKV_STATIC_SCRATCH_BYTES, W, dtype, stream);
+  int W_checked = 0;
+  rc = validate(h, &W_checked);
+  if (rc != PKV_OK) return rc;
+  if (num_seqs == 0) return ok();
   // The status word and the merge tickets are the parts of the scratch that must
   // start at zero; the partial states are always written before they are read.
-  if (num_seqs > 0)
-    PKV_CUDA(cudaMemsetAsync(scratch, 0, workspace_layout(num_q_heads / num_kv_heads, head_dim, W).ml,
-                             static_cast<cudaStream_t>(stream)));
-  return pkv_decode_attention(q, k_cache, v_cache, block_tables, max_blocks_per_seq, context_lens,
-                              num_seqs, num_q_heads, num_kv_heads, head_dim, block_size,
-                              num_blocks, scale, out, scratch, PKV_STATIC_SCRATCH_BYTES, W, dtype,
-                              stream);
+  PKV_CUDA(cudaMemsetAsync(scratch, 0, workspace_layout(num_q_heads / num_kv_heads, head_dim, W).ml,
+                           static_cast<cudaStream_t>(stream)));
+  rc = dispatch(h, W_checked);
+  return rc == PKV_OK ? ok() : rc;
 }

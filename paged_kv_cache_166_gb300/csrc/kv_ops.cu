@@ -109,13 +109,15 @@ __global__ void decode_append_kernel(const uint4* __restrict__ k, const uint4* _
     const int32_t c = static_cast<int32_t>(i - th * row_vecs);
     const int64_t s = th / Hkv;
     const int32_t h = static_cast<int32_t>(th - s * Hkv);
+    // the rows do not depend on the slot: their loads go out with the slot lookups
+    const uint4 kv = __ldg(k + i), vv = __ldg(v + i);
     const int32_t t = __ldg(ctx + s);
     if (t <= 0 || t > MAXB * B) continue;
     const int32_t b = __ldg(tables + s * MAXB + (t - 1) / B);
     if (b < 0 || b >= NB) continue;
     const int64_t dst = ((static_cast<int64_t>(b) * Hkv + h) * B + (t - 1) % B) * row_vecs + c;
-    kc[dst] = __ldg(k + i);
-    vc[dst] = __ldg(v + i);
+    kc[dst] = kv;
+    vc[dst] = vv;
   }
 }
 

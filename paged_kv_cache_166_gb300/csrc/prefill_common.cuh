@@ -1,6 +1,6 @@
-// Definitions shared by the paged prefill kernels (prefill_attention.cu,
-// prefill_tcgen05.cu): the launch arguments, the per-sequence length checks and
-// the device status word.
+// Definitions shared by the paged prefill entry point (prefill_attention.cu) and
+// its kernel (prefill_tcgen05.cu): the launch arguments, the per-sequence length
+// checks and the device status word.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -11,7 +11,6 @@
 
 namespace pkv {
 
-constexpr int kPfTok = 16;                     // tokens per cache block of the warp-level kernel
 constexpr int kPfMaxSeqs = 2048;
 constexpr uint64_t kPfWaitNs = 1000000000ull;  // 1 s per wait before giving up
 

@@ -74,6 +74,11 @@ constexpr int kTcVWarp = 2 + kTcRowWarps;  // V producer
 constexpr int kTcQWarp = 3 + kTcRowWarps;  // query-tile producer
 constexpr int kTcWarps = 4 + kTcRowWarps;
 constexpr int kTcHalfKeys = kTcKeys / 2;
+// A warp may read and write only the tensor-memory lanes of its own quarter
+// (warp % 4).  Row warp w (2 .. 9) serves lanes 32 (w % 4) .. + 31 and half
+// (w - 2) / 4 of the keys, so each quarter has exactly one warp per half.
+static_assert(kTcRowWarps == 8 && kTcRows == 4 * 32,
+              "two row warps per tensor-memory lane quarter, one per half of the keys");
 constexpr float kTcRescale = 8.f;     // log2 of the growth of the row max that moves m
 constexpr int kTcThreads = kTcWarps * 32;
 constexpr int kTcChunk = 128 * 128;   // one [128 rows x 128 B] swizzled column chunk

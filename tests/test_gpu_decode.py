@@ -12,8 +12,9 @@ norm): 1e-5 for fp32, 2e-3 for fp16/bf16.  Covered:
 * bit-identity under relabelling of physical blocks and between runs; reuse of
   one workspace across launches;
 * invalid device data flagged in the status word without a fault;
-* the decode step with the cache write folded in: bit-identical to the write
-  followed by the attention (output and caches), and against the oracle.
+* the decode step, one launch that writes each new token and attends: bit-identical
+  to the write followed by the attention (output and caches), and against the
+  oracle, invalid device data included.
 """
 import numpy as np
 import pytest
@@ -284,6 +285,45 @@ def test_decode_step_edge_lengths_against_oracle(dtype, D, G):
     got = run_step(b, 2)
     check_rows(b, seqs, got, ref)
     assert torch.all(got[torch.from_numpy(lens == 0).cuda()] == 0)
+
+
+def test_decode_step_invalid_device_data_matches_write_then_attend():
+    """A length past the table, a negative length and a block id outside the pool in
+    the last block of a sequence: the fused step writes nothing for those sequences
+    (as the cache write with their slots skipped), flags the status word, and its
+    output and caches equal the write followed by the attention, bit for bit."""
+    m = pkv()
+    w, lens = REDUCED["gqa70b"]
+    b = BT.decode_batch(w, lens)
+    b2 = clone_caches(b)
+    tables, ctx, _ = b.device_index("cuda")
+    B, MAXB, NB = w.block_size, tables.shape[1], b.kc.shape[0]
+    bad_ctx, bad_tab = ctx.clone(), tables.clone()
+    bad_ctx[2] = MAXB * B + 5                       # longer than the table can hold
+    bad_ctx[3] = -4
+    last = (int(bad_ctx[0]) - 1) // B
+    bad_tab[0, last] = NB + 1000                    # outside the pool
+    # the write of the separate path: the same new tokens, invalid ones skipped
+    slots = np.full(len(lens), -1, dtype=np.int32)
+    tab_h, ctx_h = bad_tab.cpu().numpy(), bad_ctx.cpu().numpy()
+    for s_, t in enumerate(ctx_h):
+        if 0 < t <= MAXB * B:
+            blk = int(tab_h[s_, (t - 1) // B])
+            if 0 <= blk < NB:
+                slots[s_] = blk * B + (t - 1) % B
+    ws = torch.zeros(m.workspace_bytes(w.num_q_heads, w.num_kv_heads, w.head_dim, b.q.dtype),
+                     dtype=torch.uint8, device="cuda")
+    ws2 = torch.zeros_like(ws)
+    out = torch.full_like(b.q, float("nan"))
+    m.paged_decode_step(b.q, b.k_new, b.v_new, b.kc, b.vc, bad_tab, bad_ctx, w.scale, out, ws)
+    m.paged_kv_write(b2.k_new, b2.v_new, torch.from_numpy(slots).cuda(), b2.kc, b2.vc)
+    out2 = torch.full_like(b.q, float("nan"))
+    m.paged_decode_attention(b2.q, b2.kc, b2.vc, bad_tab, bad_ctx, w.scale, out2, ws2)
+    torch.cuda.synchronize()
+    assert m.decode_status(ws) == m.decode_status(ws2) == 3
+    assert torch.equal(out.view(torch.int16), out2.view(torch.int16))
+    assert torch.equal(b.kc.view(torch.int16), b2.kc.view(torch.int16))
+    assert torch.equal(b.vc.view(torch.int16), b2.vc.view(torch.int16))
 
 
 def test_decode_step_full_mha13b_every_row():

@@ -231,7 +231,15 @@ def pool_blocks(w, lens) -> int:
     return w.fixed_pool_blocks or int(math.ceil(blocks * (1 + w.pool_spare))) + 1
 
 
-def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size: int = 0):
+def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size: int = 0,
+                grow_tokens: int = 0):
+    """The decode batch of a workload on `device`, its tables built by the library's
+    block manager (history of ctx - 1 tokens per sequence, then the new token).
+
+    grow_tokens > 0 reserves blocks past the workload's pool for a decode loop that
+    appends that many more tokens to every sequence; they are handed out only after
+    the pool's own ids, so the workload's tables are the same either way.  Returns
+    (w, lens, NB, kc, vc, host, dev, alloc, sids) with NB the workload's pool."""
     import torch
     from paged_kv_cache_166_gb300 import BlockAllocator
     from paged_kv_cache_166_gb300 import workloads as W
@@ -247,7 +255,11 @@ def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size
         lens = W.context_lengths(dataclasses.replace(w, seed=seed)) if w.length_kind != "fixed" else lens
     B = w.block_size
     NB = pool_blocks(w, lens)
-    alloc = BlockAllocator(NB, B, W.pool_order(NB, seed))
+    order = W.pool_order(NB, seed)
+    extra = len(lens) * (grow_tokens // B + 2) if grow_tokens > 0 else 0
+    if extra:
+        order = np.concatenate([order, np.arange(NB, NB + extra, dtype=np.int32)])
+    alloc = BlockAllocator(NB + extra, B, order)
     sids = [alloc.create() for _ in range(len(lens))]
     for s, t in zip(sids, lens):
         alloc.append(s, int(t) - 1)
@@ -258,20 +270,20 @@ def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size
     S, Hq, Hkv, D = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim
     if kv == "fp8":
         # E4M3 codes of N(0,1) draws with per-KV-head scales; V tiles transposed
-        kc = torch.empty((NB, Hkv, B, D), dtype=torch.uint8, device=device)
-        vc = torch.empty((NB, Hkv, D, B), dtype=torch.uint8, device=device)
+        kc = torch.empty((NB + extra, Hkv, B, D), dtype=torch.uint8, device=device)
+        vc = torch.empty((NB + extra, Hkv, D, B), dtype=torch.uint8, device=device)
         k_scale, v_scale = W.fp8_scales(Hkv, seed), W.fp8_scales(Hkv, seed + 1)
         W.fill_fp8_codes_(kc, k_scale, seed, W.STREAM_K_POOL)
         W.fill_fp8_codes_(vc, v_scale, seed, W.STREAM_V_POOL)
     elif kv == "int8":
         # int8 codes of N(0,1) draws with per-KV-head scales; V tiles transposed
-        kc = torch.empty((NB, Hkv, B, D), dtype=torch.int8, device=device)
-        vc = torch.empty((NB, Hkv, D, B), dtype=torch.int8, device=device)
+        kc = torch.empty((NB + extra, Hkv, B, D), dtype=torch.int8, device=device)
+        vc = torch.empty((NB + extra, Hkv, D, B), dtype=torch.int8, device=device)
         k_scale, v_scale = W.int8_scales(Hkv, seed), W.int8_scales(Hkv, seed + 1)
         W.fill_int8_codes_(kc, k_scale, seed, W.STREAM_K_POOL)
         W.fill_int8_codes_(vc, v_scale, seed, W.STREAM_V_POOL)
     else:
-        kc = torch.empty((NB, Hkv, B, D), dtype=dt, device=device)
+        kc = torch.empty((NB + extra, Hkv, B, D), dtype=dt, device=device)
         vc = torch.empty_like(kc)
         W.fill_normal_(kc, seed, W.STREAM_K_POOL)
         W.fill_normal_(vc, seed, W.STREAM_V_POOL)
@@ -288,7 +300,7 @@ def build_batch(name: str, device, rank: int = 0, kv: str = "native", block_size
     if kv in ("fp8", "int8"):
         dev["k_scale"] = torch.from_numpy(k_scale).to(device)
         dev["v_scale"] = torch.from_numpy(v_scale).to(device)
-    return w, lens, NB, kc, vc, host, dev
+    return w, lens, NB, kc, vc, host, dev, alloc, sids
 
 
 # --------------------------------------------------------------------------------------
@@ -411,38 +423,31 @@ def time_oracle(name: str, budget_s: float = 15.0, steps: int = 1, fill_s: float
 
 
 # --------------------------------------------------------------------------------------
-def native(args):
+E2E_STEPS = 48   # most timed steps of the end-to-end decode loop (contexts grow by one a step)
+
+
+def measure_decode(args, name, device, rank, world, pkv, flush):
+    """Times one decode workload three ways on this rank's GPU:
+    * the decode step (cache write of every sequence's new token + attention), the
+      bench's step, K times with CUDA events, L2 flushed between steps, clocks sampled;
+    * the attention kernel alone in its own loop (the roofline figure);
+    * end to end through the public API: a decode loop from the workload's state in
+      which every step runs the host block manager (one new position per sequence,
+      tables and lengths exported into page-locked staging memory), copies the
+      step's inputs to the device in one copy, runs the decode step and reads the
+      output back; contexts grow by one token a step and each step's bytes are
+      counted from its own lengths."""
     import torch
-    import torch.distributed as dist
-
-    world = int(os.environ.get("WORLD_SIZE", "1"))
-    rank = int(os.environ.get("RANK", "0"))
-    local = int(os.environ.get("LOCAL_RANK", "0"))
-    if world > 1:
-        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
-    torch.cuda.set_device(local)
-    device = torch.device("cuda", local)
-
-    # the oracle pool is spawned before the first GPU call of this process
-    cpu = time_oracle(args.workload, budget_s=args.cpu_budget, fill_s=args.cpu_budget) if (
-        rank == 0 and world == 1 and not args.no_cpu_baseline and args.kv == "native") else None
-
-    import __graft_entry__
-    __graft_entry__.build()
-    import paged_kv_cache_166_gb300 as pkv
-
-    q8 = args.kv if args.kv in ("fp8", "int8") else None   # the 8-bit cache kind
-    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, rank, args.kv,
-                                                 args.block_size)
+    q8 = args.kv if args.kv in ("fp8", "int8") else None
+    e2e_steps = max(1, min(args.steps, E2E_STEPS))
+    w, lens, NB, kc, vc, host, dev, alloc, sids = build_batch(
+        name, device, rank, args.kv, args.block_size, grow_tokens=args.warmup + e2e_steps)
     S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     elt = kc.element_size()
     q_elt = dev["q"].element_size()
-    MAXB = dev["tables"].shape[1]
     out = torch.empty_like(dev["q"])
-    ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, q8 or dev["q"].dtype,
-                                         args.num_warps),
+    ws = torch.zeros(pkv.workspace_bytes(Hq, Hkv, D, q8 or dev["q"].dtype, args.num_warps),
                      dtype=torch.uint8, device=device)
-    flush = L2Flush(device)
     stream = torch.cuda.current_stream(device)
     attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B, q_elt)
 
@@ -475,12 +480,13 @@ def native(args):
     if pkv.decode_status(ws) != 0:
         raise RuntimeError("device status reported an error during warm-up")
 
+    import torch.distributed as dist
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     starts = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
     ends = [torch.cuda.Event(enable_timing=True) for _ in range(args.steps)]
-    with ClockSampler(local) as clocks:
+    with ClockSampler(device.index) as clocks:
         # untimed soak of the same step so that the clock samples see this load
         clocks.mark("t_soak")
         t_end = time.perf_counter() + args.soak_s
@@ -501,117 +507,199 @@ def native(args):
         clocks.mark("t_done")
     if world > 1:
         dist.barrier()
-    step_ms = [a.elapsed_time(b) for a, b in zip(starts, ends)]
-    ms = float(np.mean(step_ms))
+    ms = float(np.mean([a.elapsed_time(b) for a, b in zip(starts, ends)]))
 
-    # the dominant (and only) kernel of a step, alone, for the roofline; and the
-    # attention without the folded cache write, for reference
-    def kernel_ms(fn):
-        ts = []
-        for i in range(args.warmup + args.steps):
-            flush()
-            e0.record(stream)
-            fn()
-            e1.record(stream)
-            e1.synchronize()
-            if i >= args.warmup:
-                ts.append(e0.elapsed_time(e1))
-        return float(np.mean(ts))
-    pms = kernel_ms(attention)
-
-    # end to end through the public API with pinned host buffers: the step's inputs
-    # packed into one pinned buffer, one H2D copy, the decode step, D2H of out
-    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
-    names = ["q", "k_new", "v_new", "tables", "ctx"]
-    offs, total = {}, 0
-    for k in names:
-        offs[k] = total
-        total += (host[k].numel() * host[k].element_size() + 255) & ~255
-    stage_h = torch.empty(total, dtype=torch.uint8, pin_memory=True)
-    stage_d = torch.empty(total, dtype=torch.uint8, device=device)
-    views = {}
-    for k in names:
-        n = host[k].numel() * host[k].element_size()
-        stage_h[offs[k]:offs[k] + n].copy_(host[k].contiguous().view(-1).view(torch.uint8))
-        views[k] = stage_d[offs[k]:offs[k] + n].view(host[k].dtype).view(host[k].shape)
-    h2d = total
-    d2h = out.numel() * out.element_size()
-
-    def e2e_step():
-        stage_d.copy_(stage_h, non_blocking=True)
-        decode_step(views["q"], views["k_new"], views["v_new"], views["tables"], views["ctx"])
-        out_h.copy_(out, non_blocking=True)
-
-    for _ in range(args.warmup):
-        flush()
-        e2e_step()
-    torch.cuda.synchronize()
-    e2e_ms = []
-    for _ in range(args.steps):
+    # the dominant kernel of a step, alone, for the roofline
+    ts = []
+    for i in range(args.warmup + args.steps):
         flush()
         e0.record(stream)
-        e2e_step()
+        attention()
         e1.record(stream)
         e1.synchronize()
-        e2e_ms.append(e0.elapsed_time(e1))
-    e2e = float(np.mean(e2e_ms))
+        if i >= args.warmup:
+            ts.append(e0.elapsed_time(e1))
+    pms = float(np.mean(ts))
     status = pkv.decode_status(ws)
     if status:
         raise RuntimeError(f"device status {status} after the timed steps")
 
-    ms, e2e = max_over_ranks([ms, e2e], device)
+    # end to end: the decode loop through the public API (see the docstring)
+    maxb = int(-(-(int(lens.max()) + args.warmup + e2e_steps) // B))
+    names = ["q", "k_new", "v_new", "tables", "ctx"]
+    sizes = {k: host[k].numel() * host[k].element_size() for k in names[:3]}
+    sizes["tables"] = S * maxb * 4
+    sizes["ctx"] = S * 4
+    offs, total = {}, 0
+    for k in names:
+        offs[k] = total
+        total += (sizes[k] + 255) & ~255
+    stage_h = torch.empty(total, dtype=torch.uint8, pin_memory=True)
+    stage_d = torch.empty(total, dtype=torch.uint8, device=device)
+    for k in names[:3]:
+        stage_h[offs[k]:offs[k] + sizes[k]].copy_(host[k].contiguous().view(-1).view(torch.uint8))
+    tab_h = stage_h[offs["tables"]:offs["tables"] + sizes["tables"]].view(torch.int32).view(S, maxb).numpy()
+    ctx_h = stage_h[offs["ctx"]:offs["ctx"] + sizes["ctx"]].view(torch.int32).numpy()
+    views = {}
+    for k in names:
+        shape = {"tables": (S, maxb), "ctx": (S,)}.get(k, tuple(host[k].shape))
+        dtype = torch.int32 if k in ("tables", "ctx") else host[k].dtype
+        views[k] = stage_d[offs[k]:offs[k] + sizes[k]].view(dtype).view(shape)
+    out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
+    host_step = pkv.DecodeStepTables(alloc, sids, maxb, tab_h, ctx_h)
+
+    def e2e_step():
+        host_step()            # block manager: the step's new slots, tables into staging
+        stage_d.copy_(stage_h, non_blocking=True)
+        decode_step(views["q"], views["k_new"], views["v_new"], views["tables"], views["ctx"])
+        out_h.copy_(out, non_blocking=True)
+
+    grown = 0
+    for _ in range(args.warmup):
+        flush()
+        e2e_step()
+        grown += 1
+    torch.cuda.synchronize()
+    e2e_ms, e2e_bytes = [], 0
+    for _ in range(e2e_steps):
+        flush()
+        torch.cuda.synchronize()
+        e0.record(stream)
+        e2e_step()
+        e1.record(stream)
+        e1.synchronize()
+        grown += 1
+        e2e_ms.append(e0.elapsed_time(e1))
+        e2e_bytes += attention_bytes(lens + grown, Hq, Hkv, D, elt, B, q_elt)
+    status = pkv.decode_status(ws)
+    if status:
+        raise RuntimeError(f"device status {status} after the end-to-end steps")
+    e2e_ms_mean = float(np.mean(e2e_ms))
+    e2e_bytes_per_step = e2e_bytes / e2e_steps
+    ms, pms, e2e_ms_mean = max_over_ranks([ms, pms, e2e_ms_mean], device)
+    res = {
+        "w": w, "lens": lens, "NB": NB, "q8": q8, "D": D, "bytes": attn_bytes, "ms": ms,
+        "pms": pms, "e2e_ms": e2e_ms_mean, "e2e_bytes": e2e_bytes_per_step,
+        "e2e_steps": e2e_steps, "h2d": total, "d2h": out.numel() * out.element_size(),
+        "clocks": clocks.summary(clocks.t_soak, clocks.t_done), "wall": wall,
+        "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
+        "q_dtype": w.dtype,
+    }
+    alloc.close()
+    return res
+
+
+def decode_record(res, world, peak, peak_kind, steps) -> dict:
+    """The figures of one measured decode workload (step, kernel roofline, e2e)."""
+    w, lens, q8 = res["w"], res["lens"], res["q8"]
+    gbs = whole_job_gbs(res["bytes"], world, res["ms"])
+    part_gbs = res["bytes"] / (res["pms"] * 1e-3) / 1e9
+    tag = f"decode_attention_{q8}_{w.name}" if q8 else f"decode_attention_{w.name}"
+    traffic = profile_traffic(tag)
+    return {
+        "value": round(gbs, 1), "unit": "GB/s", "ms_per_step": round(res["ms"], 4),
+        "pct_of_peak": {"measured_copy": round(100 * gbs / peak, 1),
+                        "nominal_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
+                        "peak_kind": peak_kind},
+        "seq_tokens_per_s": round(int(lens.sum()) * world / (res["ms"] * 1e-3), 1),
+        "attention_kernel": {"kv_gbs": round(part_gbs, 1), "ms": round(res["pms"], 4)},
+        "roofline": {
+            "bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
+            "frac": round(part_gbs / peak, 4),
+            "frac_of_nominal_8TBs": round(part_gbs / NOMINAL_HBM_GBS, 4),
+            "traffic": traffic,
+            "traffic_source": (f"profiles/{tag}.md (ncu dram__bytes_read.sum + "
+                               "dram__bytes_write.sum of one earlier capture of the same "
+                               "kernel code on this workload; not measured in this run)")
+                              if traffic is not None else
+                              "no ncu capture of the current kernel code on this workload",
+            "kernel": "decode_attention_kernel" + (f" ({q8} cache)" if q8 else ""),
+            "bytes_per_launch": res["bytes"],
+            "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+        },
+        "e2e": {"value": round(whole_job_gbs(res["e2e_bytes"], world, res["e2e_ms"]), 1),
+                "unit": "GB/s", "ms_per_step": round(res["e2e_ms"], 4),
+                "h2d_bytes_per_step": int(res["h2d"]), "d2h_bytes_per_step": int(res["d2h"]),
+                "steps": res["e2e_steps"],
+                "step": "host block manager (pkv_seq_append_one_each + pkv_export_tables into "
+                        "page-locked staging) + one H2D copy of q, new K/V, tables and lengths "
+                        "+ paged_decode_step + D2H of out; a decode loop from the workload's "
+                        "state, contexts one token longer each step, bytes counted per step"},
+        "gpu_launches": 2 * steps,
+        "clocks": res["clocks"],
+        "wall_s_timed_loop": round(res["wall"], 3),
+    }
+
+
+def native(args):
+    import torch
+    import torch.distributed as dist
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+
+    # the oracle pool is spawned before the first GPU call of this process
+    cpu = time_oracle(args.workload, budget_s=args.cpu_budget, fill_s=args.cpu_budget) if (
+        rank == 0 and world == 1 and not args.no_cpu_baseline and args.kv == "native") else None
+
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_166_gb300 as pkv
+
+    flush = L2Flush(device)
+    main = measure_decode(args, args.workload, device, rank, world, pkv, flush)
+    also = [] if args.also in ("", "none") else [x for x in args.also.split(",")
+                                                 if x and x != args.workload]
+    others = []
+    for name in also:
+        torch.cuda.empty_cache()   # the previous workload's caches are gone
+        others.append(measure_decode(args, name, device, rank, world, pkv, flush))
     if rank != 0:
         if world > 1:
             dist.destroy_process_group()
         return
 
     peak, peak_kind = measured_peak()
-    gbs = whole_job_gbs(attn_bytes, world, ms)
-    part_gbs = attn_bytes / (pms * 1e-3) / 1e9
-    tag = f"decode_attention_{q8}_{args.workload}" if q8 else f"decode_attention_{args.workload}"
-    traffic = profile_traffic(tag)
+    q8, w, lens = main["q8"], main["w"], main["lens"]
+    rec = decode_record(main, world, peak, peak_kind, args.steps)
     line = {
         "metric": METRIC,
-        "value": round(gbs, 1),
+        "value": rec["value"],
         "unit": "GB/s",
         "n_gpus": world,
         "steps": args.steps,
         "warmup": args.warmup,
-        "ms_per_step": round(ms, 4),
+        "ms_per_step": rec["ms_per_step"],
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
         "dtype": f"{'e4m3' if q8 == 'fp8' else 'int8'} KV, {w.dtype} q" if q8 else w.dtype,
         "data": "synthetic",
         "config": {
-            **workload_config(w, lens, NB, q8),
+            **workload_config(w, lens, main["NB"], q8),
             "step": (f"paged_decode_step_{q8}: quantising cache write of 1 new token/seq + decode "
                      "attention (2 launches, PDL-chained)") if q8 else
                     "paged_decode_step: cache write of 1 new token/seq + decode attention (2 launches, PDL-chained)",
             "l2": L2Flush.LABEL,
-            "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
+            "num_warps": main["num_warps"],
             "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
         },
-        "pct_of_peak": {"measured_copy": round(100 * gbs / peak, 1),
-                        "nominal_8TBs": round(100 * gbs / NOMINAL_HBM_GBS, 1),
-                        "peak_kind": peak_kind},
-        "seq_tokens_per_s": round(int(lens.sum()) * world / (ms * 1e-3), 1),
-        "attention_kernel": {"kv_gbs": round(part_gbs, 1), "ms": round(pms, 4)},
-        "roofline": {
-            "bound": "hbm", "achieved": round(part_gbs, 1), "peak": peak, "unit": "GB/s",
-            "frac": round(part_gbs / peak, 4), "traffic": traffic,
-            "kernel": "decode_attention_kernel" + (f" ({q8} cache)" if q8 else ""),
-            "bytes_per_launch": attn_bytes,
-            "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
-        },
-        "e2e": {"value": round(whole_job_gbs(attn_bytes, world, e2e), 1), "unit": "GB/s",
-                "ms_per_step": round(e2e, 4), "h2d_bytes_per_step": int(h2d),
-                "d2h_bytes_per_step": int(d2h)},
-        "gpu_launches": 2 * args.steps,
-        "clocks": clocks.summary(clocks.t_soak, clocks.t_done),
-        "wall_s_timed_loop": round(wall, 3),
-        "clocks_window": f"nvidia-smi every 50 ms over a {args.soak_s} s soak of the same step and the timed steps",
     }
+    line.update({k: v for k, v in rec.items() if k not in ("value", "unit", "ms_per_step")})
+    line["clocks_window"] = (f"nvidia-smi every 50 ms over a {args.soak_s} s soak of the same "
+                             "step and the timed steps")
+    if others:
+        line["workloads"] = {}
+        for o in others:
+            r = decode_record(o, world, peak, peak_kind, args.steps)
+            r["config"] = workload_config(o["w"], o["lens"], o["NB"], o["q8"])
+            r["config"]["num_warps"] = o["num_warps"]
+            line["workloads"][o["w"].name] = r
     if cpu is not None:
         cs = float(np.median(cpu["seconds"]))
         line["cpu_baseline"] = {
@@ -627,6 +715,60 @@ def native(args):
         dist.destroy_process_group()
 
 
+def kv_write_bench(args):
+    """The cache write alone (pkv_kv_write): the new tokens of every sequence of the
+    workload (256 for the 70B-shaped batch) scattered into the paged caches through a
+    slot mapping from the library's block manager, L2 flushed between steps, CUDA
+    events.  Algorithmic bytes: read k and v, write both rows, read the slots."""
+    import torch
+    import __graft_entry__
+    __graft_entry__.build()
+    import paged_kv_cache_166_gb300 as pkv
+
+    device = torch.device("cuda", 0)
+    torch.cuda.set_device(device)
+    w, lens, NB, kc, vc, host, dev, _, _ = build_batch(args.workload, device, 0)
+    T = len(lens)
+    Hkv, D = w.num_kv_heads, w.head_dim
+    elt = kc.element_size()
+    nbytes = kv_write_bytes(T, Hkv, D, elt)
+    flush = L2Flush(device)
+    stream = torch.cuda.current_stream(device)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    def step():
+        pkv.paged_kv_write(dev["k_new"], dev["v_new"], dev["slots"], kc, vc)
+
+    ts = []
+    for i in range(args.warmup + args.steps):
+        flush()
+        e0.record(stream)
+        step()
+        e1.record(stream)
+        e1.synchronize()
+        if i >= args.warmup:
+            ts.append(e0.elapsed_time(e1))
+    ms = float(np.mean(ts))
+    peak, peak_kind = measured_peak()
+    gbs = nbytes / (ms * 1e-3) / 1e9
+    print(json.dumps({
+        "metric": "paged_kv_write GB/s (new tokens' K/V scattered through slot_mapping)",
+        "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": w.dtype, "data": "synthetic",
+        "config": {"workload": f"{w.name}: {T} new tokens, {Hkv} kv heads, head_dim {D}, "
+                               f"{w.dtype}, into a pool of {NB} blocks",
+                   "l2": L2Flush.LABEL},
+        "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "kernel": "kv_write_kernel", "bytes_per_launch": nbytes,
+                     "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
+                     "note": "launch-bound at this size: the bytes take well under a "
+                             "microsecond at the copy rate"},
+        "gpu_launches": args.steps,
+    }), flush=True)
+
+
 def swap_bench(args):
     """Preemption by swapping: the blocks of a quarter of the workload's context
     (whole sequences, longest first) copied to page-locked host memory and back,
@@ -639,7 +781,7 @@ def swap_bench(args):
 
     device = torch.device("cuda", 0)
     torch.cuda.set_device(device)
-    w, lens, NB, kc, vc, host, dev = build_batch(args.workload, device, 0, args.kv)
+    w, lens, NB, kc, vc, host, dev, _, _ = build_batch(args.workload, device, 0, args.kv)
     B = w.block_size
     nb = (lens + B - 1) // B
     tables = host["tables"].numpy()
@@ -1069,14 +1211,18 @@ def main():
     ap.add_argument("--workload", default="mha13b",
                     choices=["tiny", "mha13b", "gqa70b", "prefix", "longctx"])
     ap.add_argument("--num-warps", type=int, default=0)
+    ap.add_argument("--also", default="gqa70b,longctx",
+                    help="decode workloads timed in the same run after the main one, each "
+                         "reported under 'workloads' ('none' for none)")
     ap.add_argument("--batched", type=int, default=1,
                     help="allocator bench: one batched append call per decode step (1) or one per sequence (0)")
     ap.add_argument("--op", choices=["decode", "swap", "prefill", "allocator", "cow",
-                                     "swap_layers"],
+                                     "swap_layers", "kv_write"],
                     default="decode",
                     help="decode: the decode step (default); swap: blocks to host and back; "
                          "prefill: causal prefill attention; allocator: the host block manager; "
                          "cow: copy-on-write block copies in every layer's caches; "
+                         "kv_write: the cache write of the batch's new tokens alone; "
                          "swap_layers: one sequence (--prefill-len tokens) swapped in every "
                          "layer")
     ap.add_argument("--layers", type=int, default=32, help="layers of the cow and swap_layers ops")
@@ -1115,6 +1261,9 @@ def main():
         return
     if args.op == "swap_layers":
         swap_layers_bench(args)
+        return
+    if args.op == "kv_write":
+        kv_write_bench(args)
         return
     (reference if args.impl == "reference" else native)(args)
 

@@ -16,11 +16,12 @@ Public API (all device work runs in libpkv.so's sm_103a kernels):
 * ``paged_swap_out`` / ``paged_swap_in`` — blocks to and from pinned host memory
   (preemption by swapping, with ``BlockAllocator.swap_out`` / ``swap_in``);
   ``paged_swap_out_layers`` / ``paged_swap_in_layers`` — every layer's caches, one launch
-* ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free)
+* ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free);
+  ``DecodeStepTables`` — one decode step's appends and table export, pre-bound
 
 The library is loaded on first use; importing this package needs no GPU.
 """
-from .allocator import BlockAllocator  # noqa: F401
+from .allocator import BlockAllocator, DecodeStepTables  # noqa: F401
 from ._native import OutOfBlocks, PkvError  # noqa: F401
 
 

@@ -140,11 +140,61 @@ class BlockAllocator:
         N.check(self._lib.pkv_seq_table(self._h, seq, _ptr(buf), n.value, ctypes.byref(n)))
         return buf[:n.value].tolist()
 
-    def export_tables(self, seqs: Sequence[int], max_blocks: int):
-        """Row-padded int32 [len(seqs), max_blocks] table (padding 0) and int32 lengths."""
+    def export_tables(self, seqs: Sequence[int], max_blocks: int,
+                      tables_out: Optional[np.ndarray] = None,
+                      ctx_out: Optional[np.ndarray] = None):
+        """Row-padded int32 [len(seqs), max_blocks] table (padding 0) and int32 lengths,
+        written into ``tables_out`` / ``ctx_out`` when given (C-contiguous int32 arrays
+        of those shapes, e.g. views of page-locked staging buffers)."""
         s = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
-        tab = np.zeros((len(s), max_blocks), dtype=np.int32)
-        ctx = np.zeros(len(s), dtype=np.int32)
+        tab = np.zeros((len(s), max_blocks), dtype=np.int32) if tables_out is None else tables_out
+        ctx = np.zeros(len(s), dtype=np.int32) if ctx_out is None else ctx_out
+        for a, shape in ((tab, (len(s), max_blocks)), (ctx, (len(s),))):
+            if a.dtype != np.int32 or a.shape != shape or not a.flags.c_contiguous:
+                raise ValueError(f"output must be C-contiguous int32 of shape {shape}")
         N.check(self._lib.pkv_export_tables(self._h, _ptr(s), len(s), max_blocks, _ptr(tab),
                                             _ptr(ctx)))
         return tab, ctx
+
+
+class DecodeStepTables:
+    """The host side of one decode step for a fixed set of sequences, every buffer
+    and C argument bound once: one new position for each sequence
+    (pkv_seq_append_one_each), then their tables and lengths exported
+    (pkv_export_tables) into ``tables_out`` [k, max_blocks] and ``ctx_out`` [k]
+    (C-contiguous int32 arrays, e.g. views of page-locked staging memory that the
+    step then copies to the device).  Calling it costs two library calls and no
+    allocation; it returns the step's slots (int32 [k], overwritten by the next
+    call) and its copy-on-write pairs."""
+
+    def __init__(self, alloc: BlockAllocator, seqs: Sequence[int], max_blocks: int,
+                 tables_out: np.ndarray, ctx_out: np.ndarray):
+        ids = np.ascontiguousarray(np.asarray(seqs, dtype=np.int32))
+        k = len(ids)
+        for a, shape in ((tables_out, (k, max_blocks)), (ctx_out, (k,))):
+            if a.dtype != np.int32 or a.shape != shape or not a.flags.c_contiguous:
+                raise ValueError(f"output must be C-contiguous int32 of shape {shape}")
+        self.alloc = alloc  # keeps the block manager alive
+        self._ids, self.slots = ids, np.empty(max(k, 1), dtype=np.int32)
+        self._pairs = np.empty(max(2 * k, 2), dtype=np.int32)
+        self._ncow = ctypes.c_int32(0)
+        self._tab, self._ctx = tables_out, ctx_out
+        lib = alloc._lib
+        self._append = lib.pkv_seq_append_one_each
+        self._export = lib.pkv_export_tables
+        self._a_args = (alloc._h, _ptr(ids), k, _ptr(self.slots), _ptr(self._pairs),
+                        ctypes.byref(self._ncow))
+        self._e_args = (alloc._h, _ptr(ids), k, max_blocks, _ptr(tables_out), _ptr(ctx_out))
+        self._k = k
+
+    def __call__(self) -> Tuple[np.ndarray, List[Tuple[int, int]]]:
+        rc = self._append(*self._a_args)
+        if rc:
+            N.check(rc)
+        rc = self._export(*self._e_args)
+        if rc:
+            N.check(rc)
+        n = self._ncow.value
+        cows = [(int(self._pairs[2 * i]), int(self._pairs[2 * i + 1])) for i in range(n)] if n else []
+        return self.slots[:self._k], cows
+

@@ -293,6 +293,41 @@ def test_append_one_each_equals_appends_in_list_order(seed):
     assert len(slots) == 0 and cows == []
 
 
+def test_decode_step_tables_equal_the_oracle_decode_loop():
+    """DecodeStepTables (one new position per sequence, then the tables exported into
+    caller-owned arrays, all arguments bound once) against the oracle's block manager
+    appending one token to each sequence and reading its tables: the same slots,
+    copy-on-write pairs, tables and lengths at every step of a decode loop with forked
+    siblings sharing partial blocks."""
+    from paged_kv_cache_166_gb300 import DecodeStepTables
+    r = np.random.default_rng(11)
+    B, NB = 4, 200
+    p = Pair(NB, B, r.permutation(NB).astype(np.int32))
+    seqs = []
+    for t in (1, 6, 9, 4):
+        s = p.create()
+        p.append(s, t)
+        seqs.append(s)
+    seqs.append(p.fork(seqs[1]))      # shares a partial block with its parent
+    seqs.append(p.fork(seqs[2]))
+    maxb = 12
+    tab = np.full((len(seqs), maxb), -7, dtype=np.int32)
+    ctx = np.full(len(seqs), -7, dtype=np.int32)
+    step = DecodeStepTables(p.c, seqs, maxb, tab, ctx)
+    for _ in range(20):
+        expect = [p.o.append(s, 1) for s in seqs]
+        slots, cows = step()
+        assert list(slots) == [e[0][0] for e in expect]
+        assert cows == [c for e in expect for c in e[1]]
+        for i, s in enumerate(seqs):
+            t = p.o.tables[s]
+            assert list(tab[i, :len(t)]) == list(t) and not tab[i, len(t):].any()
+            assert ctx[i] == p.o.lengths[s]
+        p.compare()
+    with pytest.raises(ValueError):
+        DecodeStepTables(p.c, seqs, maxb, tab[:, :3].copy(), ctx)
+
+
 def test_header_is_plain_c_and_links_against_the_library(tmp_path):
     """include/pkv.h compiles as strict C99 and every function it declares resolves
     against libpkv.so at link time; the program then drives the block manager through

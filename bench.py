@@ -441,7 +441,7 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
     q8 = args.kv if args.kv in ("fp8", "int8") else None
     e2e_steps = max(1, min(args.steps, E2E_STEPS))
     w, lens, NB, kc, vc, host, dev, alloc, sids = build_batch(
-        name, device, rank, args.kv, args.block_size, grow_tokens=args.warmup + e2e_steps)
+        name, device, rank, args.kv, args.block_size, grow_tokens=2 * args.warmup + e2e_steps + 2)
     S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     elt = kc.element_size()
     q_elt = dev["q"].element_size()
@@ -525,7 +525,7 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
         raise RuntimeError(f"device status {status} after the timed steps")
 
     # end to end: the decode loop through the public API (see the docstring)
-    maxb = int(-(-(int(lens.max()) + args.warmup + e2e_steps) // B))
+    maxb = int(-(-(int(lens.max()) + 2 * args.warmup + e2e_steps + 2) // B))
     names = ["q", "k_new", "v_new", "tables", "ctx"]
     sizes = {k: host[k].numel() * host[k].element_size() for k in names[:3]}
     sizes["tables"] = S * maxb * 4
@@ -548,39 +548,67 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
     out_h = torch.empty(out.shape, dtype=out.dtype, pin_memory=True)
     host_step = pkv.DecodeStepTables(alloc, sids, maxb, tab_h, ctx_h)
 
-    def e2e_step():
-        host_step()            # block manager: the step's new slots, tables into staging
+    def device_part():
         stage_d.copy_(stage_h, non_blocking=True)
         decode_step(views["q"], views["k_new"], views["v_new"], views["tables"], views["ctx"])
         out_h.copy_(out, non_blocking=True)
 
+    def e2e_step():
+        host_step()            # block manager: the step's new slots, tables into staging
+        device_part()
+
     grown = 0
-    for _ in range(args.warmup):
-        flush()
-        e2e_step()
-        grown += 1
-    torch.cuda.synchronize()
-    e2e_ms, e2e_bytes = [], 0
-    for _ in range(e2e_steps):
-        flush()
+
+    def timed_loop(step_fn, n_warm, n_steps):
+        nonlocal grown
+        for _ in range(n_warm):
+            flush()
+            step_fn()
+            grown += 1
         torch.cuda.synchronize()
-        e0.record(stream)
-        e2e_step()
-        e1.record(stream)
-        e1.synchronize()
-        grown += 1
-        e2e_ms.append(e0.elapsed_time(e1))
-        e2e_bytes += attention_bytes(lens + grown, Hq, Hkv, D, elt, B, q_elt)
+        ts, nbytes = [], 0
+        for _ in range(n_steps):
+            flush()
+            torch.cuda.synchronize()
+            e0.record(stream)
+            step_fn()
+            e1.record(stream)
+            e1.synchronize()
+            grown += 1
+            ts.append(e0.elapsed_time(e1))
+            nbytes += attention_bytes(lens + grown, Hq, Hkv, D, elt, B, q_elt)
+        return float(np.mean(ts)), nbytes / n_steps
+
+    half = max(1, e2e_steps // 2)
+    eager_ms, eager_bytes = timed_loop(e2e_step, args.warmup, half)
+    # The same step with its copies and launches captured once in a CUDA graph and
+    # replayed; the block manager still runs on the host every step and its tables
+    # reach the device through the captured copy of the staging buffer.
+    graph_ms = graph_bytes = None
+    try:
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            device_part()
+        torch.cuda.synchronize()
+
+        def graph_step():
+            host_step()
+            g.replay()
+        graph_ms, graph_bytes = timed_loop(graph_step, args.warmup, half)
+    except Exception as exc:  # capture refused: report the eager loop alone
+        print(f"e2e graph capture unavailable: {exc}", file=sys.stderr)
+        torch.cuda.synchronize()
     status = pkv.decode_status(ws)
     if status:
         raise RuntimeError(f"device status {status} after the end-to-end steps")
-    e2e_ms_mean = float(np.mean(e2e_ms))
-    e2e_bytes_per_step = e2e_bytes / e2e_steps
-    ms, pms, e2e_ms_mean = max_over_ranks([ms, pms, e2e_ms_mean], device)
+    e2e_ms_mean, e2e_bytes_per_step = (graph_ms, graph_bytes) if graph_ms else (eager_ms, eager_bytes)
+    ms, pms, e2e_ms_mean, eager_ms = max_over_ranks([ms, pms, e2e_ms_mean, eager_ms], device)
     res = {
         "w": w, "lens": lens, "NB": NB, "q8": q8, "D": D, "bytes": attn_bytes, "ms": ms,
         "pms": pms, "e2e_ms": e2e_ms_mean, "e2e_bytes": e2e_bytes_per_step,
-        "e2e_steps": e2e_steps, "h2d": total, "d2h": out.numel() * out.element_size(),
+        "e2e_graph": graph_ms is not None, "e2e_eager_ms": eager_ms,
+        "e2e_eager_bytes": eager_bytes,
+        "e2e_steps": half, "h2d": total, "d2h": out.numel() * out.element_size(),
         "clocks": clocks.summary(clocks.t_soak, clocks.t_done), "wall": wall,
         "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
         "q_dtype": w.dtype,
@@ -623,8 +651,16 @@ def decode_record(res, world, peak, peak_kind, steps) -> dict:
                 "steps": res["e2e_steps"],
                 "step": "host block manager (pkv_seq_append_one_each + pkv_export_tables into "
                         "page-locked staging) + one H2D copy of q, new K/V, tables and lengths "
-                        "+ paged_decode_step + D2H of out; a decode loop from the workload's "
-                        "state, contexts one token longer each step, bytes counted per step"},
+                        "+ paged_decode_step + D2H of out"
+                        + ("; the copies and launches captured once in a CUDA graph and "
+                           "replayed each step" if res["e2e_graph"] else "") +
+                        "; a decode loop from the workload's state, contexts one token longer "
+                        "each step, bytes counted per step",
+                "eager": {"value": round(whole_job_gbs(res["e2e_eager_bytes"], world,
+                                                       res["e2e_eager_ms"]), 1),
+                          "ms_per_step": round(res["e2e_eager_ms"], 4),
+                          "step": "the same without the graph: every step through the Python "
+                                  "API (argument checks, tensor maps, two launches, two copies)"}},
         "gpu_launches": 2 * steps,
         "clocks": res["clocks"],
         "wall_s_timed_loop": round(res["wall"], 3),

@@ -271,16 +271,16 @@ __device__ __forceinline__ Cursor cursor_at(const int32_t* pre, int S, int Hkv, 
 // Flat index of the first step whose cost position is >= P (total steps if none).
 // Step j of unit g of sequence s sits at prew[s] + g (4 nb + c) + c + 4 j.
 __device__ __forceinline__ int flat_at_cost(const int32_t* pre, const int32_t* prew, int S, int Hkv,
-                                            int unit_cost, int64_t P) {
-  if (P >= prew[S]) return pre[S];
+                                            int unit_cost, uint32_t P) {
+  if (P >= static_cast<uint32_t>(prew[S])) return pre[S];
   int lo = 0, hi = S;  // prew[lo] <= P < prew[hi]
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
-    if (prew[mid] <= P) lo = mid; else hi = mid;
+    if (static_cast<uint32_t>(prew[mid]) <= P) lo = mid; else hi = mid;
   }
   const int nb = (pre[lo + 1] - pre[lo]) / Hkv;
   const int us = 4 * nb + unit_cost;
-  const int r = static_cast<int>(P - prew[lo]);
+  const int r = static_cast<int>(P - static_cast<uint32_t>(prew[lo]));
   int g = r / us;
   const int r2 = r - g * us;
   int j = r2 <= unit_cost ? 0 : (r2 - unit_cost + 3) / 4;
@@ -1006,18 +1006,16 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
         }
       }
     }
-    if (blockIdx.x == 0) {
-      // Words 1..3 of the status area record the layout (warps, group, head_dim)
-      // of the last launch; a workspace reused under another layout holds stale
-      // tickets, which is reported rather than silently mis-merged.
-      int32_t* sig = a.status + 1;
-      const int32_t w = __ldcg(sig), g = __ldcg(sig + 1), d = __ldcg(sig + 2);
-      if (w != 0 && (w != a.total_warps || g != a.G || d != D))
-        atomicOr(a.status, PKV_DEV_WORKSPACE_MISMATCH);
-      sig[0] = a.total_warps;
-      sig[1] = a.G;
-      sig[2] = D;
-    }
+  }
+  // Words 1..3 of the status area record the layout (warps, group, head_dim) of the
+  // last launch; a workspace reused under another layout holds stale tickets, which
+  // is reported rather than silently mis-merged.  Read now, checked once the
+  // schedule is built, so the loads overlap it.
+  int32_t sig_w = 0, sig_g = 0, sig_d = 0;
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    sig_w = __ldcg(a.status + 1);
+    sig_g = __ldcg(a.status + 2);
+    sig_d = __ldcg(a.status + 3);
   }
   const uint32_t raw = ptx::smem_addr(smem_raw);
   const uint32_t base_s = (raw + 1023u) & ~1023u;
@@ -1028,6 +1026,13 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   int32_t* const prew = reinterpret_cast<int32_t*>(base + L.prew);
   build_schedule(a.context_lens, a.S, a.MAXB, a.block_size, a.Hkv, a.unit_cost, ctx_s, pre, prew,
                  reinterpret_cast<int32_t*>(base + L.scratch), a.status);
+  if (threadIdx.x == 0 && blockIdx.x == 0) {
+    if (sig_w != 0 && (sig_w != a.total_warps || sig_g != a.G || sig_d != D))
+      atomicOr(a.status, PKV_DEV_WORKSPACE_MISMATCH);
+    a.status[1] = a.total_warps;
+    a.status[2] = a.G;
+    a.status[3] = D;
+  }
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gw = blockIdx.x * Sh::kWarpsPerCta + warp;
@@ -1038,7 +1043,11 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   // Runs of R quarter steps; R is at least the widest gap between consecutive
   // step positions (4 + UC), so every warp between the first and the last owner
   // of a unit holds a piece of it.
-  const int64_t R = max(static_cast<int64_t>((prew[S] + W - 1) / W), static_cast<int64_t>(4 + UC));
+  // (cost positions stay below 2^31, checked on the host: 32-bit arithmetic holds)
+  const uint32_t R = max((static_cast<uint32_t>(prew[S]) + static_cast<uint32_t>(W) - 1u) /
+                             static_cast<uint32_t>(W),
+                         static_cast<uint32_t>(4 + UC));
+  const int64_t R64 = R;
   T* const out = reinterpret_cast<T*>(a.out);
 
   // Rows of empty contexts are zero.
@@ -1049,8 +1058,14 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
       for (int i = lane; i < a.Hq * D; i += 32) rows[i] = ptx::from_float<T>(0.f);
     }
   }
-  const int f0 = gw < W ? flat_at_cost(pre, prew, S, Hkv, UC, gw * R) : total;
-  const int f1 = gw < W ? flat_at_cost(pre, prew, S, Hkv, UC, (gw + 1) * R) : total;
+  // the run's bounds, searched by the two half-warps at once
+  int fb = total;
+  if (gw < W) {
+    const uint32_t P = static_cast<uint32_t>(gw + (lane >= 16 ? 1 : 0)) * R;
+    fb = flat_at_cost(pre, prew, S, Hkv, UC, P);
+  }
+  const int f0 = __shfl_sync(0xffffffffu, fb, 0);
+  const int f1 = __shfl_sync(0xffffffffu, fb, 16);
   const int nsteps = f1 - f0;
   if (nsteps <= 0) return;
 
@@ -1247,8 +1262,8 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
         const int slot = 2 * gw + (first_j == 0 ? 1 : 0);
         st_.write_partial(a.part_o + static_cast<int64_t>(slot) * a.G * D,
                           a.part_ml + static_cast<int64_t>(slot) * a.G * 2, a.G, lane);
-        cut[ncut++] = CutUnit{cc.s, cc.g, owner_of(pre, prew, Hkv, UC, cc.s, cc.g, 0, R),
-                              owner_of(pre, prew, Hkv, UC, cc.s, cc.g, cc.nb - 1, R)};
+        cut[ncut++] = CutUnit{cc.s, cc.g, owner_of(pre, prew, Hkv, UC, cc.s, cc.g, 0, R64),
+                              owner_of(pre, prew, Hkv, UC, cc.s, cc.g, cc.nb - 1, R64)};
       }
     }
     advance(cc, pre, S, Hkv);

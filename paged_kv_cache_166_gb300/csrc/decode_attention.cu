@@ -517,9 +517,9 @@ struct MmaState {
 // V: stored transposed, [D x 16 bytes] unswizzled, each 16-byte row holding the
 // 16 tokens in the order 0 1 8 9 2 3 10 11 4 5 12 13 6 7 14 15.  Operand
 // fragments come from ldmatrix on bytes: a lane's 32-bit word holds 4 consecutive
-// bytes of one row, widened exactly to two f16 pairs (hardware conversion), and
-// the contractions run on the f16 tensor cores with fp32 accumulation (an int8
-// code, |c| <= 127, and an E4M3 value times 2^-8 are both exact in f16):
+// bytes of one row, widened exactly to two f16 pairs with integer operations (see
+// widen), and the contractions run on the f16 tensor cores with fp32 accumulation
+// (an int8 code, |c| <= 127, and an E4M3 value times 2^-8 are both exact in f16):
 //   scores: the MMA's k index maps to head_dim as k = 2i, 2i+1 -> d = 4i, 4i+1
 //     and k = 2i+8, 2i+9 -> d = 4i+2, 4i+3 (within each 16-wide step); q is loaded
 //     in the same order, so the dot products are unchanged;
@@ -547,20 +547,25 @@ struct Q8State {
     asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(r) : "r"(b), "r"(0x64806480u));
     return r;
   }
-  // Bytes 0-1 (widen) or 2-3 (widen_hi) of w as an f16 pair holding value * 2^-8:
-  // the E4M3 exponent and mantissa bits shifted left by 7 are exactly the f16 bits
-  // of value * 2^-8 (subnormals included), and the sign moves from bit 14 to 15.
-  static __device__ __forceinline__ uint32_t spread(uint32_t pair16) {
-    const uint32_t y = pair16 << 7;
-    return y + (y & 0x40004000u);
+  // fp8: bytes 0-1 (widen) or 2-3 (widen_hi) of w as an f16 pair holding
+  // value * 2^-8: the E4M3 exponent and mantissa bits shifted left by 7 are exactly
+  // the f16 bits of value * 2^-8 (subnormals included) once the sign sits in bit 15.
+  // The byte permute puts each code in the low byte of its f16 and, in its sign
+  // mode, the code's sign bit replicated over the high byte; after the shift by 7
+  // bits 7-13 hold exponent and mantissa, bit 15 the sign, and the mask clears the
+  // rest (three integer operations per f16 pair).
+  static __device__ __forceinline__ uint32_t spread(uint32_t w, uint32_t sel) {
+    uint32_t x;
+    asm("prmt.b32 %0, %1, 0, %2;" : "=r"(x) : "r"(w), "r"(sel));
+    return (x << 7) & 0xbf80bf80u;
   }
   static __device__ __forceinline__ uint32_t widen(uint32_t w) {
     if constexpr (kInt8) return widen_i8(w, 0x4140);
-    return spread(__byte_perm(w, 0u, 0x4140));
+    return spread(w, 0x9180u);
   }
   static __device__ __forceinline__ uint32_t widen_hi(uint32_t w) {
     if constexpr (kInt8) return widen_i8(w, 0x4342);
-    return spread(__byte_perm(w, 0u, 0x4342));
+    return spread(w, 0xb3a2u);
   }
   static constexpr float kWidenScale = kInt8 ? 1.f : 256.f;
 
@@ -630,9 +635,9 @@ struct Q8State {
       mx1 = fmaxf(mx1, __shfl_xor_sync(0xffffffffu, mx1, off));
     }
     const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
-    const float al0 = exp2f(m0 - mn0), al1 = exp2f(m1 - mn1);
-    const float p0 = exp2f(x[0] - mn0), p1 = exp2f(x[1] - mn1);
-    const float p2 = exp2f(x[2] - mn0), p3 = exp2f(x[3] - mn1);
+    const float al0 = ptx::ex2(m0 - mn0), al1 = ptx::ex2(m1 - mn1);
+    const float p0 = ptx::ex2(x[0] - mn0), p1 = ptx::ex2(x[1] - mn1);
+    const float p2 = ptx::ex2(x[2] - mn0), p3 = ptx::ex2(x[3] - mn1);
     l0 = l0 * al0 + (p0 + p2);
     l1 = l1 * al1 + (p1 + p3);
     m0 = mn0;
@@ -1174,7 +1179,8 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     }
   };
 
-  Cursor pc = cursor_at(pre, S, Hkv, f0);
+  Cursor pc;
+  if constexpr (!Sh::kQ8) pc = cursor_at(pre, S, Hkv, f0);
   int p_stage = 0;
   auto issue = [&](int m) {  // warp-uniform; lane 0 issues the copies of local step m
     if ((m & 31) == 0 && m > 0) {
@@ -1193,21 +1199,42 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
 
   // Fill the ring: lanes 0..NS-1 issue the first NS steps at once, one step each.
   const int prologue = nsteps < NS ? nsteps : NS;
+  Cursor lc{0, 0, 0, 1};
+  if constexpr (Sh::kQ8) {
+    // lane NS also finds the step after them, where the producer continues
+    if (lane <= prologue) lc = cursor_at(pre, S, Hkv, min(f0 + lane, total - 1));
+  } else {
+    if (lane < prologue) lc = cursor_at(pre, S, Hkv, f0 + lane);
+  }
   if (lane < prologue) {
-    const Cursor lc = cursor_at(pre, S, Hkv, f0 + lane);
     issue_copies(lane, lc.s, lc.g, lc.j, ids[kIdStride * lane],
                  kIdStride == 2 ? ids[kIdStride * lane + 1] : -1,
                  !Sh::kQRegs && ((lane == 0) || (lc.j == 0)));
   }
   __syncwarp();
   p_stage = prologue == NS ? 0 : prologue;
-  if (prologue > 0) pc = cursor_at(pre, S, Hkv, min(f0 + prologue, total - 1));
+  if constexpr (Sh::kQ8) {
+    pc.s = __shfl_sync(0xffffffffu, lc.s, prologue);
+    pc.g = __shfl_sync(0xffffffffu, lc.g, prologue);
+    pc.j = __shfl_sync(0xffffffffu, lc.j, prologue);
+    pc.nb = __shfl_sync(0xffffffffu, lc.nb, prologue);
+  } else {
+    if (prologue > 0) pc = cursor_at(pre, S, Hkv, min(f0 + prologue, total - 1));
+  }
 
   using State = typename std::conditional<
       Sh::kQ8, Q8State<T, C, D>,
       typename std::conditional<sizeof(T) == 2, MmaState<T, D>, FmaState<D>>::type>::type;
   State st_;
-  Cursor cc = cursor_at(pre, S, Hkv, f0);
+  Cursor cc;
+  if constexpr (Sh::kQ8) {
+    cc.s = __shfl_sync(0xffffffffu, lc.s, 0);
+    cc.g = __shfl_sync(0xffffffffu, lc.g, 0);
+    cc.j = __shfl_sync(0xffffffffu, lc.j, 0);
+    cc.nb = __shfl_sync(0xffffffffu, lc.nb, 0);
+  } else {
+    cc = cursor_at(pre, S, Hkv, f0);
+  }
   int first_j = cc.j;
   CutUnit cut[2];
   int ncut = 0;

@@ -12,9 +12,9 @@ norm): 1e-5 for fp32, 2e-3 for fp16/bf16.  Covered:
 * bit-identity under relabelling of physical blocks and between runs; reuse of
   one workspace across launches;
 * invalid device data flagged in the status word without a fault;
-* the decode step, one launch that writes each new token and attends: bit-identical
-  to the write followed by the attention (output and caches), and against the
-  oracle, invalid device data included.
+* the decode step (the write of each new token, then the attention, chained in
+  one call): bit-identical to the write followed by the attention (output and
+  caches), and against the oracle, invalid device data included.
 """
 import numpy as np
 import pytest

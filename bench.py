@@ -13,9 +13,12 @@ and sigma 1.0 clipped to [1, 2048], pool = blocks + 10% shuffled).
 
 value     = algorithmic KV-read bytes of decode attention / device step time
             (CUDA events on the launching stream; L2 flushed between steps).
-e2e       = the same bytes / end-to-end step time through the public API with
-            pinned host buffers: one H2D copy of the packed q, new K/V, tables and
-            lengths, the decode step, D2H of the output.
+e2e       = the same bytes / end-to-end step time of a decode loop through the
+            public API: every step runs the host block manager, one H2D copy of the
+            packed q, new K/V, tables and lengths from page-locked memory, the
+            decode step and the D2H copy of the output; the host prepares the next
+            step while the device runs the current one (the one-step-at-a-time
+            figures are reported beside it).
 roofline  = the decode-attention kernel, the dominant launch of a step (timed
             in its own loop, L2 flushed): its algorithmic bytes / its event time,
             against the measured HBM copy bandwidth.
@@ -436,12 +439,17 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
       tables and lengths exported into page-locked staging memory), copies the
       step's inputs to the device in one copy, runs the decode step and reads the
       output back; contexts grow by one token a step and each step's bytes are
-      counted from its own lengths."""
+      counted from its own lengths.  Timed one step at a time (eager, then as a
+      CUDA graph) and as a pipelined loop, the host preparing step i + 1 while the
+      device runs step i."""
     import torch
     q8 = args.kv if args.kv in ("fp8", "int8") else None
     e2e_steps = max(1, min(args.steps, E2E_STEPS))
+    half = max(1, e2e_steps // 2)
+    # tokens every sequence gains over the three end-to-end loops (warm-up included)
+    grow = 3 * (args.warmup + half) + 2
     w, lens, NB, kc, vc, host, dev, alloc, sids = build_batch(
-        name, device, rank, args.kv, args.block_size, grow_tokens=2 * args.warmup + e2e_steps + 2)
+        name, device, rank, args.kv, args.block_size, grow_tokens=grow)
     S, Hq, Hkv, D, B = len(lens), w.num_q_heads, w.num_kv_heads, w.head_dim, w.block_size
     elt = kc.element_size()
     q_elt = dev["q"].element_size()
@@ -451,13 +459,14 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
     stream = torch.cuda.current_stream(device)
     attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B, q_elt)
 
-    def decode_step(q, k_new, v_new, tables, ctx):
+    def decode_step(q, k_new, v_new, tables, ctx, o=None):
+        o = out if o is None else o
         if q8:
             fn = pkv.paged_decode_step_fp8 if q8 == "fp8" else pkv.paged_decode_step_int8
             fn(q, k_new, v_new, kc, vc, dev["k_scale"], dev["v_scale"], tables, ctx, w.scale,
-               out, ws, args.num_warps)
+               o, ws, args.num_warps)
         else:
-            pkv.paged_decode_step(q, k_new, v_new, kc, vc, tables, ctx, w.scale, out, ws,
+            pkv.paged_decode_step(q, k_new, v_new, kc, vc, tables, ctx, w.scale, o, ws,
                                   args.num_warps)
 
     def attention():
@@ -525,7 +534,7 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
         raise RuntimeError(f"device status {status} after the timed steps")
 
     # end to end: the decode loop through the public API (see the docstring)
-    maxb = int(-(-(int(lens.max()) + 2 * args.warmup + e2e_steps + 2) // B))
+    maxb = int(-(-(int(lens.max()) + grow) // B))
     names = ["q", "k_new", "v_new", "tables", "ctx"]
     sizes = {k: host[k].numel() * host[k].element_size() for k in names[:3]}
     sizes["tables"] = S * maxb * 4
@@ -579,7 +588,6 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
             nbytes += attention_bytes(lens + grown, Hq, Hkv, D, elt, B, q_elt)
         return float(np.mean(ts)), nbytes / n_steps
 
-    half = max(1, e2e_steps // 2)
     eager_ms, eager_bytes = timed_loop(e2e_step, args.warmup, half)
     # The same step with its copies and launches captured once in a CUDA graph and
     # replayed; the block manager still runs on the host every step and its tables
@@ -598,16 +606,92 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
     except Exception as exc:  # capture refused: report the eager loop alone
         print(f"e2e graph capture unavailable: {exc}", file=sys.stderr)
         torch.cuda.synchronize()
+
+    # The decode loop as a server runs it: the host prepares step i + 1 (block
+    # manager, tables into the other of two page-locked staging buffers) while the
+    # device runs step i; each step's inputs go up on one copy stream and its output
+    # comes back on another, beside the steps.  Timed over all the steps at once; no
+    # L2 flush (a step reads the whole KV cache, several times the L2).
+    stage_h2 = [stage_h, torch.empty(total, dtype=torch.uint8, pin_memory=True)]
+    stage_h2[1].copy_(stage_h)
+    stage_d2 = [stage_d, torch.empty(total, dtype=torch.uint8, device=device)]
+    views2 = [views, {k: stage_d2[1][offs[k]:offs[k] + sizes[k]].view(v.dtype).view(v.shape)
+                      for k, v in views.items()}]
+    tab_h2 = stage_h2[1][offs["tables"]:offs["tables"] + sizes["tables"]].view(torch.int32)
+    ctx_h2 = stage_h2[1][offs["ctx"]:offs["ctx"] + sizes["ctx"]].view(torch.int32)
+    host_steps = [host_step, pkv.DecodeStepTables(alloc, sids, maxb, tab_h2.view(S, maxb).numpy(),
+                                                  ctx_h2.numpy())]
+    out_h2 = [out_h, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)]
+    out2 = [out, torch.empty_like(out)]
+    copy_stream, back_stream = torch.cuda.Stream(device), torch.cuda.Stream(device)
+    h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
+    step_done = [torch.cuda.Event(), torch.cuda.Event()]
+    d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
+
+    # the step captured once per staging buffer (eager if refused)
+    step_graphs = []
+    try:
+        for b in (0, 1):
+            g2 = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g2):
+                v = views2[b]
+                decode_step(v["q"], v["k_new"], v["v_new"], v["tables"], v["ctx"], out2[b])
+            step_graphs.append(g2)
+        torch.cuda.synchronize()
+    except Exception as exc:
+        print(f"e2e graph capture unavailable: {exc}", file=sys.stderr)
+        torch.cuda.synchronize()
+        step_graphs = []
+
+    def pipelined(n_warm, n_steps):
+        nonlocal grown
+        nbytes = 0
+        torch.cuda.synchronize()
+        for it in range(n_warm + n_steps):
+            if it == n_warm:
+                torch.cuda.synchronize()
+                e0.record(stream)
+            b = it & 1
+            h2d_done[b].synchronize()   # the copy of step it - 2 has read this staging buffer
+            host_steps[b]()
+            copy_stream.wait_event(step_done[b])  # step it - 2 is done with its device copy
+            with torch.cuda.stream(copy_stream):
+                stage_d2[b].copy_(stage_h2[b], non_blocking=True)
+                h2d_done[b].record(copy_stream)
+            stream.wait_event(h2d_done[b])
+            stream.wait_event(d2h_done[b])        # step it - 2's output has been read back
+            if step_graphs:
+                step_graphs[b].replay()
+            else:
+                v = views2[b]
+                decode_step(v["q"], v["k_new"], v["v_new"], v["tables"], v["ctx"], out2[b])
+            step_done[b].record(stream)
+            back_stream.wait_event(step_done[b])
+            with torch.cuda.stream(back_stream):
+                out_h2[b].copy_(out2[b], non_blocking=True)
+                d2h_done[b].record(back_stream)
+            grown += 1
+            if it >= n_warm:
+                nbytes += attention_bytes(lens + grown, Hq, Hkv, D, elt, B, q_elt)
+        stream.wait_event(d2h_done[(n_warm + n_steps - 1) & 1])  # the last read-back
+        e1.record(stream)
+        e1.synchronize()
+        return e0.elapsed_time(e1) / n_steps, nbytes / n_steps
+
+    pipe_ms, pipe_bytes = pipelined(args.warmup, half)
+    pipe_graph = bool(step_graphs)
     status = pkv.decode_status(ws)
     if status:
         raise RuntimeError(f"device status {status} after the end-to-end steps")
     e2e_ms_mean, e2e_bytes_per_step = (graph_ms, graph_bytes) if graph_ms else (eager_ms, eager_bytes)
-    ms, pms, e2e_ms_mean, eager_ms = max_over_ranks([ms, pms, e2e_ms_mean, eager_ms], device)
+    ms, pms, e2e_ms_mean, eager_ms, pipe_ms = max_over_ranks(
+        [ms, pms, e2e_ms_mean, eager_ms, pipe_ms], device)
     res = {
         "w": w, "lens": lens, "NB": NB, "q8": q8, "D": D, "bytes": attn_bytes, "ms": ms,
         "pms": pms, "e2e_ms": e2e_ms_mean, "e2e_bytes": e2e_bytes_per_step,
         "e2e_graph": graph_ms is not None, "e2e_eager_ms": eager_ms,
-        "e2e_eager_bytes": eager_bytes,
+        "e2e_eager_bytes": eager_bytes, "e2e_pipe_ms": pipe_ms, "e2e_pipe_bytes": pipe_bytes,
+        "e2e_pipe_graph": pipe_graph,
         "e2e_steps": half, "h2d": total, "d2h": out.numel() * out.element_size(),
         "clocks": clocks.summary(clocks.t_soak, clocks.t_done), "wall": wall,
         "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
@@ -645,22 +729,34 @@ def decode_record(res, world, peak, peak_kind, steps) -> dict:
             "bytes_per_launch": res["bytes"],
             "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
         },
-        "e2e": {"value": round(whole_job_gbs(res["e2e_bytes"], world, res["e2e_ms"]), 1),
-                "unit": "GB/s", "ms_per_step": round(res["e2e_ms"], 4),
+        "e2e": {"value": round(whole_job_gbs(res["e2e_pipe_bytes"], world, res["e2e_pipe_ms"]), 1),
+                "unit": "GB/s", "ms_per_step": round(res["e2e_pipe_ms"], 4),
                 "h2d_bytes_per_step": int(res["h2d"]), "d2h_bytes_per_step": int(res["d2h"]),
                 "steps": res["e2e_steps"],
-                "step": "host block manager (pkv_seq_append_one_each + pkv_export_tables into "
-                        "page-locked staging) + one H2D copy of q, new K/V, tables and lengths "
-                        "+ paged_decode_step + D2H of out"
-                        + ("; the copies and launches captured once in a CUDA graph and "
-                           "replayed each step" if res["e2e_graph"] else "") +
-                        "; a decode loop from the workload's state, contexts one token longer "
-                        "each step, bytes counted per step",
+                "step": "a decode loop from the workload's state through the public API, every "
+                        "step: host block manager (pkv_seq_append_one_each + pkv_export_tables "
+                        "into one of two page-locked staging buffers) + one H2D copy of q, new "
+                        "K/V, tables and lengths (copy stream) + paged_decode_step + D2H of out; "
+                        "the host prepares step i + 1 while the device runs step i"
+                        + ("; the step replayed from a CUDA graph per staging buffer"
+                           if res["e2e_pipe_graph"] else "")
+                        + "; copies on two side streams beside the steps; timed over "
+                        "all steps with CUDA events, no L2 flush (a step reads the whole KV "
+                        "cache, larger than L2); contexts one token longer each step, bytes "
+                        "counted per step",
+                "sequential": {
+                    "value": round(whole_job_gbs(res["e2e_bytes"], world, res["e2e_ms"]), 1),
+                    "ms_per_step": round(res["e2e_ms"], 4),
+                    "step": "one step at a time, timed alone with the L2 flushed before it: "
+                            "host block manager, then the copy, the step and the read-back"
+                            + ("; the copies and launches captured once in a CUDA graph and "
+                               "replayed each step" if res["e2e_graph"] else "")},
                 "eager": {"value": round(whole_job_gbs(res["e2e_eager_bytes"], world,
                                                        res["e2e_eager_ms"]), 1),
                           "ms_per_step": round(res["e2e_eager_ms"], 4),
-                          "step": "the same without the graph: every step through the Python "
-                                  "API (argument checks, tensor maps, two launches, two copies)"}},
+                          "step": "one step at a time without the graph: every step through "
+                                  "the Python API (argument checks, tensor maps, two launches, "
+                                  "two copies)"}},
         "gpu_launches": 2 * steps,
         "clocks": res["clocks"],
         "wall_s_timed_loop": round(res["wall"], 3),

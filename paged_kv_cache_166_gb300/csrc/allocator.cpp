@@ -37,8 +37,10 @@ struct pkv_allocator {
     int32_t len = 0;
     bool live = false;
     bool swapped = false;  // blocks handed back by swap-out, not yet swapped in
+    uint32_t mark = 0;     // batched append: the call that last listed it
   };
   std::vector<Seq> seqs;             // indexed by sequence id
+  uint32_t mark_epoch = 0;           // batched append: calls so far
 
   bool valid_block(int32_t b) const { return b >= 0 && b < num_blocks; }
   bool allocated(int32_t b) const { return valid_block(b) && refcount[b] > 0; }
@@ -272,11 +274,17 @@ int pkv_seq_append_one_each(pkv_allocator_t* a, const int32_t* seqs, int32_t k,
   // of its block, which it then writes in place
   std::vector<std::pair<int32_t, int32_t>> drops;  // (block, refcount dropped so far)
   int64_t need = 0;
+  // a sequence listed twice is found by its mark (this call's number), in O(k)
+  if (++a->mark_epoch == 0) {
+    for (auto& s : a->seqs) s.mark = 0;
+    a->mark_epoch = 1;
+  }
+  const uint32_t epoch = a->mark_epoch;
   for (int32_t i = 0; i < k; ++i) {
     const int32_t q = seqs[i];
     PKV_REQUIRE(a->resident_seq(q), PKV_ERR_INVALID_ARG, "unknown or swapped-out sequence %d", q);
-    for (int32_t j = 0; j < i; ++j)
-      PKV_REQUIRE(seqs[j] != q, PKV_ERR_INVALID_ARG, "sequence %d listed twice", q);
+    PKV_REQUIRE(a->seqs[q].mark != epoch, PKV_ERR_INVALID_ARG, "sequence %d listed twice", q);
+    a->seqs[q].mark = epoch;
     const auto& s = a->seqs[q];
     PKV_REQUIRE(s.len < INT32_MAX, PKV_ERR_INVALID_ARG, "sequence length overflow");
     if (s.len % B == 0) {

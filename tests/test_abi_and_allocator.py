@@ -287,6 +287,25 @@ def test_append_one_each_equals_appends_in_list_order(seed):
     if live:
         with pytest.raises(N.PkvError):  # an id listed twice
             p.c.append_one_each([live[0], live[0]])
+    if len(live) >= 2:
+        before = p.c.num_free()
+        with pytest.raises(N.PkvError):  # listed twice, not side by side: nothing changes
+            p.c.append_one_each([live[0], live[1], live[0]])
+        assert p.c.num_free() == before
+        p.compare()
+        # the refused call leaves no trace: the same ids once each behave as appends
+        trial = copy.deepcopy(p.o)
+        try:
+            expect = [trial.append(s, 1) for s in (live[1], live[0])]
+        except OracleOOB:
+            with pytest.raises(N.OutOfBlocks):
+                p.c.append_one_each([live[1], live[0]])
+        else:
+            slots, cows = p.c.append_one_each([live[1], live[0]])
+            assert list(slots) == [e[0][0] for e in expect]
+            assert cows == [c for e in expect for c in e[1]]
+            p.o = trial
+        p.compare()
     with pytest.raises(N.PkvError):  # an unknown id
         p.c.append_one_each([10 ** 6])
     slots, cows = p.c.append_one_each([])

@@ -469,14 +469,17 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
             pkv.paged_decode_step(q, k_new, v_new, kc, vc, tables, ctx, w.scale, o, ws,
                                   args.num_warps)
 
-    def attention():
+    def attention(q=None, tables=None, ctx=None, o=None):
+        q = dev["q"] if q is None else q
+        tables = dev["tables"] if tables is None else tables
+        ctx = dev["ctx"] if ctx is None else ctx
+        o = out if o is None else o
         if q8:
             fn = pkv.paged_decode_attention_fp8 if q8 == "fp8" else pkv.paged_decode_attention_int8
-            fn(dev["q"], kc, vc, dev["k_scale"], dev["v_scale"], dev["tables"], dev["ctx"],
-               w.scale, out, ws, args.num_warps)
+            fn(q, kc, vc, dev["k_scale"], dev["v_scale"], tables, ctx, w.scale, o, ws,
+               args.num_warps)
         else:
-            pkv.paged_decode_attention(dev["q"], kc, vc, dev["tables"], dev["ctx"], w.scale, out,
-                                       ws, args.num_warps)
+            pkv.paged_decode_attention(q, kc, vc, tables, ctx, w.scale, o, ws, args.num_warps)
 
     def step():
         decode_step(dev["q"], dev["k_new"], dev["v_new"], dev["tables"], dev["ctx"])
@@ -680,6 +683,16 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
 
     pipe_ms, pipe_bytes = pipelined(args.warmup, half)
     pipe_graph = bool(step_graphs)
+    # The last step's read-back against the attention recomputed from its own staged
+    # inputs (the cache already holds its new tokens): the same bits, or the loop's
+    # buffers were reused too early.
+    last = (args.warmup + half - 1) & 1
+    check = torch.empty_like(out)
+    v = views2[last]
+    attention(v["q"], v["tables"], v["ctx"], check)
+    torch.cuda.synchronize()
+    if not torch.equal(check.cpu().view(torch.int16), out_h2[last].view(torch.int16)):
+        raise RuntimeError("pipelined decode loop: the last read-back differs from a recomputation")
     status = pkv.decode_status(ws)
     if status:
         raise RuntimeError(f"device status {status} after the end-to-end steps")

@@ -19,12 +19,15 @@
 //                    arrives as one 4-D TMA box whose axes are reordered on the
 //                    way in (column, row, chunk, group);
 //   softmax          two threads per row (its tensor-memory lane), one per half
-//                    of the keys: causal mask, the row max agreed through shared
-//                    memory, P_j = exp2(S_j - m) (base 2; the exponents of a
-//                    key pair rounded to f16 and raised by one f16x2 ex2)
-//                    rounded to the input type and stored into tensor memory
+//                    of the keys: causal mask (keys past the row score -inf),
+//                    the row max (three-input max) agreed through shared memory,
+//                    P_j = exp2(S_j - m) (base 2; the exponents of a key pair
+//                    formed by one packed f32x2 FMA, rounded to f16 and raised
+//                    by one f16x2 ex2) in the input type (f16: that pair as it
+//                    is; bf16: widened and rounded) and stored into tensor memory
 //                    (two buffers; row r in lane r, keys 2c and 2c + 1 packed in
-//                    column c), the row sum in fp32;
+//                    column c), the row sum in fp32 (f16 halves added by
+//                    mixed-precision adds, or packed f32x2 adds);
 //   O += P_j V_j     tcgen05 MMA with A = P_j read from tensor memory, N =
 //                    head_dim, K = 128 keys: V_j MN-major in shared memory (rows
 //                    of keys, head_dim contiguous), O accumulating in tensor
@@ -66,6 +69,36 @@
 
 namespace pkv {
 namespace {
+
+// max(a, b, c) in one instruction.
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+// (a0, a1) * s + (c, c), two lanes of one packed fp32 instruction.
+__device__ __forceinline__ void fma2(float a0, float a1, float s, float c, float& d0, float& d1) {
+  uint64_t a, b, e, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(a0), "f"(a1));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(b) : "f"(s));
+  asm("mov.b64 %0, {%1, %1};" : "=l"(e) : "f"(c));
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(e));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(d0), "=f"(d1) : "l"(d));
+}
+// (s0, s1) += (x0, x1), one packed fp32 instruction.
+__device__ __forceinline__ void add2(float& s0, float& s1, float x0, float x1) {
+  uint64_t a, b, d;
+  asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(s0), "f"(s1));
+  asm("mov.b64 %0, {%1, %2};" : "=l"(b) : "f"(x0), "f"(x1));
+  asm("add.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
+  asm("mov.b64 {%0, %1}, %2;" : "=f"(s0), "=f"(s1) : "l"(d));
+}
+// s + each half of an f16 pair, each half widened exactly (mixed-precision adds).
+__device__ __forceinline__ void add_f16x2(float& s0, float& s1, uint32_t x) {
+  asm("{\n\t.reg .f16 l, h;\n\tmov.b32 {l, h}, %2;\n\tadd.rn.f32.f16 %0, l, %0;\n\t"
+      "add.rn.f32.f16 %1, h, %1;\n\t}"
+      : "+f"(s0), "+f"(s1) : "r"(x));
+}
 
 constexpr int kTcRows = 128;          // rows of a unit = tensor-memory lanes = MMA M
 constexpr int kTcKeys = 128;          // keys of a KV tile = N of S = K of P.V
@@ -548,14 +581,16 @@ __global__ void __launch_bounds__(kTcThreads, 1)
           ptx::tmem_ld32_nowait(sa, *reinterpret_cast<uint32_t(*)[32]>(&v[0]));
           ptx::tmem_ld32_nowait(sa + 32, *reinterpret_cast<uint32_t(*)[32]>(&v[32]));
           ptx::tmem_wait_ld();
-          if (full) {
-#pragma unroll
-            for (int i = 0; i < kTcHalfKeys; ++i) mx = fmaxf(mx, __uint_as_float(v[i]));
-          } else {
+          // keys past the row's position score -inf: they drop out of the max, and
+          // their 2^(s - m) is 0 (m is finite: key 0 of tile 0 is visible to every row)
+          if (!full) {
 #pragma unroll
             for (int i = 0; i < kTcHalfKeys; ++i)
-              if (i <= lim) mx = fmaxf(mx, __uint_as_float(v[i]));
+              if (i > lim) v[i] = __float_as_uint(-INFINITY);
           }
+#pragma unroll
+          for (int i = 0; i < kTcHalfKeys; i += 2)
+            mx = fmax3(mx, __uint_as_float(v[i]), __uint_as_float(v[i + 1]));
         }
         mx = fmaxf(mx, exchange(mx));
         if (pair_dead) break;
@@ -594,24 +629,20 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         float s0 = 0.f, s1 = 0.f;
         uint32_t pk[kTcHalfKeys / 2];
 #pragma unroll
-        for (int q = 0; q < 8; ++q) {  // keys 8 q .. 8 q + 7 of the half
-          float pe[8];
-          // exponents rounded to f16 pairs, two 2^x per ex2 instruction
-#pragma unroll
-          for (int e = 0; e < 8; e += 2) {
-            const float y0 = fmaf(__uint_as_float(v[8 * q + e]), a.scale_log2, -m);
-            const float y1 = fmaf(__uint_as_float(v[8 * q + e + 1]), a.scale_log2, -m);
+        for (int k = 0; k < kTcHalfKeys / 2; ++k) {  // keys 2k, 2k + 1 of the half
+          // exponents rounded to an f16 pair, two 2^x per ex2 instruction
+          float y0, y1;
+          fma2(__uint_as_float(v[2 * k]), __uint_as_float(v[2 * k + 1]), a.scale_log2, -m, y0, y1);
+          const uint32_t e = ptx::ex2_f16x2(ptx::f16x2_of(y0, y1));
+          if constexpr (std::is_same<T, __half>::value) {
+            pk[k] = e;  // P is the f16 pair itself
+            add_f16x2(s0, s1, e);
+          } else {
             float x0, x1;
-            ptx::f32_of_f16x2(ptx::ex2_f16x2(ptx::f16x2_of(y0, y1)), x0, x1);
-            pe[e] = (full || 8 * q + e <= lim) ? x0 : 0.f;
-            pe[e + 1] = (full || 8 * q + e + 1 <= lim) ? x1 : 0.f;
+            ptx::f32_of_f16x2(e, x0, x1);
+            pk[k] = ptx::pack2<T>(x0, x1);
+            add2(s0, s1, x0, x1);
           }
-          s0 += (pe[0] + pe[1]) + (pe[2] + pe[3]);
-          s1 += (pe[4] + pe[5]) + (pe[6] + pe[7]);
-          pk[4 * q] = ptx::pack2<T>(pe[0], pe[1]);
-          pk[4 * q + 1] = ptx::pack2<T>(pe[2], pe[3]);
-          pk[4 * q + 2] = ptx::pack2<T>(pe[4], pe[5]);
-          pk[4 * q + 3] = ptx::pack2<T>(pe[6], pe[7]);
         }
         ptx::tmem_st32(pcol + b * (kTcKeys / 2), pk);
         ptx::tc_fence_before();

@@ -1179,8 +1179,7 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     }
   };
 
-  Cursor pc;
-  if constexpr (!Sh::kQ8) pc = cursor_at(pre, S, Hkv, f0);
+  Cursor pc{0, 0, 0, 1};
   int p_stage = 0;
   auto issue = [&](int m) {  // warp-uniform; lane 0 issues the copies of local step m
     if ((m & 31) == 0 && m > 0) {
@@ -1197,15 +1196,11 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
     advance(pc, pre, S, Hkv);
   };
 
-  // Fill the ring: lanes 0..NS-1 issue the first NS steps at once, one step each.
+  // Fill the ring: lanes 0..NS-1 issue the first NS steps at once, one step each;
+  // lane NS finds the step after them, where the producer continues.
   const int prologue = nsteps < NS ? nsteps : NS;
   Cursor lc{0, 0, 0, 1};
-  if constexpr (Sh::kQ8) {
-    // lane NS also finds the step after them, where the producer continues
-    if (lane <= prologue) lc = cursor_at(pre, S, Hkv, min(f0 + lane, total - 1));
-  } else {
-    if (lane < prologue) lc = cursor_at(pre, S, Hkv, f0 + lane);
-  }
+  if (lane <= prologue) lc = cursor_at(pre, S, Hkv, min(f0 + lane, total - 1));
   if (lane < prologue) {
     issue_copies(lane, lc.s, lc.g, lc.j, ids[kIdStride * lane],
                  kIdStride == 2 ? ids[kIdStride * lane + 1] : -1,
@@ -1213,14 +1208,10 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   }
   __syncwarp();
   p_stage = prologue == NS ? 0 : prologue;
-  if constexpr (Sh::kQ8) {
-    pc.s = __shfl_sync(0xffffffffu, lc.s, prologue);
-    pc.g = __shfl_sync(0xffffffffu, lc.g, prologue);
-    pc.j = __shfl_sync(0xffffffffu, lc.j, prologue);
-    pc.nb = __shfl_sync(0xffffffffu, lc.nb, prologue);
-  } else {
-    if (prologue > 0) pc = cursor_at(pre, S, Hkv, min(f0 + prologue, total - 1));
-  }
+  pc.s = __shfl_sync(0xffffffffu, lc.s, prologue);
+  pc.g = __shfl_sync(0xffffffffu, lc.g, prologue);
+  pc.j = __shfl_sync(0xffffffffu, lc.j, prologue);
+  pc.nb = __shfl_sync(0xffffffffu, lc.nb, prologue);
 
   using State = typename std::conditional<
       Sh::kQ8, Q8State<T, C, D>,

@@ -648,7 +648,10 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
 
     def pipelined(n_warm, n_steps):
         nonlocal grown
-        nbytes = 0
+        # each timed step's bytes, counted before the loop so that the host's share of a
+        # step holds only the block manager and the launches
+        nbytes = sum(attention_bytes(lens + grown + it + 1, Hq, Hkv, D, elt, B, q_elt)
+                     for it in range(n_warm, n_warm + n_steps))
         torch.cuda.synchronize()
         for it in range(n_warm + n_steps):
             if it == n_warm:
@@ -674,8 +677,6 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
                 out_h2[b].copy_(out2[b], non_blocking=True)
                 d2h_done[b].record(back_stream)
             grown += 1
-            if it >= n_warm:
-                nbytes += attention_bytes(lens + grown, Hq, Hkv, D, elt, B, q_elt)
         stream.wait_event(d2h_done[(n_warm + n_steps - 1) & 1])  # the last read-back
         e1.record(stream)
         e1.synchronize()

@@ -169,6 +169,10 @@ struct TcSched {
   long long hi;  // the CTA's units are those with P < hi
 };
 
+// log2 of the group size (G is 1, 2, 4 or 8, checked on the host): rows R of a unit
+// are query R >> gshift, head R & (G - 1).
+__device__ __forceinline__ int tc_gshift(const PrefillArgs& a) { return __ffs(a.G) - 1; }
+
 __device__ __forceinline__ int tc_tiles(const PrefillArgs& a, int c) {
   return (c * a.G + kTcRows - 1) / kTcRows;
 }
@@ -176,7 +180,7 @@ __device__ __forceinline__ int tc_tiles(const PrefillArgs& a, int c) {
 // KV tiles a unit reads: keys 0 .. p of its last row.
 __device__ __forceinline__ int tc_kv_tiles(const PrefillArgs& a, int t, int c, int tile) {
   const int last_row = min((tile + 1) * kTcRows, c * a.G) - 1;
-  return (t - c + last_row / a.G) / kTcKeys + 1;
+  return (t - c + (last_row >> tc_gshift(a))) / kTcKeys + 1;
 }
 
 // Cost of a sequence: every unit's KV tiles + 1, for every KV head.
@@ -189,11 +193,11 @@ __device__ __forceinline__ long long tc_seq_cost(const PrefillArgs& a, int s, bo
   return cost * a.Hkv;
 }
 
-// Next unit after u (which has nkt KV tiles); u.s == S past the last.
-__device__ __forceinline__ void tc_advance(const PrefillArgs& a, TcSched& u, int nkt) {
-  int t, c, q0;
+// Next unit after u (which has nkt KV tiles, its sequence chunk length c); u.s == S
+// past the last.
+__device__ __forceinline__ void tc_advance(const PrefillArgs& a, TcSched& u, int nkt, int c) {
+  int t, q0;
   u.P += nkt + 1;
-  pf_seq(a, u.s, t, c, q0, false);
   if (++u.tile < tc_tiles(a, c)) return;
   u.tile = 0;
   if (++u.g < a.Hkv) return;
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (tile == nt) {  // lo fell inside the last unit of (l, g): start at the next one
           u.tile = nt - 1;
           u.P = P - (tc_kv_tiles(a, t, c, nt - 1) + 1);
-          tc_advance(a, u, tc_kv_tiles(a, t, c, nt - 1));
+          tc_advance(a, u, tc_kv_tiles(a, t, c, nt - 1), c);
         }
       }
       *sched = u;
@@ -330,12 +334,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 #pragma unroll
           for (int cc = 0; cc < Sh::kChunks; ++cc)
             ptx::tma_load_3d(base_s + Sh::kQOff + qb * Sh::kTile + cc * kTcChunk, &qmap, cc * 64,
-                             u.g * a.G, q0 + u.tile * (kTcRows / a.G), bar(kBarQFull + qb), qpolicy);
+                             u.g * a.G, q0 + u.tile * (kTcRows >> tc_gshift(a)), bar(kBarQFull + qb),
+                             qpolicy);
         }
       }
       if (!__shfl_sync(0xffffffffu, ok, 0)) { alive = false; break; }
       ++un;
-      tc_advance(a, u, tc_kv_tiles(a, t, c, u.tile));
+      tc_advance(a, u, tc_kv_tiles(a, t, c, u.tile), c);
     }
     if (lane == 0) {
       if (!alive) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
@@ -383,7 +388,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                            bar(full0 + st), policy);
       }
       if (!alive) break;
-      tc_advance(a, u, nkt);
+      tc_advance(a, u, nkt, c);
     }
     if (lane == 0) {
       if (!alive) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);
@@ -483,7 +488,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         pn = n;
       }
       if (!alive) break;
-      tc_advance(a, u, nkt);
+      tc_advance(a, u, nkt, c);
     }
     if (alive && pending && !pv(px, pj, pt, pn)) alive = false;
     if (lane == 0) {
@@ -546,11 +551,15 @@ __global__ void __launch_bounds__(kTcThreads, 1)
         if (pend_valid) {
 #pragma unroll
           for (int d = 0; d < 32; d += 8) {
+            float x[8];
+#pragma unroll
+            for (int e = 0; e < 8; e += 2)
+              fma2(__uint_as_float(w[d + e]), __uint_as_float(w[d + e + 1]), inv, 0.f, x[e], x[e + 1]);
             uint4 o4;
-            o4.x = ptx::pack2<T>(__uint_as_float(w[d]) * inv, __uint_as_float(w[d + 1]) * inv);
-            o4.y = ptx::pack2<T>(__uint_as_float(w[d + 2]) * inv, __uint_as_float(w[d + 3]) * inv);
-            o4.z = ptx::pack2<T>(__uint_as_float(w[d + 4]) * inv, __uint_as_float(w[d + 5]) * inv);
-            o4.w = ptx::pack2<T>(__uint_as_float(w[d + 6]) * inv, __uint_as_float(w[d + 7]) * inv);
+            o4.x = ptx::pack2<T>(x[0], x[1]);
+            o4.y = ptx::pack2<T>(x[2], x[3]);
+            o4.z = ptx::pack2<T>(x[4], x[5]);
+            o4.w = ptx::pack2<T>(x[6], x[7]);
             ptx::st_global_v4_hint(pend_row + c0 + d, o4, opolicy);
           }
         }
@@ -566,7 +575,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       const int nkt = tc_kv_tiles(a, t, c, u.tile);
       const int R = u.tile * kTcRows + r;
       const bool valid = R < c * a.G;
-      const int p = valid ? t - c + R / a.G : t - 1;
+      const int p = valid ? t - c + (R >> tc_gshift(a)) : t - 1;
       float m = -INFINITY, l = 0.f;
       for (int j = 0; j < nkt; ++j, ++it) {
         const int b = static_cast<int>(it & 1u);
@@ -660,10 +669,11 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (pair_dead) break;
       pend = true;
       pend_valid = valid;
-      pend_row = og + (static_cast<int64_t>(q0 + R / a.G) * a.Hq + u.g * a.G + R % a.G) * D + h * HD;
+      pend_row = og + (static_cast<int64_t>(q0 + (R >> tc_gshift(a))) * a.Hq + u.g * a.G +
+                        (R & (a.G - 1))) * D + h * HD;
       pend_l = l;
       pend_x = it - 1;
-      tc_advance(a, u, nkt);
+      tc_advance(a, u, nkt, c);
     }
     if (pend && !pair_dead) epilogue();
     if (pair_dead && lane == 0) pf_flag(a, PKV_DEV_WAIT_TIMEOUT);

@@ -13,12 +13,13 @@ and sigma 1.0 clipped to [1, 2048], pool = blocks + 10% shuffled).
 
 value     = algorithmic KV-read bytes of decode attention / device step time
             (CUDA events on the launching stream; L2 flushed between steps).
-e2e       = the same bytes / end-to-end step time of a decode loop through the
-            public API: every step runs the host block manager, one H2D copy of the
-            packed q, new K/V, tables and lengths from page-locked memory, the
-            decode step and the D2H copy of the output; the host prepares the next
-            step while the device runs the current one (the one-step-at-a-time
-            figures are reported beside it).
+e2e       = the same bytes / end-to-end layer-step time of a decode loop through
+            the public API over a two-layer model: every token step runs the host
+            block manager, one H2D copy of both layers' packed q and new K/V with the
+            tables and lengths from page-locked memory, the decode step on each
+            layer's cache and the D2H copies of the outputs; the host prepares the
+            next token step while the device runs the current one (the
+            one-step-at-a-time figures are reported beside it).
 roofline  = the decode-attention kernel, the dominant launch of a step (timed
             in its own loop, L2 flushed): its algorithmic bytes / its event time,
             against the measured HBM copy bandwidth.
@@ -440,8 +441,8 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
       step's inputs to the device in one copy, runs the decode step and reads the
       output back; contexts grow by one token a step and each step's bytes are
       counted from its own lengths.  Timed one step at a time (eager, then as a
-      CUDA graph) and as a pipelined loop, the host preparing step i + 1 while the
-      device runs step i."""
+      CUDA graph) and as a pipelined loop over two layers' caches, the host
+      preparing token step i + 1 while the device runs step i."""
     import torch
     q8 = args.kv if args.kv in ("fp8", "int8") else None
     e2e_steps = max(1, min(args.steps, E2E_STEPS))
@@ -459,27 +460,29 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
     stream = torch.cuda.current_stream(device)
     attn_bytes = attention_bytes(lens, Hq, Hkv, D, elt, B, q_elt)
 
-    def decode_step(q, k_new, v_new, tables, ctx, o=None):
+    def decode_step(q, k_new, v_new, tables, ctx, o=None, caches=None):
         o = out if o is None else o
+        kc_, vc_ = (kc, vc) if caches is None else caches
         if q8:
             fn = pkv.paged_decode_step_fp8 if q8 == "fp8" else pkv.paged_decode_step_int8
-            fn(q, k_new, v_new, kc, vc, dev["k_scale"], dev["v_scale"], tables, ctx, w.scale,
+            fn(q, k_new, v_new, kc_, vc_, dev["k_scale"], dev["v_scale"], tables, ctx, w.scale,
                o, ws, args.num_warps)
         else:
-            pkv.paged_decode_step(q, k_new, v_new, kc, vc, tables, ctx, w.scale, o, ws,
+            pkv.paged_decode_step(q, k_new, v_new, kc_, vc_, tables, ctx, w.scale, o, ws,
                                   args.num_warps)
 
-    def attention(q=None, tables=None, ctx=None, o=None):
+    def attention(q=None, tables=None, ctx=None, o=None, caches=None):
         q = dev["q"] if q is None else q
         tables = dev["tables"] if tables is None else tables
         ctx = dev["ctx"] if ctx is None else ctx
         o = out if o is None else o
+        kc_, vc_ = (kc, vc) if caches is None else caches
         if q8:
             fn = pkv.paged_decode_attention_fp8 if q8 == "fp8" else pkv.paged_decode_attention_int8
-            fn(q, kc, vc, dev["k_scale"], dev["v_scale"], tables, ctx, w.scale, o, ws,
+            fn(q, kc_, vc_, dev["k_scale"], dev["v_scale"], tables, ctx, w.scale, o, ws,
                args.num_warps)
         else:
-            pkv.paged_decode_attention(q, kc, vc, tables, ctx, w.scale, o, ws, args.num_warps)
+            pkv.paged_decode_attention(q, kc_, vc_, tables, ctx, w.scale, o, ws, args.num_warps)
 
     def step():
         decode_step(dev["q"], dev["k_new"], dev["v_new"], dev["tables"], dev["ctx"])
@@ -610,35 +613,65 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
         print(f"e2e graph capture unavailable: {exc}", file=sys.stderr)
         torch.cuda.synchronize()
 
-    # The decode loop as a server runs it: the host prepares step i + 1 (block
-    # manager, tables into the other of two page-locked staging buffers) while the
-    # device runs step i; each step's inputs go up on one copy stream and its output
-    # comes back on another, beside the steps.  Timed over all the steps at once; no
-    # L2 flush (a step reads the whole KV cache, several times the L2).
-    stage_h2 = [stage_h, torch.empty(total, dtype=torch.uint8, pin_memory=True)]
-    stage_h2[1].copy_(stage_h)
-    stage_d2 = [stage_d, torch.empty(total, dtype=torch.uint8, device=device)]
-    views2 = [views, {k: stage_d2[1][offs[k]:offs[k] + sizes[k]].view(v.dtype).view(v.shape)
-                      for k, v in views.items()}]
-    tab_h2 = stage_h2[1][offs["tables"]:offs["tables"] + sizes["tables"]].view(torch.int32)
-    ctx_h2 = stage_h2[1][offs["ctx"]:offs["ctx"] + sizes["ctx"]].view(torch.int32)
-    host_steps = [host_step, pkv.DecodeStepTables(alloc, sids, maxb, tab_h2.view(S, maxb).numpy(),
-                                                  ctx_h2.numpy())]
-    out_h2 = [out_h, torch.empty(out.shape, dtype=out.dtype, pin_memory=True)]
-    out2 = [out, torch.empty_like(out)]
+    # The decode loop as a server runs it, over a model of LAYERS layers: each token
+    # step runs the host block manager once (one new position per sequence, tables and
+    # lengths into one of two page-locked staging buffers), copies every layer's q and
+    # new K/V with the tables in one H2D copy, runs the decode step on each layer's
+    # cache in turn (the second cache holds the same history) and reads every layer's
+    # output back.  The host prepares token step i + 1 while the device runs step i; the
+    # copies go on two side streams beside the steps.  Consecutive launches read
+    # different caches, so none finds the K/V of the launch before in L2 (no flush in
+    # this loop); time and bytes are per layer step, all steps timed together.
+    LAYERS = 2
+    kc_l, vc_l = [kc, kc.clone()], [vc, vc.clone()]
+    pnames = [f"{k}{l}" for l in range(LAYERS) for k in names[:3]] + ["tables", "ctx"]
+    psizes = {f"{k}{l}": sizes[k] for l in range(LAYERS) for k in names[:3]}
+    psizes["tables"], psizes["ctx"] = sizes["tables"], sizes["ctx"]
+    poffs, ptotal = {}, 0
+    for k in pnames:
+        poffs[k] = ptotal
+        ptotal += (psizes[k] + 255) & ~255
+    stage_h2 = [torch.empty(ptotal, dtype=torch.uint8, pin_memory=True) for _ in range(2)]
+    stage_d2 = [torch.empty(ptotal, dtype=torch.uint8, device=device) for _ in range(2)]
+    views2, host_steps = [], []
+    for b in range(2):
+        for l in range(LAYERS):
+            for k in names[:3]:
+                o_ = poffs[f"{k}{l}"]
+                stage_h2[b][o_:o_ + sizes[k]].copy_(host[k].contiguous().view(-1).view(torch.uint8))
+        tab_hb = stage_h2[b][poffs["tables"]:poffs["tables"] + sizes["tables"]].view(torch.int32)
+        ctx_hb = stage_h2[b][poffs["ctx"]:poffs["ctx"] + sizes["ctx"]].view(torch.int32)
+        host_steps.append(pkv.DecodeStepTables(alloc, sids, maxb, tab_hb.view(S, maxb).numpy(),
+                                               ctx_hb.numpy()))
+
+        def dview(k, o_):
+            v = views[k]
+            return stage_d2[b][o_:o_ + sizes[k]].view(v.dtype).view(v.shape)
+        tables_b, ctx_b = dview("tables", poffs["tables"]), dview("ctx", poffs["ctx"])
+        views2.append([{**{k: dview(k, poffs[f"{k}{l}"]) for k in names[:3]},
+                        "tables": tables_b, "ctx": ctx_b} for l in range(LAYERS)])
+    out2 = [[out if (b, l) == (0, 0) else torch.empty_like(out) for l in range(LAYERS)]
+            for b in range(2)]
+    out_h2 = [[torch.empty(out.shape, dtype=out.dtype, pin_memory=True) for _ in range(LAYERS)]
+              for _ in range(2)]
     copy_stream, back_stream = torch.cuda.Stream(device), torch.cuda.Stream(device)
     h2d_done = [torch.cuda.Event(), torch.cuda.Event()]
     step_done = [torch.cuda.Event(), torch.cuda.Event()]
     d2h_done = [torch.cuda.Event(), torch.cuda.Event()]
 
-    # the step captured once per staging buffer (eager if refused)
+    def layer_steps(b):
+        for l in range(LAYERS):
+            v = views2[b][l]
+            decode_step(v["q"], v["k_new"], v["v_new"], v["tables"], v["ctx"], out2[b][l],
+                        (kc_l[l], vc_l[l]))
+
+    # a token step's launches captured once per staging buffer (eager if refused)
     step_graphs = []
     try:
         for b in (0, 1):
             g2 = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g2):
-                v = views2[b]
-                decode_step(v["q"], v["k_new"], v["v_new"], v["tables"], v["ctx"], out2[b])
+                layer_steps(b)
             step_graphs.append(g2)
         torch.cuda.synchronize()
     except Exception as exc:
@@ -648,10 +681,10 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
 
     def pipelined(n_warm, n_steps):
         nonlocal grown
-        # each timed step's bytes, counted before the loop so that the host's share of a
-        # step holds only the block manager and the launches
-        nbytes = sum(attention_bytes(lens + grown + it + 1, Hq, Hkv, D, elt, B, q_elt)
-                     for it in range(n_warm, n_warm + n_steps))
+        # each timed token step's bytes, counted before the loop so that the host's share
+        # of a step holds only the block manager and the launches
+        nbytes = LAYERS * sum(attention_bytes(lens + grown + it + 1, Hq, Hkv, D, elt, B, q_elt)
+                              for it in range(n_warm, n_warm + n_steps))
         torch.cuda.synchronize()
         for it in range(n_warm + n_steps):
             if it == n_warm:
@@ -665,35 +698,36 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
                 stage_d2[b].copy_(stage_h2[b], non_blocking=True)
                 h2d_done[b].record(copy_stream)
             stream.wait_event(h2d_done[b])
-            stream.wait_event(d2h_done[b])        # step it - 2's output has been read back
+            stream.wait_event(d2h_done[b])        # step it - 2's outputs have been read back
             if step_graphs:
                 step_graphs[b].replay()
             else:
-                v = views2[b]
-                decode_step(v["q"], v["k_new"], v["v_new"], v["tables"], v["ctx"], out2[b])
+                layer_steps(b)
             step_done[b].record(stream)
             back_stream.wait_event(step_done[b])
             with torch.cuda.stream(back_stream):
-                out_h2[b].copy_(out2[b], non_blocking=True)
+                for l in range(LAYERS):
+                    out_h2[b][l].copy_(out2[b][l], non_blocking=True)
                 d2h_done[b].record(back_stream)
             grown += 1
         stream.wait_event(d2h_done[(n_warm + n_steps - 1) & 1])  # the last read-back
         e1.record(stream)
         e1.synchronize()
-        return e0.elapsed_time(e1) / n_steps, nbytes / n_steps
+        return e0.elapsed_time(e1) / (n_steps * LAYERS), nbytes / (n_steps * LAYERS)
 
     pipe_ms, pipe_bytes = pipelined(args.warmup, half)
     pipe_graph = bool(step_graphs)
-    # The last step's read-back against the attention recomputed from its own staged
-    # inputs (the cache already holds its new tokens): the same bits, or the loop's
-    # buffers were reused too early.
+    # The last layer step's read-back against the attention recomputed from its own
+    # staged inputs (the cache already holds its new tokens): the same bits, or the
+    # loop's buffers were reused too early.
     last = (args.warmup + half - 1) & 1
     check = torch.empty_like(out)
-    v = views2[last]
-    attention(v["q"], v["tables"], v["ctx"], check)
+    v = views2[last][LAYERS - 1]
+    attention(v["q"], v["tables"], v["ctx"], check, (kc_l[LAYERS - 1], vc_l[LAYERS - 1]))
     torch.cuda.synchronize()
-    if not torch.equal(check.cpu().view(torch.int16), out_h2[last].view(torch.int16)):
+    if not torch.equal(check.cpu().view(torch.int16), out_h2[last][LAYERS - 1].view(torch.int16)):
         raise RuntimeError("pipelined decode loop: the last read-back differs from a recomputation")
+    del kc_l, vc_l
     status = pkv.decode_status(ws)
     if status:
         raise RuntimeError(f"device status {status} after the end-to-end steps")
@@ -705,7 +739,7 @@ def measure_decode(args, name, device, rank, world, pkv, flush):
         "pms": pms, "e2e_ms": e2e_ms_mean, "e2e_bytes": e2e_bytes_per_step,
         "e2e_graph": graph_ms is not None, "e2e_eager_ms": eager_ms,
         "e2e_eager_bytes": eager_bytes, "e2e_pipe_ms": pipe_ms, "e2e_pipe_bytes": pipe_bytes,
-        "e2e_pipe_graph": pipe_graph,
+        "e2e_pipe_graph": pipe_graph, "e2e_pipe_h2d": ptotal / LAYERS,
         "e2e_steps": half, "h2d": total, "d2h": out.numel() * out.element_size(),
         "clocks": clocks.summary(clocks.t_soak, clocks.t_done), "wall": wall,
         "num_warps": args.num_warps or pkv.default_num_warps(D, q8 or dev["q"].dtype),
@@ -745,22 +779,26 @@ def decode_record(res, world, peak, peak_kind, steps) -> dict:
         },
         "e2e": {"value": round(whole_job_gbs(res["e2e_pipe_bytes"], world, res["e2e_pipe_ms"]), 1),
                 "unit": "GB/s", "ms_per_step": round(res["e2e_pipe_ms"], 4),
-                "h2d_bytes_per_step": int(res["h2d"]), "d2h_bytes_per_step": int(res["d2h"]),
+                "h2d_bytes_per_step": int(res["e2e_pipe_h2d"]), "d2h_bytes_per_step": int(res["d2h"]),
                 "steps": res["e2e_steps"],
-                "step": "a decode loop from the workload's state through the public API, every "
-                        "step: host block manager (pkv_seq_append_one_each + pkv_export_tables "
-                        "into one of two page-locked staging buffers) + one H2D copy of q, new "
-                        "K/V, tables and lengths (copy stream) + paged_decode_step + D2H of out; "
-                        "the host prepares step i + 1 while the device runs step i"
-                        + ("; the step replayed from a CUDA graph per staging buffer"
-                           if res["e2e_pipe_graph"] else "")
-                        + "; copies on two side streams beside the steps; timed over "
-                        "all steps with CUDA events, no L2 flush (a step reads the whole KV "
-                        "cache, larger than L2); contexts one token longer each step, bytes "
-                        "counted per step",
+                "step": "one layer step of a decode loop over a two-layer model through the "
+                        "public API; every token step: host block manager once "
+                        "(pkv_seq_append_one_each + pkv_export_tables into one of two "
+                        "page-locked staging buffers), one H2D copy of both layers' q and new "
+                        "K/V with the tables and lengths (copy stream), paged_decode_step on "
+                        "each layer's cache (the second a copy of the first's history), D2H of "
+                        "both outputs; the host prepares token step i + 1 while the device runs "
+                        "step i"
+                        + ("; a token step's launches replayed from a CUDA graph per staging "
+                           "buffer" if res["e2e_pipe_graph"] else "")
+                        + "; copies on two side streams beside the steps; consecutive launches "
+                        "read different caches (no L2 flush needed); all steps timed together "
+                        "with CUDA events; contexts one token longer each token step; time, "
+                        "bytes and copies per layer step",
                 "sequential": {
                     "value": round(whole_job_gbs(res["e2e_bytes"], world, res["e2e_ms"]), 1),
                     "ms_per_step": round(res["e2e_ms"], 4),
+                    "h2d_bytes_per_step": int(res["h2d"]),
                     "step": "one step at a time, timed alone with the L2 flushed before it: "
                             "host block manager, then the copy, the step and the read-back"
                             + ("; the copies and launches captured once in a CUDA graph and "

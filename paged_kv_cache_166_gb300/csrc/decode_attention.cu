@@ -1092,24 +1092,29 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   // block ids each 16-token step reads: table[s][j] (block size 16), table[s][j/2]
   // (32), or table[s][2j] and table[s][2j+1] (8; the second only if the context
   // reaches it).
+  // (copies of one lane's entry of window k, for the step at cursor c)
+  auto put_window = [&](int k, const Cursor& c) {
+    const int32_t* row = a.block_tables + static_cast<int64_t>(c.s) * MAXB;
+    const uint32_t slot = ids_s + (((k & 1) * 32 + lane) * kIdStride) * 4;
+    if (kBlk == kTok || Bsz == 16) {
+      ptx::cp_async_4(slot, row + c.j);
+    } else if (Bsz == 32) {
+      ptx::cp_async_4(slot, row + (c.j >> 1));
+    } else {
+      ptx::cp_async_4(slot, row + 2 * c.j);
+      if (2 * c.j + 1 < (ctx_s[c.s] + 7) / 8) ptx::cp_async_4(slot + 4, row + 2 * c.j + 1);
+    }
+  };
   auto load_window = [&](int k) {
     const int m = 32 * k + lane;
-    if (m < nsteps) {
-      const Cursor c = cursor_at(pre, S, Hkv, f0 + m);
-      const int32_t* row = a.block_tables + static_cast<int64_t>(c.s) * MAXB;
-      const uint32_t slot = ids_s + (((k & 1) * 32 + lane) * kIdStride) * 4;
-      if (kBlk == kTok || Bsz == 16) {
-        ptx::cp_async_4(slot, row + c.j);
-      } else if (Bsz == 32) {
-        ptx::cp_async_4(slot, row + (c.j >> 1));
-      } else {
-        ptx::cp_async_4(slot, row + 2 * c.j);
-        if (2 * c.j + 1 < (ctx_s[c.s] + 7) / 8) ptx::cp_async_4(slot + 4, row + 2 * c.j + 1);
-      }
-    }
+    if (m < nsteps) put_window(k, cursor_at(pre, S, Hkv, f0 + m));
     ptx::cp_async_commit();
   };
-  load_window(0);
+  // The cursors of the run's first 32 steps, one a lane (clamped to the run's last
+  // step): the first table window and the ring fill below both start from them.
+  const Cursor lc = cursor_at(pre, S, Hkv, min(f0 + lane, total - 1));
+  if (lane < nsteps) put_window(0, lc);
+  ptx::cp_async_commit();
   load_window(1);
   ptx::cp_async_wait<1>();
   __syncwarp();
@@ -1199,8 +1204,6 @@ __global__ void __launch_bounds__(Shape<C, D>::kWarpsPerCta * 32, 1)
   // Fill the ring: lanes 0..NS-1 issue the first NS steps at once, one step each;
   // lane NS finds the step after them, where the producer continues.
   const int prologue = nsteps < NS ? nsteps : NS;
-  Cursor lc{0, 0, 0, 1};
-  if (lane <= prologue) lc = cursor_at(pre, S, Hkv, min(f0 + lane, total - 1));
   if (lane < prologue) {
     issue_copies(lane, lc.s, lc.g, lc.j, ids[kIdStride * lane],
                  kIdStride == 2 ? ids[kIdStride * lane + 1] : -1,

@@ -70,6 +70,16 @@
 namespace pkv {
 namespace {
 
+// 32-byte global store (address 32-byte aligned), evict-first in L2, not kept in L1.
+__device__ __forceinline__ void st_global_v8_hint(void* ptr, const uint32_t (&v)[8],
+                                                  uint64_t policy) {
+  asm volatile(
+      "st.global.L1::no_allocate.L2::cache_hint.v8.b32 [%0], {%1, %2, %3, %4, %5, %6, %7, %8}, %9;"
+      ::"l"(ptr), "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]),
+        "r"(v[7]), "l"(policy)
+      : "memory");
+}
+
 // max(a, b, c) in one instruction.
 __device__ __forceinline__ float fmax3(float a, float b, float c) {
   float d;
@@ -544,23 +554,30 @@ __global__ void __launch_bounds__(kTcThreads, 1)
       if (dead) return;
       ptx::tc_fence_after();
       const float inv = 1.f / lt;
+      // 32-byte stores when the output allows them (it need only be 16-byte aligned)
+      const bool wide = (reinterpret_cast<uintptr_t>(pend_row) & 31u) == 0;
 #pragma unroll
       for (int c0 = 0; c0 < HD; c0 += 32) {
         uint32_t w[32];
         ptx::tmem_ld32(oa + c0, w);
         if (pend_valid) {
 #pragma unroll
-          for (int d = 0; d < 32; d += 8) {
-            float x[8];
+          for (int d = 0; d < 32; d += 16) {
+            uint32_t pk8[8];
 #pragma unroll
-            for (int e = 0; e < 8; e += 2)
-              fma2(__uint_as_float(w[d + e]), __uint_as_float(w[d + e + 1]), inv, 0.f, x[e], x[e + 1]);
-            uint4 o4;
-            o4.x = ptx::pack2<T>(x[0], x[1]);
-            o4.y = ptx::pack2<T>(x[2], x[3]);
-            o4.z = ptx::pack2<T>(x[4], x[5]);
-            o4.w = ptx::pack2<T>(x[6], x[7]);
-            ptx::st_global_v4_hint(pend_row + c0 + d, o4, opolicy);
+            for (int e = 0; e < 16; e += 2) {
+              float x0, x1;
+              fma2(__uint_as_float(w[d + e]), __uint_as_float(w[d + e + 1]), inv, 0.f, x0, x1);
+              pk8[e / 2] = ptx::pack2<T>(x0, x1);
+            }
+            if (wide) {
+              st_global_v8_hint(pend_row + c0 + d, pk8, opolicy);
+            } else {
+              ptx::st_global_v4_hint(pend_row + c0 + d, make_uint4(pk8[0], pk8[1], pk8[2], pk8[3]),
+                                     opolicy);
+              ptx::st_global_v4_hint(pend_row + c0 + d + 8,
+                                     make_uint4(pk8[4], pk8[5], pk8[6], pk8[7]), opolicy);
+            }
           }
         }
       }

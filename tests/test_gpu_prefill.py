@@ -9,8 +9,9 @@ word; rows outside the chunks left untouched; keys whose magnitude grows with
 their position (scores rising along the sequence by many factors of 2^8, so
 the kernel's running reference max moves again and again); cache blocks of 8
 and 32 tokens (a 128-key tile read as 16 or 4 blocks; lengths ending inside a
-block, on a block boundary and on a tile boundary); and the bench's own
-workload at full size (16 prompts of 2048 tokens, 70B shape) on sampled rows.
+block, on a block boundary and on a tile boundary); an output only 16-byte
+aligned (the same bits as an aligned one); and the bench's own workload at full
+size (16 prompts of 2048 tokens, 70B shape) on sampled rows.
 """
 import numpy as np
 import pytest
@@ -97,6 +98,33 @@ def test_prefill_matches_oracle(dtype, Hq, Hkv, D, lens, chunks):
     err = BT.row_errors(got[:T], ref)
     assert np.isfinite(got[:T]).all()
     assert err.max() <= BT.tolerance(dtype), f"row error {err.max():.3e}"
+
+
+@pytest.mark.parametrize("dtype,Hq,Hkv,D,lens,chunks", [
+    ("f16", 8, 8, 128, (300, 17), None),
+    ("bf16", 16, 4, 64, (200, 129), (200, 50)),
+])
+def test_prefill_output_only_16_byte_aligned(dtype, Hq, Hkv, D, lens, chunks):
+    """The output rows are written 32 bytes at a time when the output allows it; an
+    output that is 16-byte aligned but not 32 gets the same bits through 16-byte
+    stores, and nothing outside its rows is written."""
+    chunks = lens if chunks is None else chunks
+    kc, vc, q, tables, ctx, qstart = case(dtype, Hq, Hkv, D, lens, chunks, seed=21)
+    args = (torch.from_numpy(tables).cuda(), torch.from_numpy(ctx).cuda(),
+            torch.from_numpy(qstart).cuda(), 1 / np.sqrt(D))
+    out = torch.full_like(q, 7.0)
+    pkv().paged_prefill_attention(q, kc, vc, *args, out)
+    n = q.numel()
+    buf = torch.full((n + 32,), 5.0, dtype=q.dtype, device="cuda")
+    shifted = buf[8:8 + n].view(q.shape)      # 16 bytes past a 256-byte aligned start
+    assert shifted.data_ptr() % 32 == 16
+    shifted.fill_(7.0)
+    status = torch.zeros(1, dtype=torch.int32, device="cuda")
+    pkv().paged_prefill_attention(q, kc, vc, *args, shifted, status)
+    torch.cuda.synchronize()
+    assert int(status.item()) == 0
+    assert torch.equal(shifted.view(torch.int16), out.view(torch.int16))
+    assert torch.all(buf[:8] == 5.0) and torch.all(buf[8 + n:] == 5.0)
 
 
 @pytest.mark.parametrize("dtype,Hq,Hkv,D,lens,chunks", [

@@ -4,10 +4,15 @@
  * The library implements the data-parallel hot path of PagedAttention:
  *   - the cache write that scatters each new token's K and V into its slot,
  *   - single-token decode attention read through per-sequence block tables,
- *     split over the context and merged with a log-sum-exp reduce,
- *   - the whole-block copy that copy-on-write needs,
+ *     split over the context and merged with a log-sum-exp reduce, alone or as
+ *     one decode step together with the write of each sequence's new token,
+ *   - the whole-block copy that copy-on-write needs (one layer, or every layer
+ *     in one launch),
  *   - a host-side block manager (O(1) free list, per-block refcounts, fork,
- *     append with copy-on-write, free).
+ *     append with copy-on-write, free, swap out and in),
+ * and beyond it: fp8 (E4M3) and int8 caches (quantising write, decode over the
+ * codes), swapping of blocks to and from page-locked host memory, and causal
+ * prefill attention over the paged cache on the 5th-generation tensor cores.
  *
  * Conventions (all entry points):
  *   - Every function returns an int status: PKV_OK (0) or a negative PKV_ERR_*.
@@ -170,8 +175,8 @@ int pkv_decode_workspace_size(int32_t num_q_heads, int32_t num_kv_heads, int32_t
  * size); dtype F16/BF16 with head_dim 64, 128 or 256, or F32 with head_dim 32,
  * 64 or 128; G in {1, 2, 4, 8}; num_seqs <= 2048;
  * num_blocks*num_kv_heads*block_size*4 < 2^31; num_seqs*max_blocks_per_seq*num_kv_heads < 2^31.
- * Invalid device data (a context length outside [0, max_blocks_per_seq*16], a
- * block id outside [0, num_blocks)) never faults: it is clamped or read as zeros
+ * Invalid device data (a context length outside [0, max_blocks_per_seq *
+ * block_size], a block id outside [0, num_blocks)) never faults: it is clamped or read as zeros
  * and recorded in the workspace status word (see pkv_decode_status).
  * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_DTYPE, PKV_ERR_UNSUPPORTED, PKV_ERR_CUDA.
  */
@@ -363,8 +368,9 @@ int pkv_kv_write_fp8(const void* k, const void* v, const int32_t* slot_mapping,
  * scores, softmax and accumulation are fp32.  The workspace, num_warps,
  * determinism, status reporting and the programmatic-launch chaining are those
  * of pkv_decode_attention; size the workspace with pkv_decode_workspace_size
- * for dtype PKV_FP8_E4M3 and the same head shape and num_warps (one CTA of 8
- * worker warps per SM by default: the 4 KB fp8 stages leave room for them).
+ * for dtype PKV_FP8_E4M3 and the same head shape and num_warps (by default one
+ * CTA per SM of 16 worker warps at head_dim 128 and 8 at head_dim 256: the 4 KB
+ * 8-bit stages leave room for more warps than the 16-bit caches' 8 KB ones).
  * Supported: block_size 16, head_dim 128 or 256, G in {1, 2, 4, 8}.
  * Errors: as pkv_decode_attention.
  */

@@ -29,6 +29,10 @@ __global__ void kv_write_kernel(const uint4* __restrict__ k, const uint4* __rest
   const int64_t stride = static_cast<int64_t>(gridDim.x) * blockDim.x;
   for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < total_vecs;
        i += stride) {
+    // The rows are loaded before the slot is known (i < total_vecs keeps them in
+    // bounds), so the row and slot loads are in flight together: one memory round
+    // trip before the stores instead of two.
+    const uint4 kr = __ldg(k + i), vr = __ldg(v + i);
     const int64_t th = i / row_vecs;
     const int32_t c = static_cast<int32_t>(i - th * row_vecs);
     const int64_t t = th / Hkv;
@@ -36,8 +40,8 @@ __global__ void kv_write_kernel(const uint4* __restrict__ k, const uint4* __rest
     const int32_t slot = __ldg(slots + t);
     if (slot < 0 || slot >= num_slots) continue;
     const int64_t dst = ((static_cast<int64_t>(slot / B) * Hkv + h) * B + slot % B) * row_vecs + c;
-    kc[dst] = __ldg(k + i);
-    vc[dst] = __ldg(v + i);
+    kc[dst] = kr;
+    vc[dst] = vr;
   }
 }
 
@@ -128,22 +132,33 @@ __device__ __forceinline__ int fp8_v_pos(int t) {
   return t < 8 ? 4 * (t >> 1) + (t & 1) : 4 * ((t - 8) >> 1) + 2 + (t & 1);
 }
 
-// 16 consecutive input elements widened to fp32 (16-byte aligned source).
-__device__ __forceinline__ void load16(const float* p, float (&x)[16]) {
+// The bytes of 16 consecutive input elements (16-byte aligned source), loaded as
+// they are: widened to fp32 by widen16 once they are needed.
+template <typename Tin>
+struct Raw16 {
+  uint4 u[sizeof(Tin)];
+};
+template <typename Tin>
+__device__ __forceinline__ Raw16<Tin> load_raw16(const Tin* p) {
+  Raw16<Tin> r;
+#pragma unroll
+  for (int i = 0; i < static_cast<int>(sizeof(Tin)); ++i)
+    r.u[i] = __ldg(reinterpret_cast<const uint4*>(p) + i);
+  return r;
+}
+__device__ __forceinline__ void widen16(const Raw16<float>& r, float (&x)[16]) {
 #pragma unroll
   for (int i = 0; i < 4; ++i) {
-    const float4 f = __ldg(reinterpret_cast<const float4*>(p) + i);
-    x[4 * i] = f.x;
-    x[4 * i + 1] = f.y;
-    x[4 * i + 2] = f.z;
-    x[4 * i + 3] = f.w;
+    x[4 * i] = __uint_as_float(r.u[i].x);
+    x[4 * i + 1] = __uint_as_float(r.u[i].y);
+    x[4 * i + 2] = __uint_as_float(r.u[i].z);
+    x[4 * i + 3] = __uint_as_float(r.u[i].w);
   }
 }
-__device__ __forceinline__ void load16(const __half* p, float (&x)[16]) {
+__device__ __forceinline__ void widen16(const Raw16<__half>& r, float (&x)[16]) {
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const uint32_t w[4] = {r.u[i].x, r.u[i].y, r.u[i].z, r.u[i].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[j]));
@@ -152,11 +167,10 @@ __device__ __forceinline__ void load16(const __half* p, float (&x)[16]) {
     }
   }
 }
-__device__ __forceinline__ void load16(const __nv_bfloat16* p, float (&x)[16]) {
+__device__ __forceinline__ void widen16(const Raw16<__nv_bfloat16>& r, float (&x)[16]) {
 #pragma unroll
   for (int i = 0; i < 2; ++i) {
-    const uint4 u = __ldg(reinterpret_cast<const uint4*>(p) + i);
-    const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+    const uint32_t w[4] = {r.u[i].x, r.u[i].y, r.u[i].z, r.u[i].w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
       const float2 f = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&w[j]));
@@ -223,6 +237,10 @@ __global__ void kv_write_q8_kernel(const Tin* __restrict__ k, const Tin* __restr
     const int32_t c = static_cast<int32_t>(i - th * groups);
     const int64_t t = th / Hkv;
     const int32_t h = static_cast<int32_t>(th - t * Hkv);
+    // The rows and scales do not depend on the slot, and th * D + 16 * c = 16 i lies
+    // inside the [total * 16] inputs: their loads go out with the slot lookup's.
+    const Raw16<Tin> rk = load_raw16(k + th * D + 16 * c), rv = load_raw16(v + th * D + 16 * c);
+    const float sk = __ldg(ks + h), sv = __ldg(vs + h);
     int32_t slot;
     if (slots != nullptr) {
       slot = __ldg(slots + t);
@@ -236,13 +254,11 @@ __global__ void kv_write_q8_kernel(const Tin* __restrict__ k, const Tin* __restr
     }
     const int64_t tile = static_cast<int64_t>(slot / 16) * Hkv + h;
     const int32_t off = slot % 16;
-    const int64_t src = th * D + 16 * c;
     float x[16];
-    load16(k + src, x);
-    *reinterpret_cast<uint4*>(kc + (tile * 16 + off) * D + 16 * c) =
-        quantize16_as<kInt8>(x, __ldg(ks + h));
-    load16(v + src, x);
-    const uint4 q = quantize16_as<kInt8>(x, __ldg(vs + h));
+    widen16(rk, x);
+    *reinterpret_cast<uint4*>(kc + (tile * 16 + off) * D + 16 * c) = quantize16_as<kInt8>(x, sk);
+    widen16(rv, x);
+    const uint4 q = quantize16_as<kInt8>(x, sv);
     const uint32_t w[4] = {q.x, q.y, q.z, q.w};
     uint8_t* const col = vc + (tile * D + 16 * c) * 16 + fp8_v_pos(off);
 #pragma unroll

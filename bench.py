@@ -935,6 +935,7 @@ def kv_write_bench(args):
     ms = float(np.mean(ts))
     peak, peak_kind = measured_peak()
     gbs = nbytes / (ms * 1e-3) / 1e9
+    traffic = profile_traffic(f"kv_write_{w.name}", "kv_ops.cu")
     print(json.dumps({
         "metric": "paged_kv_write GB/s (new tokens' K/V scattered through slot_mapping)",
         "value": round(gbs, 1), "unit": "GB/s", "n_gpus": 1, "steps": args.steps,
@@ -944,7 +945,12 @@ def kv_write_bench(args):
                                f"{w.dtype}, into a pool of {NB} blocks",
                    "l2": L2Flush.LABEL},
         "roofline": {"bound": "hbm", "achieved": round(gbs, 1), "peak": peak, "unit": "GB/s",
-                     "frac": round(gbs / peak, 4), "traffic": None,
+                     "frac": round(gbs / peak, 4), "traffic": traffic,
+                     "traffic_source": (f"profiles/kv_write_{w.name}.md (ncu dram__bytes_read.sum "
+                                        "+ dram__bytes_write.sum of one earlier capture of the "
+                                        "same kernel code on this workload; not measured in "
+                                        "this run)") if traffic is not None else
+                                       "no ncu capture of the current kernel code on this workload",
                      "kernel": "kv_write_kernel", "bytes_per_launch": nbytes,
                      "peak_source": f"MEASURED_PEAKS.json hbm_gbs ({peak_kind})",
                      "note": "launch-bound at this size: the bytes take well under a "

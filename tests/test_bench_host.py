@@ -19,7 +19,8 @@ def test_code_sha_ignores_comments_and_whitespace_only():
 
 
 def test_every_profile_summary_parses_and_names_its_capture():
-    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", "*_attention_*.md")))
+    paths = sorted(glob.glob(os.path.join(ROOT, "profiles", "*_attention_*.md")) +
+                   glob.glob(os.path.join(ROOT, "profiles", "kv_write_*.md")))
     assert paths
     for p in paths:
         fields = dict(l.strip("- ").split(": ", 1) for l in open(p).read().splitlines()
@@ -27,7 +28,8 @@ def test_every_profile_summary_parses_and_names_its_capture():
         assert len(fields["source_sha"]) == 16 and len(fields["code_sha"]) == 16, p
         assert int(fields["traffic_bytes_per_launch"]) > 0, p
         tag = os.path.basename(p)[:-3]
-        src = "prefill_tcgen05.cu" if tag.startswith("prefill") else "decode_attention.cu"
+        src = ("prefill_tcgen05.cu" if tag.startswith("prefill") else
+               "kv_ops.cu" if tag.startswith("kv_write") else "decode_attention.cu")
         got = bench.profile_traffic(tag, src, fields.get("workload_key"))
         # the figure is reported exactly when the kernel's code is the captured one
         text = open(os.path.join(ROOT, "paged_kv_cache_166_gb300", "csrc", src)).read()

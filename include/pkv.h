@@ -80,6 +80,22 @@ const char* pkv_last_error_string(void);
 /* Library version, encoded as major*10000 + minor*100 + patch. */
 int pkv_version(void);
 
+/*
+ * pkv_wait_timeout_selftest — exercises on the current device the bounded wait that
+ * every kernel of the library uses on its mbarriers (TMA copies, tensor-core commits,
+ * hand-offs between warps), without a fault: one thread waits on an mbarrier that
+ * nothing completes, gives up after limit_us microseconds, ORs PKV_DEV_WAIT_TIMEOUT
+ * into *status and writes the nanoseconds it waited to report[0]; it then completes
+ * the barrier's phase itself and waits again, writing 1 to report[1] if that wait
+ * succeeded.  A healthy device ends with the bit set, report[0] >= limit_us * 1000 and
+ * report[1] == 1, and stays usable afterwards.
+ * status   device int32 word, 4-byte aligned (bits are ORed in, never cleared).
+ * report   device int64 [2], 8-byte aligned.
+ * limit_us 1 .. 1,000,000.
+ * Errors: PKV_ERR_INVALID_ARG, PKV_ERR_CUDA.
+ */
+int pkv_wait_timeout_selftest(int32_t* status, int64_t* report, int32_t limit_us, void* stream);
+
 /* ------------------------------------------------------------------------- */
 /* Cache write                                                                */
 /* ------------------------------------------------------------------------- */

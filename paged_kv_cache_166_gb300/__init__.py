@@ -18,6 +18,8 @@ Public API (all device work runs in libpkv.so's sm_103a kernels):
   ``paged_swap_out_layers`` / ``paged_swap_in_layers`` — every layer's caches, one launch
 * ``BlockAllocator`` — host block manager (free list, refcounts, fork, CoW, free);
   ``DecodeStepTables`` — one decode step's appends and table export, pre-bound
+* ``decode_status(workspace)`` — the device-side status bits of the decode kernels;
+  ``wait_timeout_selftest()`` — the kernels' bounded wait made to run out on purpose
 
 The library is loaded on first use; importing this package needs no GPU.
 """
@@ -33,7 +35,8 @@ def __getattr__(name):
                 "paged_decode_step_fp8", "paged_kv_write_int8", "paged_decode_attention_int8",
                 "paged_decode_step_int8", "paged_swap_out", "paged_swap_in", "paged_swap_out_layers", "paged_swap_in_layers",
                 "paged_prefill_attention",
-                "decode_status", "workspace_bytes", "default_num_warps", "get_workspace"):
+                "decode_status", "workspace_bytes", "default_num_warps", "get_workspace",
+                "wait_timeout_selftest"):
         from . import ops
         return getattr(ops, name)
     raise AttributeError(name)

@@ -38,6 +38,7 @@ _f = ctypes.c_float
 SIGNATURES = {
     "pkv_last_error_string": (ctypes.c_char_p, []),
     "pkv_version": (ctypes.c_int, []),
+    "pkv_wait_timeout_selftest": (ctypes.c_int, [_p, _p, _i32, _p]),
     "pkv_kv_write": (ctypes.c_int, [_p, _p, _p, _i32, _p, _p, _i32, _i32, _i32, _i32, _i32, _p]),
     "pkv_decode_workspace_size": (ctypes.c_int, [_i32, _i32, _i32, _i32, _i32, ctypes.POINTER(_sz)]),
     "pkv_decode_attention": (ctypes.c_int, [_p, _p, _p, _p, _i32, _p, _i32, _i32, _i32, _i32, _i32,

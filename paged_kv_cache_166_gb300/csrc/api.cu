@@ -10,11 +10,31 @@
 #include <mutex>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace pkv {
 namespace {
 thread_local char g_message[512] = {0};
+
+// One thread waits on an mbarrier that nothing completes, through the bounded wait
+// every kernel of the library uses (ptx::mbar_wait); once it gives up it records
+// PKV_DEV_WAIT_TIMEOUT and the time it waited, then completes the barrier's phase
+// itself and waits again, which must succeed at once.
+__global__ void wait_timeout_selftest_kernel(int32_t* status, int64_t* report,
+                                             uint64_t limit_ns) {
+  __shared__ alignas(8) uint64_t bar_word;
+  if (threadIdx.x != 0) return;
+  const uint32_t bar = ptx::smem_addr(&bar_word);
+  ptx::mbar_init(bar, 1);
+  ptx::fence_barrier_init();
+  const uint64_t t0 = ptx::globaltimer_ns();
+  const bool landed = ptx::mbar_wait(bar, 0, limit_ns);
+  report[0] = static_cast<int64_t>(ptx::globaltimer_ns() - t0);
+  if (!landed) atomicOr(status, PKV_DEV_WAIT_TIMEOUT);
+  ptx::mbar_arrive(bar);
+  report[1] = ptx::mbar_wait(bar, 0, limit_ns) ? 1 : 0;
 }
+}  // namespace
 
 int fail(int code, const char* fmt, ...) {
   va_list ap;
@@ -147,5 +167,18 @@ extern "C" {
 const char* pkv_last_error_string(void) { return pkv::g_message; }
 
 int pkv_version(void) { return 100; }
+
+int pkv_wait_timeout_selftest(int32_t* status, int64_t* report, int32_t limit_us, void* stream) {
+  PKV_REQUIRE(status != nullptr && report != nullptr, PKV_ERR_INVALID_ARG,
+              "status and report must be device pointers");
+  PKV_REQUIRE(limit_us >= 1 && limit_us <= 1000000, PKV_ERR_INVALID_ARG,
+              "limit_us %d outside [1, 1000000]", limit_us);
+  PKV_REQUIRE(pkv::aligned(report, 8) && pkv::aligned(status, 4), PKV_ERR_INVALID_ARG,
+              "report must be 8-byte and status 4-byte aligned");
+  pkv::wait_timeout_selftest_kernel<<<1, 32, 0, static_cast<cudaStream_t>(stream)>>>(
+      status, report, static_cast<uint64_t>(limit_us) * 1000u);
+  PKV_CUDA(cudaGetLastError());
+  return pkv::ok();
+}
 
 }  // extern "C"

@@ -444,6 +444,20 @@ def decode_status(workspace: torch.Tensor) -> int:
     return v.value
 
 
+def wait_timeout_selftest(limit_us: int = 20000, device=None) -> tuple:
+    """Runs the library's bounded-wait self-test on ``device`` (default: the current
+    CUDA device) and returns (status bits, nanoseconds the first wait lasted, whether
+    the wait after completing the barrier succeeded).  A healthy device gives
+    (PKV_DEV_WAIT_TIMEOUT, >= limit_us * 1000, True)."""
+    dev = torch.device("cuda", torch.cuda.current_device()) if device is None else torch.device(device)
+    status = torch.zeros(1, dtype=torch.int32, device=dev)
+    report = torch.zeros(2, dtype=torch.int64, device=dev)
+    N.check(N.lib().pkv_wait_timeout_selftest(status.data_ptr(), report.data_ptr(), int(limit_us),
+                                              _stream(dev)))
+    r = report.cpu()
+    return int(status.item()), int(r[0]), bool(r[1] == 1)
+
+
 def _copy_code(cache: torch.Tensor) -> int:
     if cache.dtype in (torch.uint8, getattr(torch, "float8_e4m3fn", None)):
         return N.PKV_FP8_E4M3

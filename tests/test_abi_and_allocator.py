@@ -57,6 +57,12 @@ def test_error_codes_and_messages_without_gpu():
     # status word, 8 tickets, m/l and accumulator partials of 2 pieces per warp
     assert n.value == 256 + 256 + 2 * 8 * 8 * 2 * 4 + 2 * 8 * 8 * 128 * 4
     assert lib.pkv_kv_write(None, None, None, 0, None, None, 4, 2, 16, 100, N.PKV_F16, None) == N.PKV_ERR_INVALID_ARG
+    # the bounded-wait self-test checks its arguments before it launches anything
+    assert lib.pkv_wait_timeout_selftest(None, None, 1000, None) == N.PKV_ERR_INVALID_ARG
+    for limit in (0, -5, 1000001):
+        assert lib.pkv_wait_timeout_selftest(64, 128, limit, None) == N.PKV_ERR_INVALID_ARG
+        assert b"limit_us" in lib.pkv_last_error_string()
+    assert lib.pkv_wait_timeout_selftest(66, 128, 1000, None) == N.PKV_ERR_INVALID_ARG
 
 
 class Pair:

@@ -40,6 +40,14 @@
 // accumulate), P^T is re-laid out in registers with movmatrix, and
 // O^T[D x 8] += V^T P^T on the tensor cores.  fp32: CUDA-core FMA.
 //
+// Block sizes 8 and 32 (16-bit caches) keep the 16-token steps: a step reads half
+// of a 32-token block or two 8-token blocks, and the block-id windows hold two ids
+// per step, so the schedule, the cut points and the results are those of block
+// size 16.  fp8 (E4M3) and int8 caches: the same schedule and merges with 4 KB
+// stages of codes (V tiles stored transposed), more warps per CTA, the codes widened
+// exactly to f16 pairs by integer operations and scaled per KV head around the same
+// tensor-core contractions.
+//
 // The kernel is launched with programmatic stream serialisation: its prologue
 // (schedule, block-table prefetch) overlaps the tail of the preceding cache write
 // (pkv_kv_write, or the decode step's write of each new token), and

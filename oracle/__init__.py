@@ -1,4 +1,5 @@
-"""fp64 CPU oracle for paged decode attention, the cache write and the block manager.
+"""fp64 CPU oracle of the paged KV-cache hot path: decode and prefill attention, the
+cache writes (16-bit and 8-bit), block copies, swapping and the block manager.
 
 TEST INFRASTRUCTURE.  Only ``tests/``, ``__graft_entry__.smoke()`` and the
 ``cpu_baseline`` / reference legs of ``bench.py`` may import or run anything in
@@ -15,7 +16,10 @@ written from the pages that describe PagedAttention:
   section "The PagedAttention kernel: computing attention over scattered
   blocks"; slot formula from "What is paged attention?", section "How it
   works").
-* ``cache_ops``        — the cache-write scatter and the copy-on-write block copy.
+* ``cache_ops``        — the cache-write scatter, the copy-on-write block copy and
+  the block copies of swapping to and from host memory ("PagedAttention — how
+  vLLM stopped wasting 80%...", section "Preemption: what happens when memory
+  runs out anyway").
 * ``block_manager``    — free list, refcounts, fork, append with copy-on-write,
   free ("PagedAttention: How vLLM Borrowed Virtual Memory...", sections
   "The OS-Inspired Insight" and "Walking Through the Lifecycle").

@@ -1,8 +1,9 @@
 """Host-side tests of the C ABI (no GPU needed).
 
 * libpkv.so loads without a GPU and exports every function include/pkv.h declares,
-  each with a ctypes signature in the binding; the header compiles as strict C99
-  and a C program links and runs against the library.
+  each with a ctypes signature in the binding whose arguments match the prototype
+  kind for kind; the header compiles as strict C99 and a C program links and runs
+  against the library.
 * The library's block manager matches the oracle model bit for bit — tables,
   lengths, slots, copy-on-write pairs, refcounts and free counts after every
   operation — on the pages' worked examples and on seeded random operation
@@ -43,6 +44,60 @@ def test_library_exports_every_declared_function():
         assert name in N.SIGNATURES, f"no binding signature for {name}"
     assert set(N.SIGNATURES) == set(names)
     assert lib.pkv_version() >= 100
+
+
+def _c_kind(param: str) -> str:
+    param = " ".join(param.split())
+    if "*" in param:
+        return "ptr"
+    for ctype, kind in (("int32_t", "i32"), ("int64_t", "i64"), ("size_t", "size"),
+                        ("float", "f32"), ("int", "i32"), ("char", "char")):
+        if re.search(r"\b" + ctype + r"\b", param):
+            return kind
+    return "unknown: " + param
+
+
+def _ctypes_kind(t) -> str:
+    import ctypes
+    if t in (ctypes.c_void_p, ctypes.c_char_p) or (isinstance(t, type) and
+                                                   issubclass(t, ctypes._Pointer)):
+        return "ptr"
+    return {ctypes.c_int32: "i32", ctypes.c_int64: "i64", ctypes.c_size_t: "size",
+            ctypes.c_float: "f32"}.get(t, f"unknown: {t}")
+
+
+def _signature_mismatches(signatures) -> list:
+    """(name, header kinds, binding kinds) for every prototype of include/pkv.h whose
+    ctypes declaration differs in argument count, an argument's kind (pointer, int32,
+    int64, size_t, float) or the return kind."""
+    text = open(os.path.join(ROOT, "include", "pkv.h")).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    text = re.sub(r"#[^\n]*", "", text)
+    protos = re.findall(r"([A-Za-z_][A-Za-z_0-9 *]*?)\b(pkv_[a-z_0-9]+)\s*\(([^;{]*?)\)\s*;",
+                        text, flags=re.S)
+    assert sorted(name for _, name, _ in protos) == header_functions()
+    bad = []
+    for ret, name, params in protos:
+        args = [p.strip() for p in params.split(",") if p.strip() and p.strip() != "void"]
+        restype, argtypes = signatures[name]
+        want = [_c_kind(ret)] + [_c_kind(p) for p in args]
+        got = [_ctypes_kind(restype)] + [_ctypes_kind(t) for t in argtypes]
+        if want != got:
+            bad.append((name, want, got))
+    return bad
+
+
+def test_binding_signatures_match_the_header():
+    """A misdeclared argument would otherwise pass a wrong value silently."""
+    assert _signature_mismatches(N.SIGNATURES) == []
+    # planted: one argument dropped, one int32 declared as int64
+    import ctypes
+    planted = dict(N.SIGNATURES)
+    ret, args = planted["pkv_kv_write"]
+    planted["pkv_kv_write"] = (ret, args[:-1])
+    ret, args = planted["pkv_copy_blocks"]
+    planted["pkv_copy_blocks"] = (ret, [args[0], args[1], args[2], ctypes.c_int64] + args[4:])
+    assert [b[0] for b in _signature_mismatches(planted)] == ["pkv_kv_write", "pkv_copy_blocks"]
 
 
 def test_error_codes_and_messages_without_gpu():

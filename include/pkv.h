@@ -586,7 +586,9 @@ int pkv_swap_in_blocks_layers(const void* host_k, const void* host_v, const int3
  *     the slot is table[p / block_size] * block_size + p % block_size;
  *   - freeing a sequence decrements its table in reverse order.
  * Sequence ids are 0, 1, 2, ... in creation order and never reused.
- * Every failing call leaves the state unchanged.  A handle is not thread-safe.
+ * Every failing call leaves the state unchanged, including one whose host memory
+ * allocation fails (PKV_ERR_INVALID_ARG, "host memory exhausted": every call makes
+ * its room before it changes anything).  A handle is not thread-safe.
  */
 typedef struct pkv_allocator pkv_allocator_t;
 

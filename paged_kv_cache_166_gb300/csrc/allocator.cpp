@@ -17,15 +17,43 @@
 //     blocks, all or nothing.
 // Every public call validates first and mutates only once it cannot fail, so a
 // failing call leaves the state unchanged.
+#include <algorithm>
 #include <climits>
 #include <cstdint>
 #include <cstring>
+#include <exception>
+#include <memory>
 #include <new>
 #include <utility>
 #include <vector>
 
 #include "pkv.h"
 #include "status.h"
+
+namespace {
+
+// Runs the body of an entry point that may allocate host memory; a failed
+// allocation becomes an error code, so no C++ exception crosses the C ABI.  The
+// bodies allocate before they change any state, so such a failure leaves the
+// state unchanged like every other failing call.
+template <typename F>
+int guarded(F&& body) {
+  try {
+    return body();
+  } catch (const std::bad_alloc&) {
+    return pkv::fail(PKV_ERR_INVALID_ARG, "host memory exhausted");
+  } catch (const std::exception& e) {
+    return pkv::fail(PKV_ERR_INVALID_ARG, "host error: %s", e.what());
+  }
+}
+
+// Makes room for `extra` more entries (growing geometrically), so that the
+// push_backs which follow cannot allocate.
+void ensure_room(std::vector<int32_t>& v, size_t extra) {
+  if (v.size() + extra > v.capacity()) v.reserve(std::max(v.size() + extra, 2 * v.capacity()));
+}
+
+}  // namespace
 
 struct pkv_allocator {
   int32_t num_blocks = 0;
@@ -80,27 +108,29 @@ int pkv_allocator_create(int32_t num_blocks, int32_t block_size, const int32_t* 
               "num_blocks (%d) and block_size (%d) must be positive", num_blocks, block_size);
   PKV_REQUIRE(static_cast<int64_t>(num_blocks) * block_size < (int64_t(1) << 31),
               PKV_ERR_INVALID_ARG, "num_blocks * block_size must be < 2^31");
-  std::vector<int32_t> order(num_blocks);
-  if (pop_order) {
-    std::vector<char> seen(num_blocks, 0);
-    for (int32_t i = 0; i < num_blocks; ++i) {
-      int32_t b = pop_order[i];
-      PKV_REQUIRE(b >= 0 && b < num_blocks && !seen[b], PKV_ERR_INVALID_ARG,
-                  "pop_order is not a permutation of 0..%d (entry %d = %d)", num_blocks - 1, i, b);
-      seen[b] = 1;
-      order[i] = b;
+  return guarded([&] {
+    std::vector<int32_t> order(num_blocks);
+    if (pop_order) {
+      std::vector<char> seen(num_blocks, 0);
+      for (int32_t i = 0; i < num_blocks; ++i) {
+        int32_t b = pop_order[i];
+        PKV_REQUIRE(b >= 0 && b < num_blocks && !seen[b], PKV_ERR_INVALID_ARG,
+                    "pop_order is not a permutation of 0..%d (entry %d = %d)", num_blocks - 1, i,
+                    b);
+        seen[b] = 1;
+        order[i] = b;
+      }
+    } else {
+      for (int32_t i = 0; i < num_blocks; ++i) order[i] = i;
     }
-  } else {
-    for (int32_t i = 0; i < num_blocks; ++i) order[i] = i;
-  }
-  auto* a = new (std::nothrow) pkv_allocator();
-  PKV_REQUIRE(a != nullptr, PKV_ERR_INVALID_ARG, "host allocation failed");
-  a->num_blocks = num_blocks;
-  a->block_size = block_size;
-  a->free_stack.assign(order.rbegin(), order.rend());
-  a->refcount.assign(num_blocks, 0);
-  *out = a;
-  return pkv::ok();
+    std::unique_ptr<pkv_allocator> a(new pkv_allocator());
+    a->num_blocks = num_blocks;
+    a->block_size = block_size;
+    a->free_stack.assign(order.rbegin(), order.rend());
+    a->refcount.assign(num_blocks, 0);
+    *out = a.release();
+    return pkv::ok();
+  });
 }
 
 int pkv_allocator_destroy(pkv_allocator_t* a) {
@@ -146,25 +176,30 @@ int pkv_seq_create(pkv_allocator_t* a, int32_t* seq) {
   PKV_REQUIRE(a && seq, PKV_ERR_INVALID_ARG, "NULL argument");
   PKV_REQUIRE(a->seqs.size() < static_cast<size_t>(INT32_MAX), PKV_ERR_INVALID_ARG,
               "sequence ids exhausted");
-  a->seqs.emplace_back();
-  a->seqs.back().live = true;
-  *seq = static_cast<int32_t>(a->seqs.size() - 1);
-  return pkv::ok();
+  return guarded([&] {
+    a->seqs.emplace_back();  // no effect if it throws
+    a->seqs.back().live = true;
+    *seq = static_cast<int32_t>(a->seqs.size() - 1);
+    return pkv::ok();
+  });
 }
 
 int pkv_seq_fork(pkv_allocator_t* a, int32_t parent, int32_t* child) {
   PKV_REQUIRE(a && child, PKV_ERR_INVALID_ARG, "NULL argument");
   PKV_REQUIRE(a->resident_seq(parent), PKV_ERR_INVALID_ARG,
               "unknown or swapped-out sequence %d", parent);
-  a->seqs.emplace_back();
-  auto& c = a->seqs.back();
-  const auto& p = a->seqs[parent];
-  c.table = p.table;
-  c.len = p.len;
-  c.live = true;
-  for (int32_t b : c.table) a->refcount[b] += 1;
-  *child = static_cast<int32_t>(a->seqs.size() - 1);
-  return pkv::ok();
+  PKV_REQUIRE(a->seqs.size() < static_cast<size_t>(INT32_MAX), PKV_ERR_INVALID_ARG,
+              "sequence ids exhausted");
+  return guarded([&] {
+    pkv_allocator::Seq c;
+    c.table = a->seqs[parent].table;
+    c.len = a->seqs[parent].len;
+    c.live = true;
+    a->seqs.push_back(std::move(c));  // no effect if it throws
+    for (int32_t b : a->seqs.back().table) a->refcount[b] += 1;
+    *child = static_cast<int32_t>(a->seqs.size() - 1);
+    return pkv::ok();
+  });
 }
 
 int pkv_seq_free(pkv_allocator_t* a, int32_t seq) {
@@ -209,11 +244,13 @@ int pkv_seq_swap_in(pkv_allocator_t* a, int32_t seq, int32_t* ids_out, int32_t c
               "ids_out holds %d ids, the sequence needs %d blocks", capacity, m);
   PKV_REQUIRE(static_cast<size_t>(m) <= a->free_stack.size(), PKV_ERR_OUT_OF_BLOCKS,
               "swap-in needs %d blocks, %zu free", m, a->free_stack.size());
-  s.table.resize(m);
-  for (int32_t j = 0; j < m; ++j) s.table[j] = ids_out[j] = a->pop();
-  s.swapped = false;
-  *n = m;
-  return pkv::ok();
+  return guarded([&] {
+    s.table.resize(m);  // before any block is taken; no effect if it throws
+    for (int32_t j = 0; j < m; ++j) s.table[j] = ids_out[j] = a->pop();
+    s.swapped = false;
+    *n = m;
+    return pkv::ok();
+  });
 }
 
 int pkv_seq_blocks_needed(pkv_allocator_t* a, int32_t seq, int32_t n, int32_t* needed) {
@@ -242,6 +279,11 @@ int pkv_seq_append(pkv_allocator_t* a, int32_t seq, int32_t n, int32_t* slots_ou
               a->free_stack.size());
   PKV_REQUIRE(need == 0 || cow_pair_out || !(s.len % B != 0 && a->refcount[s.table.back()] > 1),
               PKV_ERR_INVALID_ARG, "cow_pair_out is NULL but the append needs a copy");
+  const int rc = guarded([&] {
+    ensure_room(s.table, static_cast<size_t>(need));  // the loop below then cannot allocate
+    return pkv::ok();
+  });
+  if (rc != PKV_OK) return rc;
   *n_cow = 0;
   for (int32_t i = 0; i < n; ++i) {
     const int64_t p = s.len;
@@ -268,62 +310,66 @@ int pkv_seq_append_one_each(pkv_allocator_t* a, const int32_t* seqs, int32_t k,
   PKV_REQUIRE(k >= 0, PKV_ERR_INVALID_ARG, "negative sequence count");
   PKV_REQUIRE(k == 0 || (seqs && slots_out && cow_pairs_out), PKV_ERR_INVALID_ARG,
               "NULL array");
-  const int64_t B = a->block_size;
-  // validate every sequence, and count the blocks the appends take in order: a
-  // copy-on-write earlier in the list may leave a later sequence the last holder
-  // of its block, which it then writes in place
-  std::vector<std::pair<int32_t, int32_t>> drops;  // (block, refcount dropped so far)
-  int64_t need = 0;
-  // a sequence listed twice is found by its mark (this call's number), in O(k)
-  if (++a->mark_epoch == 0) {
-    for (auto& s : a->seqs) s.mark = 0;
-    a->mark_epoch = 1;
-  }
-  const uint32_t epoch = a->mark_epoch;
-  for (int32_t i = 0; i < k; ++i) {
-    const int32_t q = seqs[i];
-    PKV_REQUIRE(a->resident_seq(q), PKV_ERR_INVALID_ARG, "unknown or swapped-out sequence %d", q);
-    PKV_REQUIRE(a->seqs[q].mark != epoch, PKV_ERR_INVALID_ARG, "sequence %d listed twice", q);
-    a->seqs[q].mark = epoch;
-    const auto& s = a->seqs[q];
-    PKV_REQUIRE(s.len < INT32_MAX, PKV_ERR_INVALID_ARG, "sequence length overflow");
-    if (s.len % B == 0) {
-      ++need;
-      continue;
+  return guarded([&] {
+    const int64_t B = a->block_size;
+    // validate every sequence, and count the blocks the appends take in order: a
+    // copy-on-write earlier in the list may leave a later sequence the last holder
+    // of its block, which it then writes in place
+    std::vector<std::pair<int32_t, int32_t>> drops;  // (block, refcount dropped so far)
+    int64_t need = 0;
+    // a sequence listed twice is found by its mark (this call's number), in O(k)
+    if (++a->mark_epoch == 0) {
+      for (auto& s : a->seqs) s.mark = 0;
+      a->mark_epoch = 1;
     }
-    const int32_t last = s.table.back();
-    int32_t rc = a->refcount[last];
-    size_t d = 0;
-    while (d < drops.size() && drops[d].first != last) ++d;
-    if (d < drops.size()) rc -= drops[d].second;
-    if (rc > 1) {
-      ++need;
-      if (d < drops.size()) ++drops[d].second; else drops.emplace_back(last, 1);
+    const uint32_t epoch = a->mark_epoch;
+    for (int32_t i = 0; i < k; ++i) {
+      const int32_t q = seqs[i];
+      PKV_REQUIRE(a->resident_seq(q), PKV_ERR_INVALID_ARG, "unknown or swapped-out sequence %d",
+                  q);
+      PKV_REQUIRE(a->seqs[q].mark != epoch, PKV_ERR_INVALID_ARG, "sequence %d listed twice", q);
+      a->seqs[q].mark = epoch;
+      auto& s = a->seqs[q];
+      PKV_REQUIRE(s.len < INT32_MAX, PKV_ERR_INVALID_ARG, "sequence length overflow");
+      if (s.len % B == 0) {
+        ++need;
+        ensure_room(s.table, 1);  // its push_back below then cannot allocate
+        continue;
+      }
+      const int32_t last = s.table.back();
+      int32_t rc = a->refcount[last];
+      size_t d = 0;
+      while (d < drops.size() && drops[d].first != last) ++d;
+      if (d < drops.size()) rc -= drops[d].second;
+      if (rc > 1) {
+        ++need;
+        if (d < drops.size()) ++drops[d].second; else drops.emplace_back(last, 1);
+      }
     }
-  }
-  PKV_REQUIRE(need <= static_cast<int64_t>(a->free_stack.size()), PKV_ERR_OUT_OF_BLOCKS,
-              "appending one token to each of %d sequences needs %lld blocks, %zu free", k,
-              static_cast<long long>(need), a->free_stack.size());
-  int32_t nc = 0;
-  for (int32_t i = 0; i < k; ++i) {
-    auto& s = a->seqs[seqs[i]];
-    const int64_t p = s.len;
-    if (p % B == 0) {
-      s.table.push_back(a->pop());
-    } else if (a->refcount[s.table.back()] > 1) {
-      const int32_t old_id = s.table.back();
-      const int32_t new_id = a->pop();
-      cow_pairs_out[2 * nc] = old_id;
-      cow_pairs_out[2 * nc + 1] = new_id;
-      ++nc;
-      a->decref(old_id);
-      s.table.back() = new_id;
+    PKV_REQUIRE(need <= static_cast<int64_t>(a->free_stack.size()), PKV_ERR_OUT_OF_BLOCKS,
+                "appending one token to each of %d sequences needs %lld blocks, %zu free", k,
+                static_cast<long long>(need), a->free_stack.size());
+    int32_t nc = 0;
+    for (int32_t i = 0; i < k; ++i) {
+      auto& s = a->seqs[seqs[i]];
+      const int64_t p = s.len;
+      if (p % B == 0) {
+        s.table.push_back(a->pop());
+      } else if (a->refcount[s.table.back()] > 1) {
+        const int32_t old_id = s.table.back();
+        const int32_t new_id = a->pop();
+        cow_pairs_out[2 * nc] = old_id;
+        cow_pairs_out[2 * nc + 1] = new_id;
+        ++nc;
+        a->decref(old_id);
+        s.table.back() = new_id;
+      }
+      slots_out[i] = static_cast<int32_t>(s.table[p / B] * B + p % B);
+      s.len = static_cast<int32_t>(p + 1);
     }
-    slots_out[i] = static_cast<int32_t>(s.table[p / B] * B + p % B);
-    s.len = static_cast<int32_t>(p + 1);
-  }
-  *n_cow = nc;
-  return pkv::ok();
+    *n_cow = nc;
+    return pkv::ok();
+  });
 }
 
 int pkv_seq_len(pkv_allocator_t* a, int32_t seq, int32_t* len) {
